@@ -1,0 +1,169 @@
+"""fp64 CPU oracle for the paged KV store and GQA paged attention.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or run
+anything in this package.  It shares no code with the CUDA library and never
+imports it; the two meet only in the seeded input generators
+(``paged_kv_gqa_store_gb300.workload``), which hold none of the method's
+arithmetic.
+
+What it computes (each function cites its page and section; see ``oracle.c``):
+
+* ``metadata``          -- qo_indptr, kv_len, positions and out_loc of a batch
+                           ("核心数据结构" Batch table; "Engine 与采样器", 手工驱动引擎).
+* ``store_kv``          -- the out_loc row scatter into the K and V pools
+                           ("Mini-SGLang 完整剖析" 4.4.3).
+* ``paged_attention``   -- softmax(q.k / sqrt(D)) v with causal offset and
+                           GQA mapping h -> h / (Hq/Hkv), K/V gathered token by
+                           token through the page table ("第 0 步" attention
+                           operator).
+* ``complete_one``      -- the request length transition after a forward
+                           ("核心数据结构", Req：请求的三个长度).
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(worked examples printed on the pages, a brute-force contiguous attention,
+torch's scaled_dot_product_attention in float64 for the cached_len = 0 case,
+closed forms and invariants).  None is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (OpenMP if available) into oracle/_build."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:4] + ["-fopenmp"] + base[4:], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True, text=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+            lib.oracle_metadata.argtypes = [P, I64, P, P, P, I32, P, P, P, P]
+            lib.oracle_metadata.restype = None
+            lib.oracle_store_kv.argtypes = [P, P, I64, I64, I64, P, P, P, I64]
+            lib.oracle_store_kv.restype = None
+            lib.oracle_paged_attention_rows.argtypes = [
+                P, I64, P, P, I64, P, I64, P, P, P, I32, I32, I32, I32, D, P, I64, P]
+            lib.oracle_paged_attention_rows.restype = None
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def metadata(page_table, cached_len, extend_len, req_rows=None):
+    """Return dict(qo_indptr, kv_len, positions, out_loc) of a batch.
+
+    page_table: int32 [rows, stride] token-granular slots; cached_len,
+    extend_len: int32 [num_reqs]; req_rows: int32 [num_reqs] or None (row r).
+    """
+    pt = _c(page_table, np.int32)
+    c = _c(cached_len, np.int32)
+    e = _c(extend_len, np.int32)
+    rows = None if req_rows is None else _c(req_rows, np.int32)
+    n = int(c.shape[0])
+    total = int(e.sum())
+    qo = np.zeros(n + 1, np.int32)
+    kv = np.zeros(n, np.int32)
+    loc = np.zeros(total, np.int64)
+    pos = np.zeros(total, np.int32)
+    _load().oracle_metadata(_ptr(pt), pt.shape[1], _ptr(rows), _ptr(c), _ptr(e), n,
+                            _ptr(qo), _ptr(kv), _ptr(loc), _ptr(pos))
+    return {"qo_indptr": qo, "kv_len": kv, "positions": pos, "out_loc": loc}
+
+
+def store_kv(k, v, out_loc, k_pool, v_pool):
+    """Scatter new rows into the pools in place.
+
+    k, v: uint16 (bf16 bits) [T, ...] flattened to [T, row_elems];
+    out_loc: [T] integer slots; k_pool, v_pool: uint16 [num_slots, ...] C-contiguous.
+    """
+    kk = _c(k, np.uint16).reshape(k.shape[0], -1)
+    vv = _c(v, np.uint16).reshape(v.shape[0], -1)
+    loc = _c(out_loc, np.int64)
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    assert k_pool.dtype == np.uint16 and v_pool.dtype == np.uint16
+    row = kk.shape[1]
+    pool_stride = int(np.prod(k_pool.shape[1:]))
+    assert row <= pool_stride and loc.shape[0] == kk.shape[0]
+    if loc.size:
+        assert loc.min() >= 0 and loc.max() < k_pool.shape[0]
+    _load().oracle_store_kv(_ptr(kk), _ptr(vv), row, kk.shape[0], row, _ptr(loc),
+                            _ptr(k_pool), _ptr(v_pool), pool_stride)
+
+
+def paged_attention(q, k_pool, v_pool, page_table, cached_len, qo_indptr,
+                    num_qo_heads, num_kv_heads, head_dim, scale=None,
+                    req_rows=None, rows=None):
+    """fp64 paged GQA attention.
+
+    q: uint16 (bf16 bits) [total_q, Hq, D]; pools: uint16 [num_slots, Hkv, D];
+    page_table: int32 [rows, stride]; cached_len: int32 [num_reqs];
+    qo_indptr: int32 [num_reqs + 1]; rows: optional int64 list of query rows
+    (default all).  Returns float64 [len(rows), Hq, D].
+    """
+    if scale is None:
+        scale = 1.0 / np.sqrt(head_dim)
+    qq = _c(q, np.uint16).reshape(q.shape[0], -1)
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    pt = _c(page_table, np.int32)
+    c = _c(cached_len, np.int32)
+    qo = _c(qo_indptr, np.int32)
+    rr = None if req_rows is None else _c(req_rows, np.int32)
+    if rows is None:
+        rows = np.arange(qq.shape[0], dtype=np.int64)
+    rows = _c(rows, np.int64)
+    assert num_qo_heads % num_kv_heads == 0
+    out = np.empty((rows.shape[0], num_qo_heads, head_dim), np.float64)
+    pool_stride = int(np.prod(k_pool.shape[1:]))
+    _load().oracle_paged_attention_rows(
+        _ptr(qq), qq.shape[1], _ptr(k_pool), _ptr(v_pool), pool_stride, _ptr(pt),
+        pt.shape[1], _ptr(rr), _ptr(c), _ptr(qo), c.shape[0], num_qo_heads,
+        num_kv_heads, head_dim, float(scale), _ptr(rows), rows.shape[0], _ptr(out))
+    return out
+
+
+def complete_one(cached_len: int, device_len: int) -> tuple[int, int]:
+    """Request length transition after one forward ("核心数据结构", Req section):
+    every token of this step is now cached, and the next step computes one more
+    position.  Returns the new (cached_len, device_len)."""
+    return device_len, device_len + 1

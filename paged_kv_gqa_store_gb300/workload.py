@@ -1,0 +1,205 @@
+"""Seeded synthetic inputs for the paged KV store and GQA paged attention.
+
+This module only generates inputs: request lengths, page assignments (the
+token-granular page table) and iid N(0,1) bf16 values.  It computes none of the
+method's arithmetic (no out_loc, positions, qo_indptr, scores or softmax), so the
+CUDA library and the CPU oracle can both consume what it produces without
+sharing code.
+
+Shapes follow the Qwen3 attention of "第 0 步：一个能跑的最小推理引擎": 16 query
+heads, 8 KV heads, head_dim 128, bf16.  The page table is token-granular, as
+"核心数据结构：Req、Batch、Context" (Context) states: entry [row, j] is the pool
+slot of token j of that request.  With page_size P > 1, each page is P
+consecutive, P-aligned slots, so entry [row, j] = P * page(j // P) + j % P.
+
+Unreferenced pool rows are filled with a NaN canary so that a stray read shows up
+in the output and a stray write shows up in the pool.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+HQ = 16
+HKV = 8
+HEAD_DIM = 128
+CANARY_BF16 = 0xFFC1          # a quiet NaN in bf16, never produced by N(0,1)
+
+
+def align_up(x: int, a: int) -> int:
+    return (x + a - 1) // a * a
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (round to nearest, ties to even); return uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(
+        np.float32).astype(np.float64)
+
+
+def random_bf16(rng: np.random.Generator, shape) -> np.ndarray:
+    return f32_to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
+
+
+@dataclass
+class BatchSpec:
+    """One batch: per-request lengths and the page table, plus pool geometry."""
+    name: str
+    cached_len: np.ndarray            # int32 [num_reqs]
+    extend_len: np.ndarray            # int32 [num_reqs]
+    req_rows: np.ndarray              # int32 [num_reqs], row in page_table
+    page_table: np.ndarray            # int32 [rows, width], token-granular slots
+    page_size: int
+    num_slots: int                    # pool rows (pages * page_size)
+    seed: int
+    num_layers: int = 1
+    num_qo_heads: int = HQ
+    num_kv_heads: int = HKV
+    head_dim: int = HEAD_DIM
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def num_reqs(self) -> int:
+        return int(self.cached_len.shape[0])
+
+    @property
+    def total_q(self) -> int:
+        return int(self.extend_len.sum())
+
+    @property
+    def device_len(self) -> np.ndarray:
+        return self.cached_len.astype(np.int64) + self.extend_len
+
+    @property
+    def max_kv_len(self) -> int:
+        return int(self.device_len.max()) if self.num_reqs else 0
+
+    @property
+    def row_elems(self) -> int:
+        return self.num_kv_heads * self.head_dim
+
+
+def assign_pages(rng: np.random.Generator, device_lens, page_size: int,
+                 num_pages: int, num_rows: int | None = None,
+                 row_of=None) -> np.ndarray:
+    """Token-granular page table: each request gets ceil(len / P) distinct pages
+    drawn without replacement from [0, num_pages), in random order."""
+    device_lens = np.asarray(device_lens, dtype=np.int64)
+    n = device_lens.shape[0]
+    pages_needed = (device_lens + page_size - 1) // page_size
+    total_pages = int(pages_needed.sum())
+    if total_pages > num_pages:
+        raise ValueError(f"pool of {num_pages} pages cannot hold {total_pages}")
+    chosen = rng.choice(num_pages, size=total_pages, replace=False).astype(np.int64)
+    width = align_up(max(int(device_lens.max()) if n else 1, 1), 32)
+    rows = num_rows if num_rows is not None else n
+    table = np.zeros((rows, width), dtype=np.int32)
+    off = 0
+    for r in range(n):
+        L, npg = int(device_lens[r]), int(pages_needed[r])
+        pages = chosen[off:off + npg]
+        off += npg
+        j = np.arange(L, dtype=np.int64)
+        row = r if row_of is None else int(row_of[r])
+        table[row, :L] = (pages[j // page_size] * page_size + j % page_size).astype(np.int32)
+    return table
+
+
+def make_batch(name: str, seed: int, cached_len, extend_len, page_size: int,
+               num_pages: int, num_layers: int = 1, shuffle_rows: bool = False,
+               extra_rows: int = 0, **kw) -> BatchSpec:
+    rng = np.random.default_rng(seed)
+    cached_len = np.asarray(cached_len, dtype=np.int32)
+    extend_len = np.asarray(extend_len, dtype=np.int32)
+    n = cached_len.shape[0]
+    rows = np.arange(n, dtype=np.int32)
+    if shuffle_rows:
+        rows = rng.permutation(n + extra_rows)[:n].astype(np.int32)
+    table = assign_pages(rng, cached_len.astype(np.int64) + extend_len, page_size,
+                         num_pages, num_rows=n + extra_rows, row_of=rows)
+    return BatchSpec(name=name, cached_len=cached_len, extend_len=extend_len,
+                     req_rows=rows, page_table=table, page_size=page_size,
+                     num_slots=num_pages * page_size, seed=seed,
+                     num_layers=num_layers, **kw)
+
+
+# ---------------------------------------------------------------- the 5 configs
+# A decode request's "context length" is read as its device_len (the KV length
+# after this step, including the new token): cached_len = context - 1, extend 1.
+
+def config_tiny_mixed(seed: int = 1001) -> BatchSpec:
+    """1 extend (prompt 6, cached 2 -> extend 4) + decode at context 5, 17, 64;
+    page_size 1, pool of 4096 pages, slots a seeded random permutation."""
+    return make_batch("tiny_mixed", seed, cached_len=[2, 4, 16, 63],
+                      extend_len=[4, 1, 1, 1], page_size=1, num_pages=4096)
+
+
+def config_decode_28_layers(seed: int = 1002) -> BatchSpec:
+    """64 decode requests, context U[512, 4096], page_size 1, 28 layer pools of
+    300k pages each, one shared page table."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(512, 4096 + 1, size=64)
+    return make_batch("decode_64x28", seed + 1, cached_len=ctx - 1,
+                      extend_len=np.ones(64, np.int32), page_size=1,
+                      num_pages=300_000, num_layers=28)
+
+
+def config_large_decode(num_pages: int, seed: int = 1003) -> BatchSpec:
+    """256 decode requests, context U[1024, 8192], page_size 16, pages drawn at
+    random from a pool of num_pages pages (sized by the caller to 90% of free
+    HBM for one layer)."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(1024, 8192 + 1, size=256)
+    return make_batch("decode_256_p16", seed + 1, cached_len=ctx - 1,
+                      extend_len=np.ones(256, np.int32), page_size=16,
+                      num_pages=num_pages)
+
+
+def config_extend(seed: int = 1004, num_pages: int = 65536) -> BatchSpec:
+    """8 extend requests, cached U[0, 2048], extend U[512, 4096], page_size 1,
+    random slot permutation over a 65536-slot pool."""
+    rng = np.random.default_rng(seed)
+    cached = rng.integers(0, 2048 + 1, size=8)
+    ext = rng.integers(512, 4096 + 1, size=8)
+    return make_batch("extend_8", seed + 1, cached_len=cached, extend_len=ext,
+                      page_size=1, num_pages=num_pages)
+
+
+def config_long_mixed(seed: int = 1005, num_pages: int = 32768) -> BatchSpec:
+    """32 decode requests at context 32768 + 2 extend requests of 2048 tokens
+    over 16384 cached; page_size 64, pages randomly permuted."""
+    cached = [32767] * 32 + [16384] * 2
+    ext = [1] * 32 + [2048] * 2
+    return make_batch("long_mixed_p64", seed, cached_len=cached, extend_len=ext,
+                      page_size=64, num_pages=num_pages)
+
+
+def prefix_slots(spec: BatchSpec) -> np.ndarray:
+    """Pool slots holding each request's cached prefix (positions < cached_len)."""
+    out = []
+    for r in range(spec.num_reqs):
+        c = int(spec.cached_len[r])
+        out.append(spec.page_table[spec.req_rows[r], :c].astype(np.int64))
+    return np.concatenate(out) if out else np.zeros(0, np.int64)
+
+
+def host_tensors(spec: BatchSpec, layer: int = 0) -> dict:
+    """Host-side inputs for one layer (small configs): q, new k/v and both
+    pools (canary everywhere except the cached prefixes), all bf16 bits."""
+    rng = np.random.default_rng([spec.seed, layer])
+    T, H, Hk, D = spec.total_q, spec.num_qo_heads, spec.num_kv_heads, spec.head_dim
+    q = random_bf16(rng, (T, H, D))
+    k_new = random_bf16(rng, (T, Hk, D))
+    v_new = random_bf16(rng, (T, Hk, D))
+    k_pool = np.full((spec.num_slots, Hk, D), CANARY_BF16, np.uint16)
+    v_pool = np.full((spec.num_slots, Hk, D), CANARY_BF16, np.uint16)
+    slots = prefix_slots(spec)
+    k_pool[slots] = random_bf16(rng, (slots.shape[0], Hk, D))
+    v_pool[slots] = random_bf16(rng, (slots.shape[0], Hk, D))
+    return {"q": q, "k_new": k_new, "v_new": v_new, "k_pool": k_pool, "v_pool": v_pool}
