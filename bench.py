@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark: paged KV store + GQA paged attention on GB300.
+
+One step = one pass of the whole hot path over one batch: the metadata plan,
+then for each of the 28 layers store_kv of the step's new K/V and the paged
+attention over the 64-request decode batch (context U[512, 4096], page_size 1,
+16 query / 8 KV heads, head_dim 128, bf16, 28 independent 300k-slot layer
+pools, one shared page table).  The headline metric is decode KV-read GB/s
+(algorithmic bytes: every needed K/V row once, q, out and page-table entries,
+plus the store_kv rows) over the device time of the step.
+
+Also printed, in the same JSON line:
+  roofline      -- the decode kernel's achieved GB/s against the measured HBM peak,
+                   timed with CUDA events around each launch in the timed region;
+  e2e           -- the same metric through the C ABI with the step's inputs in
+                   pinned host memory (H2D copies and the D2H of the outputs timed);
+  extend        -- extend attention TFLOP/s on the 8-request extend batch;
+  cpu_baseline  -- the fp64 oracle on the host cores, on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) each rank runs its own batch (weak scaling, no
+collective on the data path); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_gqa_store_gb300 import workload as wl  # noqa: E402
+
+METRIC = "paged GQA attn: decode KV-read GB/s (% HBM peak); extend TFLOP/s"
+KV_ROW = wl.HKV * wl.HEAD_DIM * 2            # bytes of one token's K (or V) row, one layer
+QO_ROW = wl.HQ * wl.HEAD_DIM * 2             # bytes of one token's q (or out) row
+
+
+def decode_attn_bytes(spec) -> int:
+    """Algorithmic bytes of one layer's attention: K and V of every key once,
+    q and out rows, one page-table entry per page read."""
+    dev = spec.device_len
+    pages = (dev + spec.page_size - 1) // spec.page_size
+    return int(dev.sum() * 2 * KV_ROW + spec.total_q * 2 * QO_ROW + pages.sum() * 4)
+
+
+def store_bytes(spec) -> int:
+    return int(spec.total_q * 2 * KV_ROW * 2)   # read k,v rows + write them
+
+
+def extend_flops(spec) -> float:
+    """4 * D * Hq per unmasked (query, key) pair: 2 for Q.K^T, 2 for P.V."""
+    c = spec.cached_len.astype(np.float64)
+    e = spec.extend_len.astype(np.float64)
+    pairs = (e * c + e * (e + 1) / 2).sum()
+    return 4.0 * wl.HEAD_DIM * wl.HQ * pairs
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, only if the kernel
+    source is unchanged since the counters were taken."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kernel]
+        if d["source_hash"] != source_hash(d["sources"]):
+            return None
+        return d
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our implementation
+def run_ours(args, rank, world, dist):
+    import torch
+    import paged_kv_gqa_store_gb300 as msg
+
+    msg.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+
+    spec = wl.config_decode_28_layers()
+    L = args.layers
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    pt, cached, ext, rows = (i32(spec.page_table), i32(spec.cached_len), i32(spec.extend_len),
+                             i32(spec.req_rows))
+    T, R = spec.total_q, spec.num_reqs
+    qo = torch.zeros(R + 1, dtype=torch.int32, device=dev)
+    loc = torch.zeros(T, dtype=torch.int64, device=dev)
+    ws = torch.zeros(msg.msg_workspace_size(R, T), dtype=torch.uint8, device=dev)
+    layers = [wl.device_tensors(spec, layer, device=dev) for layer in range(L)]
+    outs = [torch.empty_like(t["q"]) for t in layers]
+    flags = msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_DECODE_ONLY
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(L * args.steps)]
+
+    def step(ev=None):
+        msg.msg_plan(pt, cached, ext, T, spec.num_slots, ws, req_rows=rows, qo_indptr_out=qo,
+                     out_loc_out=loc)
+        for i, t in enumerate(layers):
+            msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], loc)
+            if ev is not None:
+                ev[i][0].record(stream)
+            msg.msg_paged_attention(t["q"], t["k_pool"], t["v_pool"], pt, cached, ext, qo,
+                                    outs[i], ws, page_size=spec.page_size, req_rows=rows,
+                                    max_kv_len=spec.max_kv_len, flags=flags)
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    launches_per_step = 2 + 2 * L                 # plan + token meta, store + decode per layer
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st, info = msg.msg_read_device_status(ws)
+    if st != msg.MSG_OK:
+        raise RuntimeError(f"device status after warm-up: {info}")
+
+    clocks = ClockSampler(dev.index)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(attn_ev[k * L:(k + 1) * L])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms = max_over_ranks(t0.elapsed_time(t1)) / args.steps
+
+    bytes_layer = decode_attn_bytes(spec)
+    bytes_step = L * (bytes_layer + store_bytes(spec))
+    value = bytes_step * world / (ms * 1e-3) / 1e9
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+    achieved = bytes_layer / (attn_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("decode_kernel")
+
+    # ---- end to end through the C ABI from pinned host buffers
+    if args.no_e2e:
+        return finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms,
+                           bytes_layer, bytes_step, traffic, launches_per_step, clk, None, dev, msg)
+    host_q = [t["q"].cpu().pin_memory() for t in layers]
+    host_k = [t["k_new"].cpu().pin_memory() for t in layers]
+    host_v = [t["v_new"].cpu().pin_memory() for t in layers]
+    host_meta = [torch.from_numpy(np.ascontiguousarray(a, np.int32)).pin_memory()
+                 for a in (spec.cached_len, spec.extend_len, spec.req_rows)]
+    host_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+    h2d = sum(x.numel() * x.element_size() for x in host_q + host_k + host_v + host_meta)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    def e2e_step():
+        for dst, src in zip((cached, ext, rows), host_meta):
+            dst.copy_(src, non_blocking=True)
+        for i, t in enumerate(layers):
+            t["q"].copy_(host_q[i], non_blocking=True)
+            t["k_new"].copy_(host_k[i], non_blocking=True)
+            t["v_new"].copy_(host_v[i], non_blocking=True)
+        step()
+        for i in range(L):
+            host_out[i].copy_(outs[i], non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+    e2e_value = bytes_step * world / (e2e_ms * 1e-3) / 1e9
+    e2e = {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+    del layers, outs, host_q, host_k, host_v
+    return finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, bytes_layer,
+                       bytes_step, traffic, launches_per_step, clk, e2e, dev, msg)
+
+
+def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, bytes_layer,
+                bytes_step, traffic, launches_per_step, clk, e2e, dev, msg):
+    import torch
+    torch.cuda.empty_cache()
+    R, L = spec.num_reqs, args.layers
+    extend = run_extend(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
+    cpu = cpu_baseline(spec) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v, seeded page permutation)",
+        "config": {
+            "workload": f"decode_64req_ctx512-4096_{L}layers_page1",
+            "requests": R, "layers": L, "page_size": spec.page_size, "pool_slots_per_layer":
+            spec.num_slots, "q_heads": wl.HQ, "kv_heads": wl.HKV, "head_dim": wl.HEAD_DIM,
+            "kv_tokens": int(spec.device_len.sum()), "bytes_per_step": bytes_step,
+            "l2": "inputs larger than L2: 28 distinct layer pools, ~604 MB read per layer",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {
+            "kernel": "decode_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "peak_source": peaks["source"], "bytes_per_launch": bytes_layer,
+            "launch_ms": round(attn_ms, 5),
+            "traffic": None if traffic is None else traffic["bytes_per_launch"]},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if extend is not None:
+        line["extend"] = extend
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def run_extend(args, dev, msg, peaks):
+    """Extend attention TFLOP/s on the 8-request extend batch (store first)."""
+    import torch
+    spec = wl.config_extend()
+    t = wl.device_tensors(spec, device=dev)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    pt, cached, ext, rows = (i32(spec.page_table), i32(spec.cached_len), i32(spec.extend_len),
+                             i32(spec.req_rows))
+    T, R = spec.total_q, spec.num_reqs
+    qo = torch.zeros(R + 1, dtype=torch.int32, device=dev)
+    loc = torch.zeros(T, dtype=torch.int64, device=dev)
+    ws = torch.zeros(msg.msg_workspace_size(R, T), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(t["q"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
+    msg.msg_plan(pt, cached, ext, T, spec.num_slots, ws, req_rows=rows, qo_indptr_out=qo,
+                 out_loc_out=loc)
+    flags = msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_EXTEND_ONLY
+
+    def attn():
+        msg.msg_paged_attention(t["q"], t["k_pool"], t["v_pool"], pt, cached, ext, qo, out, ws,
+                                page_size=1, req_rows=rows, max_kv_len=spec.max_kv_len,
+                                flags=flags)
+
+    def store():
+        msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], loc)
+
+    for _ in range(3):
+        store()
+        attn()
+    n = max(args.steps, 5)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    s = torch.cuda.current_stream()
+    for k in range(n):
+        flush.zero_()
+        ev[k][0].record(s)
+        store()
+        ev[k][1].record(s)
+        flush.zero_()
+        ev[k][2].record(s)
+        attn()
+        ev[k][3].record(s)
+    torch.cuda.synchronize()
+    st_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    at_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
+    fl = extend_flops(spec)
+    tf = fl / (at_ms * 1e-3) / 1e12
+    sb = store_bytes(spec)
+    return {"workload": "extend_8req_cached0-2048_ext512-4096_page1", "tflops": round(tf, 1),
+            "peak_tflops": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4),
+            "peak_source": peaks["source"], "attn_ms": round(at_ms, 4), "flops": fl,
+            "store_kv_gbs": round(sb / (st_ms * 1e-3) / 1e9, 1), "store_kv_ms": round(st_ms, 4),
+            "l2": "flushed (256 MB write) before every timed launch"}
+
+
+# ------------------------------------------------------------ CPU oracle baseline
+def oracle_layer_inputs(spec, layer):
+    """Host copies of one layer's inputs for the oracle (all requests, compacted)."""
+    rng = np.random.default_rng([spec.seed, layer])
+    sub, src = wl.compact_requests(spec, np.arange(spec.num_reqs))
+    n = src.shape[0]
+    kp = wl.random_bf16(rng, (n, wl.HKV, wl.HEAD_DIM))
+    vp = wl.random_bf16(rng, (n, wl.HKV, wl.HEAD_DIM))
+    T = spec.total_q
+    return sub, {"q": wl.random_bf16(rng, (T, wl.HQ, wl.HEAD_DIM)),
+                 "k_new": wl.random_bf16(rng, (T, wl.HKV, wl.HEAD_DIM)),
+                 "v_new": wl.random_bf16(rng, (T, wl.HKV, wl.HEAD_DIM)), "k_pool": kp, "v_pool": vp}
+
+
+def oracle_step_time(spec, sub, data):
+    import oracle
+    t0 = time.perf_counter()
+    meta = oracle.metadata(sub.page_table, sub.cached_len, sub.extend_len, sub.req_rows)
+    oracle.store_kv(data["k_new"], data["v_new"], meta["out_loc"], data["k_pool"], data["v_pool"])
+    oracle.paged_attention(data["q"], data["k_pool"], data["v_pool"], sub.page_table,
+                           sub.cached_len, meta["qo_indptr"], wl.HQ, wl.HKV, wl.HEAD_DIM,
+                           req_rows=sub.req_rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(spec, budget_s: float = 12.0):
+    """The fp64 oracle, as it stands, on whole layers of the same workload (all 64
+    requests), repeated until about budget_s of CPU time; GB/s in the same unit."""
+    import oracle
+    sub, data = oracle_layer_inputs(spec, 0)
+    per_layer = decode_attn_bytes(spec) + store_bytes(spec)
+    done, elapsed = 0, 0.0
+    while elapsed < budget_s and done < spec.num_layers:
+        elapsed += oracle_step_time(spec, sub, data)
+        done += 1
+    return {"value": round(per_layer * done / elapsed / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} of 28 layers (all 64 requests each), fp64 C oracle with OpenMP, "
+                      f"{elapsed:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is one layer of the same workload."""
+    import oracle
+    spec = wl.config_decode_28_layers()
+    sub, data = oracle_layer_inputs(spec, 0)
+    for _ in range(args.warmup):
+        oracle_step_time(spec, sub, data)
+    t = [oracle_step_time(spec, sub, data) for _ in range(args.steps)]
+    per = decode_attn_bytes(spec) + store_bytes(spec)
+    value = per * len(t) / sum(t) / 1e9
+    ms = 1e3 * sum(t) / len(t)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v, seeded page permutation)",
+            "config": {"workload": "decode_64req_ctx512-4096_28layers_page1",
+                       "step": "one layer of the 28 (all 64 requests): store + attention"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s",
+                             "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "one of the 28 layers per step, all 64 requests"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-extend", action="store_true", help="skip the extend sub-benchmark")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
+    ap.add_argument("--layers", type=int, default=28,
+                    help="layers per step (28 for the benchmark; fewer only for profiling)")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            import oracle
+            oracle.build()
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        line = run_ours(args, rank, world, dist)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

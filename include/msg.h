@@ -1,0 +1,218 @@
+/*
+ * msg.h -- C ABI of the GB300 (sm_103a) paged KV store and GQA paged attention.
+ *
+ * The library implements the attention step inside a mini-sglang style
+ * Engine.forward_batch: the step's new K/V rows are scattered into a paged KV
+ * pool (store_kv through out_loc), then GQA attention runs for a mixed batch of
+ * decode and causal extend requests, reading K/V straight through the page
+ * table.  Sources (page title, section):
+ *   [CORE]   "核心数据结构：Req、Batch、Context" (mini-sglang handbook, core):
+ *            sections "Req：请求的三个长度", "Batch：谁来填哪个字段", "Context".
+ *   [ENGINE] "Engine 与采样器" (mini-sglang handbook, engine): sections
+ *            "初始化的顺序" and "手工驱动引擎".
+ *   [TINY]   "第 0 步：一个能跑的最小推理引擎": section "这份代码在做什么"
+ *            (the attention operator: GQA by repeat_interleave, scale
+ *            1/sqrt(D), causal mask at absolute positions).
+ *   [WALK]   "Mini-SGLang 完整剖析": 4.4.3 (KV pool layout, store_kv),
+ *            4.6.4 (page table reading per backend), 4.6.5 (cu_seqlens),
+ *            4.6.7 (store before attend), 4.9.4-4.9.5 (store kernel contract).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are DEVICE pointers unless stated otherwise.  The caller allocates
+ *   and owns every buffer (inputs, outputs, workspace).  The library allocates
+ *   no device memory, never synchronises the stream, and enqueues all work on
+ *   `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
+ * - bf16 tensors are raw bf16 bit patterns.  head_dim must be 128, num_qo_heads
+ *   = 2 * num_kv_heads (the Qwen3 GQA group of 2) and num_kv_heads one of 1, 2,
+ *   4, 8; other shapes return MSG_ERR_UNSUPPORTED.
+ * - Pool layout ([WALK] 4.4.3): one K pool and one V pool per layer, each a
+ *   [num_slots, num_kv_heads, head_dim] bf16 array whose consecutive slots are
+ *   pool_row_stride elements apart.  slot = page * page_size + offset.
+ * - page_table ([CORE] Context; [ENGINE] 初始化的顺序): int32 [rows,
+ *   page_table_stride], token granular: entry [row, j] is the pool slot of
+ *   token j of the request in that row.  With page_size P > 1 the caller
+ *   guarantees that every page is P consecutive, P-aligned slots; the attention
+ *   kernels then read one entry per page (the first token's) and add the offset
+ *   ([WALK] 4.6.4, FlashAttention/TRT-LLM reading).
+ * - Requests ([CORE] Req): cached_len[r] tokens already in the pool, extend_len[r]
+ *   new tokens this step, device_len = cached_len + extend_len.  A request with
+ *   extend_len == 1 is a decode request; extend_len >= 2 is an extend (prefill,
+ *   chunked prefill or prefix-cache hit) request.  extend_len == 0 contributes
+ *   nothing.  New tokens are concatenated in request order without padding;
+ *   qo_indptr[r] is the first token of request r ([CORE] Batch).
+ * - Alignment: every bf16 base pointer 16-byte aligned, every row stride a
+ *   multiple of 8 elements; otherwise MSG_ERR_ALIGNMENT.
+ * - Errors: entry points return MSG_OK (0) or a negative status before
+ *   enqueuing anything; no exception crosses the ABI, nothing aborts and no
+ *   kernel traps.  Data-dependent problems found on the device (a slot outside
+ *   [0, num_slots), a misaligned page, inconsistent lengths, a bounded wait that
+ *   expired) are recorded in a device status block and the offending access is
+ *   redirected to slot 0 or skipped; read the block with msg_read_device_status.
+ */
+#ifndef MSG_H
+#define MSG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side status codes returned by every entry point. */
+#define MSG_OK 0
+#define MSG_ERR_INVALID_ARG -1    /* null pointer, negative size, bad stride    */
+#define MSG_ERR_UNSUPPORTED -2    /* head_dim, head counts or page_size         */
+#define MSG_ERR_ALIGNMENT -3      /* 16-byte alignment of a pointer or stride   */
+#define MSG_ERR_WORKSPACE -4      /* workspace missing or too small             */
+#define MSG_ERR_CUDA -5           /* a CUDA runtime call or launch failed       */
+#define MSG_ERR_DEVICE_CHECK -6   /* msg_read_device_status found a device error */
+
+/* Device-side error codes (first field of the device status block). */
+#define MSG_DEV_OK 0
+#define MSG_DEV_SLOT_OUT_OF_RANGE 1  /* out_loc or page-table slot not in [0, num_slots) */
+#define MSG_DEV_PAGE_MISALIGNED 2    /* page_size > 1 and a page's first slot % page_size != 0 */
+#define MSG_DEV_BAD_LENGTHS 3        /* negative length, device_len > page_table_stride,
+                                        or qo_indptr inconsistent with extend_len */
+#define MSG_DEV_TIMEOUT 4            /* a bounded wait inside a kernel expired */
+#define MSG_DEV_WRONG_PHASE 5        /* decode-only / extend-only flag contradicted */
+
+/* Flags of msg_paged_attention. */
+#define MSG_ATTN_REUSE_PLAN 1u   /* workspace already holds the plan of this batch
+                                    (made by msg_plan, or by a previous
+                                    msg_paged_attention with the same metadata);
+                                    skip the plan kernel */
+#define MSG_ATTN_DECODE_ONLY 2u  /* every request has extend_len <= 1: skip the
+                                    extend kernel launch */
+#define MSG_ATTN_EXTEND_ONLY 4u  /* no request has extend_len == 1: skip the
+                                    decode kernel launch */
+
+/* Size in bytes of the device status block (4 x int32: code, request index,
+ * low and high 32 bits of the offending value).  It sits at the start of the
+ * workspace; a standalone block may be passed to msg_store_kv. */
+#define MSG_STATUS_BYTES 16
+
+/* Human-readable text for a host status code (static storage). */
+const char *msg_status_string(int status);
+
+/* ABI version (major * 10000 + minor * 100 + patch). */
+int msg_version(void);
+
+/*
+ * Workspace bytes needed by msg_plan and msg_paged_attention for batches of at
+ * most max_reqs requests and max_total_q new tokens, with num_qo_heads query
+ * heads of head_dim.  The workspace holds the status block, the plan (per
+ * request lengths, decode partition, extend tile list, merge counters) and the
+ * split-KV partial results.  Returns 0 on invalid arguments.  Any workspace of
+ * at least this size serves every smaller batch.
+ */
+size_t msg_workspace_size(int32_t max_reqs, int64_t max_total_q,
+                          int32_t num_qo_heads, int32_t head_dim);
+
+/*
+ * a1. Per-batch metadata prep ([CORE] Batch table; [ENGINE] 手工驱动引擎;
+ * [WALK] 4.6.5).  From per-request (req_rows, cached_len, extend_len):
+ *   qo_indptr[r+1] = qo_indptr[r] + extend_len[r]          (qo_indptr[0] = 0)
+ *   positions[qo_indptr[r] + i] = cached_len[r] + i          (i < extend_len[r])
+ *   out_loc[qo_indptr[r] + i]   = page_table[row_r, cached_len[r] + i]
+ * and writes the attention plan (decode partition, extend tile list, zeroed
+ * merge counters) into `workspace`, so msg_paged_attention may pass
+ * MSG_ATTN_REUSE_PLAN for this batch.
+ *
+ * page_table      int32 [*, page_table_stride]; rows read: req_rows[r].
+ * req_rows        int32 [num_reqs] page-table row per request, or NULL = r.
+ * cached_len      int32 [num_reqs];  extend_len  int32 [num_reqs].
+ * total_q         host value: sum of extend_len (sizes the output arrays and
+ *                 the launch; a mismatch is reported as MSG_DEV_BAD_LENGTHS).
+ * num_slots       pool rows, for the range check of out_loc.
+ * qo_indptr_out   int32 [num_reqs + 1] or NULL.
+ * out_loc_out     [total_q] int32 (out_loc_is_int64 = 0) or int64 (= 1), or NULL.
+ * positions_out   int32 [total_q] or NULL.
+ * workspace       device buffer of workspace_bytes >= msg_workspace_size(...).
+ * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_WORKSPACE, MSG_ERR_CUDA.
+ */
+int msg_plan(const int32_t *page_table, int64_t page_table_stride,
+             const int32_t *req_rows, const int32_t *cached_len,
+             const int32_t *extend_len, int32_t num_reqs, int64_t total_q,
+             int64_t num_slots, int32_t *qo_indptr_out, void *out_loc_out,
+             int32_t out_loc_is_int64, int32_t *positions_out, void *workspace,
+             size_t workspace_bytes, void *stream);
+
+/*
+ * a2. store_kv ([WALK] 4.4.3, 4.6.7 step 1; shape contract of 4.9.4):
+ *   k_pool[out_loc[i], :, :] = k[i, :, :];  v_pool[out_loc[i], :, :] = v[i, :, :]
+ * for i < num_tokens, bit-exact copies of num_kv_heads * head_dim bf16 values.
+ *
+ * k, v            bf16 [num_tokens, num_kv_heads, head_dim], rows kv_row_stride
+ *                 elements apart (heads contiguous inside a row).
+ * k_pool, v_pool  bf16 pools, rows pool_row_stride elements apart, num_slots rows.
+ * out_loc         [num_tokens] int32 (out_loc_is_int64 = 0) or int64 (= 1).
+ *                 Only padding may repeat a slot (the dummy slot); which
+ *                 duplicate lands is unspecified.
+ * dev_status      MSG_STATUS_BYTES device block or NULL.  A slot outside
+ *                 [0, num_slots) is recorded there and its row is not written.
+ * Must be enqueued before msg_paged_attention on the same stream: attention
+ * reads the step's own K/V from the pool.  num_tokens == 0 is a no-op.
+ * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_UNSUPPORTED, MSG_ERR_ALIGNMENT, MSG_ERR_CUDA.
+ */
+int msg_store_kv(const void *k, const void *v, int64_t kv_row_stride,
+                 void *k_pool, void *v_pool, int64_t pool_row_stride,
+                 int64_t num_slots, const void *out_loc, int32_t out_loc_is_int64,
+                 int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                 int32_t *dev_status, void *stream);
+
+/*
+ * a3-a6. GQA paged attention for a mixed batch ([TINY] attention operator;
+ * [WALK] 4.6.4, 4.6.7 step 2).  For new token i of request r (absolute position
+ * p = cached_len[r] + i) and query head h with kv head g = h / 2:
+ *   out[qo_indptr[r] + i, h, :] = sum_{j <= p} softmax_j(scale * q.K_j[g]) V_j[g]
+ * where K_j, V_j are read from the pools at the slot the page table gives for
+ * token j of row req_rows[r].  Decode requests (extend_len == 1) run a split-KV,
+ * bandwidth-bound kernel whose partial results are merged by log-sum-exp in the
+ * workspace; extend requests run a tensor-core kernel tiled over query chunks
+ * with the causal mask offset by cached_len.
+ *
+ * q               bf16 [total_q, num_qo_heads, head_dim], rows q_row_stride apart.
+ * k_pool, v_pool  as in msg_store_kv; the step's K/V must already be stored.
+ * qo_indptr       int32 [num_reqs + 1] (e.g. from msg_plan), consistent with
+ *                 extend_len.
+ * max_kv_len      host hint: an upper bound of device_len, or 0 if unknown; it
+ *                 only sizes the decode launch for tiny batches.
+ * page_size       power of two in [1, 128]; see the page_table convention.
+ * scale           softmax scale (1/sqrt(head_dim) for the configs here).
+ * out             bf16 [total_q, num_qo_heads, head_dim], contiguous.
+ * workspace       >= msg_workspace_size(num_reqs, total_q, num_qo_heads, head_dim).
+ * flags           MSG_ATTN_* bits.
+ * Consecutive calls that share one workspace must be ordered on one stream.
+ * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_UNSUPPORTED, MSG_ERR_ALIGNMENT,
+ *         MSG_ERR_WORKSPACE, MSG_ERR_CUDA.
+ */
+int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
+                        const void *v_pool, int64_t pool_row_stride,
+                        int64_t num_slots, const int32_t *page_table,
+                        int64_t page_table_stride, const int32_t *req_rows,
+                        const int32_t *cached_len, const int32_t *extend_len,
+                        const int32_t *qo_indptr, int32_t num_reqs,
+                        int64_t total_q, int32_t max_kv_len, int32_t page_size,
+                        int32_t num_qo_heads, int32_t num_kv_heads,
+                        int32_t head_dim, float scale, void *out,
+                        void *workspace, size_t workspace_bytes, uint32_t flags,
+                        void *stream);
+
+/*
+ * Copy the device status block (a workspace, or a standalone
+ * MSG_STATUS_BYTES block) to the host array host_out[4], synchronising
+ * `stream`.  Returns MSG_OK if no device error was recorded,
+ * MSG_ERR_DEVICE_CHECK if one was (host_out[0] holds its MSG_DEV_* code),
+ * MSG_ERR_CUDA if the copy failed.
+ */
+int msg_read_device_status(const void *dev_status, int32_t *host_out, void *stream);
+
+/* Zero a device status block (asynchronously, on `stream`). */
+int msg_clear_device_status(void *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSG_H */

@@ -1,0 +1,256 @@
+"""GB300 (sm_103a) paged KV store + GQA paged attention -- Python binding.
+
+A thin ctypes layer over the C ABI in ``include/msg.h``: the functions below
+carry the same names as the C entry points and only marshal arguments (device
+pointers, sizes, strides and the current CUDA stream) from torch tensors.  All
+of the work runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback.  If the library has not been built, every call raises.
+
+Typical step of one layer (the step's new K/V must be stored before attention):
+
+    ws = torch.empty(msg_workspace_size(num_reqs, total_q), dtype=torch.uint8, device="cuda")
+    msg_plan(page_table, cached_len, extend_len, total_q, num_slots, ws,
+             qo_indptr_out=qo, out_loc_out=out_loc)
+    msg_store_kv(k, v, k_pool, v_pool, out_loc)
+    msg_paged_attention(q, k_pool, v_pool, page_table, cached_len, extend_len,
+                        qo, out, ws, page_size=P, flags=MSG_ATTN_REUSE_PLAN)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+from . import build as _build
+
+MSG_OK = 0
+MSG_ERR_INVALID_ARG = -1
+MSG_ERR_UNSUPPORTED = -2
+MSG_ERR_ALIGNMENT = -3
+MSG_ERR_WORKSPACE = -4
+MSG_ERR_CUDA = -5
+MSG_ERR_DEVICE_CHECK = -6
+
+MSG_DEV_OK = 0
+MSG_DEV_SLOT_OUT_OF_RANGE = 1
+MSG_DEV_PAGE_MISALIGNED = 2
+MSG_DEV_BAD_LENGTHS = 3
+MSG_DEV_TIMEOUT = 4
+MSG_DEV_WRONG_PHASE = 5
+
+MSG_ATTN_REUSE_PLAN = 1
+MSG_ATTN_DECODE_ONLY = 2
+MSG_ATTN_EXTEND_ONLY = 4
+
+MSG_STATUS_BYTES = 16
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "msg.h")
+LIB_PATH = _build.LIB
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MsgError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: status {status} ({text})")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the entry points declared in include/msg.h."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msg_\w+)\s*\(", src)))
+
+
+def load_library(path: str | None = None):
+    """Load the CUDA library (ctypes) and declare every signature.  Raises if the
+    library was not built: there is deliberately no fallback."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing: build it with "
+                "`python -m paged_kv_gqa_store_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(path)
+        P, I32, I64, U32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                ctypes.c_uint32, ctypes.c_size_t)
+        lib.msg_status_string.argtypes = [ctypes.c_int]
+        lib.msg_status_string.restype = ctypes.c_char_p
+        lib.msg_version.argtypes = []
+        lib.msg_version.restype = ctypes.c_int
+        lib.msg_workspace_size.argtypes = [I32, I64, I32, I32]
+        lib.msg_workspace_size.restype = SZ
+        lib.msg_plan.argtypes = [P, I64, P, P, P, I32, I64, I64, P, P, I32, P, P, SZ, P]
+        lib.msg_plan.restype = ctypes.c_int
+        lib.msg_store_kv.argtypes = [P, P, I64, P, P, I64, I64, P, I32, I64, I32, I32, P, P]
+        lib.msg_store_kv.restype = ctypes.c_int
+        lib.msg_paged_attention.argtypes = [
+            P, I64, P, P, I64, I64, P, I64, P, P, P, P, I32, I64, I32, I32, I32, I32, I32,
+            ctypes.c_float, P, P, SZ, U32, P]
+        lib.msg_paged_attention.restype = ctypes.c_int
+        lib.msg_read_device_status.argtypes = [P, P, P]
+        lib.msg_read_device_status.restype = ctypes.c_int
+        lib.msg_clear_device_status.argtypes = [P, P]
+        lib.msg_clear_device_status.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def msg_status_string(status: int) -> str:
+    return load_library().msg_status_string(int(status)).decode()
+
+
+def msg_version() -> int:
+    return int(load_library().msg_version())
+
+
+def _check(fn: str, status: int):
+    if status != MSG_OK:
+        raise MsgError(fn, status, msg_status_string(status))
+
+
+# ------------------------------------------------------------ marshalling
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _row_stride(t, name: str) -> int:
+    """Elements between consecutive rows of a [rows, heads, dim] (or [rows, heads*dim])
+    tensor whose inner part is contiguous."""
+    if t.dim() == 3:
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{name}: heads and dims must be contiguous")
+    elif t.dim() == 2:
+        if t.stride(1) != 1:
+            raise ValueError(f"{name}: inner dim must be contiguous")
+    else:
+        raise ValueError(f"{name}: expected 2 or 3 dims, got {t.dim()}")
+    return int(t.stride(0))
+
+
+def _expect(t, dtype, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+# ------------------------------------------------------------ entry points
+def msg_workspace_size(max_reqs: int, max_total_q: int, num_qo_heads: int = 16,
+                       head_dim: int = 128) -> int:
+    n = int(load_library().msg_workspace_size(int(max_reqs), int(max_total_q),
+                                              int(num_qo_heads), int(head_dim)))
+    if n == 0:
+        raise ValueError("msg_workspace_size: invalid arguments")
+    return n
+
+
+def msg_plan(page_table, cached_len, extend_len, total_q: int, num_slots: int, workspace,
+             req_rows=None, qo_indptr_out=None, out_loc_out=None, positions_out=None,
+             stream=None) -> None:
+    import torch
+    _expect(page_table, torch.int32, "page_table")
+    _expect(cached_len, torch.int32, "cached_len")
+    _expect(extend_len, torch.int32, "extend_len")
+    if page_table.numel() and page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    is64 = 0
+    if out_loc_out is not None:
+        if out_loc_out.dtype not in (torch.int32, torch.int64):
+            raise ValueError("out_loc_out must be int32 or int64")
+        is64 = int(out_loc_out.dtype == torch.int64)
+    st = load_library().msg_plan(
+        _ptr(page_table), int(page_table.stride(0)), _ptr(req_rows), _ptr(cached_len),
+        _ptr(extend_len), int(cached_len.numel()), int(total_q), int(num_slots),
+        _ptr(qo_indptr_out), _ptr(out_loc_out), is64, _ptr(positions_out), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check("msg_plan", st)
+
+
+def msg_store_kv(k, v, k_pool, v_pool, out_loc, dev_status=None, stream=None) -> None:
+    import torch
+    for t, n in ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _expect(t, torch.bfloat16, n)
+    if out_loc.dtype not in (torch.int32, torch.int64):
+        raise ValueError("out_loc must be int32 or int64")
+    if k.shape != v.shape or k_pool.shape != v_pool.shape:
+        raise ValueError("k/v and k_pool/v_pool shapes must match")
+    hkv, d = (k.shape[1], k.shape[2]) if k.dim() == 3 else (1, k.shape[1])
+    kst, vst = _row_stride(k, "k"), _row_stride(v, "v")
+    pst, pvst = _row_stride(k_pool, "k_pool"), _row_stride(v_pool, "v_pool")
+    if kst != vst or pst != pvst:
+        raise ValueError("k and v (and the two pools) must share a row stride")
+    st = load_library().msg_store_kv(
+        _ptr(k), _ptr(v), kst, _ptr(k_pool), _ptr(v_pool), pst, int(k_pool.shape[0]),
+        _ptr(out_loc), int(out_loc.dtype == torch.int64), int(k.shape[0]), int(hkv), int(d),
+        _ptr(dev_status), _stream(stream))
+    _check("msg_store_kv", st)
+
+
+def msg_paged_attention(q, k_pool, v_pool, page_table, cached_len, extend_len, qo_indptr, out,
+                        workspace, page_size: int = 1, scale: float | None = None,
+                        req_rows=None, max_kv_len: int = 0, flags: int = 0, stream=None) -> None:
+    import torch
+    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (out, "out")):
+        _expect(t, torch.bfloat16, n)
+    _expect(page_table, torch.int32, "page_table")
+    if q.dim() != 3 or k_pool.dim() != 3:
+        raise ValueError("q is [total_q, Hq, D] and the pools are [slots, Hkv, D]")
+    if not out.is_contiguous() or out.shape != q.shape:
+        raise ValueError("out must be contiguous with q's shape")
+    if page_table.numel() and page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    hq, d = int(q.shape[1]), int(q.shape[2])
+    hkv = int(k_pool.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pst = _row_stride(k_pool, "k_pool")
+    if _row_stride(v_pool, "v_pool") != pst:
+        raise ValueError("k_pool and v_pool must share a row stride")
+    st = load_library().msg_paged_attention(
+        _ptr(q), _row_stride(q, "q"), _ptr(k_pool), _ptr(v_pool), pst, int(k_pool.shape[0]),
+        _ptr(page_table), int(page_table.stride(0)), _ptr(req_rows), _ptr(cached_len),
+        _ptr(extend_len), _ptr(qo_indptr), int(cached_len.numel()), int(q.shape[0]),
+        int(max_kv_len), int(page_size), hq, hkv, d, float(scale), _ptr(out), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream))
+    _check("msg_paged_attention", st)
+
+
+def msg_read_device_status(dev_status, stream=None) -> tuple[int, list[int]]:
+    """Synchronise and read a status block; returns (status, [code, req, lo, hi])."""
+    buf = (ctypes.c_int32 * 4)()
+    st = load_library().msg_read_device_status(_ptr(dev_status), ctypes.addressof(buf),
+                                               _stream(stream))
+    if st not in (MSG_OK, MSG_ERR_DEVICE_CHECK):
+        _check("msg_read_device_status", st)
+    return st, list(buf)
+
+
+def msg_clear_device_status(dev_status, stream=None) -> None:
+    _check("msg_clear_device_status",
+           load_library().msg_clear_device_status(_ptr(dev_status), _stream(stream)))
+
+
+__all__ = [n for n in dir() if n.startswith(("msg_", "MSG_"))] + [
+    "MsgError", "load_library", "header_functions", "LIB_PATH"]

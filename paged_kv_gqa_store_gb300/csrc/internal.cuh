@@ -1,0 +1,294 @@
+// internal.cuh -- shared definitions of the sm_103a kernels behind msg.h:
+// workspace layout, kernel parameter blocks and small device helpers
+// (bf16 unpacking, mbarrier / bulk-copy PTX, the device status block).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/msg.h"
+
+namespace msg {
+
+constexpr int kHeadDim = 128;
+constexpr int kGroup = 2;                 // query heads per KV head
+constexpr int kMaxDecodeCtas = 512;       // partial-result slots are 2 per CTA
+constexpr int kExtendTileTokens = 64;     // query tokens per extend tile
+constexpr int kPlanThreads = 1024;
+
+// Bound of every mbarrier wait (2 s, far beyond any legitimate wait); on expiry
+// the kernel records MSG_DEV_TIMEOUT and unwinds instead of hanging the GPU.
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout.  Per-request arrays come first and depend only on the
+// batch size (num_reqs, total_q), so msg_plan and msg_paged_attention agree on
+// them; the split-KV partials (which depend on the head count) follow.
+struct WsLayout {
+  size_t status = 0;       // int32[4]
+  size_t header = 0;       // PlanHeader
+  size_t qo_indptr = 0;    // int32[num_reqs + 1]   (plan's own, checked copy)
+  size_t dec_req = 0;      // int32[num_reqs]       decode request list
+  size_t dec_start = 0;    // int64[num_reqs + 1]   prefix of decode kv lengths
+  size_t counters = 0;     // int32[num_reqs]       split merge counters
+  size_t ext_tiles = 0;    // int32x2[max_tiles]    (request, query tile)
+  size_t part_lse = 0;     // float[2 * kMaxDecodeCtas * Hq]
+  size_t part_o = 0;       // float[2 * kMaxDecodeCtas * Hq * D]
+  size_t plan_end = 0;     // bytes used by the plan part
+  size_t total = 0;
+  int64_t max_tiles = 0;
+};
+
+struct PlanHeader {
+  int32_t num_reqs;        // requests planned
+  int32_t dec_count;       // decode requests
+  int32_t ext_tile_count;  // extend tiles
+  int32_t ext_count;       // extend requests
+  int64_t dec_keys;        // sum of decode kv lengths
+  int64_t total_q;         // sum of extend lengths
+};
+
+inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t d) {
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+  L.status = take(MSG_STATUS_BYTES);
+  L.header = take(sizeof(PlanHeader));
+  L.qo_indptr = take(sizeof(int32_t) * (num_reqs + 1));
+  L.dec_req = take(sizeof(int32_t) * (num_reqs + 1));
+  L.dec_start = take(sizeof(int64_t) * (num_reqs + 1));
+  L.counters = take(sizeof(int32_t) * (num_reqs + 1));
+  L.max_tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + num_reqs + 1;
+  L.ext_tiles = take(sizeof(int32_t) * 2 * L.max_tiles);
+  L.plan_end = off;
+  L.part_lse = take(sizeof(float) * 2 * kMaxDecodeCtas * hq);
+  L.part_o = take(sizeof(float) * 2 * (size_t)kMaxDecodeCtas * hq * d);
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------ params
+struct PlanParams {
+  const int32_t *req_rows;      // may be null
+  const int32_t *cached_len;
+  const int32_t *extend_len;
+  const int32_t *qo_in;         // caller's qo_indptr to check, or null
+  int32_t num_reqs;
+  int64_t total_q;
+  int64_t pt_stride;
+  int32_t *status;
+  PlanHeader *hdr;
+  int32_t *qo_ws;               // plan's qo_indptr
+  int32_t *qo_out;              // optional user copy
+  int32_t *dec_req;
+  int64_t *dec_start;
+  int32_t *counters;
+  int32_t *ext_tiles;           // pairs
+  int64_t max_tiles;
+};
+
+struct TokenMetaParams {
+  const int32_t *page_table;
+  int64_t pt_stride;
+  const int32_t *req_rows;
+  const int32_t *cached_len;
+  const int32_t *qo_ws;
+  int32_t num_reqs;
+  int64_t total_q;
+  int64_t num_slots;
+  void *out_loc;
+  int32_t out_loc_is_int64;
+  int32_t *positions;
+  int32_t *status;
+};
+
+struct StoreParams {
+  const uint8_t *k;
+  const uint8_t *v;
+  int64_t in_stride_bytes;
+  uint8_t *k_pool;
+  uint8_t *v_pool;
+  int64_t pool_stride_bytes;
+  int64_t num_slots;
+  const void *out_loc;
+  int32_t out_loc_is_int64;
+  int64_t num_tokens;
+  int32_t row_chunks;           // 16-byte chunks per row
+  int32_t *status;
+};
+
+struct AttnParams {
+  const uint16_t *q;
+  int64_t q_stride;             // elements between tokens
+  const uint8_t *k_pool;
+  const uint8_t *v_pool;
+  int64_t pool_stride_bytes;
+  int64_t num_slots;
+  const int32_t *page_table;
+  int64_t pt_stride;
+  const int32_t *req_rows;
+  const int32_t *cached_len;
+  const int32_t *extend_len;
+  const int32_t *qo_indptr;
+  int32_t num_reqs;
+  int64_t total_q;
+  uint32_t flags;
+  int32_t page_size;
+  int32_t page_shift;           // log2(page_size)
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  float scale_log2;             // scale * log2(e)
+  uint16_t *out;
+  int32_t *status;
+  const PlanHeader *hdr;
+  const int32_t *dec_req;
+  const int64_t *dec_start;
+  int32_t *counters;
+  const int32_t *ext_tiles;
+  float *part_lse;
+  float *part_o;
+};
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
+cudaError_t launch_token_meta(const TokenMetaParams &p, cudaStream_t s);
+cudaError_t launch_store_kv(const StoreParams &p, cudaStream_t s);
+cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s);
+int device_sm_count();
+
+}  // namespace msg
+
+// ------------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+namespace msg {
+
+// Record the first device error: code, request index, value (lo/hi words).
+__device__ __forceinline__ void report(int32_t *status, int32_t code, int32_t idx,
+                                       int64_t val) {
+  if (status == nullptr) return;
+  if (atomicCAS(status, 0, code) == 0) {
+    status[1] = idx;
+    status[2] = (int32_t)(uint32_t)((uint64_t)val & 0xffffffffu);
+    status[3] = (int32_t)(uint32_t)((uint64_t)val >> 32);
+  }
+}
+
+// Two bf16 in a 32-bit word -> two floats (exact: bf16 is the high half of fp32).
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two floats -> packed bf16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier (shared::cta)
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase with the given parity to complete: gives up after
+// kWaitNs of wall-clock time (far beyond any legitimate wait) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_ns() - t0 > kWaitNs) return false;
+  }
+}
+
+// ---- bulk global -> shared copy completing on an mbarrier (TMA, non-tensor)
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- Ampere-style 16-byte async copy (used by the extend kernel)
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Named barrier over a subset of warps (id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Slot of token j of a page-table row: one entry per page (the page's first
+// token) plus the offset inside the page.  Invalid slots are reported and
+// replaced by slot 0 so that no access leaves the pool.
+__device__ __forceinline__ int64_t page_slot(const int32_t *row_ptr, int64_t j, int32_t page_size,
+                                             int32_t page_shift, int64_t num_slots,
+                                             int32_t *status, int32_t req) {
+  if (page_size == 1) {
+    int64_t s = __ldg(row_ptr + j);
+    if (s < 0 || s >= num_slots) {
+      report(status, MSG_DEV_SLOT_OUT_OF_RANGE, req, s);
+      return 0;
+    }
+    return s;
+  }
+  int64_t off = j & (page_size - 1);
+  int64_t first = __ldg(row_ptr + (j - off));
+  if (first < 0 || first + page_size > num_slots) {
+    report(status, MSG_DEV_SLOT_OUT_OF_RANGE, req, first);
+    return 0;
+  }
+  if (first & (page_size - 1)) {
+    report(status, MSG_DEV_PAGE_MISALIGNED, req, first);
+    return 0;
+  }
+  return first + off;
+}
+
+}  // namespace msg
+#endif

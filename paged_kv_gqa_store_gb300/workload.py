@@ -203,3 +203,86 @@ def host_tensors(spec: BatchSpec, layer: int = 0) -> dict:
     k_pool[slots] = random_bf16(rng, (slots.shape[0], Hk, D))
     v_pool[slots] = random_bf16(rng, (slots.shape[0], Hk, D))
     return {"q": q, "k_new": k_new, "v_new": v_new, "k_pool": k_pool, "v_pool": v_pool}
+
+
+# ---------------------------------------------------------------- device side
+def bits_to_torch(bits: np.ndarray, device=None):
+    """uint16 bf16 bits -> torch.bfloat16 tensor (optionally moved to device)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device) if device is not None else t
+
+
+def torch_to_bits(t) -> np.ndarray:
+    """torch.bfloat16 tensor -> uint16 numpy bits (copied to host)."""
+    import torch
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def device_tensors(spec: BatchSpec, layer: int = 0, device="cuda", pools=True,
+                   chunk_rows: int = 1 << 16) -> dict:
+    """Inputs for one layer generated directly on the GPU (large configs): q and
+    the new k/v as N(0,1) bf16, and (if pools) K/V pools filled with the canary
+    except the cached prefixes, which get N(0,1) bf16 rows.  Values come from
+    torch's CUDA generator seeded by (seed, layer); nothing of the method runs."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(spec.seed) * 1009 + layer)
+    T, H, Hk, D = spec.total_q, spec.num_qo_heads, spec.num_kv_heads, spec.head_dim
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(
+            torch.bfloat16)
+
+    out = {"q": randn(T, H, D), "k_new": randn(T, Hk, D), "v_new": randn(T, Hk, D)}
+    if pools:
+        canary = torch.tensor([CANARY_BF16], dtype=torch.int32).to(torch.int16).view(
+            torch.bfloat16).item()
+        kp = torch.full((spec.num_slots, Hk, D), canary, dtype=torch.bfloat16, device=device)
+        vp = torch.full((spec.num_slots, Hk, D), canary, dtype=torch.bfloat16, device=device)
+        slots = torch.from_numpy(prefix_slots(spec)).to(device)
+        for i in range(0, slots.numel(), chunk_rows):
+            idx = slots[i:i + chunk_rows]
+            kp.index_copy_(0, idx, randn(idx.numel(), Hk, D))
+            vp.index_copy_(0, idx, randn(idx.numel(), Hk, D))
+        out["k_pool"], out["v_pool"] = kp, vp
+    return out
+
+
+def compact_requests(spec: BatchSpec, reqs) -> tuple[BatchSpec, np.ndarray]:
+    """Relabel the pages of a subset of requests into a small dense pool.
+
+    Returns (sub_spec, src_slots): sub_spec holds the chosen requests (in the
+    given order) with a page table that points into a pool of
+    len(src_slots) slots, whose slot i holds what src_slots[i] holds in the full
+    pool.  Pages keep their size and alignment, so page geometry is preserved;
+    only the labels change.
+    """
+    reqs = np.asarray(reqs, dtype=np.int64)
+    P = spec.page_size
+    dev = spec.device_len
+    width = align_up(max(int(dev[reqs].max()), 1), 32)
+    table = np.zeros((len(reqs), width), np.int32)
+    page_ids: dict[int, int] = {}
+    src_pages = []
+    for n, r in enumerate(reqs):
+        L = int(dev[r])
+        row = spec.page_table[spec.req_rows[r], :L].astype(np.int64)
+        first = row[::P] if P > 1 else row
+        for pg in (first // P):
+            pg = int(pg)
+            if pg not in page_ids:
+                page_ids[pg] = len(src_pages)
+                src_pages.append(pg)
+        j = np.arange(L)
+        new_pages = np.array([page_ids[int(x)] for x in (row[j - j % P] // P)], np.int64)
+        table[n, :L] = (new_pages * P + j % P).astype(np.int32)
+    src_pages = np.asarray(src_pages, np.int64)
+    src_slots = (src_pages[:, None] * P + np.arange(P)[None, :]).reshape(-1)
+    sub = BatchSpec(name=spec.name + "_sub", cached_len=spec.cached_len[reqs].copy(),
+                    extend_len=spec.extend_len[reqs].copy(),
+                    req_rows=np.arange(len(reqs), dtype=np.int32), page_table=table,
+                    page_size=P, num_slots=int(src_slots.shape[0]), seed=spec.seed,
+                    num_qo_heads=spec.num_qo_heads, num_kv_heads=spec.num_kv_heads,
+                    head_dim=spec.head_dim)
+    return sub, src_slots

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI, no GPU needed: the library builds for sm_103a,
+loads, exports every entry point include/msg.h declares, and rejects bad
+arguments with the documented status before touching the device."""
+import ctypes
+import subprocess
+
+import pytest
+
+import paged_kv_gqa_store_gb300 as msg
+from paged_kv_gqa_store_gb300 import build as msg_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    msg_build.build()
+    return msg.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = msg.header_functions()
+    for want in ("msg_plan", "msg_store_kv", "msg_paged_attention", "msg_workspace_size",
+                 "msg_read_device_status", "msg_clear_device_status", "msg_status_string",
+                 "msg_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", msg.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in msg.header_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings_and_version(lib):
+    assert msg.msg_status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5, -6):
+        assert msg.msg_status_string(code) != "unknown status"
+    assert msg.msg_version() >= 100
+
+
+def test_workspace_size_monotone(lib):
+    a = msg.msg_workspace_size(64, 64)
+    b = msg.msg_workspace_size(256, 18432)
+    assert 0 < a < b
+    assert lib.msg_workspace_size(-1, 0, 16, 128) == 0
+
+
+FAKE = 1 << 20          # a 16-byte-aligned fake device address, never dereferenced
+
+
+def _attn(lib, **kw):
+    a = dict(q=FAKE, q_row_stride=2048, k_pool=FAKE, v_pool=FAKE, pool_row_stride=1024,
+             num_slots=100, page_table=FAKE, page_table_stride=32, req_rows=None,
+             cached_len=FAKE, extend_len=FAKE, qo_indptr=FAKE, num_reqs=2, total_q=2,
+             max_kv_len=0, page_size=1, num_qo_heads=16, num_kv_heads=8, head_dim=128,
+             scale=0.088, out=FAKE, workspace=FAKE, workspace_bytes=1 << 30, flags=0,
+             stream=None)
+    a.update(kw)
+    return lib.msg_paged_attention(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=24), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=6, num_kv_heads=3), msg.MSG_ERR_UNSUPPORTED),
+    (dict(page_size=3), msg.MSG_ERR_UNSUPPORTED),
+    (dict(page_size=256), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_reqs=-1), msg.MSG_ERR_INVALID_ARG),
+    (dict(scale=0.0), msg.MSG_ERR_INVALID_ARG),
+    (dict(flags=msg.MSG_ATTN_DECODE_ONLY | msg.MSG_ATTN_EXTEND_ONLY), msg.MSG_ERR_INVALID_ARG),
+    (dict(flags=64), msg.MSG_ERR_INVALID_ARG),
+    (dict(q=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(q_row_stride=100), msg.MSG_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), msg.MSG_ERR_ALIGNMENT),
+    (dict(pool_row_stride=1028), msg.MSG_ERR_ALIGNMENT),
+    (dict(workspace=None), msg.MSG_ERR_WORKSPACE),
+    (dict(workspace_bytes=1024), msg.MSG_ERR_WORKSPACE),
+    (dict(num_reqs=0), msg.MSG_OK),
+    (dict(total_q=0), msg.MSG_OK),
+])
+def test_attention_argument_validation(lib, kw, status):
+    assert _attn(lib, **kw) == status
+
+
+def _store(lib, **kw):
+    a = dict(k=FAKE, v=FAKE, kv_row_stride=1024, k_pool=FAKE, v_pool=FAKE,
+             pool_row_stride=1024, num_slots=10, out_loc=FAKE, is64=0, num_tokens=3,
+             num_kv_heads=8, head_dim=128, dev_status=None, stream=None)
+    a.update(kw)
+    return lib.msg_store_kv(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_tokens=0), msg.MSG_OK),
+    (dict(num_tokens=-1), msg.MSG_ERR_INVALID_ARG),
+    (dict(k=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(kv_row_stride=512), msg.MSG_ERR_INVALID_ARG),
+    (dict(k=FAKE + 2), msg.MSG_ERR_ALIGNMENT),
+    (dict(pool_row_stride=1030), msg.MSG_ERR_ALIGNMENT),
+    (dict(num_kv_heads=1, head_dim=4, kv_row_stride=8, pool_row_stride=8), msg.MSG_ERR_UNSUPPORTED),
+])
+def test_store_argument_validation(lib, kw, status):
+    assert _store(lib, **kw) == status
+
+
+def test_plan_argument_validation(lib):
+    P = FAKE
+    assert lib.msg_plan(P, 32, None, P, P, -1, 0, 10, None, None, 0, None, P, 1 << 20, None) \
+        == msg.MSG_ERR_INVALID_ARG
+    assert lib.msg_plan(P, 32, None, P, P, 4, 4, 10, None, None, 0, None, None, 1 << 20, None) \
+        == msg.MSG_ERR_WORKSPACE
+    assert lib.msg_plan(P, 32, None, P, P, 4, 4, 10, None, None, 0, None, P, 16, None) \
+        == msg.MSG_ERR_WORKSPACE
