@@ -212,6 +212,50 @@ int msg_read_device_status(const void *dev_status, int32_t *host_out, void *stre
 /* Zero a device status block (asynchronously, on `stream`). */
 int msg_clear_device_status(void *dev_status, void *stream);
 
+/*
+ * Paged attention without a caller-allocated workspace.  (No counterpart on
+ * the pages: this is a convenience of this library.)
+ *
+ * Identical to msg_paged_attention, except that its scratch (plan, split-KV
+ * partial results, merge counters, status block) lives in one fixed array of
+ * MSG_NOALLOC_SCRATCH_BYTES inside the library rather than in a workspace the
+ * caller allocates.  It exists for callers that cannot allocate device memory:
+ * code running under a framework whose allocator owns all device memory and
+ * forbids raw cudaMalloc, C or plugin callers with no device allocator at hand,
+ * and latency-critical loops that cannot pay for cudaMalloc / cudaFree (which
+ * may synchronise the device).  The caller still passes its inputs and outputs.
+ *
+ * - The array is a file-scope device object: every GPU that loads the library
+ *   holds MSG_NOALLOC_SCRATCH_BYTES until the process exits.  That fits every
+ *   batch of up to 1024 requests and 65536 new tokens at 16 query heads of
+ *   head_dim 128; a batch whose msg_workspace_size(...) exceeds it is rejected
+ *   with MSG_ERR_WORKSPACE before anything is enqueued.
+ * - The first call on a device looks up the array's device address (with that
+ *   device current) and caches it; make that first call before any stream
+ *   capture.
+ * - Every call shares the one array and it keeps the last call's contents: the
+ *   status block is cleared at the start of each call, and MSG_ATTN_REUSE_PLAN
+ *   reuses the plan left by the previous call of this entry point.  Calls that
+ *   overlap on the GPU (different streams, or unordered threads) race on the
+ *   array and must not be issued.
+ * - dev_status: optional MSG_STATUS_BYTES device block that receives this
+ *   call's device status (copied at the end of the call), or NULL.
+ * - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ * Errors: as msg_paged_attention.
+ */
+#define MSG_NOALLOC_SCRATCH_BYTES (9u << 20)
+
+int msg_paged_attention_noalloc(const void *q, int64_t q_row_stride, const void *k_pool,
+                                const void *v_pool, int64_t pool_row_stride,
+                                int64_t num_slots, const int32_t *page_table,
+                                int64_t page_table_stride, const int32_t *req_rows,
+                                const int32_t *cached_len, const int32_t *extend_len,
+                                const int32_t *qo_indptr, int32_t num_reqs,
+                                int64_t total_q, int32_t max_kv_len, int32_t page_size,
+                                int32_t num_qo_heads, int32_t num_kv_heads,
+                                int32_t head_dim, float scale, void *out, uint32_t flags,
+                                int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

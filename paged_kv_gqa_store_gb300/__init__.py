@@ -254,3 +254,34 @@ def msg_clear_device_status(dev_status, stream=None) -> None:
 
 __all__ = [n for n in dir() if n.startswith(("msg_", "MSG_"))] + [
     "MsgError", "load_library", "header_functions", "LIB_PATH"]
+
+
+def msg_paged_attention_noalloc(q, k_pool, v_pool, page_table, cached_len, extend_len,
+                                qo_indptr, out, page_size: int = 1, scale: float | None = None,
+                                req_rows=None, max_kv_len: int = 0, flags: int = 0,
+                                dev_status=None, stream=None) -> None:
+    """msg_paged_attention with the library's fixed scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    import torch
+    lib = load_library()
+    fn = lib.msg_paged_attention_noalloc
+    if not getattr(fn, "_msg_declared", False):
+        P, I32, I64, U32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+        fn.argtypes = [P, I64, P, P, I64, I64, P, I64, P, P, P, P, I32, I64, I32, I32, I32, I32,
+                       I32, ctypes.c_float, P, U32, P, P]
+        fn.restype = ctypes.c_int
+        fn._msg_declared = True
+    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (out, "out")):
+        _expect(t, torch.bfloat16, n)
+    _expect(page_table, torch.int32, "page_table")
+    if not out.is_contiguous() or out.shape != q.shape:
+        raise ValueError("out must be contiguous with q's shape")
+    d = int(q.shape[2])
+    pst = _row_stride(k_pool, "k_pool")
+    st = fn(_ptr(q), _row_stride(q, "q"), _ptr(k_pool), _ptr(v_pool), pst, int(k_pool.shape[0]),
+            _ptr(page_table), int(page_table.stride(0)), _ptr(req_rows), _ptr(cached_len),
+            _ptr(extend_len), _ptr(qo_indptr), int(cached_len.numel()), int(q.shape[0]),
+            int(max_kv_len), int(page_size), int(q.shape[1]), int(k_pool.shape[1]), d,
+            float(1.0 / math.sqrt(d) if scale is None else scale), _ptr(out), int(flags),
+            _ptr(dev_status), _stream(stream))
+    _check("msg_paged_attention_noalloc", st)
