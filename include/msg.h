@@ -23,9 +23,10 @@
  *   and owns every buffer (inputs, outputs, workspace).  The library allocates
  *   no device memory, never synchronises the stream, and enqueues all work on
  *   `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
- * - bf16 tensors are raw bf16 bit patterns.  head_dim must be 128, num_qo_heads
- *   = 2 * num_kv_heads (the Qwen3 GQA group of 2) and num_kv_heads one of 1, 2,
- *   4, 8; other shapes return MSG_ERR_UNSUPPORTED.
+ * - bf16 tensors are raw bf16 bit patterns.  Attention shapes are the Qwen3
+ *   ones: head_dim 128, 16 query heads over 8 KV heads (GQA group of 2); other
+ *   shapes return MSG_ERR_UNSUPPORTED.  store_kv accepts any row of
+ *   num_kv_heads * head_dim bf16 values that is a multiple of 16 bytes.
  * - Pool layout ([WALK] 4.4.3): one K pool and one V pool per layer, each a
  *   [num_slots, num_kv_heads, head_dim] bf16 array whose consecutive slots are
  *   pool_row_stride elements apart.  slot = page * page_size + offset.

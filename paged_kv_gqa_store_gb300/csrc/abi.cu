@@ -33,9 +33,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_heads(int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim) {
   if (num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return MSG_ERR_INVALID_ARG;
   if (head_dim != kHeadDim) return MSG_ERR_UNSUPPORTED;
-  if (num_qo_heads != kGroup * num_kv_heads) return MSG_ERR_UNSUPPORTED;
-  if (num_kv_heads != 1 && num_kv_heads != 2 && num_kv_heads != 4 && num_kv_heads != 8)
-    return MSG_ERR_UNSUPPORTED;
+  if (num_kv_heads != kKvHeads || num_qo_heads != kGroup * kKvHeads) return MSG_ERR_UNSUPPORTED;
   return MSG_OK;
 }
 
@@ -49,8 +47,8 @@ const char *msg_status_string(int status) {
   switch (status) {
     case MSG_OK: return "ok";
     case MSG_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad stride)";
-    case MSG_ERR_UNSUPPORTED: return "unsupported shape (needs head_dim 128, 2 query heads per KV head, "
-                                     "1/2/4/8 KV heads, page_size a power of two <= 128)";
+    case MSG_ERR_UNSUPPORTED: return "unsupported shape (needs head_dim 128, 16 query heads over 8 KV "
+                                     "heads, page_size a power of two <= 128)";
     case MSG_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
     case MSG_ERR_WORKSPACE: return "workspace missing or smaller than msg_workspace_size()";
     case MSG_ERR_CUDA: return "CUDA runtime error (launch or copy failed)";
@@ -241,7 +239,7 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
   ap.part_o = reinterpret_cast<float *>(ws + L.part_o);
 
   if (!(flags & MSG_ATTN_EXTEND_ONLY)) {
-    int64_t grid = device_sm_count();
+    int64_t grid = (int64_t)device_sm_count() * decode_ctas_per_sm();
     if (grid > kMaxDecodeCtas) grid = kMaxDecodeCtas;
     if (max_kv_len > 0) {
       const int64_t want = ((int64_t)num_reqs * max_kv_len + 63) / 64;

@@ -7,26 +7,31 @@
 //   o[h] = sum_j exp(s_j - m) V_j[h/2] / sum_j exp(s_j - m),  s_j = scale * q[h].K_j[h/2].
 // K_j / V_j are gathered through the page table ("Mini-SGLang 完整剖析" 4.6.4).
 //
-// GB300 design (bandwidth bound, ~1 flop per byte):
+// GB300 design (bandwidth bound, ~1 flop per byte; 16 query / 8 KV heads):
 // - Work split.  The decode requests' keys are laid end to end (prefix sum from
-//   the plan) and cut into gridDim.x equal ranges, one per persistent CTA (one
-//   CTA per SM).  A CTA walks the requests its range touches; a request cut by
-//   a range boundary yields per-CTA partials (normalised o and lse) that the
-//   last CTA to finish that request merges (atomic counter + fence, no CTA
-//   ever waits on another).  This balances any length mix to within one tile.
-// - Data movement.  One producer warp gathers whole token rows (all KV heads,
-//   kv_heads * 256 B) with cp.async.bulk (TMA, non-tensor) into a 3-stage
-//   shared-memory ring guarded by mbarriers (full: transaction bytes; empty:
-//   16 consumer-warp arrivals).  Each 2 KiB row is one contiguous HBM read.
-// - Compute.  16 consumer warps; warp w owns KV head w % Hkv and 8 keys of each
-//   tile, and computes BOTH query heads of the GQA group from each K/V load.
-//   A lane holds 4 of the 128 dims; the 16 partial dot products (8 keys x 2
-//   heads) are reduce-scattered across the warp in 16 shuffles (one score per
-//   lane pair), followed by an fp32 online softmax in base 2 (scale * log2 e
-//   folded into q) and the P.V accumulation.
-// - Waits are bounded: an expired wait records MSG_DEV_TIMEOUT, sets an abort
-//   flag that short-circuits every later wait, and the producer drains its
-//   copies before the CTA exits.
+//   the plan) and cut into equal ranges, one per CTA, two CTAs per SM.  A CTA
+//   walks the requests its range touches.  A request cut by a range boundary
+//   leaves per-CTA partials (normalised o and its log-sum-exp) for each KV
+//   head; the warp that finishes last for (request, KV head) -- an atomic
+//   counter after a fence -- merges them.  No CTA or warp ever waits on another.
+// - Data movement.  One producer warp owns all global reads: it prefetches the
+//   page-table entries one tile ahead, gathers whole token rows (8 KV heads x
+//   256 B = 2 KiB) of K and V with cp.async.bulk (TMA, non-tensor) into a
+//   3-stage shared-memory ring, copies the request's q row with the first tile
+//   of a segment, and writes a small tile header (request, output row, split
+//   slot).  mbarriers guard the ring (full: transaction bytes; empty: one
+//   arrival per consumer warp).
+// - Compute.  8 consumer warps, one per KV head; each computes BOTH query heads
+//   of its GQA group from every K/V row it reads.  A lane holds 4 of the 128
+//   dims; the 16 partial dot products of a tile (8 keys x 2 heads) are
+//   reduce-scattered across the warp in 16 shuffles with no selects (each lane
+//   walks the keys and heads in an XOR-permuted order so that the butterfly
+//   never has to pick halves), then an fp32 online softmax in base 2 (scale *
+//   log2 e folded into q) and the P.V accumulation, with packed f32x2 FMAs.
+// - Waits are bounded by wall-clock time: an expired wait records
+//   MSG_DEV_TIMEOUT, raises an abort flag that ends every loop, and the
+//   producer drains its copies before the CTA exits.  There are no CTA-wide
+//   barriers after set-up.
 #include <math.h>
 
 #include "internal.cuh"
@@ -35,24 +40,28 @@ namespace msg {
 
 namespace {
 
+constexpr int kHkv = 8;
+constexpr int kHq = 16;
+constexpr int kWarps = 8;                           // consumer warps, one per KV head
+constexpr int kThreads = (kWarps + 1) * 32;         // + producer warp
+constexpr int kTileKeys = 8;
+constexpr int kRowBytes = kHkv * kHeadDim * 2;      // 2 KiB: one token's K row
+constexpr int kKBytes = kTileKeys * kRowBytes;      // 16 KiB
+constexpr int kQBytes = kHq * kHeadDim * 2;         // 4 KiB: one q row
+constexpr int kStages = 3;
+constexpr int kOffV = kKBytes;
+constexpr int kOffQ = 2 * kKBytes;
+constexpr int kOffHdr = 2 * kKBytes + kQBytes;
+constexpr int kStageBytes = kOffHdr + 64;
+constexpr int kPbufBytes = kWarps * kTileKeys * 4 * 4;   // per key: {p0,p0,p1,p1}
+constexpr size_t kSmem = (size_t)kStages * kStageBytes + kPbufBytes + 2 * kStages * 8 + 16;
 constexpr int64_t kMinKeysPerCta = 64;
 
-template <int HKV>
-struct Dec {
-  static constexpr int kNsub = 16 / HKV;                   // warps per KV head
-  static constexpr int kConsumerWarps = 16;
-  static constexpr int kConsumerThreads = kConsumerWarps * 32;
-  static constexpr int kThreads = kConsumerThreads + 32;   // + producer warp
-  static constexpr int kTileKeys = 8 * kNsub;              // keys per stage
-  static constexpr int kRowBytes = HKV * kHeadDim * 2;     // one token's K row
-  static constexpr int kStages = 3;
-  static constexpr int kHalfStage = kTileKeys * kRowBytes; // 32 KiB (K or V)
-  static constexpr int kStageBytes = 2 * kHalfStage;
-  static constexpr int kStateFloats = 4 + 2 * kHeadDim;    // m0 m1 l0 l1 o0[128] o1[128]
-  static constexpr int kMergeBytes = kConsumerWarps * kStateFloats * 4;
-  static constexpr int kPbufBytes = kConsumerWarps * 16 * 4;
-  static constexpr size_t kSmem =
-      (size_t)kStages * kStageBytes + kMergeBytes + kPbufBytes + 2 * kStages * 8 + 16;
+enum : int32_t { kFirst = 1, kLast = 2, kFinal = 4, kNoRow = 8 };
+
+struct TileHdr {
+  int32_t nkeys, flags, r, qrow;
+  int32_t part_slot, bf, bl, head_shift;
 };
 
 __device__ __forceinline__ int64_t cta_begin(int64_t b, int64_t K, int64_t g) { return b * K / g; }
@@ -62,16 +71,86 @@ __device__ __forceinline__ int64_t cta_of_key(int64_t s, int64_t K, int64_t g) {
   return b < g - 1 ? b : g - 1;
 }
 
-template <int HKV>
-__global__ void __launch_bounds__(Dec<HKV>::kThreads, 1) decode_kernel(AttnParams p) {
-  using C = Dec<HKV>;
+// ---- packed fp32x2 arithmetic (sm_100+)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
+// One segment: the part of decode request i that lies in this CTA's range.
+struct Seg {
+  int64_t S, E, lo, hi;        // request keys [S, E) and this CTA's part [lo, hi)
+  const int32_t *row;          // page-table row
+  int32_t r, qrow, part_slot, bf, bl, head_shift;
+};
+
+__device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t begin, int64_t end,
+                                        int64_t b, int64_t K, int64_t g) {
+  Seg s;
+  s.S = p.dec_start[i];
+  s.E = p.dec_start[i + 1];
+  s.lo = s.S > begin ? s.S : begin;
+  s.hi = s.E < end ? s.E : end;
+  s.r = p.dec_req[i];
+  const int64_t row = p.req_rows ? p.req_rows[s.r] : s.r;
+  s.row = p.page_table + row * p.pt_stride;
+  const int64_t q = p.qo_indptr[s.r];
+  s.qrow = (q >= 0 && q < p.total_q) ? (int32_t)q : -1;
+  const bool whole = s.S >= begin && s.E <= end;
+  s.part_slot = whole ? -1 : (int32_t)(2 * b + (s.lo == begin ? 0 : 1));
+  s.bf = (int32_t)cta_of_key(s.S, K, g);
+  s.bl = (int32_t)cta_of_key(s.E - 1, K, g);
+  s.head_shift = s.S > cta_begin(s.bf, K, g) ? 1 : 0;
+  return s;
+}
+
+// Raw page-table entry for local key j (page_size 1: the slot; else the page's
+// first slot).  Loaded ahead of use; validated by raw_to_slot.
+__device__ __forceinline__ int32_t load_raw(const AttnParams &p, const int32_t *row, int64_t j) {
+  return __ldg(row + (p.page_size == 1 ? j : (j & ~(int64_t)(p.page_size - 1))));
+}
+__device__ __forceinline__ int64_t raw_to_slot(const AttnParams &p, int32_t raw, int64_t j,
+                                               int32_t r) {
+  const int64_t first = raw;
+  if (p.page_size == 1) {
+    if (first < 0 || first >= p.num_slots) {
+      report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
+      return 0;
+    }
+    return first;
+  }
+  if (first < 0 || first + p.page_size > p.num_slots) {
+    report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
+    return 0;
+  }
+  if (first & (p.page_size - 1)) {
+    report(p.status, MSG_DEV_PAGE_MISALIGNED, r, first);
+    return 0;
+  }
+  return first + (j & (p.page_size - 1));
+}
+
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *stages = smem;
-  float *merge = reinterpret_cast<float *>(smem + (size_t)C::kStages * C::kStageBytes);
-  float *pbuf = merge + C::kMergeBytes / 4;
-  uint64_t *full = reinterpret_cast<uint64_t *>(pbuf + C::kPbufBytes / 4);
-  uint64_t *empty = full + C::kStages;
-  volatile int32_t *flag = reinterpret_cast<volatile int32_t *>(empty + C::kStages);  // [0] abort [1] merge
+  float *pbuf = reinterpret_cast<float *>(smem + (size_t)kStages * kStageBytes);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStageBytes + kPbufBytes);
+  uint64_t *empty = full + kStages;
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(empty + kStages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PlanHeader hdr = *p.hdr;
@@ -88,325 +167,296 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, 1) decode_kernel(AttnParam
   const int64_t begin = cta_begin(b, K, g), end = cta_begin(b + 1, K, g);
 
   if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::kConsumerWarps);
+      mbar_init(&empty[s], kWarps);
     }
-    flag[0] = 0;
-    flag[1] = 0;
+    *abort_flag = 0;
     mbar_fence_init();
   }
   __syncthreads();
 
-  // First decode request whose keys reach this CTA's range.
-  int32_t i0 = 0;
-  {
-    int32_t lo = 0, hi = nd;   // dec_start[lo] <= begin < dec_start[hi]
-    while (hi - lo > 1) {
-      const int32_t mid = (lo + hi) >> 1;
-      if (p.dec_start[mid] <= begin) lo = mid; else hi = mid;
-    }
-    i0 = lo;
-  }
-
-  if (warp == C::kConsumerWarps) {
+  if (warp == kWarps) {
     // ------------------------------------------------------------ producer
+    int32_t i = 0;
+    {
+      int32_t lo = 0, hi = nd;   // dec_start[lo] <= begin < dec_start[hi]
+      while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (p.dec_start[mid] <= begin) lo = mid; else hi = mid;
+      }
+      i = lo;
+    }
+    Seg sg = load_seg(p, i, begin, end, b, K, g);
+    int64_t kt = sg.lo;                        // flattened key index of the tile
+    int32_t raw = 0;
+    {
+      const int64_t n0 = imin64(kTileKeys, sg.hi - kt);
+      if (lane < n0) raw = load_raw(p, sg.row, kt - sg.S + lane);
+    }
     uint32_t it = 0, issued = 0;
     bool ok = true;
-    int64_t pos = begin;
-    for (int32_t i = i0; pos < end; ++i) {
-      const int64_t S = p.dec_start[i], E = p.dec_start[i + 1];
-      const int64_t seg_end = E < end ? E : end;
-      const int32_t r = p.dec_req[i];
-      const int64_t row = p.req_rows ? p.req_rows[r] : r;
-      const int32_t *row_ptr = p.page_table + row * p.pt_stride;
-      for (int64_t kt = pos - S; kt < seg_end - S; kt += C::kTileKeys) {
-        const int nkeys = (int)imin64(C::kTileKeys, seg_end - S - kt);
-        const int st = it % C::kStages;
-        if (ok && it >= (uint32_t)C::kStages &&
-            !mbar_wait(&empty[st], ((it / C::kStages) & 1) ^ 1)) {
-          ok = false;
-          if (lane == 0) {
-            flag[0] = 1;
-            report(p.status, MSG_DEV_TIMEOUT, r, kt);
-          }
+    while (true) {
+      const int nkeys = (int)imin64(kTileKeys, sg.hi - kt);
+      const bool first = (kt == sg.lo);
+      const bool last = (kt + nkeys == sg.hi);
+      const bool fin = last && sg.hi == end;
+      // look one tile ahead: next segment metadata and page-table entries
+      Seg nsg = sg;
+      int64_t nkt = kt + nkeys;
+      int32_t nraw = 0;
+      if (!fin) {
+        if (last) {
+          nsg = load_seg(p, i + 1, begin, end, b, K, g);
+          nkt = nsg.lo;
         }
-        if (flag[0]) ok = false;
-        if (ok) {
-          if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)nkeys * C::kRowBytes * 2);
-          __syncwarp();
-          uint8_t *kdst = stages + (size_t)st * C::kStageBytes;
-          uint8_t *vdst = kdst + C::kHalfStage;
-          for (int l = lane; l < nkeys; l += 32) {
-            const int64_t slot =
-                page_slot(row_ptr, kt + l, p.page_size, p.page_shift, p.num_slots, p.status, r);
-            const int64_t off = slot * p.pool_stride_bytes;
-            bulk_g2s(kdst + l * C::kRowBytes, p.k_pool + off, C::kRowBytes, &full[st]);
-            bulk_g2s(vdst + l * C::kRowBytes, p.v_pool + off, C::kRowBytes, &full[st]);
-          }
-          issued = it + 1;
-        }
-        ++it;
+        const int64_t nn = imin64(kTileKeys, nsg.hi - nkt);
+        if (lane < nn) nraw = load_raw(p, nsg.row, nkt - nsg.S + lane);
       }
-      pos = seg_end;
+      const int st = it % kStages;
+      if (ok && it >= (uint32_t)kStages && !mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1)) {
+        ok = false;
+        if (lane == 0) {
+          *abort_flag = 1;
+          report(p.status, MSG_DEV_TIMEOUT, sg.r, kt);
+        }
+      }
+      if (*abort_flag) ok = false;
+      if (ok) {
+        uint8_t *stage = smem + (size_t)st * kStageBytes;
+        int64_t slot = 0;
+        if (lane < nkeys) slot = raw_to_slot(p, raw, kt - sg.S + lane, sg.r);
+        if (lane == 0) {
+          TileHdr *h = reinterpret_cast<TileHdr *>(stage + kOffHdr);
+          h->nkeys = nkeys;
+          h->flags = (first ? kFirst : 0) | (last ? kLast : 0) | (fin ? kFinal : 0) |
+                     (sg.qrow < 0 ? kNoRow : 0);
+          h->r = sg.r;
+          h->qrow = sg.qrow;
+          h->part_slot = sg.part_slot;
+          h->bf = sg.bf;
+          h->bl = sg.bl;
+          h->head_shift = sg.head_shift;
+          if (first && sg.qrow < 0) report(p.status, MSG_DEV_BAD_LENGTHS, sg.r, p.qo_indptr[sg.r]);
+          mbar_arrive_expect_tx(&full[st], (uint32_t)nkeys * 2 * kRowBytes + (first ? kQBytes : 0));
+        }
+        __syncwarp();
+        if (lane < nkeys) {
+          const int64_t off = slot * p.pool_stride_bytes;
+          bulk_g2s(stage + lane * kRowBytes, p.k_pool + off, kRowBytes, &full[st]);
+          bulk_g2s(stage + kOffV + lane * kRowBytes, p.v_pool + off, kRowBytes, &full[st]);
+        }
+        if (first && lane == 0) {
+          const int64_t qr = sg.qrow < 0 ? 0 : sg.qrow;
+          bulk_g2s(stage + kOffQ, p.q + qr * p.q_stride, kQBytes, &full[st]);
+        }
+        issued = it + 1;
+      }
+      ++it;
+      if (fin || !ok) break;
+      if (last) {
+        sg = nsg;
+        ++i;
+      }
+      kt = nkt;
+      raw = nraw;
     }
     // Drain: the last issued use of every stage must have landed before exit.
-    for (uint32_t j = issued > (uint32_t)C::kStages ? issued - C::kStages : 0; j < issued; ++j)
-      mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1);
+    for (uint32_t j = issued > (uint32_t)kStages ? issued - kStages : 0; j < issued; ++j)
+      mbar_wait(&full[j % kStages], (j / kStages) & 1);
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  const int gh = warp % HKV;            // KV head of this warp
-  const int sub = warp / HKV;           // which 8 keys of each tile
-  const int hq = p.num_qo_heads;
-  float *my_p = pbuf + warp * 16;
-  uint32_t it = 0;
-  int64_t pos = begin;
-  for (int32_t i = i0; pos < end; ++i) {
-    const int64_t S = p.dec_start[i], E = p.dec_start[i + 1];
-    const int64_t seg_end = E < end ? E : end;
-    const int32_t r = p.dec_req[i];
-    const bool whole = (pos == S) && (seg_end == E);
-    const int64_t qrow = p.qo_indptr[r];
-    const bool row_ok = qrow >= 0 && qrow < p.total_q;
-    if (!row_ok && tid == 0) report(p.status, MSG_DEV_BAD_LENGTHS, r, qrow);
+  const int gh = warp;                          // KV head
+  const int kx = (lane >> 2) & 7, hx = (lane >> 1) & 1;
+  const int kl = kx, hl = hx;                   // after the butterfly: this lane's key / head
+  uint32_t koff[kTileKeys];
+#pragma unroll
+  for (int t = 0; t < kTileKeys; ++t)
+    koff[t] = (uint32_t)((t ^ kx) * kRowBytes + gh * (kHeadDim * 2) + lane * 8);
+  const uint32_t voff = (uint32_t)(kOffV + gh * (kHeadDim * 2) + lane * 8);
+  float *my_p = pbuf + warp * kTileKeys * 4;
+  const float sl2 = p.scale_log2;
 
-    float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
-    if (row_ok) {
-      const uint16_t *qp = p.q + qrow * p.q_stride + (2 * gh) * kHeadDim + lane * 4;
-      const uint2 a = *reinterpret_cast<const uint2 *>(qp);
-      const uint2 c = *reinterpret_cast<const uint2 *>(qp + kHeadDim);
-      q0[0] = bf16lo(a.x) * p.scale_log2; q0[1] = bf16hi(a.x) * p.scale_log2;
-      q0[2] = bf16lo(a.y) * p.scale_log2; q0[3] = bf16hi(a.y) * p.scale_log2;
-      q1[0] = bf16lo(c.x) * p.scale_log2; q1[1] = bf16hi(c.x) * p.scale_log2;
-      q1[2] = bf16lo(c.y) * p.scale_log2; q1[3] = bf16hi(c.y) * p.scale_log2;
-    }
-    float m0 = -INFINITY, m1 = -INFINITY, lsum = 0.f;
-    float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 qa01 = make_float2(0.f, 0.f), qa23 = qa01, qb01 = qa01, qb23 = qa01;
+  float m0 = -INFINITY, m1 = -INFINITY, lsum = 0.f;
+  float2 o0a = make_float2(0.f, 0.f), o0b = o0a, o1a = o0a, o1b = o0a;
 
-    for (int64_t kt = pos - S; kt < seg_end - S; kt += C::kTileKeys) {
-      const int nkeys = (int)imin64(C::kTileKeys, seg_end - S - kt);
-      const int st = it % C::kStages;
-      bool ok = !flag[0];
-      if (ok && !mbar_wait(&full[st], (it / C::kStages) & 1)) {
-        ok = false;
-        if (lane == 0) {
-          flag[0] = 1;
-          report(p.status, MSG_DEV_TIMEOUT, r, kt);
-        }
-      }
-      int nk = nkeys - sub * 8;
-      nk = nk < 0 ? 0 : (nk > 8 ? 8 : nk);
-      if (ok && nk > 0) {
-        const uint8_t *kb = stages + (size_t)st * C::kStageBytes + (sub * 8) * C::kRowBytes +
-                            gh * (kHeadDim * 2) + lane * 8;
-        const uint8_t *vb = kb + C::kHalfStage;
-        float s[16];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const uint2 w = *reinterpret_cast<const uint2 *>(kb + t * C::kRowBytes);
-          const float k0 = bf16lo(w.x), k1 = bf16hi(w.x), k2 = bf16lo(w.y), k3 = bf16hi(w.y);
-          s[2 * t] = fmaf(q0[0], k0, fmaf(q0[1], k1, fmaf(q0[2], k2, q0[3] * k3)));
-          s[2 * t + 1] = fmaf(q1[0], k0, fmaf(q1[1], k1, fmaf(q1[2], k2, q1[3] * k3)));
-        }
-        // Reduce-scatter the 16 partial dots: afterwards lane l holds the full
-        // score of key (l >> 2) for head ((l >> 1) & 1).
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const bool up = lane & 16;
-          const float send = up ? s[j] : s[j + 8];
-          const float keep = up ? s[j + 8] : s[j];
-          s[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const bool up = lane & 8;
-          const float send = up ? s[j] : s[j + 4];
-          const float keep = up ? s[j + 4] : s[j];
-          s[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const bool up = lane & 4;
-          const float send = up ? s[j] : s[j + 2];
-          const float keep = up ? s[j + 2] : s[j];
-          s[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        {
-          const bool up = lane & 2;
-          const float send = up ? s[0] : s[1];
-          const float keep = up ? s[1] : s[0];
-          s[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-        s[0] += __shfl_xor_sync(0xffffffffu, s[0], 1);
-
-        const int kl = lane >> 2, hm = (lane >> 1) & 1;
-        const float sc = kl < nk ? s[0] : -INFINITY;
-        float mx = sc;
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mo = __shfl_xor_sync(0xffffffffu, mx, 2);
-        const float mn0 = fmaxf(m0, hm ? mo : mx), mn1 = fmaxf(m1, hm ? mx : mo);
-        const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        const float pr = exp2f(sc - (hm ? mn1 : mn0));
-        lsum = lsum * (hm ? a1 : a0) + pr;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          o0[c] *= a0;
-          o1[c] *= a1;
-        }
-        if (!(lane & 1)) my_p[lane >> 1] = pr;
-        __syncwarp();
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (t < nk) {
-            const float2 pp = *reinterpret_cast<const float2 *>(my_p + 2 * t);
-            const uint2 w = *reinterpret_cast<const uint2 *>(vb + t * C::kRowBytes);
-            const float v[4] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y)};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              o0[c] = fmaf(pp.x, v[c], o0[c]);
-              o1[c] = fmaf(pp.y, v[c], o1[c]);
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      ++it;
-    }
-
-    // ---- end of segment: combine the kNsub warps of each KV head
-    float lv = (lane & 1) ? 0.f : lsum;
-    lv += __shfl_xor_sync(0xffffffffu, lv, 4);
-    lv += __shfl_xor_sync(0xffffffffu, lv, 8);
-    lv += __shfl_xor_sync(0xffffffffu, lv, 16);
-    const float l0 = __shfl_sync(0xffffffffu, lv, 0), l1 = __shfl_sync(0xffffffffu, lv, 2);
-    {
-      float *ms = merge + warp * C::kStateFloats;
+  for (uint32_t it = 0;; ++it) {
+    const int st = it % kStages;
+    const uint8_t *stage = smem + (size_t)st * kStageBytes;
+    if (*abort_flag) break;
+    if (!mbar_wait(&full[st], (it / kStages) & 1)) {
       if (lane == 0) {
-        ms[0] = m0; ms[1] = m1; ms[2] = l0; ms[3] = l1;
+        *abort_flag = 1;
+        report(p.status, MSG_DEV_TIMEOUT, -1, (int64_t)it);
       }
-      *reinterpret_cast<float4 *>(ms + 4 + lane * 4) = make_float4(o0[0], o0[1], o0[2], o0[3]);
-      *reinterpret_cast<float4 *>(ms + 4 + kHeadDim + lane * 4) =
-          make_float4(o1[0], o1[1], o1[2], o1[3]);
+      break;
     }
-    named_barrier(1, C::kConsumerThreads);
-    if (sub == 0) {
-      float M0 = -INFINITY, M1 = -INFINITY;
+    const TileHdr h = *reinterpret_cast<const TileHdr *>(stage + kOffHdr);
+    if (h.flags & kFirst) {
+      const uint2 wa = *reinterpret_cast<const uint2 *>(stage + kOffQ + (2 * gh + hx) * 256 + lane * 8);
+      const uint2 wb =
+          *reinterpret_cast<const uint2 *>(stage + kOffQ + (2 * gh + (hx ^ 1)) * 256 + lane * 8);
+      const float2 sc2 = make_float2(sl2, sl2);
+      qa01 = fmul2(bf2(wa.x), sc2);
+      qa23 = fmul2(bf2(wa.y), sc2);
+      qb01 = fmul2(bf2(wb.x), sc2);
+      qb23 = fmul2(bf2(wb.y), sc2);
+      m0 = m1 = -INFINITY;
+      lsum = 0.f;
+      o0a = o0b = o1a = o1b = make_float2(0.f, 0.f);
+    }
+    const int nk = h.nkeys;
+
+    // ---- scores: slot (t, hh) of this lane holds key t ^ kx, head hh ^ hx
+    float s[16];
 #pragma unroll
-      for (int s = 0; s < C::kNsub; ++s) {
-        const float *ms = merge + (s * HKV + gh) * C::kStateFloats;
-        M0 = fmaxf(M0, ms[0]);
-        M1 = fmaxf(M1, ms[1]);
-      }
-      float L0 = 0.f, L1 = 0.f, O0[4] = {0.f, 0.f, 0.f, 0.f}, O1[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int t = 0; t < kTileKeys; ++t) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(stage + koff[t]);
+      const float2 k01 = bf2(w.x), k23 = bf2(w.y);
+      float2 a = fmul2(k01, qa01);
+      a = ffma2(k23, qa23, a);
+      float2 c = fmul2(k01, qb01);
+      c = ffma2(k23, qb23, c);
+      s[2 * t] = a.x + a.y;
+      s[2 * t + 1] = c.x + c.y;
+    }
 #pragma unroll
-      for (int s = 0; s < C::kNsub; ++s) {
-        const float *ms = merge + (s * HKV + gh) * C::kStateFloats;
-        const float w0 = exp2f(ms[0] - M0), w1 = exp2f(ms[1] - M1);
-        L0 = fmaf(ms[2], w0, L0);
-        L1 = fmaf(ms[3], w1, L1);
-        const float4 x = *reinterpret_cast<const float4 *>(ms + 4 + lane * 4);
-        const float4 y = *reinterpret_cast<const float4 *>(ms + 4 + kHeadDim + lane * 4);
-        O0[0] = fmaf(x.x, w0, O0[0]); O0[1] = fmaf(x.y, w0, O0[1]);
-        O0[2] = fmaf(x.z, w0, O0[2]); O0[3] = fmaf(x.w, w0, O0[3]);
-        O1[0] = fmaf(y.x, w1, O1[0]); O1[1] = fmaf(y.y, w1, O1[1]);
-        O1[2] = fmaf(y.z, w1, O1[2]); O1[3] = fmaf(y.w, w1, O1[3]);
+    for (int j = 0; j < 8; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j + 8], 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j + 4], 8);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) s[j] += __shfl_xor_sync(0xffffffffu, s[j + 2], 4);
+    s[0] += __shfl_xor_sync(0xffffffffu, s[1], 2);
+    s[0] += __shfl_xor_sync(0xffffffffu, s[0], 1);
+
+    // ---- online softmax (lane holds key kl, head hl)
+    const float sc = kl < nk ? s[0] : -INFINITY;
+    float mx = sc;
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mo = __shfl_xor_sync(0xffffffffu, mx, 2);
+    const float mn0 = fmaxf(m0, hl ? mo : mx), mn1 = fmaxf(m1, hl ? mx : mo);
+    const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const float pr = exp2f(sc - (hl ? mn1 : mn0));
+    lsum = lsum * (hl ? a1 : a0) + pr;
+    o0a = fmul2(o0a, make_float2(a0, a0));
+    o0b = fmul2(o0b, make_float2(a0, a0));
+    o1a = fmul2(o1a, make_float2(a1, a1));
+    o1b = fmul2(o1b, make_float2(a1, a1));
+    if (!(lane & 1)) *reinterpret_cast<float2 *>(my_p + kl * 4 + hl * 2) = make_float2(pr, pr);
+    __syncwarp();
+#pragma unroll
+    for (int t = 0; t < kTileKeys; ++t) {
+      if (t < nk) {
+        const float4 pp = *reinterpret_cast<const float4 *>(my_p + t * 4);
+        const uint2 w = *reinterpret_cast<const uint2 *>(stage + voff + t * kRowBytes);
+        const float2 v01 = bf2(w.x), v23 = bf2(w.y);
+        o0a = ffma2(v01, make_float2(pp.x, pp.y), o0a);
+        o0b = ffma2(v23, make_float2(pp.x, pp.y), o0b);
+        o1a = ffma2(v01, make_float2(pp.z, pp.w), o1a);
+        o1b = ffma2(v23, make_float2(pp.z, pp.w), o1b);
       }
-      const float i0f = 1.f / L0, i1f = 1.f / L1;
-      if (whole) {
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+
+    if (h.flags & kLast) {
+      // ---- end of this request's part: normalise and write out or a partial
+      float lv = (lane & 1) ? 0.f : lsum;
+      lv += __shfl_xor_sync(0xffffffffu, lv, 4);
+      lv += __shfl_xor_sync(0xffffffffu, lv, 8);
+      lv += __shfl_xor_sync(0xffffffffu, lv, 16);
+      const float l0 = __shfl_sync(0xffffffffu, lv, 0), l1 = __shfl_sync(0xffffffffu, lv, 2);
+      const float i0f = 1.f / l0, i1f = 1.f / l1;
+      const bool row_ok = !(h.flags & kNoRow);
+      uint16_t *op = p.out + (int64_t)h.qrow * kHq * kHeadDim + (2 * gh) * kHeadDim + lane * 4;
+      if (h.part_slot < 0) {
         if (row_ok) {
-          uint16_t *op = p.out + qrow * (int64_t)hq * kHeadDim + (2 * gh) * kHeadDim + lane * 4;
-          *reinterpret_cast<uint2 *>(op) =
-              make_uint2(pack_bf16(O0[0] * i0f, O0[1] * i0f), pack_bf16(O0[2] * i0f, O0[3] * i0f));
-          *reinterpret_cast<uint2 *>(op + kHeadDim) =
-              make_uint2(pack_bf16(O1[0] * i1f, O1[1] * i1f), pack_bf16(O1[2] * i1f, O1[3] * i1f));
+          *reinterpret_cast<uint2 *>(op) = make_uint2(pack_bf16(o0a.x * i0f, o0a.y * i0f),
+                                                      pack_bf16(o0b.x * i0f, o0b.y * i0f));
+          *reinterpret_cast<uint2 *>(op + kHeadDim) = make_uint2(
+              pack_bf16(o1a.x * i1f, o1a.y * i1f), pack_bf16(o1b.x * i1f, o1b.y * i1f));
         }
       } else {
-        const int64_t slot = 2 * b + (pos == begin ? 0 : 1);
-        float *po = p.part_o + (slot * hq + 2 * gh) * kHeadDim + lane * 4;
-        *reinterpret_cast<float4 *>(po) = make_float4(O0[0] * i0f, O0[1] * i0f, O0[2] * i0f, O0[3] * i0f);
+        const int64_t slot = h.part_slot;
+        float *po = p.part_o + (slot * kHq + 2 * gh) * kHeadDim + lane * 4;
+        *reinterpret_cast<float4 *>(po) =
+            make_float4(o0a.x * i0f, o0a.y * i0f, o0b.x * i0f, o0b.y * i0f);
         *reinterpret_cast<float4 *>(po + kHeadDim) =
-            make_float4(O1[0] * i1f, O1[1] * i1f, O1[2] * i1f, O1[3] * i1f);
+            make_float4(o1a.x * i1f, o1a.y * i1f, o1b.x * i1f, o1b.y * i1f);
         if (lane == 0) {
-          p.part_lse[slot * hq + 2 * gh] = M0 + log2f(L0);
-          p.part_lse[slot * hq + 2 * gh + 1] = M1 + log2f(L1);
+          p.part_lse[slot * kHq + 2 * gh] = m0 + log2f(l0);
+          p.part_lse[slot * kHq + 2 * gh + 1] = m1 + log2f(l1);
         }
-      }
-    }
-    if (!whole) {
-      __threadfence();
-      named_barrier(1, C::kConsumerThreads);
-      if (tid == 0) {
-        const int64_t nsplit = cta_of_key(E - 1, K, g) - cta_of_key(S, K, g) + 1;
-        const int old = atomicAdd(&p.counters[r], 1);
-        flag[1] = (old == nsplit - 1) ? 1 : 0;
-      }
-      named_barrier(1, C::kConsumerThreads);
-      if (flag[1]) {
         __threadfence();
-        const int64_t bf = cta_of_key(S, K, g), bl = cta_of_key(E - 1, K, g);
-        const int64_t head_shift = (S > cta_begin(bf, K, g)) ? 1 : 0;
-        for (int idx = tid; idx < hq * kHeadDim; idx += C::kConsumerThreads) {
-          const int h = idx / kHeadDim, d = idx % kHeadDim;
-          float L = -INFINITY;
-          for (int64_t bb = bf; bb <= bl; ++bb) {
-            const int64_t slot = 2 * bb + (bb == bf ? head_shift : 0);
-            L = fmaxf(L, __ldcg(p.part_lse + slot * hq + h));
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(&p.counters[(int64_t)h.r * kHkv + gh], 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == h.bl - h.bf) {
+          // last of the (request, KV head) splits: merge them
+          __threadfence();
+          float L0 = -INFINITY, L1 = -INFINITY;
+          for (int bb = h.bf; bb <= h.bl; ++bb) {
+            const int64_t sl = 2 * (int64_t)bb + (bb == h.bf ? h.head_shift : 0);
+            L0 = fmaxf(L0, __ldcg(p.part_lse + sl * kHq + 2 * gh));
+            L1 = fmaxf(L1, __ldcg(p.part_lse + sl * kHq + 2 * gh + 1));
           }
-          float num = 0.f, den = 0.f;
-          for (int64_t bb = bf; bb <= bl; ++bb) {
-            const int64_t slot = 2 * bb + (bb == bf ? head_shift : 0);
-            const float w = exp2f(__ldcg(p.part_lse + slot * hq + h) - L);
-            num = fmaf(w, __ldcg(p.part_o + (slot * hq + h) * kHeadDim + d), num);
-            den += w;
+          float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
+          float d0 = 0.f, d1 = 0.f;
+          for (int bb = h.bf; bb <= h.bl; ++bb) {
+            const int64_t sl = 2 * (int64_t)bb + (bb == h.bf ? h.head_shift : 0);
+            const float w0 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh) - L0);
+            const float w1 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh + 1) - L1);
+            const float *pr0 = p.part_o + (sl * kHq + 2 * gh) * kHeadDim + lane * 4;
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(pr0));
+            const float4 y = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+            n0.x = fmaf(w0, x.x, n0.x); n0.y = fmaf(w0, x.y, n0.y);
+            n0.z = fmaf(w0, x.z, n0.z); n0.w = fmaf(w0, x.w, n0.w);
+            n1.x = fmaf(w1, y.x, n1.x); n1.y = fmaf(w1, y.y, n1.y);
+            n1.z = fmaf(w1, y.z, n1.z); n1.w = fmaf(w1, y.w, n1.w);
+            d0 += w0;
+            d1 += w1;
           }
           if (row_ok) {
-            __nv_bfloat16 ob = __float2bfloat16_rn(num / den);
-            p.out[qrow * (int64_t)hq * kHeadDim + idx] = *reinterpret_cast<uint16_t *>(&ob);
+            const float e0 = 1.f / d0, e1 = 1.f / d1;
+            *reinterpret_cast<uint2 *>(op) =
+                make_uint2(pack_bf16(n0.x * e0, n0.y * e0), pack_bf16(n0.z * e0, n0.w * e0));
+            *reinterpret_cast<uint2 *>(op + kHeadDim) =
+                make_uint2(pack_bf16(n1.x * e1, n1.y * e1), pack_bf16(n1.z * e1, n1.w * e1));
           }
+          if (lane == 0) p.counters[(int64_t)h.r * kHkv + gh] = 0;
         }
-        if (tid == 0) p.counters[r] = 0;
       }
     }
-    named_barrier(1, C::kConsumerThreads);
-    pos = seg_end;
+    if (h.flags & kFinal) break;
   }
 }
 
-template <int HKV>
-cudaError_t launch_decode_t(const AttnParams &p, int grid, cudaStream_t s) {
-  using C = Dec<HKV>;
+}  // namespace
+
+cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s) {
+  if (p.num_kv_heads != kHkv || p.num_qo_heads != kHq) return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<HKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::kSmem);
+    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  decode_kernel<HKV><<<grid, C::kThreads, C::kSmem, s>>>(p);
+  decode_kernel<<<grid, kThreads, kSmem, s>>>(p);
   return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s) {
-  switch (p.num_kv_heads) {
-    case 1: return launch_decode_t<1>(p, grid, s);
-    case 2: return launch_decode_t<2>(p, grid, s);
-    case 4: return launch_decode_t<4>(p, grid, s);
-    case 8: return launch_decode_t<8>(p, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
+int decode_ctas_per_sm() { return 2; }
 
 }  // namespace msg

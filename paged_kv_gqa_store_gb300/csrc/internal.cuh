@@ -14,6 +14,7 @@ namespace msg {
 
 constexpr int kHeadDim = 128;
 constexpr int kGroup = 2;                 // query heads per KV head
+constexpr int kKvHeads = 8;               // KV heads (16 query heads)
 constexpr int kMaxDecodeCtas = 512;       // partial-result slots are 2 per CTA
 constexpr int kExtendTileTokens = 64;     // query tokens per extend tile
 constexpr int kPlanThreads = 1024;
@@ -33,7 +34,7 @@ struct WsLayout {
   size_t qo_indptr = 0;    // int32[num_reqs + 1]   (plan's own, checked copy)
   size_t dec_req = 0;      // int32[num_reqs]       decode request list
   size_t dec_start = 0;    // int64[num_reqs + 1]   prefix of decode kv lengths
-  size_t counters = 0;     // int32[num_reqs]       split merge counters
+  size_t counters = 0;     // int32[num_reqs * 8]   split merge counters (request, KV head)
   size_t ext_tiles = 0;    // int32x2[max_tiles]    (request, query tile)
   size_t part_lse = 0;     // float[2 * kMaxDecodeCtas * Hq]
   size_t part_o = 0;       // float[2 * kMaxDecodeCtas * Hq * D]
@@ -60,7 +61,7 @@ inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t
   L.qo_indptr = take(sizeof(int32_t) * (num_reqs + 1));
   L.dec_req = take(sizeof(int32_t) * (num_reqs + 1));
   L.dec_start = take(sizeof(int64_t) * (num_reqs + 1));
-  L.counters = take(sizeof(int32_t) * (num_reqs + 1));
+  L.counters = take(sizeof(int32_t) * (num_reqs + 1) * kKvHeads);
   L.max_tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + num_reqs + 1;
   L.ext_tiles = take(sizeof(int32_t) * 2 * L.max_tiles);
   L.plan_end = off;
@@ -159,6 +160,7 @@ cudaError_t launch_store_kv(const StoreParams &p, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s);
 cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s);
 int device_sm_count();
+int decode_ctas_per_sm();
 
 }  // namespace msg
 

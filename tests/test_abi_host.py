@@ -65,6 +65,8 @@ def _attn(lib, **kw):
     (dict(head_dim=64), msg.MSG_ERR_UNSUPPORTED),
     (dict(num_qo_heads=24), msg.MSG_ERR_UNSUPPORTED),
     (dict(num_qo_heads=6, num_kv_heads=3), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=8, num_kv_heads=4), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=16, num_kv_heads=16), msg.MSG_ERR_UNSUPPORTED),
     (dict(page_size=3), msg.MSG_ERR_UNSUPPORTED),
     (dict(page_size=256), msg.MSG_ERR_UNSUPPORTED),
     (dict(num_reqs=-1), msg.MSG_ERR_INVALID_ARG),
