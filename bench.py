@@ -434,6 +434,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extend", action="store_true", help="skip the extend sub-benchmark")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
+    ap.add_argument("--extend-only", action="store_true",
+                    help="run only the extend sub-benchmark and print its JSON (profiling)")
     ap.add_argument("--layers", type=int, default=28,
                     help="layers per step (28 for the benchmark; fewer only for profiling)")
     args = ap.parse_args()
@@ -444,6 +446,14 @@ def main():
             import oracle
             oracle.build()
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.extend_only:
+        import torch
+        import paged_kv_gqa_store_gb300 as msg
+        msg.load_library()
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+        torch.cuda.set_device(dev)
+        print(json.dumps(run_extend(args, dev, msg, measured_peaks())), flush=True)
         return
     dist = None
     if world > 1:

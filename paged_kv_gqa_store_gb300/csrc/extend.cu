@@ -1,18 +1,36 @@
 // extend.cu -- a5: causal GQA extend (prefill / chunked prefill / prefix hit)
-// attention through the page table, on tensor cores.
+// attention through the page table, on the sm_100-family tensor cores
+// (tcgen05 MMA with TMEM accumulators, TMA loads).
 //
 // Math ("第 0 步：一个能跑的最小推理引擎", attention operator): new token i of
 // request r sits at absolute position p = cached_len + i and sees keys j <= p;
 // query head h reads KV head h / 2; scores are scale * q.k, softmax, weighted V.
 //
-// Tiling: one CTA per (request, 64-token query tile, KV head).  The two query
-// heads of the GQA group are stacked, so the tile is M = 128 rows (row = head *
-// 64 + token) against key tiles of 64 gathered through the page table.  Q.K^T
-// and P.V run as bf16 MMAs with fp32 accumulation; the online softmax is fp32 in
-// base 2.  P is rounded to bf16 for the P.V product and the row sums add up the
-// same rounded values, so a constant V is reproduced exactly.  Key tiles that
-// lie wholly below the causal diagonal skip the mask; tiles past the last query
-// position are never visited.
+// One CTA per (request, 64-token query tile, KV head).  The two query heads of
+// the GQA group are stacked, so the tile is M = 128 rows (row = head * 64 +
+// token) against key tiles of N = 128 keys.
+//
+//  warp 0      producer: Q by TMA (3-D tensor map over q), K and V rows gathered
+//              through the page table with TMA tile::gather4 (4 rows per
+//              instruction) into 128B-swizzled shared memory, two stages.
+//  warp 1      allocates TMEM (S0 | S1 | O, 128 fp32 columns each) and one lane
+//              issues the MMAs: S = Q.K^T (8 steps of K = 16, both operands
+//              K-major in shared memory) into S[j % 2]; then O += P.V with P
+//              read from TMEM and V from shared memory (MN-major).
+//  warps 4-7   softmax, one thread per row (= TMEM lane): reads its S row with
+//              tcgen05.ld, applies scale * log2 e and the causal mask (only on
+//              tiles that reach the diagonal), keeps the running max (O is
+//              rescaled in TMEM only when the max grows by more than 2^8, so the
+//              rescale is rare; the normalisation stays exact), writes P back
+//              over S as a bf16 pair hi + lo (a single bf16 P costs ~2.2e-3
+//              relative L2 on top of the output rounding; the pair keeps ~16
+//              bits) and sums the same pair into the row's denominator.  The
+//              epilogue normalises O and stores bf16 rows.
+//
+// All cross-role hand-offs are mbarriers; every wait is bounded in time and an
+// expired one records MSG_DEV_TIMEOUT and unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include "internal.cuh"
@@ -22,45 +40,149 @@ namespace msg {
 namespace {
 
 constexpr int kBM = kExtendTileTokens;        // 64 query tokens
-constexpr int kRows = kBM * kGroup;           // 128 rows
-constexpr int kBN = 64;                       // keys per tile
-constexpr int kThreads = 256;                 // 8 warps x 16 rows
-constexpr int kRowBytes = kHeadDim * 2;       // 256 B per (token, head)
-constexpr int kQBytes = kRows * kRowBytes;    // 32 KiB
-constexpr int kKVBytes = kBN * kRowBytes;     // 16 KiB
-constexpr size_t kSmem = kQBytes + 4 * (size_t)kKVBytes;   // Q + 2 x (K, V)
+constexpr int kBN = 128;                      // keys per tile
+constexpr int kThreads = 256;
+constexpr int kHalf = 128 * 128;              // one 64-element-wide region of 128 rows (16 KiB)
+constexpr int kQBytes = 2 * kHalf;            // 32 KiB
+constexpr int kKBytes = 2 * kHalf;            // 32 KiB per stage (two 64-wide halves)
+constexpr int kStages = 2;
+constexpr int kOffQ = 0;
+constexpr int kOffK = kQBytes;
+constexpr int kOffV = kOffK + kStages * kKBytes;
+constexpr int kOffBar = kOffV + kStages * kKBytes;
+constexpr int kBarBytes = 512;
+constexpr size_t kSmem = (size_t)kOffBar + kBarBytes + 1024;   // + slack for 1 KiB alignment
+constexpr uint32_t kTmemCols = 512;           // S0 [0,128) | S1 [128,256) | O [256,384)
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max grows > 2^8
 
-// 16-byte chunk c of row r in a 256-byte-row tile, XOR-swizzled so that the 8
-// rows an ldmatrix phase touches fall in 8 different bank groups.
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (uint32_t)(r * kRowBytes + ((c ^ (r & 7)) << 4));
-}
+// mbarrier slots inside the barrier block
+enum {
+  kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKVEmpty = 5, kBarSFull = 7, kBarPReady = 9,
+  kBarODone = 11, kBarEpi = 12, kBarFinal = 13, kNumBars = 14
+};
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *bar) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, int col, int r0,
+                                            int r1, int r2, int r3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1) extend_kernel(AttnParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *qs = smem;
-  uint8_t *ks[2] = {smem + kQBytes, smem + kQBytes + 2 * kKVBytes};
-  uint8_t *vs[2] = {smem + kQBytes + kKVBytes, smem + kQBytes + 3 * kKVBytes};
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format: start,
+// leading and stride byte offsets in 16-byte units, version 1, layout 2).
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, M = 128, N = 128.
+constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                              ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = kIdescQK | (1u << 16);   // B (V) is MN-major
+
+struct ExtParams {
+  AttnParams a;
+  int32_t kv_rows_per_slot;     // 64-element rows per pool slot (pool_row_stride / 64)
+  int32_t kv_rows_total;        // rows of the K/V gather maps (row >= this: zero fill)
+};
+
+__device__ __forceinline__ bool aborted(volatile int32_t *f) { return *f != 0; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_kernel(const __grid_constant__ ExtParams ep, const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v) {
+  extern __shared__ uint8_t smem_raw[];
+  const AttnParams &p = ep.a;
+  // 1 KiB-aligned base: the 128B swizzle pattern repeats every 1 KiB.
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + kNumBars * 8);
+  volatile int32_t *abort_flag =
+      reinterpret_cast<volatile int32_t *>(smem + kOffBar + kNumBars * 8 + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PlanHeader hdr = *p.hdr;
@@ -80,189 +202,330 @@ __global__ void __launch_bounds__(kThreads, 1) extend_kernel(AttnParams p) {
     if (tid == 0 && gh == 0) report(p.status, MSG_DEV_BAD_LENGTHS, r, qrow0);
     return;
   }
-  const int64_t row = p.req_rows ? p.req_rows[r] : r;
-  const int32_t *row_ptr = p.page_table + row * p.pt_stride;
   const int64_t kv_end = cached + q0 + nq;              // keys [0, kv_end)
   const int n_tiles = (int)((kv_end + kBN - 1) / kBN);
-  const int hq = p.num_qo_heads;
+  const int64_t min_pos = cached + q0;                  // smallest query position
 
-  // ---- Q tile: rows m = h * 64 + t (t < nq), zero rows past the extend
-  for (int idx = tid; idx < kRows * 16; idx += kThreads) {
-    const int m = idx >> 4, c = idx & 15;
-    const int h = m / kBM, t = m % kBM;
-    uint8_t *dst = qs + swz(m, c);
-    if (t < nq) {
-      const uint16_t *src = p.q + (qrow0 + t) * p.q_stride + (2 * gh + h) * kHeadDim + c * 8;
-      cp_async16(dst, src);
-    } else {
-      *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    mbar_init(&bars[kBarQ], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kBarKFull + s], 1);
+      mbar_init(&bars[kBarVFull + s], 1);
+      mbar_init(&bars[kBarKVEmpty + s], 1);
+      mbar_init(&bars[kBarSFull + s], 1);
+      mbar_init(&bars[kBarPReady + s], 4);
     }
+    mbar_init(&bars[kBarODone], 1);
+    mbar_init(&bars[kBarEpi], 4);
+    mbar_init(&bars[kBarFinal], 1);
+    *abort_flag = 0;
+    mbar_fence_init();
   }
-  auto load_kv = [&](int kt, int stage) {
-    for (int idx = tid; idx < kBN * 16; idx += kThreads) {
-      const int n = idx >> 4, c = idx & 15;
-      const int64_t j = (int64_t)kt * kBN + n;
-      uint8_t *kd = ks[stage] + swz(n, c);
-      uint8_t *vd = vs[stage] + swz(n, c);
-      if (j < kv_end) {
-        const int64_t slot =
-            page_slot(row_ptr, j, p.page_size, p.page_shift, p.num_slots, p.status, r);
-        const int64_t off = slot * p.pool_stride_bytes + gh * kRowBytes + c * 16;
-        cp_async16(kd, p.k_pool + off);
-        cp_async16(vd, p.v_pool + off);
-      } else {
-        *reinterpret_cast<uint4 *>(kd) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(vd) = make_uint4(0, 0, 0, 0);
-      }
-    }
-  };
-  load_kv(0, 0);
-  cp_async_commit();
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  const uint32_t qs_a = smem_u32(qs);
-  uint32_t qf[8][4];
-  float oacc[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const int lr = lane >> 2;                       // local row (and +8)
-  const int m_base = warp * 16;
-  const int h_warp = m_base / kBM;                // head of this warp's rows
-  const int64_t pos0 = cached + q0 + (m_base % kBM) + lr;   // position of row lr
-  const int64_t min_pos = cached + q0;                       // smallest position in the tile
-  const float sl2 = p.scale_log2;
-
-  for (int kt = 0; kt < n_tiles; ++kt) {
-    const int st = kt & 1;
-    if (kt + 1 < n_tiles) {
-      load_kv(kt + 1, st ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int64_t row = p.req_rows ? p.req_rows[r] : r;
+    const int32_t *row_ptr = p.page_table + row * p.pt_stride;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[kBarQ], kQBytes);
+      for (int h = 0; h < 2; ++h)
+        for (int half = 0; half < 2; ++half)
+          tma_load_3d(smem + kOffQ + half * kHalf + h * (kHalf / 2), &tmap_q, 0,
+                      (2 * gh + h) * 2 + half, (int)qrow0, &bars[kBarQ]);
     }
-    __syncthreads();
-    if (kt == 0) {
+    const int oob = ep.kv_rows_total;          // a row past the map: zero fill
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int s = j % kStages;
+      // gather rows of this lane's 4 keys (page-table reads before the wait)
+      int rk[4];
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int m = m_base + (lane & 15), c = kk * 2 + (lane >> 4);
-        ldsm_x4(qs_a + swz(m, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-      }
-    }
-    // ---- S = Q K^T (16 rows x 64 keys per warp)
-    float sacc[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
-    const uint32_t ks_a = smem_u32(ks[st]);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int n = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int c = kk * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ks_a + swz(n, c), b0, b1, b2, b3);
-        mma_bf16(sacc[2 * np], qf[kk], b0, b1);
-        mma_bf16(sacc[2 * np + 1], qf[kk], b2, b3);
-      }
-    }
-    // ---- scale, causal mask, online softmax (rows lr and lr + 8)
-    const int64_t kbase = (int64_t)kt * kBN;
-    const bool need_mask = kbase + kBN - 1 > min_pos;
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = sacc[j][e] * sl2;
-        if (need_mask) {
-          const int64_t key = kbase + j * 8 + 2 * (lane & 3) + (e & 1);
-          const int64_t pos = pos0 + ((e >> 1) << 3);
-          if (key > pos) v = -INFINITY;
+      for (int u = 0; u < 4; ++u) {
+        const int64_t key = (int64_t)j * kBN + lane * 4 + u;
+        rk[u] = oob;
+        if (key < kv_end) {
+          const int64_t first =
+              __ldg(row_ptr + (p.page_size == 1 ? key : (key & ~(int64_t)(p.page_size - 1))));
+          int64_t slot = -1;
+          if (p.page_size == 1) {
+            if (first >= 0 && first < p.num_slots) slot = first;
+            else report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
+          } else if (first < 0 || first + p.page_size > p.num_slots) {
+            report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
+          } else if (first & (p.page_size - 1)) {
+            report(p.status, MSG_DEV_PAGE_MISALIGNED, r, first);
+          } else {
+            slot = first + (key & (p.page_size - 1));
+          }
+          if (slot >= 0) rk[u] = (int)(slot * ep.kv_rows_per_slot + 2 * gh);
         }
-        sacc[j][e] = v;
-        mx[e >> 1] = fmaxf(mx[e >> 1], v);
       }
-    }
-    float alpha[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-      const float mn = fmaxf(mrow[i], mx[i]);
-      alpha[i] = exp2f(mrow[i] - mn);
-      mrow[i] = mn;
-      lrow[i] *= alpha[i];
-    }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      oacc[j][0] *= alpha[0];
-      oacc[j][1] *= alpha[0];
-      oacc[j][2] *= alpha[1];
-      oacc[j][3] *= alpha[1];
-    }
-    // ---- O += P V with P carried as a bf16 pair (hi + lo): a single bf16 P
-    // costs ~2.2e-3 relative L2 on top of the output rounding; the pair keeps
-    // ~16 bits of P.  Row sums add the same hi + lo values.
-    const uint32_t vs_a = smem_u32(vs[st]);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t ph[4], pl[4];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int j = 2 * kk + half;
-        const float p0 = exp2f(sacc[j][0] - mrow[0]), p1 = exp2f(sacc[j][1] - mrow[0]);
-        const float p2 = exp2f(sacc[j][2] - mrow[1]), p3 = exp2f(sacc[j][3] - mrow[1]);
-        const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-        const float r0 = p0 - bf16lo(h01), r1 = p1 - bf16hi(h01);
-        const float r2 = p2 - bf16lo(h23), r3 = p3 - bf16hi(h23);
-        const uint32_t l01 = pack_bf16(r0, r1), l23 = pack_bf16(r2, r3);
-        lrow[0] += (bf16lo(h01) + bf16lo(l01)) + (bf16hi(h01) + bf16hi(l01));
-        lrow[1] += (bf16lo(h23) + bf16lo(l23)) + (bf16hi(h23) + bf16hi(l23));
-        ph[half * 2 + 0] = h01;
-        ph[half * 2 + 1] = h23;
-        pl[half * 2 + 0] = l01;
-        pl[half * 2 + 1] = l23;
+      if (j >= kStages && !mbar_wait(&bars[kBarKVEmpty + s], ((j / kStages) - 1) & 1)) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          report(p.status, MSG_DEV_TIMEOUT, r, j);
+        }
+        break;
       }
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        const int n = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int c = dp * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vs_a + swz(n, c), b0, b1, b2, b3);
-        mma_bf16(oacc[2 * dp], ph, b0, b1);
-        mma_bf16(oacc[2 * dp + 1], ph, b2, b3);
-        mma_bf16(oacc[2 * dp], pl, b0, b1);
-        mma_bf16(oacc[2 * dp + 1], pl, b2, b3);
+      if (aborted(abort_flag)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[kBarKFull + s], kKBytes);
+        mbar_arrive_expect_tx(&bars[kBarVFull + s], kKBytes);
       }
+      __syncwarp();
+      uint8_t *kd = smem + kOffK + s * kKBytes + lane * 4 * 128;
+      uint8_t *vd = smem + kOffV + s * kKBytes + lane * 4 * 128;
+      int rr[2][4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) rr[half][u] = rk[u] == oob ? oob : rk[u] + half;
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+        tma_gather4(kd + half * kHalf, &tmap_k, 0, rr[half][0], rr[half][1], rr[half][2],
+                    rr[half][3], &bars[kBarKFull + s]);
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+        tma_gather4(vd + half * kHalf, &tmap_v, 0, rr[half][0], rr[half][1], rr[half][2],
+                    rr[half][3], &bars[kBarVFull + s]);
+      issued = j + 1;
     }
-    __syncthreads();
+    // drain: every issued stage must have landed before the CTA can exit
+    for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+      mbar_wait(&bars[kBarKFull + j % kStages], (j / kStages) & 1);
+      mbar_wait(&bars[kBarVFull + j % kStages], (j / kStages) & 1);
+    }
+    return;
   }
 
-  // ---- normalise and store rows with t < nq
+  if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t q_base = smem_u32(smem + kOffQ);
+      bool ok = mbar_wait(&bars[kBarQ], 0);
+      for (int j = 0; ok && j <= n_tiles; ++j) {
+        if (j < n_tiles) {
+          // S[j % 2] = Q . K_j^T
+          const int s = j % kStages;
+          if (aborted(abort_flag) || !mbar_wait(&bars[kBarKFull + s], (j / kStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(smem + kOffK + s * kKBytes);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 1);
-    lrow[i] += __shfl_xor_sync(0xffffffffu, lrow[i], 2);
-  }
-  const float inv[2] = {1.f / lrow[0], 1.f / lrow[1]};
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (uint32_t)((k >> 2) * kHalf + (k & 3) * 32);
+            mma_ss(tmem + (uint32_t)(s * 128), sdesc(q_base + off, 16, 1024),
+                   sdesc(k_base + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars[kBarSFull + s]);
+        }
+        if (j >= 1) {
+          // O += P_{j-1} . V_{j-1}, P as the pair hi + lo
+          const int jj = j - 1, s = jj % kStages;
+          if (aborted(abort_flag) || !mbar_wait(&bars[kBarPReady + s], (jj / kStages) & 1) ||
+              !mbar_wait(&bars[kBarVFull + s], (jj / kStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(smem + kOffV + s * kKBytes);
+          const uint32_t p_col = tmem + (uint32_t)(s * 128);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int t = (m_base % kBM) + lr + i * 8;
-    if (t < nq) {
-      uint16_t *op = p.out + (qrow0 + t) * (int64_t)hq * kHeadDim + (2 * gh + h_warp) * kHeadDim +
-                     2 * (lane & 3);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        *reinterpret_cast<uint32_t *>(op + j * 8) =
-            pack_bf16(oacc[j][2 * i] * inv[i], oacc[j][2 * i + 1] * inv[i]);
+          for (int kk = 0; kk < 8; ++kk) {
+            // keys 16kk .. 16kk+15: P hi at columns 32(kk/2) + 8(kk%2), lo 16 further
+            const uint32_t pc = p_col + 32u * (kk >> 1) + 8u * (kk & 1);
+            const uint64_t bd = sdesc(v_base + kk * 2048, kHalf, 1024);
+            mma_ts(tmem + kColO, pc, bd, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kColO, pc + 16u, bd, kIdescPV, 1u);
+          }
+          mma_commit(&bars[kBarKVEmpty + s]);
+          mma_commit(&bars[kBarODone]);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        report(p.status, MSG_DEV_TIMEOUT, r, -1);
+      }
+      // every MMA of this thread must complete before TMEM is released
+      mma_commit(&bars[kBarFinal]);
+      mbar_wait(&bars[kBarFinal], 0);
+      mbar_wait(&bars[kBarEpi], 0);
     }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+    return;
   }
+
+  if (warp < 4) return;   // warps 2 and 3 have no role
+
+  // ---------------------------------------------------------------- softmax
+  const int row = (warp - 4) * 32 + lane;          // = TMEM lane
+  const int t = row % kBM;                          // token inside the tile
+  const int hh = row / kBM;                         // head inside the GQA group
+  const int64_t pos = cached + q0 + t;              // this row's absolute position
+  const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+  const float sl2 = p.scale_log2;
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n_tiles; ++j) {
+    const int s = j % kStages;
+    if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + s], (j / kStages) & 1)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t sa = lane_base + (uint32_t)(s * 128);
+    const int64_t kbase = (int64_t)j * kBN;
+    const bool need_mask = kbase + kBN - 1 > min_pos;
+    // pass 1: row max of the tile
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(sa + 32u * c, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float x = __uint_as_float(v[i]) * sl2;
+        if (need_mask && kbase + 32 * c + i > pos) x = -INFINITY;
+        mx = fmaxf(mx, x);
+      }
+    }
+    if (j == 0) {
+      m = mx;
+    } else if (mx > m + kRescaleThreshold) {
+      // O holds tiles < j: wait for their P.V, then rescale O and l in place
+      if (!mbar_wait(&bars[kBarODone], (j - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float alpha = exp2f(m - mx);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + kColO + 32u * c, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+        tmem_st32(lane_base + kColO + 32u * c, v);
+      }
+      tmem_wait_st();
+      l *= alpha;
+      m = mx;
+    }
+    // pass 2: P = exp2(x - m) as a bf16 pair, written over this row's S columns
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(sa + 32u * c, v);
+      tmem_wait_ld();
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float x0 = __uint_as_float(v[i]) * sl2, x1 = __uint_as_float(v[i + 1]) * sl2;
+        if (need_mask) {
+          if (kbase + 32 * c + i > pos) x0 = -INFINITY;
+          if (kbase + 32 * c + i + 1 > pos) x1 = -INFINITY;
+        }
+        const float p0 = exp2f(x0 - m), p1 = exp2f(x1 - m);
+        const uint32_t hi = pack_bf16(p0, p1);
+        const float r0 = p0 - bf16lo(hi), r1 = p1 - bf16hi(hi);
+        const uint32_t lo = pack_bf16(r0, r1);
+        l += (bf16lo(hi) + bf16lo(lo)) + (bf16hi(hi) + bf16hi(lo));
+        w[i >> 1] = hi;
+        w[16 + (i >> 1)] = lo;
+      }
+      tmem_st32(sa + 32u * c, w);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kBarPReady + s]);
+  }
+  // ---- epilogue: O / l -> bf16
+  if (ok && n_tiles > 0 && mbar_wait(&bars[kBarODone], (n_tiles - 1) & 1)) {
+    tc_fence_after();
+    const float inv = 1.f / l;
+    uint16_t *op =
+        p.out + (qrow0 + t) * (int64_t)p.num_qo_heads * kHeadDim + (2 * gh + hh) * kHeadDim;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(lane_base + kColO + 32u * c, v);
+      tmem_wait_ld();
+      if (t < nq) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          uint4 o;
+          o.x = pack_bf16(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv);
+          o.y = pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+          o.z = pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
+          o.w = pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
+          *reinterpret_cast<uint4 *>(op + 32 * c + i) = o;
+        }
+      }
+    }
+  } else if (lane == 0) {
+    *abort_flag = 1;
+    report(p.status, MSG_DEV_TIMEOUT, r, -2);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars[kBarEpi]);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D map over a pool viewed as rows of 64 bf16 (128 B): box 64 x 1, 128B swizzle.
+bool encode_rows(CUtensorMap *m, const void *base, uint64_t rows) {
+  const cuuint64_t dims[2] = {64, rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// 3-D map over q: (64-element half rows, 2 per head, tokens); box 64 x 1 x 64.
+bool encode_q(CUtensorMap *m, const void *q, int32_t hq, int64_t total_q, int64_t row_stride) {
+  const cuuint64_t dims[3] = {64, (cuuint64_t)hq * 2, (cuuint64_t)total_q};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)row_stride * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
 }  // namespace
 
 cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s) {
+  if (max_tiles <= 0) return cudaSuccess;
+  if (encode_fn() == nullptr) return cudaErrorNotSupported;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -273,9 +536,20 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  if (max_tiles <= 0) return cudaSuccess;
+  ExtParams ep{};
+  ep.a = p;
+  const int64_t pool_stride_elems = p.pool_stride_bytes / 2;
+  if (pool_stride_elems % 64 != 0) return cudaErrorInvalidValue;
+  ep.kv_rows_per_slot = (int32_t)(pool_stride_elems / 64);
+  const uint64_t rows = (uint64_t)p.num_slots * (uint64_t)ep.kv_rows_per_slot;
+  if (rows == 0 || rows >= (1ull << 31)) return cudaErrorInvalidValue;
+  ep.kv_rows_total = (int32_t)rows;
+  CUtensorMap mq, mk, mv;
+  if (!encode_q(&mq, p.q, p.num_qo_heads, p.total_q, p.q_stride) ||
+      !encode_rows(&mk, p.k_pool, rows) || !encode_rows(&mv, p.v_pool, rows))
+    return cudaErrorInvalidValue;
   dim3 grid((unsigned)max_tiles, (unsigned)p.num_kv_heads);
-  extend_kernel<<<grid, kThreads, kSmem, s>>>(p);
+  extend_kernel<<<grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
   return cudaGetLastError();
 }
 
