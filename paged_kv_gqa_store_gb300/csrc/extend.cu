@@ -6,26 +6,31 @@
 // request r sits at absolute position p = cached_len + i and sees keys j <= p;
 // query head h reads KV head h / 2; scores are scale * q.k, softmax, weighted V.
 //
-// One CTA per (request, 64-token query tile, KV head).  The two query heads of
-// the GQA group are stacked, so the tile is M = 128 rows (row = head * 64 +
-// token) against key tiles of N = 128 keys.
+// One CTA per (request, 128-token query tile, KV head), as two sub-tiles a / b
+// of 64 tokens.  In a sub-tile the two query heads of the GQA group are
+// stacked, so each sub-tile is M = 128 rows (row = head * 64 + token) and both
+// sub-tiles share every K/V tile of N = 128 keys (twice the MMA work per byte
+// loaded).
 //
-//  warp 0      producer: Q by TMA (3-D tensor map over q), K and V rows gathered
-//              through the page table with TMA tile::gather4 (4 rows per
-//              instruction) into 128B-swizzled shared memory, two stages.
-//  warp 1      allocates TMEM (S0 | S1 | O, 128 fp32 columns each) and one lane
-//              issues the MMAs: S = Q.K^T (8 steps of K = 16, both operands
-//              K-major in shared memory) into S[j % 2]; then O += P.V with P
-//              read from TMEM and V from shared memory (MN-major).
-//  warps 4-7   softmax, one thread per row (= TMEM lane): reads its S row with
-//              tcgen05.ld, applies scale * log2 e and the causal mask (only on
-//              tiles that reach the diagonal), keeps the running max (O is
-//              rescaled in TMEM only when the max grows by more than 2^8, so the
-//              rescale is rare; the normalisation stays exact), writes P back
-//              over S as a bf16 pair hi + lo (a single bf16 P costs ~2.2e-3
-//              relative L2 on top of the output rounding; the pair keeps ~16
-//              bits) and sums the same pair into the row's denominator.  The
-//              epilogue normalises O and stores bf16 rows.
+//  warp 0       producer: Q by TMA (3-D tensor map over q); K and V rows
+//               gathered through the page table with TMA tile::gather4 (4 rows
+//               of 128 B per instruction) into 128B-swizzled shared memory, in
+//               a ring of four 32 KiB slots (K_j, V_j, K_j+1, ...).
+//  warp 1       allocates TMEM (S_a | S_b | O_a | O_b, 128 fp32 columns each)
+//               and one lane issues the MMAs, alternating the sub-tiles:
+//               O_a += P_a V_{j-1}, S_a = Q_a K_j^T, O_b += P_b V_{j-1},
+//               S_b = Q_b K_j^T.  Q.K^T has both operands K-major in shared
+//               memory; P.V reads P from TMEM and V (MN-major) from shared
+//               memory.  So each sub-tile's softmax overlaps the other's MMAs.
+//  warps 4-7,   softmax of sub-tile a, b: one thread per row (= TMEM lane).
+//  8-11         Reads S with tcgen05.ld, scale * log2 e and the causal mask
+//               (only on tiles that reach the diagonal), running max (O is
+//               rescaled in TMEM only when the max grows by more than 2^8 --
+//               rare, and the normalisation stays exact), then writes P back
+//               over S as a bf16 pair hi + lo (a single bf16 P costs ~2.2e-3
+//               relative L2 on top of the output rounding; the pair keeps ~16
+//               bits).  The row's denominator sums the fp32 P (within 2^-16 of
+//               the pair).  The epilogue normalises O and stores bf16 rows.
 //
 // All cross-role hand-offs are mbarriers; every wait is bounded in time and an
 // expired one records MSG_DEV_TIMEOUT and unwinds.
@@ -39,27 +44,26 @@ namespace msg {
 
 namespace {
 
-constexpr int kBM = kExtendTileTokens;        // 64 query tokens
+constexpr int kSubTok = 64;                   // tokens per sub-tile
 constexpr int kBN = 128;                      // keys per tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;                 // 12 warps
 constexpr int kHalf = 128 * 128;              // one 64-element-wide region of 128 rows (16 KiB)
-constexpr int kQBytes = 2 * kHalf;            // 32 KiB
-constexpr int kKBytes = 2 * kHalf;            // 32 KiB per stage (two 64-wide halves)
-constexpr int kStages = 2;
+constexpr int kQSub = 2 * kHalf;              // 32 KiB of Q per sub-tile
+constexpr int kSlot = 2 * kHalf;              // 32 KiB ring slot: a K or V tile (two halves)
+constexpr int kSlots = 4;
 constexpr int kOffQ = 0;
-constexpr int kOffK = kQBytes;
-constexpr int kOffV = kOffK + kStages * kKBytes;
-constexpr int kOffBar = kOffV + kStages * kKBytes;
+constexpr int kOffRing = 2 * kQSub;
+constexpr int kOffBar = kOffRing + kSlots * kSlot;
 constexpr int kBarBytes = 512;
 constexpr size_t kSmem = (size_t)kOffBar + kBarBytes + 1024;   // + slack for 1 KiB alignment
-constexpr uint32_t kTmemCols = 512;           // S0 [0,128) | S1 [128,256) | O [256,384)
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kTmemCols = 512;           // S_a | S_b | O_a | O_b
+constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max grows > 2^8
 
 // mbarrier slots inside the barrier block
 enum {
-  kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKVEmpty = 5, kBarSFull = 7, kBarPReady = 9,
-  kBarODone = 11, kBarEpi = 12, kBarFinal = 13, kNumBars = 14
+  kBarQ = 0, kBarFull = 1, kBarEmpty = 5, kBarSFull = 9, kBarPReady = 11, kBarODone = 13,
+  kBarEpi = 15, kBarFinal = 16, kNumBars = 17
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -151,6 +155,30 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format: start,
 // leading and stride byte offsets in 16-byte units, version 1, layout 2).
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -195,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int gh = blockIdx.y;
   const int64_t cached = p.cached_len[r];
   const int64_t ext = p.extend_len[r];
-  const int64_t q0 = (int64_t)qt * kBM;
-  const int nq = (int)imin64(kBM, ext - q0);
+  const int64_t q0 = (int64_t)qt * kExtendTileTokens;
+  const int nq = (int)imin64(kExtendTileTokens, ext - q0);
   const int64_t qrow0 = (int64_t)p.qo_indptr[r] + q0;
   if (qrow0 < 0 || qrow0 + nq > p.total_q) {
     if (tid == 0 && gh == 0) report(p.status, MSG_DEV_BAD_LENGTHS, r, qrow0);
@@ -204,19 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int64_t kv_end = cached + q0 + nq;              // keys [0, kv_end)
   const int n_tiles = (int)((kv_end + kBN - 1) / kBN);
-  const int64_t min_pos = cached + q0;                  // smallest query position
 
   if (tid == 0) {
     mbar_init(&bars[kBarQ], 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars[kBarKFull + s], 1);
-      mbar_init(&bars[kBarVFull + s], 1);
-      mbar_init(&bars[kBarKVEmpty + s], 1);
-      mbar_init(&bars[kBarSFull + s], 1);
-      mbar_init(&bars[kBarPReady + s], 4);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&bars[kBarFull + s], 1);
+      mbar_init(&bars[kBarEmpty + s], 1);
     }
-    mbar_init(&bars[kBarODone], 1);
-    mbar_init(&bars[kBarEpi], 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars[kBarSFull + x], 1);
+      mbar_init(&bars[kBarPReady + x], 4);
+      mbar_init(&bars[kBarODone + x], 1);
+    }
+    mbar_init(&bars[kBarEpi], 8);
     mbar_init(&bars[kBarFinal], 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -232,17 +260,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t row = p.req_rows ? p.req_rows[r] : r;
     const int32_t *row_ptr = p.page_table + row * p.pt_stride;
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[kBarQ], kQBytes);
-      for (int h = 0; h < 2; ++h)
-        for (int half = 0; half < 2; ++half)
-          tma_load_3d(smem + kOffQ + half * kHalf + h * (kHalf / 2), &tmap_q, 0,
-                      (2 * gh + h) * 2 + half, (int)qrow0, &bars[kBarQ]);
+      mbar_arrive_expect_tx(&bars[kBarQ], 2 * kQSub);
+      for (int x = 0; x < 2; ++x)
+        for (int h = 0; h < 2; ++h)
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(smem + kOffQ + x * kQSub + half * kHalf + h * (kHalf / 2), &tmap_q, 0,
+                        (2 * gh + h) * 2 + half, (int)(qrow0 + x * kSubTok), &bars[kBarQ]);
     }
     const int oob = ep.kv_rows_total;          // a row past the map: zero fill
-    int issued = 0;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % kStages;
-      // gather rows of this lane's 4 keys (page-table reads before the wait)
+    int issued = 0;                            // ring items issued
+    bool ok = true;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      // gather rows of this lane's 4 keys (page-table reads before the waits)
       int rk[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -265,41 +294,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (slot >= 0) rk[u] = (int)(slot * ep.kv_rows_per_slot + 2 * gh);
         }
       }
-      if (j >= kStages && !mbar_wait(&bars[kBarKVEmpty + s], ((j / kStages) - 1) & 1)) {
-        if (lane == 0) {
-          *abort_flag = 1;
-          report(p.status, MSG_DEV_TIMEOUT, r, j);
-        }
-        break;
-      }
-      if (aborted(abort_flag)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[kBarKFull + s], kKBytes);
-        mbar_arrive_expect_tx(&bars[kBarVFull + s], kKBytes);
-      }
-      __syncwarp();
-      uint8_t *kd = smem + kOffK + s * kKBytes + lane * 4 * 128;
-      uint8_t *vd = smem + kOffV + s * kKBytes + lane * 4 * 128;
       int rr[2][4];
 #pragma unroll
       for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int u = 0; u < 4; ++u) rr[half][u] = rk[u] == oob ? oob : rk[u] + half;
 #pragma unroll
-      for (int half = 0; half < 2; ++half)
-        tma_gather4(kd + half * kHalf, &tmap_k, 0, rr[half][0], rr[half][1], rr[half][2],
-                    rr[half][3], &bars[kBarKFull + s]);
+      for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
+        const int n = 2 * j + kv, s = n % kSlots;
+        if (n >= kSlots && !mbar_wait(&bars[kBarEmpty + s], ((n / kSlots) & 1) ^ 1)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report(p.status, MSG_DEV_TIMEOUT, r, j);
+          }
+          ok = false;
+          break;
+        }
+        if (aborted(abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], kSlot);
+        __syncwarp();
+        uint8_t *dst = smem + kOffRing + s * kSlot + lane * 4 * 128;
+        const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
 #pragma unroll
-      for (int half = 0; half < 2; ++half)
-        tma_gather4(vd + half * kHalf, &tmap_v, 0, rr[half][0], rr[half][1], rr[half][2],
-                    rr[half][3], &bars[kBarVFull + s]);
-      issued = j + 1;
+        for (int half = 0; half < 2; ++half)
+          tma_gather4(dst + half * kHalf, map, 0, rr[half][0], rr[half][1], rr[half][2],
+                      rr[half][3], &bars[kBarFull + s]);
+        issued = n + 1;
+      }
     }
-    // drain: every issued stage must have landed before the CTA can exit
-    for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
-      mbar_wait(&bars[kBarKFull + j % kStages], (j / kStages) & 1);
-      mbar_wait(&bars[kBarVFull + j % kStages], (j / kStages) & 1);
-    }
+    // drain: every issued ring item must have landed before the CTA can exit
+    for (int n = issued > kSlots ? issued - kSlots : 0; n < issued; ++n)
+      mbar_wait(&bars[kBarFull + n % kSlots], (n / kSlots) & 1);
     return;
   }
 
@@ -307,46 +335,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t q_base = smem_u32(smem + kOffQ);
+      const uint32_t ring = smem_u32(smem + kOffRing);
       bool ok = mbar_wait(&bars[kBarQ], 0);
       for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          // S[j % 2] = Q . K_j^T
-          const int s = j % kStages;
-          if (aborted(abort_flag) || !mbar_wait(&bars[kBarKFull + s], (j / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_base = smem_u32(smem + kOffK + s * kKBytes);
+        const int nk = 2 * j, nv = 2 * j - 1;          // ring items K_j and V_{j-1}
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (j >= 1) {
+            // O_x += P_x(j-1) . V_{j-1}, P as the pair hi + lo
+            if (aborted(abort_flag) || !mbar_wait(&bars[kBarPReady + x], (j - 1) & 1) ||
+                (x == 0 && !mbar_wait(&bars[kBarFull + nv % kSlots], (nv / kSlots) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t v_base = ring + (uint32_t)((nv % kSlots) * kSlot);
+            const uint32_t p_col = tmem + kColS + 128u * x;
+            const uint32_t o_col = tmem + kColO + 128u * x;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (uint32_t)((k >> 2) * kHalf + (k & 3) * 32);
-            mma_ss(tmem + (uint32_t)(s * 128), sdesc(q_base + off, 16, 1024),
-                   sdesc(k_base + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              // keys 16kk .. 16kk+15: P hi at columns 32(kk/2) + 8(kk%2), lo 16 further
+              const uint32_t pc = p_col + 32u * (kk >> 1) + 8u * (kk & 1);
+              const uint64_t bd = sdesc(v_base + kk * 2048, kHalf, 1024);
+              mma_ts(o_col, pc, bd, kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+              mma_ts(o_col, pc + 16u, bd, kIdescPV, 1u);
+            }
+            mma_commit(&bars[kBarODone + x]);
+            if (x == 1) mma_commit(&bars[kBarEmpty + nv % kSlots]);
           }
-          mma_commit(&bars[kBarSFull + s]);
-        }
-        if (j >= 1) {
-          // O += P_{j-1} . V_{j-1}, P as the pair hi + lo
-          const int jj = j - 1, s = jj % kStages;
-          if (aborted(abort_flag) || !mbar_wait(&bars[kBarPReady + s], (jj / kStages) & 1) ||
-              !mbar_wait(&bars[kBarVFull + s], (jj / kStages) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(smem + kOffV + s * kKBytes);
-          const uint32_t p_col = tmem + (uint32_t)(s * 128);
+          if (j < n_tiles) {
+            // S_x = Q_x . K_j^T
+            if (aborted(abort_flag) ||
+                (x == 0 && !mbar_wait(&bars[kBarFull + nk % kSlots], (nk / kSlots) & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t k_base = ring + (uint32_t)((nk % kSlots) * kSlot);
+            const uint32_t qx = q_base + (uint32_t)(x * kQSub);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // keys 16kk .. 16kk+15: P hi at columns 32(kk/2) + 8(kk%2), lo 16 further
-            const uint32_t pc = p_col + 32u * (kk >> 1) + 8u * (kk & 1);
-            const uint64_t bd = sdesc(v_base + kk * 2048, kHalf, 1024);
-            mma_ts(tmem + kColO, pc, bd, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
-            mma_ts(tmem + kColO, pc + 16u, bd, kIdescPV, 1u);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t off = (uint32_t)((k >> 2) * kHalf + (k & 3) * 32);
+              mma_ss(tmem + kColS + 128u * x, sdesc(qx + off, 16, 1024),
+                     sdesc(k_base + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars[kBarSFull + x]);
+            if (x == 1) mma_commit(&bars[kBarEmpty + nk % kSlots]);
           }
-          mma_commit(&bars[kBarKVEmpty + s]);
-          mma_commit(&bars[kBarODone]);
         }
       }
       if (!ok) {
@@ -367,100 +401,110 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) return;   // warps 2 and 3 have no role
 
   // ---------------------------------------------------------------- softmax
-  const int row = (warp - 4) * 32 + lane;          // = TMEM lane
-  const int t = row % kBM;                          // token inside the tile
-  const int hh = row / kBM;                         // head inside the GQA group
+  const int x = (warp - 4) >> 2;                    // sub-tile
+  const int row = (warp & 3) * 32 + lane;           // = TMEM lane
+  const int t = x * kSubTok + (row % kSubTok);      // token inside the CTA tile
+  const int hh = row / kSubTok;                     // head inside the GQA group
   const int64_t pos = cached + q0 + t;              // this row's absolute position
-  const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+  const int64_t min_pos = cached + q0 + x * kSubTok;
+  const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  const uint32_t s_col = lane_base + kColS + 128u * x;
+  const uint32_t o_col = lane_base + kColO + 128u * x;
   const float sl2 = p.scale_log2;
-  float m = -INFINITY, l = 0.f;
+  float m = -INFINITY;
+  float2 l2 = make_float2(0.f, 0.f);
   bool ok = true;
   for (int j = 0; j < n_tiles; ++j) {
-    const int s = j % kStages;
-    if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + s], (j / kStages) & 1)) {
+    if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + x], j & 1)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    const uint32_t sa = lane_base + (uint32_t)(s * 128);
     const int64_t kbase = (int64_t)j * kBN;
     const bool need_mask = kbase + kBN - 1 > min_pos;
-    // pass 1: row max of the tile
+    // keys i of the tile with i > lim are masked (only on diagonal tiles)
+    const int lim = need_mask ? (int)imin64(pos - kbase, kBN) : kBN;
+    // pass 1: row max of the tile (raw scores; the scale is positive)
     float mx = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
-      tmem_ld32(sa + 32u * c, v);
+      tmem_ld32(s_col + 32u * c, v);
       tmem_wait_ld();
+      if (need_mask) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float x = __uint_as_float(v[i]) * sl2;
-        if (need_mask && kbase + 32 * c + i > pos) x = -INFINITY;
-        mx = fmaxf(mx, x);
+        for (int i = 0; i < 32; ++i)
+          mx = fmaxf(mx, (32 * c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
       }
     }
+    mx *= sl2;
     if (j == 0) {
       m = mx;
     } else if (mx > m + kRescaleThreshold) {
-      // O holds tiles < j: wait for their P.V, then rescale O and l in place
-      if (!mbar_wait(&bars[kBarODone], (j - 1) & 1)) {
+      // O_x holds tiles < j (their P.V completed before this S): rescale in place
+      if (!mbar_wait(&bars[kBarODone + x], (j - 1) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float alpha = exp2f(m - mx);
+      const float alpha = ex2(m - mx);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_base + kColO + 32u * c, v);
+        tmem_ld32(o_col + 32u * c, v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tmem_st32(lane_base + kColO + 32u * c, v);
+        tmem_st32(o_col + 32u * c, v);
       }
       tmem_wait_st();
-      l *= alpha;
+      l2.x *= alpha;
+      l2.y *= alpha;
       m = mx;
     }
-    // pass 2: P = exp2(x - m) as a bf16 pair, written over this row's S columns
+    // pass 2: P = exp2(s * scale - m) as a bf16 pair, written over S
+    const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
+    const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
-      tmem_ld32(sa + 32u * c, v);
+      tmem_ld32(s_col + 32u * c, v);
       tmem_wait_ld();
       uint32_t w[32];
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
-        float x0 = __uint_as_float(v[i]) * sl2, x1 = __uint_as_float(v[i + 1]) * sl2;
+        float2 xx = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc2, nm2);
         if (need_mask) {
-          if (kbase + 32 * c + i > pos) x0 = -INFINITY;
-          if (kbase + 32 * c + i + 1 > pos) x1 = -INFINITY;
+          if (32 * c + i > lim) xx.x = -INFINITY;
+          if (32 * c + i + 1 > lim) xx.y = -INFINITY;
         }
-        const float p0 = exp2f(x0 - m), p1 = exp2f(x1 - m);
-        const uint32_t hi = pack_bf16(p0, p1);
-        const float r0 = p0 - bf16lo(hi), r1 = p1 - bf16hi(hi);
-        const uint32_t lo = pack_bf16(r0, r1);
-        l += (bf16lo(hi) + bf16lo(lo)) + (bf16hi(hi) + bf16hi(lo));
+        const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+        const uint32_t hi = pack_bf16(pp.x, pp.y);
+        const float2 rr = ffma2(make_float2(bf16lo(hi), bf16hi(hi)), neg1, pp);
         w[i >> 1] = hi;
-        w[16 + (i >> 1)] = lo;
+        w[16 + (i >> 1)] = pack_bf16(rr.x, rr.y);
+        l2 = fadd2(l2, pp);
       }
-      tmem_st32(sa + 32u * c, w);
+      tmem_st32(s_col + 32u * c, w);
     }
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[kBarPReady + s]);
+    if (lane == 0) mbar_arrive(&bars[kBarPReady + x]);
   }
   // ---- epilogue: O / l -> bf16
-  if (ok && n_tiles > 0 && mbar_wait(&bars[kBarODone], (n_tiles - 1) & 1)) {
+  if (ok && n_tiles > 0 && mbar_wait(&bars[kBarODone + x], (n_tiles - 1) & 1)) {
     tc_fence_after();
-    const float inv = 1.f / l;
+    const float inv = 1.f / (l2.x + l2.y);
     uint16_t *op =
         p.out + (qrow0 + t) * (int64_t)p.num_qo_heads * kHeadDim + (2 * gh + hh) * kHeadDim;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
-      tmem_ld32(lane_base + kColO + 32u * c, v);
+      tmem_ld32(o_col + 32u * c, v);
       tmem_wait_ld();
       if (t < nq) {
 #pragma unroll
@@ -513,7 +557,7 @@ bool encode_rows(CUtensorMap *m, const void *base, uint64_t rows) {
 bool encode_q(CUtensorMap *m, const void *q, int32_t hq, int64_t total_q, int64_t row_stride) {
   const cuuint64_t dims[3] = {64, (cuuint64_t)hq * 2, (cuuint64_t)total_q};
   const cuuint64_t strides[2] = {128, (cuuint64_t)row_stride * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kBM};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kSubTok};
   const cuuint32_t es[3] = {1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

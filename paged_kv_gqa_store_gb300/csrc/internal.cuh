@@ -16,7 +16,7 @@ constexpr int kHeadDim = 128;
 constexpr int kGroup = 2;                 // query heads per KV head
 constexpr int kKvHeads = 8;               // KV heads (16 query heads)
 constexpr int kMaxDecodeCtas = 512;       // partial-result slots are 2 per CTA
-constexpr int kExtendTileTokens = 64;     // query tokens per extend tile
+constexpr int kExtendTileTokens = 128;    // query tokens per extend tile
 constexpr int kPlanThreads = 1024;
 
 // Bound of every mbarrier wait (2 s, far beyond any legitimate wait); on expiry

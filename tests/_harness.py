@@ -143,7 +143,7 @@ def sampled_oracle(spec: wl.BatchSpec, pools_before: tuple, q, k_new, v_new, req
             lo, hi = int(meta["qo_indptr"][n]), int(meta["qo_indptr"][n + 1])
             e = hi - lo
             cand = np.unique(np.concatenate([
-                [0, e - 1, min(63, e - 1), min(64, e - 1)],
+                [0, e - 1, min(63, e - 1), min(64, e - 1), min(127, e - 1), min(128, e - 1)],
                 rng.integers(0, e, size=min(rows_per_req, e))]))
             pick.append(lo + cand)
         sub_rows = np.concatenate(pick).astype(np.int64)
