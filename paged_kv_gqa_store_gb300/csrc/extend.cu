@@ -12,18 +12,19 @@
 // sub-tiles share every K/V tile of N = 128 keys (twice the MMA work per byte
 // loaded).
 //
-//  warp 0       producer: Q by TMA (3-D tensor map over q); K and V rows
-//               gathered through the page table with TMA tile::gather4 (4 rows
-//               of 128 B per instruction) into 128B-swizzled shared memory, in
-//               a ring of four 32 KiB slots (K_j, V_j, K_j+1, ...).
-//  warp 1       allocates TMEM (S_a | S_b | O_a | O_b, 128 fp32 columns each)
-//               and one lane issues the MMAs, alternating the sub-tiles:
+//  warps 1-2    producers: K and V rows gathered through the page table with
+//               TMA tile::gather4 (4 rows of 128 B per instruction; warp 1 the
+//               first 64 dims of each key, warp 2 the second) into 128B-swizzled
+//               shared memory, in a ring of five 32 KiB slots (K_j, V_j, ...).
+//  warp 0       allocates TMEM (S_a | S_b | O_a | O_b, 128 fp32 columns each),
+//               loads Q by TMA (3-D tensor map over q), and one lane issues the
+//               MMAs, alternating the sub-tiles:
 //               O_a += P_a V_{j-1}, S_a = Q_a K_j^T, O_b += P_b V_{j-1},
 //               S_b = Q_b K_j^T.  Q.K^T has both operands K-major in shared
 //               memory; P.V reads P from TMEM and V (MN-major) from shared
 //               memory.  So each sub-tile's softmax overlaps the other's MMAs.
-//  warps 4-7,   softmax of sub-tile a, b: one thread per row (= TMEM lane).
-//  8-11         Reads S with tcgen05.ld, scale * log2 e and the causal mask
+//  warps 4-7,   softmax of sub-tile a, b: one thread per row (= TMEM lane
+//  8-11         32 (warp % 4) + lane).  Reads its whole S row with tcgen05.ld, scale * log2 e and the causal mask
 //               (only on tiles that reach the diagonal), running max (O is
 //               rescaled in TMEM only when the max grows by more than 2^8 --
 //               rare, and the normalisation stays exact), then writes P back
@@ -50,7 +51,7 @@ constexpr int kThreads = 384;                 // 12 warps
 constexpr int kHalf = 128 * 128;              // one 64-element-wide region of 128 rows (16 KiB)
 constexpr int kQSub = 2 * kHalf;              // 32 KiB of Q per sub-tile
 constexpr int kSlot = 2 * kHalf;              // 32 KiB ring slot: a K or V tile (two halves)
-constexpr int kSlots = 4;
+constexpr int kSlots = 5;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = 2 * kQSub;
 constexpr int kOffBar = kOffRing + kSlots * kSlot;
@@ -62,8 +63,8 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max 
 
 // mbarrier slots inside the barrier block
 enum {
-  kBarQ = 0, kBarFull = 1, kBarEmpty = 5, kBarSFull = 9, kBarPReady = 11, kBarODone = 13,
-  kBarEpi = 15, kBarFinal = 16, kNumBars = 17
+  kBarQ = 0, kBarFull = 1, kBarEmpty = 6, kBarSFull = 11, kBarPReady = 13, kBarODone = 15,
+  kBarEpi = 17, kBarFinal = 18, kNumBars = 19
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -148,6 +149,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -167,6 +186,15 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
       "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
@@ -236,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars[kBarQ], 1);
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&bars[kBarFull + s], 1);
+      mbar_init(&bars[kBarFull + s], 2);          // one expect-tx arrival per producer warp
       mbar_init(&bars[kBarEmpty + s], 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -249,24 +277,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ producers
+    // warp 1 gathers the first 64 dims of each key's head slice, warp 2 the
+    // second; each lane owns 4 consecutive keys of the tile (one gather4).
+    const int half = warp - 1;
     const int64_t row = p.req_rows ? p.req_rows[r] : r;
     const int32_t *row_ptr = p.page_table + row * p.pt_stride;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[kBarQ], 2 * kQSub);
-      for (int x = 0; x < 2; ++x)
-        for (int h = 0; h < 2; ++h)
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(smem + kOffQ + x * kQSub + half * kHalf + h * (kHalf / 2), &tmap_q, 0,
-                        (2 * gh + h) * 2 + half, (int)(qrow0 + x * kSubTok), &bars[kBarQ]);
-    }
     const int oob = ep.kv_rows_total;          // a row past the map: zero fill
     int issued = 0;                            // ring items issued
     bool ok = true;
@@ -283,22 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           int64_t slot = -1;
           if (p.page_size == 1) {
             if (first >= 0 && first < p.num_slots) slot = first;
-            else report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
+            else if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
           } else if (first < 0 || first + p.page_size > p.num_slots) {
-            report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
+            if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
           } else if (first & (p.page_size - 1)) {
-            report(p.status, MSG_DEV_PAGE_MISALIGNED, r, first);
+            if (half == 0) report(p.status, MSG_DEV_PAGE_MISALIGNED, r, first);
           } else {
             slot = first + (key & (p.page_size - 1));
           }
-          if (slot >= 0) rk[u] = (int)(slot * ep.kv_rows_per_slot + 2 * gh);
+          if (slot >= 0) rk[u] = (int)(slot * ep.kv_rows_per_slot + 2 * gh + half);
         }
       }
-      int rr[2][4];
-#pragma unroll
-      for (int half = 0; half < 2; ++half)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) rr[half][u] = rk[u] == oob ? oob : rk[u] + half;
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
         const int n = 2 * j + kv, s = n % kSlots;
@@ -314,14 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], kSlot);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], kHalf);
         __syncwarp();
-        uint8_t *dst = smem + kOffRing + s * kSlot + lane * 4 * 128;
-        const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-          tma_gather4(dst + half * kHalf, map, 0, rr[half][0], rr[half][1], rr[half][2],
-                      rr[half][3], &bars[kBarFull + s]);
+        tma_gather4(smem + kOffRing + s * kSlot + half * kHalf + lane * 4 * 128,
+                    kv ? &tmap_v : &tmap_k, 0, rk[0], rk[1], rk[2], rk[3], &bars[kBarFull + s]);
         issued = n + 1;
       }
     }
@@ -331,9 +345,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  if (warp == 1) {
+  if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[kBarQ], 2 * kQSub);
+      for (int x = 0; x < 2; ++x)
+        for (int h = 0; h < 2; ++h)
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(smem + kOffQ + x * kQSub + half * kHalf + h * (kHalf / 2), &tmap_q, 0,
+                        (2 * gh + h) * 2 + half, (int)(qrow0 + x * kSubTok), &bars[kBarQ]);
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t ring = smem_u32(smem + kOffRing);
       bool ok = mbar_wait(&bars[kBarQ], 0);
@@ -398,11 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  if (warp < 4) return;   // warps 2 and 3 have no role
-
   // ---------------------------------------------------------------- softmax
+  if (warp < 4) return;   // warp 3 has no role
+
   const int x = (warp - 4) >> 2;                    // sub-tile
-  const int row = (warp & 3) * 32 + lane;           // = TMEM lane
+  const int row = (warp & 3) * 32 + lane;           // = TMEM lane (warp % 4 picks the quarter)
   const int t = x * kSubTok + (row % kSubTok);      // token inside the CTA tile
   const int hh = row / kSubTok;                     // head inside the GQA group
   const int64_t pos = cached + q0 + t;              // this row's absolute position
@@ -412,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t o_col = lane_base + kColO + 128u * x;
   const float sl2 = p.scale_log2;
   float m = -INFINITY;
-  float2 l2 = make_float2(0.f, 0.f);
+  float2 la = make_float2(0.f, 0.f), lb = la;      // independent partial sums
   bool ok = true;
   for (int j = 0; j < n_tiles; ++j) {
     if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + x], j & 1)) {
@@ -424,23 +444,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool need_mask = kbase + kBN - 1 > min_pos;
     // keys i of the tile with i > lim are masked (only on diagonal tiles)
     const int lim = need_mask ? (int)imin64(pos - kbase, kBN) : kBN;
-    // pass 1: row max of the tile (raw scores; the scale is positive)
-    float mx = -INFINITY;
+    uint32_t v[4][32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld32(s_col + 32u * c, v);
-      tmem_wait_ld();
-      if (need_mask) {
+    for (int c = 0; c < 4; ++c) tmem_ld32(s_col + 32u * c, v[c]);
+    tmem_wait_ld();
+    if (need_mask) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          mx = fmaxf(mx, (32 * c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
-      }
+          if (32 * c + i > lim) v[c][i] = __float_as_uint(-INFINITY);
     }
-    mx *= sl2;
+    // row max of the tile (raw scores; the scale is positive), 8 independent chains
+    float mm[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) mm[u] = __uint_as_float(v[0][u]);
+#pragma unroll
+    for (int i = 4; i < 128; ++i)
+      mm[i & 3] = fmaxf(mm[i & 3], __uint_as_float(v[i >> 5][i & 31]));
+    const float mx = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])) * sl2;
     if (j == 0) {
       m = mx;
     } else if (mx > m + kRescaleThreshold) {
@@ -451,54 +473,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float alpha = ex2(m - mx);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(o_col + 32u * c, v);
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t o[16];
+        tmem_ld16(o_col + 16u * c, o);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tmem_st32(o_col + 32u * c, v);
+        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st16(o_col + 16u * c, o);
       }
       tmem_wait_st();
-      l2.x *= alpha;
-      l2.y *= alpha;
+      const float2 a2 = make_float2(alpha, alpha);
+      la = fmul2(la, a2);
+      lb = fmul2(lb, a2);
       m = mx;
     }
-    // pass 2: P = exp2(s * scale - m) as a bf16 pair, written over S
+    // P = exp2(s * scale - m) as a bf16 pair (hi, lo), written over S chunk by chunk:
+    // chunk c (keys 32c..32c+31) -> hi in columns 32c..+15, lo in 32c+16..+31
     const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
     const float2 neg1 = make_float2(-1.f, -1.f);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld32(s_col + 32u * c, v);
-      tmem_wait_ld();
-      uint32_t w[32];
+      uint32_t wh[16], wl[16];
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
-        float2 xx = ffma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), sc2, nm2);
-        if (need_mask) {
-          if (32 * c + i > lim) xx.x = -INFINITY;
-          if (32 * c + i + 1 > lim) xx.y = -INFINITY;
-        }
+        const float2 xx =
+            ffma2(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])), sc2, nm2);
         const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
         const uint32_t hi = pack_bf16(pp.x, pp.y);
         const float2 rr = ffma2(make_float2(bf16lo(hi), bf16hi(hi)), neg1, pp);
-        w[i >> 1] = hi;
-        w[16 + (i >> 1)] = pack_bf16(rr.x, rr.y);
-        l2 = fadd2(l2, pp);
+        wh[i >> 1] = hi;
+        wl[i >> 1] = pack_bf16(rr.x, rr.y);
+        if ((i >> 1) & 1) lb = fadd2(lb, pp);
+        else la = fadd2(la, pp);
       }
-      tmem_st32(s_col + 32u * c, w);
+      tmem_st16(s_col + 32u * c, wh);
+      tmem_st16(s_col + 32u * c + 16u, wl);
     }
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kBarPReady + x]);
   }
+  const float2 lsum2 = fadd2(la, lb);
+  const float lsum = lsum2.x + lsum2.y;
   // ---- epilogue: O / l -> bf16
   if (ok && n_tiles > 0 && mbar_wait(&bars[kBarODone + x], (n_tiles - 1) & 1)) {
     tc_fence_after();
-    const float inv = 1.f / (l2.x + l2.y);
+    const float inv = 1.f / lsum;
     uint16_t *op =
         p.out + (qrow0 + t) * (int64_t)p.num_qo_heads * kHeadDim + (2 * gh + hh) * kHeadDim;
 #pragma unroll
