@@ -12,10 +12,11 @@
 // sub-tiles share every K/V tile of N = 128 keys (twice the MMA work per byte
 // loaded).
 //
-//  warps 1-2    producers: K and V rows gathered through the page table with
-//               TMA tile::gather4 (4 rows of 128 B per instruction; warp 1 the
-//               first 64 dims of each key, warp 2 the second) into 128B-swizzled
-//               shared memory, in a ring of five 32 KiB slots (K_j, V_j, ...).
+//  warps 1-3    producers: K and V rows gathered through the page table with
+//               TMA tile::gather4 (4 rows of 128 B per instruction, the 64
+//               instructions of a tile spread over the three warps) into
+//               128B-swizzled shared memory, in a ring of five 32 KiB slots
+//               (K_j, V_j, K_j+1, ...).
 //  warp 0       allocates TMEM (S_a | S_b | O_a | O_b, 128 fp32 columns each),
 //               loads Q by TMA (3-D tensor map over q), and one lane issues the
 //               MMAs, alternating the sub-tiles:
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars[kBarQ], 1);
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(&bars[kBarFull + s], 2);          // one expect-tx arrival per producer warp
+      mbar_init(&bars[kBarFull + s], 3);          // one expect-tx arrival per producer warp
       mbar_init(&bars[kBarEmpty + s], 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -283,11 +284,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 1 || warp == 2) {
+  if (warp >= 1 && warp <= 3) {
     // ------------------------------------------------------------ producers
-    // warp 1 gathers the first 64 dims of each key's head slice, warp 2 the
-    // second; each lane owns 4 consecutive keys of the tile (one gather4).
-    const int half = warp - 1;
+    // Each ring item is 64 gather4 units u = half * 32 + g (keys 4g .. 4g+3,
+    // 64-dim half `half` of the head slice); unit u is issued by warp
+    // 1 + u % 3, lane u / 3.
+    const int u = (warp - 1) + 3 * lane;
+    const bool active = u < 64;
+    const int half = u >> 5, kg4 = u & 31;
+    const int n_units = (64 - (warp - 1) + 2) / 3;     // units of this warp: 22, 21, 21
     const int64_t row = p.req_rows ? p.req_rows[r] : r;
     const int32_t *row_ptr = p.page_table + row * p.pt_stride;
     const int oob = ep.kv_rows_total;          // a row past the map: zero fill
@@ -297,10 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // gather rows of this lane's 4 keys (page-table reads before the waits)
       int rk[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t key = (int64_t)j * kBN + lane * 4 + u;
-        rk[u] = oob;
-        if (key < kv_end) {
+      for (int e = 0; e < 4; ++e) {
+        const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
+        rk[e] = oob;
+        if (active && key < kv_end) {
           const int64_t first =
               __ldg(row_ptr + (p.page_size == 1 ? key : (key & ~(int64_t)(p.page_size - 1))));
           int64_t slot = -1;
@@ -314,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             slot = first + (key & (p.page_size - 1));
           }
-          if (slot >= 0) rk[u] = (int)(slot * ep.kv_rows_per_slot + 2 * gh + half);
+          if (slot >= 0) rk[e] = (int)(slot * ep.kv_rows_per_slot + 2 * gh + half);
         }
       }
 #pragma unroll
@@ -332,10 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], kHalf);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)n_units * 512u);
         __syncwarp();
-        tma_gather4(smem + kOffRing + s * kSlot + half * kHalf + lane * 4 * 128,
-                    kv ? &tmap_v : &tmap_k, 0, rk[0], rk[1], rk[2], rk[3], &bars[kBarFull + s]);
+        if (active)
+          tma_gather4(smem + kOffRing + s * kSlot + half * kHalf + kg4 * 4 * 128,
+                      kv ? &tmap_v : &tmap_k, 0, rk[0], rk[1], rk[2], rk[3], &bars[kBarFull + s]);
         issued = n + 1;
       }
     }
@@ -419,8 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------------------- softmax
-  if (warp < 4) return;   // warp 3 has no role
-
   const int x = (warp - 4) >> 2;                    // sub-tile
   const int row = (warp & 3) * 32 + lane;           // = TMEM lane (warp % 4 picks the quarter)
   const int t = x * kSubTok + (row % kSubTok);      // token inside the CTA tile
