@@ -249,6 +249,10 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
     if (rc != MSG_OK) return rc;
   }
   if (!(flags & MSG_ATTN_DECODE_ONLY)) {
+    // the persistent extend kernel takes work items from a counter in the plan header
+    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + L.header);
+    rc = from_cuda(cudaMemsetAsync(&hdr->ext_next, 0, sizeof(int32_t), s));
+    if (rc != MSG_OK) return rc;
     rc = from_cuda(launch_extend(ap, L.max_tiles, s));
     if (rc != MSG_OK) return rc;
   }

@@ -6,8 +6,9 @@
 // request r sits at absolute position p = cached_len + i and sees keys j <= p;
 // query head h reads KV head h / 2; scores are scale * q.k, softmax, weighted V.
 //
-// One CTA per (request, 128-token query tile, KV head), as two sub-tiles a / b
-// of 64 tokens.  In a sub-tile the two query heads of the GQA group are
+// Work item = (request, 128-token query tile, KV head), as two sub-tiles a / b
+// of 64 tokens; one persistent CTA per SM takes items until none is left.  In a
+// sub-tile the two query heads of the GQA group are
 // stacked, so each sub-tile is M = 128 rows (row = head * 64 + token) and both
 // sub-tiles share every K/V tile of N = 128 keys (twice the MMA work per byte
 // loaded).
@@ -56,7 +57,7 @@ constexpr int kSlots = 5;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = 2 * kQSub;
 constexpr int kOffBar = kOffRing + kSlots * kSlot;
-constexpr int kBarBytes = 512;
+constexpr int kBarBytes = 512;               // mbarriers, item queue, TMEM address, abort flag
 constexpr size_t kSmem = (size_t)kOffBar + kBarBytes + 1024;   // + slack for 1 KiB alignment
 constexpr uint32_t kTmemCols = 512;           // S_a | S_b | O_a | O_b
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -64,9 +65,10 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max 
 
 // mbarrier slots inside the barrier block
 enum {
-  kBarQ = 0, kBarFull = 1, kBarEmpty = 6, kBarSFull = 11, kBarPReady = 13, kBarODone = 15,
-  kBarEpi = 17, kBarFinal = 18, kNumBars = 19
+  kBarQFull = 0, kBarQFree = 1, kBarFull = 2, kBarEmpty = 7, kBarSFull = 12, kBarPReady = 14,
+  kBarODone = 16, kBarOFree = 18, kBarEpi = 20, kBarFinal = 21, kBarItem = 22, kNumBars = 38
 };
+constexpr int kItemQueue = 16;                // work items published ahead of the slowest role
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
@@ -227,6 +229,35 @@ struct ExtParams {
 
 __device__ __forceinline__ bool aborted(volatile int32_t *f) { return *f != 0; }
 
+// One work item: (extend tile of 128 query tokens, KV head).
+struct Item {
+  int64_t cached, q0, qrow0, kv_end;
+  int32_t r, gh, nq, n_tiles;
+  bool ok;
+};
+
+__device__ __forceinline__ Item load_item(const AttnParams &p, int w) {
+  Item it;
+  const int tile = w / kKvHeads;
+  it.gh = w % kKvHeads;
+  it.r = p.ext_tiles[2 * tile];
+  const int32_t qt = p.ext_tiles[2 * tile + 1];
+  it.cached = p.cached_len[it.r];
+  const int64_t ext = p.extend_len[it.r];
+  it.q0 = (int64_t)qt * kExtendTileTokens;
+  it.nq = (int)imin64(kExtendTileTokens, ext - it.q0);
+  it.qrow0 = (int64_t)p.qo_indptr[it.r] + it.q0;
+  it.ok = it.nq > 0 && it.qrow0 >= 0 && it.qrow0 + it.nq <= p.total_q;
+  it.kv_end = it.cached + it.q0 + it.nq;              // keys [0, kv_end)
+  it.n_tiles = it.ok ? (int)((it.kv_end + kBN - 1) / kBN) : 0;
+  return it;
+}
+
+// Persistent: each CTA takes work items of the plan's extend tile list x KV
+// heads (heaviest tiles first) from a global counter until none is left.  TMEM,
+// the mbarriers and the K/V ring live across items; every role counts tiles,
+// ring items and items globally, so the phases line up without any CTA-wide
+// sync.
 __global__ void __launch_bounds__(kThreads, 1)
     extend_kernel(const __grid_constant__ ExtParams ep, const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
@@ -240,30 +271,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + kNumBars * 8);
   volatile int32_t *abort_flag =
       reinterpret_cast<volatile int32_t *>(smem + kOffBar + kNumBars * 8 + 8);
+  volatile int32_t *item_q =
+      reinterpret_cast<volatile int32_t *>(smem + kOffBar + kNumBars * 8 + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PlanHeader hdr = *p.hdr;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0 && (p.flags & MSG_ATTN_EXTEND_ONLY) &&
-      hdr.dec_count > 0)
+  int32_t *next_ctr = const_cast<int32_t *>(&p.hdr->ext_next);
+  // k-th work item of this CTA: grabbed from the global counter by the producer
+  // warp 1 (lane 0) just before it starts loading it, published through a
+  // 16-entry queue; every role reads the same sequence.  -1 = no more work.
+  auto fetch_item = [&](uint32_t k, bool grab, bool whole_warp) -> int {
+    const int e = (int)(k % kItemQueue);
+    if (grab) {
+      int w = atomicAdd(next_ctr, 1);
+      if (w >= hdr.ext_tile_count * kKvHeads) w = -1;
+      item_q[e] = w;
+      mbar_arrive(&bars[kBarItem + e]);
+    }
+    if (whole_warp) __syncwarp();
+    if (!mbar_wait(&bars[kBarItem + e], (k / kItemQueue) & 1)) {
+      *abort_flag = 1;
+      report(p.status, MSG_DEV_TIMEOUT, -1, -3);
+      return -1;
+    }
+    return item_q[e];
+  };
+  if (blockIdx.x == 0 && tid == 0 && (p.flags & MSG_ATTN_EXTEND_ONLY) && hdr.dec_count > 0)
     report(p.status, MSG_DEV_WRONG_PHASE, hdr.dec_count, hdr.dec_keys);
-  if ((int)blockIdx.x >= hdr.ext_tile_count) return;
-  const int32_t r = p.ext_tiles[2 * blockIdx.x];
-  const int32_t qt = p.ext_tiles[2 * blockIdx.x + 1];
-  const int gh = blockIdx.y;
-  const int64_t cached = p.cached_len[r];
-  const int64_t ext = p.extend_len[r];
-  const int64_t q0 = (int64_t)qt * kExtendTileTokens;
-  const int nq = (int)imin64(kExtendTileTokens, ext - q0);
-  const int64_t qrow0 = (int64_t)p.qo_indptr[r] + q0;
-  if (qrow0 < 0 || qrow0 + nq > p.total_q) {
-    if (tid == 0 && gh == 0) report(p.status, MSG_DEV_BAD_LENGTHS, r, qrow0);
-    return;
-  }
-  const int64_t kv_end = cached + q0 + nq;              // keys [0, kv_end)
-  const int n_tiles = (int)((kv_end + kBN - 1) / kBN);
+  const int items = hdr.ext_tile_count * kKvHeads;
+  if ((int)blockIdx.x >= items) return;
 
   if (tid == 0) {
-    mbar_init(&bars[kBarQ], 1);
+    mbar_init(&bars[kBarQFull], 1);
+    mbar_init(&bars[kBarQFree], 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&bars[kBarFull + s], 3);          // one expect-tx arrival per producer warp
       mbar_init(&bars[kBarEmpty + s], 1);
@@ -272,9 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kBarSFull + x], 1);
       mbar_init(&bars[kBarPReady + x], 4);
       mbar_init(&bars[kBarODone + x], 1);
+      mbar_init(&bars[kBarOFree + x], 4);
     }
     mbar_init(&bars[kBarEpi], 8);
     mbar_init(&bars[kBarFinal], 1);
+    for (int e = 0; e < kItemQueue; ++e) mbar_init(&bars[kBarItem + e], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -293,60 +335,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool active = u < 64;
     const int half = u >> 5, kg4 = u & 31;
     const int n_units = (64 - (warp - 1) + 2) / 3;     // units of this warp: 22, 21, 21
-    const int64_t row = p.req_rows ? p.req_rows[r] : r;
-    const int32_t *row_ptr = p.page_table + row * p.pt_stride;
-    const int oob = ep.kv_rows_total;          // a row past the map: zero fill
-    int issued = 0;                            // ring items issued
+    const int oob = ep.kv_rows_total;                   // a row past the map: zero fill
+    uint32_t N = 0;                                     // ring items issued
     bool ok = true;
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      // gather rows of this lane's 4 keys (page-table reads before the waits)
-      int rk[4];
+    for (uint32_t k = 0; ok; ++k) {
+      const int w = fetch_item(k, warp == 1 && lane == 0, true);
+      if (w < 0) break;
+      const Item it = load_item(p, w);
+      const int64_t row = p.req_rows ? p.req_rows[it.r] : it.r;
+      const int32_t *row_ptr = p.page_table + row * p.pt_stride;
+      for (int j = 0; ok && j < it.n_tiles; ++j) {
+        // gather rows of this lane's 4 keys (page-table reads before the waits)
+        int rk[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
-        rk[e] = oob;
-        if (active && key < kv_end) {
-          const int64_t first =
-              __ldg(row_ptr + (p.page_size == 1 ? key : (key & ~(int64_t)(p.page_size - 1))));
-          int64_t slot = -1;
-          if (p.page_size == 1) {
-            if (first >= 0 && first < p.num_slots) slot = first;
-            else if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
-          } else if (first < 0 || first + p.page_size > p.num_slots) {
-            if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
-          } else if (first & (p.page_size - 1)) {
-            if (half == 0) report(p.status, MSG_DEV_PAGE_MISALIGNED, r, first);
-          } else {
-            slot = first + (key & (p.page_size - 1));
+        for (int e = 0; e < 4; ++e) {
+          const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
+          rk[e] = oob;
+          if (active && key < it.kv_end) {
+            const int64_t first =
+                __ldg(row_ptr + (p.page_size == 1 ? key : (key & ~(int64_t)(p.page_size - 1))));
+            int64_t slot = -1;
+            if (p.page_size == 1) {
+              if (first >= 0 && first < p.num_slots) slot = first;
+              else if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, it.r, first);
+            } else if (first < 0 || first + p.page_size > p.num_slots) {
+              if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, it.r, first);
+            } else if (first & (p.page_size - 1)) {
+              if (half == 0) report(p.status, MSG_DEV_PAGE_MISALIGNED, it.r, first);
+            } else {
+              slot = first + (key & (p.page_size - 1));
+            }
+            if (slot >= 0) rk[e] = (int)(slot * ep.kv_rows_per_slot + 2 * it.gh + half);
           }
-          if (slot >= 0) rk[e] = (int)(slot * ep.kv_rows_per_slot + 2 * gh + half);
+        }
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
+          const uint32_t n = N + 2 * j + kv;
+          const int s = n % kSlots;
+          if (n >= (uint32_t)kSlots && !mbar_wait(&bars[kBarEmpty + s], ((n / kSlots) & 1) ^ 1)) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              report(p.status, MSG_DEV_TIMEOUT, it.r, j);
+            }
+            ok = false;
+            break;
+          }
+          if (aborted(abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)n_units * 512u);
+          __syncwarp();
+          if (active)
+            tma_gather4(smem + kOffRing + s * kSlot + half * kHalf + kg4 * 4 * 128,
+                        kv ? &tmap_v : &tmap_k, 0, rk[0], rk[1], rk[2], rk[3], &bars[kBarFull + s]);
         }
       }
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
-        const int n = 2 * j + kv, s = n % kSlots;
-        if (n >= kSlots && !mbar_wait(&bars[kBarEmpty + s], ((n / kSlots) & 1) ^ 1)) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            report(p.status, MSG_DEV_TIMEOUT, r, j);
-          }
-          ok = false;
-          break;
-        }
-        if (aborted(abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)n_units * 512u);
-        __syncwarp();
-        if (active)
-          tma_gather4(smem + kOffRing + s * kSlot + half * kHalf + kg4 * 4 * 128,
-                      kv ? &tmap_v : &tmap_k, 0, rk[0], rk[1], rk[2], rk[3], &bars[kBarFull + s]);
-        issued = n + 1;
-      }
+      N += 2u * it.n_tiles;
     }
     // drain: every issued ring item must have landed before the CTA can exit
-    for (int n = issued > kSlots ? issued - kSlots : 0; n < issued; ++n)
+    for (uint32_t n = N > (uint32_t)kSlots ? N - kSlots : 0; n < N; ++n)
       mbar_wait(&bars[kBarFull + n % kSlots], (n / kSlots) & 1);
     return;
   }
@@ -354,64 +402,90 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[kBarQ], 2 * kQSub);
-      for (int x = 0; x < 2; ++x)
-        for (int h = 0; h < 2; ++h)
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(smem + kOffQ + x * kQSub + half * kHalf + h * (kHalf / 2), &tmap_q, 0,
-                        (2 * gh + h) * 2 + half, (int)(qrow0 + x * kSubTok), &bars[kBarQ]);
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t ring = smem_u32(smem + kOffRing);
-      bool ok = mbar_wait(&bars[kBarQ], 0);
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        const int nk = 2 * j, nv = 2 * j - 1;          // ring items K_j and V_{j-1}
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (j >= 1) {
-            // O_x += P_x(j-1) . V_{j-1}, P as the pair hi + lo
-            if (aborted(abort_flag) || !mbar_wait(&bars[kBarPReady + x], (j - 1) & 1) ||
-                (x == 0 && !mbar_wait(&bars[kBarFull + nv % kSlots], (nv / kSlots) & 1))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t v_base = ring + (uint32_t)((nv % kSlots) * kSlot);
-            const uint32_t p_col = tmem + kColS + 128u * x;
-            const uint32_t o_col = tmem + kColO + 128u * x;
+      uint32_t T = 0, N = 0, V = 0;                // tiles, ring items, items done
+      bool ok = true;
+      for (uint32_t k = 0; ok; ++k) {
+        const int w = fetch_item(k, false, false);   // lane 0 alone
+        if (w < 0) break;
+        const Item it = load_item(p, w);
+        const int n = it.n_tiles;
+        if (n == 0) continue;
+        // Q of this item, once the previous item's Q.K^T products are done
+        if (V > 0 && !mbar_wait(&bars[kBarQFree], (V - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars[kBarQFull], 2 * kQSub);
+        for (int x = 0; x < 2; ++x)
+          for (int h = 0; h < 2; ++h)
+            for (int half = 0; half < 2; ++half)
+              tma_load_3d(smem + kOffQ + x * kQSub + half * kHalf + h * (kHalf / 2), &tmap_q, 0,
+                          (2 * it.gh + h) * 2 + half, (int)(it.qrow0 + x * kSubTok),
+                          &bars[kBarQFull]);
+        if (!mbar_wait(&bars[kBarQFull], V & 1)) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; ok && j <= n; ++j) {
+          const uint32_t nk = N + 2 * j, nv = N + 2 * j - 1;   // ring items K_j and V_{j-1}
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (j >= 1) {
+              // O_x += P_x(j-1) . V_{j-1}, P as the pair hi + lo
+              if (aborted(abort_flag) ||
+                  !mbar_wait(&bars[kBarPReady + x], (T + j - 1) & 1) ||
+                  (x == 0 && !mbar_wait(&bars[kBarFull + nv % kSlots], (nv / kSlots) & 1)) ||
+                  (j == 1 && V > 0 && !mbar_wait(&bars[kBarOFree + x], (V - 1) & 1))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t v_base = ring + (uint32_t)((nv % kSlots) * kSlot);
+              const uint32_t p_col = tmem + kColS + 128u * x;
+              const uint32_t o_col = tmem + kColO + 128u * x;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              // keys 16kk .. 16kk+15: P hi at columns 32(kk/2) + 8(kk%2), lo 16 further
-              const uint32_t pc = p_col + 32u * (kk >> 1) + 8u * (kk & 1);
-              const uint64_t bd = sdesc(v_base + kk * 2048, kHalf, 1024);
-              mma_ts(o_col, pc, bd, kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
-              mma_ts(o_col, pc + 16u, bd, kIdescPV, 1u);
+              for (int kk = 0; kk < 8; ++kk) {
+                // keys 16kk .. 16kk+15: P hi at columns 32(kk/2) + 8(kk%2), lo 16 further
+                const uint32_t pc = p_col + 32u * (kk >> 1) + 8u * (kk & 1);
+                const uint64_t bd = sdesc(v_base + kk * 2048, kHalf, 1024);
+                mma_ts(o_col, pc, bd, kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+                mma_ts(o_col, pc + 16u, bd, kIdescPV, 1u);
+              }
+              mma_commit(&bars[kBarODone + x]);
+              if (x == 1) mma_commit(&bars[kBarEmpty + nv % kSlots]);
             }
-            mma_commit(&bars[kBarODone + x]);
-            if (x == 1) mma_commit(&bars[kBarEmpty + nv % kSlots]);
-          }
-          if (j < n_tiles) {
-            // S_x = Q_x . K_j^T
-            if (aborted(abort_flag) ||
-                (x == 0 && !mbar_wait(&bars[kBarFull + nk % kSlots], (nk / kSlots) & 1))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t k_base = ring + (uint32_t)((nk % kSlots) * kSlot);
-            const uint32_t qx = q_base + (uint32_t)(x * kQSub);
+            if (j < n) {
+              // S_x = Q_x . K_j^T
+              if (aborted(abort_flag) ||
+                  (x == 0 && !mbar_wait(&bars[kBarFull + nk % kSlots], (nk / kSlots) & 1))) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t k_base = ring + (uint32_t)((nk % kSlots) * kSlot);
+              const uint32_t qx = q_base + (uint32_t)(x * kQSub);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const uint32_t off = (uint32_t)((k >> 2) * kHalf + (k & 3) * 32);
-              mma_ss(tmem + kColS + 128u * x, sdesc(qx + off, 16, 1024),
-                     sdesc(k_base + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+              for (int k = 0; k < 8; ++k) {
+                const uint32_t off = (uint32_t)((k >> 2) * kHalf + (k & 3) * 32);
+                mma_ss(tmem + kColS + 128u * x, sdesc(qx + off, 16, 1024),
+                       sdesc(k_base + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+              }
+              mma_commit(&bars[kBarSFull + x]);
+              if (x == 1) {
+                mma_commit(&bars[kBarEmpty + nk % kSlots]);
+                if (j == n - 1) mma_commit(&bars[kBarQFree]);   // Q no longer read
+              }
             }
-            mma_commit(&bars[kBarSFull + x]);
-            if (x == 1) mma_commit(&bars[kBarEmpty + nk % kSlots]);
           }
         }
+        T += (uint32_t)n;
+        N += 2u * (uint32_t)n;
+        V += 1;
       }
       if (!ok) {
         *abort_flag = 1;
-        report(p.status, MSG_DEV_TIMEOUT, r, -1);
+        report(p.status, MSG_DEV_TIMEOUT, -1, -1);
       }
       // every MMA of this thread must complete before TMEM is released
       mma_commit(&bars[kBarFinal]);
@@ -427,126 +501,143 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- softmax
   const int x = (warp - 4) >> 2;                    // sub-tile
   const int row = (warp & 3) * 32 + lane;           // = TMEM lane (warp % 4 picks the quarter)
-  const int t = x * kSubTok + (row % kSubTok);      // token inside the CTA tile
+  const int tsub = x * kSubTok + (row % kSubTok);   // token inside the item's 128-token tile
   const int hh = row / kSubTok;                     // head inside the GQA group
-  const int64_t pos = cached + q0 + t;              // this row's absolute position
-  const int64_t min_pos = cached + q0 + x * kSubTok;
   const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t s_col = lane_base + kColS + 128u * x;
   const uint32_t o_col = lane_base + kColO + 128u * x;
   const float sl2 = p.scale_log2;
-  float m = -INFINITY;
-  float2 la = make_float2(0.f, 0.f), lb = la;      // independent partial sums
+  uint32_t T = 0;
   bool ok = true;
-  for (int j = 0; j < n_tiles; ++j) {
-    if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + x], j & 1)) {
-      ok = false;
-      break;
+  for (uint32_t k = 0; ok; ++k) {
+    const int w = fetch_item(k, false, true);
+    if (w < 0) break;
+    const Item it = load_item(p, w);
+    if (it.n_tiles == 0) {
+      if (x == 0 && row == 0 && !it.ok) report(p.status, MSG_DEV_BAD_LENGTHS, it.r, it.qrow0);
+      continue;
     }
-    tc_fence_after();
-    const int64_t kbase = (int64_t)j * kBN;
-    const bool need_mask = kbase + kBN - 1 > min_pos;
-    // keys i of the tile with i > lim are masked (only on diagonal tiles)
-    const int lim = need_mask ? (int)imin64(pos - kbase, kBN) : kBN;
-    uint32_t v[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(s_col + 32u * c, v[c]);
-    tmem_wait_ld();
-    if (need_mask) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (32 * c + i > lim) v[c][i] = __float_as_uint(-INFINITY);
-    }
-    // row max of the tile (raw scores; the scale is positive), 8 independent chains
-    float mm[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) mm[u] = __uint_as_float(v[0][u]);
-#pragma unroll
-    for (int i = 4; i < 128; ++i)
-      mm[i & 3] = fmaxf(mm[i & 3], __uint_as_float(v[i >> 5][i & 31]));
-    const float mx = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])) * sl2;
-    if (j == 0) {
-      m = mx;
-    } else if (mx > m + kRescaleThreshold) {
-      // O_x holds tiles < j (their P.V completed before this S): rescale in place
-      if (!mbar_wait(&bars[kBarODone + x], (j - 1) & 1)) {
+    const int64_t pos = it.cached + it.q0 + tsub;   // this row's absolute position
+    const int64_t min_pos = it.cached + it.q0 + x * kSubTok;
+    float m = -INFINITY;
+    float2 la = make_float2(0.f, 0.f), lb = la;      // independent partial sums
+    for (int j = 0; j < it.n_tiles; ++j) {
+      if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + x], (T + j) & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float alpha = ex2(m - mx);
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t o[16];
-        tmem_ld16(o_col + 16u * c, o);
-        tmem_wait_ld();
+      const int64_t kbase = (int64_t)j * kBN;
+      const bool need_mask = kbase + kBN - 1 > min_pos;
+      // keys i of the tile with i > lim are masked (only on diagonal tiles)
+      const int lim = need_mask ? (int)imin64(pos - kbase, kBN) : kBN;
+      uint32_t v[4][32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st16(o_col + 16u * c, o);
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_col + 32u * c, v[c]);
+      tmem_wait_ld();
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i > lim) v[c][i] = __float_as_uint(-INFINITY);
+      }
+      // row max of the tile (raw scores; the scale is positive), 4 independent chains
+      float mm[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mm[q] = __uint_as_float(v[0][q]);
+#pragma unroll
+      for (int i = 4; i < 128; ++i)
+        mm[i & 3] = fmaxf(mm[i & 3], __uint_as_float(v[i >> 5][i & 31]));
+      const float mx = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])) * sl2;
+      if (j == 0) {
+        m = mx;
+      } else if (mx > m + kRescaleThreshold) {
+        // O_x holds tiles < j (their P.V completed before this S): rescale in place
+        if (!mbar_wait(&bars[kBarODone + x], (T + j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = ex2(m - mx);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t o[16];
+          tmem_ld16(o_col + 16u * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(o_col + 16u * c, o);
+        }
+        tmem_wait_st();
+        const float2 a2 = make_float2(alpha, alpha);
+        la = fmul2(la, a2);
+        lb = fmul2(lb, a2);
+        m = mx;
+      }
+      // P = exp2(s * scale - m) as a bf16 pair (hi, lo), written over S chunk by chunk:
+      // chunk c (keys 32c..32c+31) -> hi in columns 32c..+15, lo in 32c+16..+31
+      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
+      const float2 neg1 = make_float2(-1.f, -1.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t wh[16], wl[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 xx = ffma2(
+              make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])), sc2, nm2);
+          const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+          const uint32_t hi = pack_bf16(pp.x, pp.y);
+          const float2 rr = ffma2(make_float2(bf16lo(hi), bf16hi(hi)), neg1, pp);
+          wh[i >> 1] = hi;
+          wl[i >> 1] = pack_bf16(rr.x, rr.y);
+          if ((i >> 1) & 1) lb = fadd2(lb, pp);
+          else la = fadd2(la, pp);
+        }
+        tmem_st16(s_col + 32u * c, wh);
+        tmem_st16(s_col + 32u * c + 16u, wl);
       }
       tmem_wait_st();
-      const float2 a2 = make_float2(alpha, alpha);
-      la = fmul2(la, a2);
-      lb = fmul2(lb, a2);
-      m = mx;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarPReady + x]);
     }
-    // P = exp2(s * scale - m) as a bf16 pair (hi, lo), written over S chunk by chunk:
-    // chunk c (keys 32c..32c+31) -> hi in columns 32c..+15, lo in 32c+16..+31
-    const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m, -m);
-    const float2 neg1 = make_float2(-1.f, -1.f);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t wh[16], wl[16];
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float2 xx =
-            ffma2(make_float2(__uint_as_float(v[c][i]), __uint_as_float(v[c][i + 1])), sc2, nm2);
-        const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
-        const uint32_t hi = pack_bf16(pp.x, pp.y);
-        const float2 rr = ffma2(make_float2(bf16lo(hi), bf16hi(hi)), neg1, pp);
-        wh[i >> 1] = hi;
-        wl[i >> 1] = pack_bf16(rr.x, rr.y);
-        if ((i >> 1) & 1) lb = fadd2(lb, pp);
-        else la = fadd2(la, pp);
-      }
-      tmem_st16(s_col + 32u * c, wh);
-      tmem_st16(s_col + 32u * c + 16u, wl);
+    if (!ok) break;
+    // ---- epilogue: O / l -> bf16, then hand O_x back to the MMA issuer
+    if (!mbar_wait(&bars[kBarODone + x], (T + it.n_tiles - 1) & 1)) {
+      ok = false;
+      break;
     }
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[kBarPReady + x]);
-  }
-  const float2 lsum2 = fadd2(la, lb);
-  const float lsum = lsum2.x + lsum2.y;
-  // ---- epilogue: O / l -> bf16
-  if (ok && n_tiles > 0 && mbar_wait(&bars[kBarODone + x], (n_tiles - 1) & 1)) {
     tc_fence_after();
-    const float inv = 1.f / lsum;
-    uint16_t *op =
-        p.out + (qrow0 + t) * (int64_t)p.num_qo_heads * kHeadDim + (2 * gh + hh) * kHeadDim;
+    const float2 lsum2 = fadd2(la, lb);
+    const float inv = 1.f / (lsum2.x + lsum2.y);
+    uint16_t *op = p.out + (it.qrow0 + tsub) * (int64_t)p.num_qo_heads * kHeadDim +
+                   (2 * it.gh + hh) * kHeadDim;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld32(o_col + 32u * c, v);
+      uint32_t o[32];
+      tmem_ld32(o_col + 32u * c, o);
       tmem_wait_ld();
-      if (t < nq) {
+      if (tsub < it.nq) {
 #pragma unroll
         for (int i = 0; i < 32; i += 8) {
-          uint4 o;
-          o.x = pack_bf16(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv);
-          o.y = pack_bf16(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
-          o.z = pack_bf16(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
-          o.w = pack_bf16(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
-          *reinterpret_cast<uint4 *>(op + 32 * c + i) = o;
+          uint4 q4;
+          q4.x = pack_bf16(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv);
+          q4.y = pack_bf16(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+          q4.z = pack_bf16(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv);
+          q4.w = pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
+          *reinterpret_cast<uint4 *>(op + 32 * c + i) = q4;
         }
       }
     }
-  } else if (lane == 0) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kBarOFree + x]);
+    T += (uint32_t)it.n_tiles;
+  }
+  if (!ok && lane == 0) {
     *abort_flag = 1;
-    report(p.status, MSG_DEV_TIMEOUT, r, -2);
+    report(p.status, MSG_DEV_TIMEOUT, -1, -2);
   }
   tc_fence_before();
   __syncwarp();
@@ -618,8 +709,10 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s
   if (!encode_q(&mq, p.q, p.num_qo_heads, p.total_q, p.q_stride) ||
       !encode_rows(&mk, p.k_pool, rows) || !encode_rows(&mv, p.v_pool, rows))
     return cudaErrorInvalidValue;
-  dim3 grid((unsigned)max_tiles, (unsigned)p.num_kv_heads);
-  extend_kernel<<<grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
+  // persistent: one CTA per SM (the kernel's shared memory allows no more)
+  int64_t grid = (int64_t)device_sm_count();
+  if (grid > max_tiles * kKvHeads) grid = max_tiles * kKvHeads;
+  extend_kernel<<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
   return cudaGetLastError();
 }
 

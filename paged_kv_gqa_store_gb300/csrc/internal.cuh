@@ -50,6 +50,8 @@ struct PlanHeader {
   int32_t ext_count;       // extend requests
   int64_t dec_keys;        // sum of decode kv lengths
   int64_t total_q;         // sum of extend lengths
+  int32_t ext_next;        // extend work-item counter (zeroed before each extend launch)
+  int32_t pad;
 };
 
 inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t d) {
