@@ -283,6 +283,7 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     torch.cuda.empty_cache()
     R, L = spec.num_reqs, args.layers
     extend = run_extend(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
+    small = run_graph_decode(args, dev, msg) if rank == 0 and not args.no_extend else None
     cpu = cpu_baseline(spec) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     line = {
@@ -309,9 +310,64 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     }
     if extend is not None:
         line["extend"] = extend
+    if small is not None:
+        line["small_batch_graph"] = small
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
+
+
+def run_graph_decode(args, dev, msg):
+    """Small-batch decode step (8 requests x 28 layers), eager vs CUDA-graph replay:
+    at this size the step is launch-bound, which is what graph replay removes."""
+    import torch
+    rng = np.random.default_rng(2002)
+    ctx = rng.integers(512, 4096 + 1, size=8)
+    spec = wl.make_batch("decode_8x28", 2003, cached_len=ctx - 1, extend_len=np.ones(8, np.int32),
+                         page_size=1, num_pages=int(ctx.sum()) + 1024, num_layers=28)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    pt, cached, ext, rows = (i32(spec.page_table), i32(spec.cached_len), i32(spec.extend_len),
+                             i32(spec.req_rows))
+    T, R = spec.total_q, spec.num_reqs
+    qo = torch.zeros(R + 1, dtype=torch.int32, device=dev)
+    loc = torch.zeros(T, dtype=torch.int64, device=dev)
+    ws = torch.zeros(msg.msg_workspace_size(R, T), dtype=torch.uint8, device=dev)
+    layers = [wl.device_tensors(spec, layer, device=dev) for layer in range(spec.num_layers)]
+    outs = [torch.empty_like(t["q"]) for t in layers]
+    flags = msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_DECODE_ONLY
+
+    def step():
+        msg.msg_plan(pt, cached, ext, T, spec.num_slots, ws, req_rows=rows, qo_indptr_out=qo,
+                     out_loc_out=loc)
+        for i, t in enumerate(layers):
+            msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], loc)
+            msg.msg_paged_attention(t["q"], t["k_pool"], t["v_pool"], pt, cached, ext, qo, outs[i],
+                                    ws, page_size=1, req_rows=rows, max_kv_len=0, flags=flags)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(True), torch.cuda.Event(True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    n = max(args.steps, 20)
+    eager_ms = timed(step, n)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    graph_ms = timed(g.replay, n)
+    del layers, outs, g
+    torch.cuda.empty_cache()
+    by = spec.num_layers * (decode_attn_bytes(spec) + store_bytes(spec))
+    return {"workload": "decode_8req_ctx512-4096_28layers_page1", "eager_ms": round(eager_ms, 4),
+            "graph_ms": round(graph_ms, 4), "eager_gbs": round(by / (eager_ms * 1e-3) / 1e9, 1),
+            "graph_gbs": round(by / (graph_ms * 1e-3) / 1e9, 1), "launches_per_step": 2 + 2 * 28}
 
 
 def run_extend(args, dev, msg, peaks):
