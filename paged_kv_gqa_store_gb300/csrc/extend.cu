@@ -66,8 +66,8 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max 
 // mbarrier slots inside the barrier block
 enum {
   kBarQFull = 0, kBarQFree = 1, kBarFull = 2, kBarEmpty = 7, kBarSFull = 12, kBarPReady = 14,
-  kBarODone = 16, kBarOFree = 18, kBarEpi = 20, kBarFinal = 21, kBarItem = 22, kNumBars = 38
-};
+  kBarODone = 18, kBarOFree = 20, kBarEpi = 22, kBarFinal = 23, kBarItem = 24, kNumBars = 40
+};  // kBarPReady + 2 x + h: P of sub-tile x, key half h written
 constexpr int kItemQueue = 16;                // work items published ahead of the slowest role
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -233,6 +233,7 @@ __device__ __forceinline__ bool aborted(volatile int32_t *f) { return *f != 0; }
 struct Item {
   int64_t cached, q0, qrow0, kv_end;
   int32_t r, gh, nq, n_tiles;
+  int32_t n_a;        // key tiles sub-tile a needs (its last query sits 64 tokens earlier)
   bool ok;
 };
 
@@ -250,6 +251,8 @@ __device__ __forceinline__ Item load_item(const AttnParams &p, int w) {
   it.ok = it.nq > 0 && it.qrow0 >= 0 && it.qrow0 + it.nq <= p.total_q;
   it.kv_end = it.cached + it.q0 + it.nq;              // keys [0, kv_end)
   it.n_tiles = it.ok ? (int)((it.kv_end + kBN - 1) / kBN) : 0;
+  const int64_t kv_a = it.cached + it.q0 + (it.nq < kSubTok ? it.nq : kSubTok);
+  it.n_a = it.ok ? (int)((kv_a + kBN - 1) / kBN) : 0;
   return it;
 }
 
@@ -310,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kBarSFull + x], 1);
-      mbar_init(&bars[kBarPReady + x], 4);
+      mbar_init(&bars[kBarPReady + 2 * x], 4);
+      mbar_init(&bars[kBarPReady + 2 * x + 1], 4);
       mbar_init(&bars[kBarODone + x], 1);
       mbar_init(&bars[kBarOFree + x], 4);
     }
@@ -404,7 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t q_base = smem_u32(smem + kOffQ);
       const uint32_t ring = smem_u32(smem + kOffRing);
-      uint32_t T = 0, N = 0, V = 0;                // tiles, ring items, items done
+      // descriptors differ only in the start address (low 14 bits, 16-byte units)
+      const uint64_t dq0 = sdesc(q_base, 16, 1024);
+      const uint64_t dring = sdesc(ring, 16, 1024);
+      const uint64_t dv0 = sdesc(ring, kHalf, 1024);
+      uint32_t Ts[2] = {0, 0}, N = 0, V = 0;       // tiles per sub-tile, ring items, items done
       bool ok = true;
       for (uint32_t k = 0; ok; ++k) {
         const int w = fetch_item(k, false, false);   // lane 0 alone
@@ -430,56 +438,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; ok && j <= n; ++j) {
           const uint32_t nk = N + 2 * j, nv = N + 2 * j - 1;   // ring items K_j and V_{j-1}
+          bool k_ready = false, v_ready = false;
           for (int x = 0; x < 2 && ok; ++x) {
-            if (j >= 1) {
+            const int nx = x ? n : it.n_a;             // tiles this sub-tile uses
+            if (j >= 1 && j - 1 < nx) {
               // O_x += P_x(j-1) . V_{j-1}, P as the pair hi + lo
               if (aborted(abort_flag) ||
-                  !mbar_wait(&bars[kBarPReady + x], (T + j - 1) & 1) ||
-                  (x == 0 && !mbar_wait(&bars[kBarFull + nv % kSlots], (nv / kSlots) & 1)) ||
+                  !mbar_wait(&bars[kBarPReady + 2 * x], (Ts[x] + j - 1) & 1) ||
+                  (!v_ready && !mbar_wait(&bars[kBarFull + nv % kSlots], (nv / kSlots) & 1)) ||
                   (j == 1 && V > 0 && !mbar_wait(&bars[kBarOFree + x], (V - 1) & 1))) {
                 ok = false;
                 break;
               }
+              v_ready = true;
               tc_fence_after();
-              const uint32_t v_base = ring + (uint32_t)((nv % kSlots) * kSlot);
+              const uint64_t vd = dv0 + (uint64_t)(((nv % kSlots) * kSlot) >> 4);
               const uint32_t p_col = tmem + kColS + 128u * x;
               const uint32_t o_col = tmem + kColO + 128u * x;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
+                if (kk == 4) {
+                  // keys 64..127: wait for the second half of P
+                  if (!mbar_wait(&bars[kBarPReady + 2 * x + 1], (Ts[x] + j - 1) & 1)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                }
                 // keys 16kk .. 16kk+15: P hi at columns 32(kk/2) + 8(kk%2), lo 16 further
                 const uint32_t pc = p_col + 32u * (kk >> 1) + 8u * (kk & 1);
-                const uint64_t bd = sdesc(v_base + kk * 2048, kHalf, 1024);
+                const uint64_t bd = vd + (uint64_t)((kk * 2048) >> 4);
                 mma_ts(o_col, pc, bd, kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
                 mma_ts(o_col, pc + 16u, bd, kIdescPV, 1u);
               }
+              if (!ok) break;
               mma_commit(&bars[kBarODone + x]);
-              if (x == 1) mma_commit(&bars[kBarEmpty + nv % kSlots]);
             }
-            if (j < n) {
+            if (x == 1 && j >= 1) mma_commit(&bars[kBarEmpty + nv % kSlots]);
+            if (j < nx) {
               // S_x = Q_x . K_j^T
               if (aborted(abort_flag) ||
-                  (x == 0 && !mbar_wait(&bars[kBarFull + nk % kSlots], (nk / kSlots) & 1))) {
+                  (!k_ready && !mbar_wait(&bars[kBarFull + nk % kSlots], (nk / kSlots) & 1))) {
                 ok = false;
                 break;
               }
+              k_ready = true;
               tc_fence_after();
-              const uint32_t k_base = ring + (uint32_t)((nk % kSlots) * kSlot);
-              const uint32_t qx = q_base + (uint32_t)(x * kQSub);
+              const uint64_t kd = dring + (uint64_t)(((nk % kSlots) * kSlot) >> 4);
+              const uint64_t qd = dq0 + (uint64_t)((x * kQSub) >> 4);
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
-                const uint32_t off = (uint32_t)((k >> 2) * kHalf + (k & 3) * 32);
-                mma_ss(tmem + kColS + 128u * x, sdesc(qx + off, 16, 1024),
-                       sdesc(k_base + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+                const uint64_t off = (uint64_t)(((k >> 2) * kHalf + (k & 3) * 32) >> 4);
+                mma_ss(tmem + kColS + 128u * x, qd + off, kd + off, kIdescQK, k > 0 ? 1u : 0u);
               }
               mma_commit(&bars[kBarSFull + x]);
-              if (x == 1) {
-                mma_commit(&bars[kBarEmpty + nk % kSlots]);
-                if (j == n - 1) mma_commit(&bars[kBarQFree]);   // Q no longer read
-              }
+            }
+            if (x == 1 && j < n) {
+              mma_commit(&bars[kBarEmpty + nk % kSlots]);
+              if (j == n - 1) mma_commit(&bars[kBarQFree]);   // Q no longer read
             }
           }
         }
-        T += (uint32_t)n;
+        Ts[0] += (uint32_t)it.n_a;
+        Ts[1] += (uint32_t)n;
         N += 2u * (uint32_t)n;
         V += 1;
       }
@@ -519,9 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int64_t pos = it.cached + it.q0 + tsub;   // this row's absolute position
     const int64_t min_pos = it.cached + it.q0 + x * kSubTok;
+    const int nx = x ? it.n_tiles : it.n_a;          // key tiles this sub-tile uses
     float m = -INFINITY;
     float2 la = make_float2(0.f, 0.f), lb = la;      // independent partial sums
-    for (int j = 0; j < it.n_tiles; ++j) {
+    for (int j = 0; j < nx; ++j) {
       if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + x], (T + j) & 1)) {
         ok = false;
         break;
@@ -596,15 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st16(s_col + 32u * c, wh);
         tmem_st16(s_col + 32u * c + 16u, wl);
+        if (c & 1) {
+          // keys 64 (c >> 1) .. +63 of P are in TMEM: let the MMA issuer use them
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kBarPReady + 2 * x + (c >> 1)]);
+        }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarPReady + x]);
     }
     if (!ok) break;
     // ---- epilogue: O / l -> bf16, then hand O_x back to the MMA issuer
-    if (!mbar_wait(&bars[kBarODone + x], (T + it.n_tiles - 1) & 1)) {
+    if (!mbar_wait(&bars[kBarODone + x], (T + nx - 1) & 1)) {
       ok = false;
       break;
     }
@@ -633,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kBarOFree + x]);
-    T += (uint32_t)it.n_tiles;
+    T += (uint32_t)nx;
   }
   if (!ok && lane == 0) {
     *abort_flag = 1;
