@@ -15,6 +15,10 @@ Also printed, in the same JSON line:
   e2e           -- the same metric through the C ABI with the step's inputs in
                    pinned host memory (H2D copies and the D2H of the outputs timed);
   extend        -- extend attention TFLOP/s on the 8-request extend batch;
+  small_batch_graph -- an 8-request x 28-layer decode step, eager vs CUDA-graph replay;
+  large_decode  -- 256 decode requests, page_size 16, pools at 90% of free HBM;
+  long_mixed    -- 32 long decodes + 2 extends (page_size 64): each part alone and
+                   the mixed call against the max() and sum() of the two bounds;
   cpu_baseline  -- the fp64 oracle on the host cores, on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -284,6 +288,8 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     R, L = spec.num_reqs, args.layers
     extend = run_extend(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     small = run_graph_decode(args, dev, msg) if rank == 0 and not args.no_extend else None
+    large = run_large_decode(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
+    mixed = run_long_mixed(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     cpu = cpu_baseline(spec) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     line = {
@@ -312,6 +318,10 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
         line["extend"] = extend
     if small is not None:
         line["small_batch_graph"] = small
+    if large is not None:
+        line["large_decode"] = large
+    if mixed is not None:
+        line["long_mixed"] = mixed
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
@@ -427,6 +437,140 @@ def run_extend(args, dev, msg, peaks):
             "l2": "flushed (256 MB write) before every timed launch"}
 
 
+
+def _planned_batch(spec, dev, msg, sel=None):
+    """Device copies of a batch's metadata, planned once (qo_indptr, out_loc).
+    sel (a contiguous range of request indices) makes a sub-batch of the same
+    page table: its requests' tokens are rows tok[0]:tok[1] of the full q."""
+    import torch
+    sel = np.arange(spec.num_reqs) if sel is None else np.asarray(sel)
+    qo_full = np.concatenate([[0], np.cumsum(spec.extend_len)])
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    ext = spec.extend_len[sel]
+    T = int(ext.sum())
+    b = {"pt": i32(spec.page_table), "cached": i32(spec.cached_len[sel]), "ext": i32(ext),
+         "rows": i32(spec.req_rows[sel]), "T": T, "R": len(sel),
+         "tok": (int(qo_full[sel[0]]), int(qo_full[sel[0]]) + T),
+         "qo": torch.zeros(len(sel) + 1, dtype=torch.int32, device=dev),
+         "loc": torch.zeros(T, dtype=torch.int64, device=dev),
+         "ws": torch.zeros(msg.msg_workspace_size(len(sel), T), dtype=torch.uint8, device=dev)}
+    msg.msg_plan(b["pt"], b["cached"], b["ext"], T, spec.num_slots, b["ws"],
+                 req_rows=b["rows"], qo_indptr_out=b["qo"], out_loc_out=b["loc"])
+    return b
+
+
+def _median_launch_ms(fn, n, flush=None):
+    """Median CUDA-event time of fn over n launches after 3 warm-ups; the L2
+    flush (if any) is written before each timed launch, outside the events."""
+    import torch
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        if flush is not None:
+            flush.zero_()
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def _attn_call(msg, spec, t, b, out, flags):
+    t0, t1 = b["tok"]
+    q, o = t["q"][t0:t1], out[t0:t1]
+
+    def call():
+        msg.msg_paged_attention(q, t["k_pool"], t["v_pool"], b["pt"], b["cached"], b["ext"],
+                                b["qo"], o, b["ws"], page_size=spec.page_size,
+                                req_rows=b["rows"], max_kv_len=spec.max_kv_len, flags=flags)
+    return call
+
+
+def _check_status(msg, b, what):
+    st, info = msg.msg_read_device_status(b["ws"])
+    if st != msg.MSG_OK:
+        raise RuntimeError(f"{what}: device status {info}")
+
+
+def run_large_decode(args, dev, msg, peaks):
+    """256 decode requests, context U[1024, 8192], page_size 16, pools sized to
+    90% of free HBM with the pages drawn at random from the whole pool."""
+    import torch
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info()
+    pages = int(0.9 * free) // (2 * 16 * KV_ROW)
+    spec = wl.config_large_decode(pages)
+    t = wl.device_tensors(spec, device=dev, canary=False)
+    b = _planned_batch(spec, dev, msg)
+    msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], b["loc"])
+    out = torch.empty_like(t["q"])
+    attn = _attn_call(msg, spec, t, b, out,
+                      msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_DECODE_ONLY)
+    ms = _median_launch_ms(attn, max(args.steps, 20))
+    _check_status(msg, b, "large decode")
+    by = decode_attn_bytes(spec)
+    gbs = by / (ms * 1e-3) / 1e9
+    del t, b, out
+    torch.cuda.empty_cache()
+    return {"workload": "decode_256req_ctx1024-8192_page16_pool90pct", "gbs": round(gbs, 1),
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "attn_ms": round(ms, 4),
+            "bytes_per_launch": by, "pool_pages": pages,
+            "pool_gb_k_plus_v": round(2 * spec.num_slots * KV_ROW / 1e9, 1),
+            "kv_tokens": int(spec.device_len.sum()),
+            "l2": "inputs larger than L2 (~4.8 GB of K/V per launch)"}
+
+
+def run_long_mixed(args, dev, msg, peaks):
+    """32 decode requests at context 32768 + 2 extend requests of 2048 over 16384
+    cached, page_size 64: decode-only, extend-only and the mixed call, the mixed
+    call against the max() and sum() of the two roofline bounds."""
+    import torch
+    torch.cuda.empty_cache()
+    spec = wl.config_long_mixed()
+    t = wl.device_tensors(spec, device=dev, canary=False)
+    dec = spec.extend_len == 1
+    b = _planned_batch(spec, dev, msg)
+    # the same requests as a decode-only and an extend-only batch (decodes come first)
+    bd = _planned_batch(spec, dev, msg, np.flatnonzero(dec))
+    be = _planned_batch(spec, dev, msg, np.flatnonzero(~dec))
+    msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], b["loc"])
+    out = torch.empty_like(t["q"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    n = max(args.steps, 20)
+    reuse = msg.MSG_ATTN_REUSE_PLAN
+    dec_ms = _median_launch_ms(_attn_call(msg, spec, t, bd, out, reuse | msg.MSG_ATTN_DECODE_ONLY),
+                               n, flush)
+    ext_ms = _median_launch_ms(_attn_call(msg, spec, t, be, out, reuse | msg.MSG_ATTN_EXTEND_ONLY),
+                               n, flush)
+    mix_ms = _median_launch_ms(_attn_call(msg, spec, t, b, out, reuse), n, flush)
+    for x, what in ((b, "long mixed"), (bd, "long mixed, decode part"),
+                    (be, "long mixed, extend part")):
+        _check_status(msg, x, what)
+    pages = (spec.device_len + spec.page_size - 1) // spec.page_size
+    dec_bytes = int((spec.device_len[dec].sum() * 2 * KV_ROW + dec.sum() * 2 * QO_ROW
+                     + pages[dec].sum() * 4))
+    fl = extend_flops(spec)
+    hbm_ms = dec_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+    tc_ms = fl / (peaks["bf16_tflops"] * 1e12) * 1e3
+    del t, b, bd, be, out, flush
+    torch.cuda.empty_cache()
+    return {"workload": "mixed_32dec_ctx32768_2ext2048_cached16384_page64",
+            "decode_only_ms": round(dec_ms, 4),
+            "decode_gbs": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
+            "decode_frac": round(hbm_ms / dec_ms, 4),
+            "extend_only_ms": round(ext_ms, 4),
+            "extend_tflops": round(fl / (ext_ms * 1e-3) / 1e12, 1),
+            "extend_frac": round(tc_ms / ext_ms, 4),
+            "mixed_ms": round(mix_ms, 4), "bound_max_ms": round(max(hbm_ms, tc_ms), 4),
+            "bound_sum_ms": round(hbm_ms + tc_ms, 4),
+            "mixed_frac_of_max_bound": round(max(hbm_ms, tc_ms) / mix_ms, 4),
+            "mixed_frac_of_sum_bound": round((hbm_ms + tc_ms) / mix_ms, 4),
+            "decode_bytes": dec_bytes, "extend_flops": fl,
+            "l2": "flushed (256 MB write) before every timed launch"}
+
 # ------------------------------------------------------------ CPU oracle baseline
 def oracle_layer_inputs(spec, layer):
     """Host copies of one layer's inputs for the oracle (all requests, compacted)."""
@@ -499,10 +643,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--no-extend", action="store_true", help="skip the extend sub-benchmark")
+    ap.add_argument("--no-extend", action="store_true",
+                    help="skip the sub-benchmarks (extend, graph, large decode, mixed)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--extend-only", action="store_true",
                     help="run only the extend sub-benchmark and print its JSON (profiling)")
+    ap.add_argument("--only", choices=["extend", "graph", "large", "mixed"], default=None,
+                    help="run only one sub-benchmark and print its JSON (profiling)")
     ap.add_argument("--layers", type=int, default=28,
                     help="layers per step (28 for the benchmark; fewer only for profiling)")
     args = ap.parse_args()
@@ -515,12 +662,19 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
     if args.extend_only:
+        args.only = "extend"
+    if args.only:
         import torch
         import paged_kv_gqa_store_gb300 as msg
         msg.load_library()
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
         torch.cuda.set_device(dev)
-        print(json.dumps(run_extend(args, dev, msg, measured_peaks())), flush=True)
+        peaks = measured_peaks()
+        legs = {"extend": lambda: run_extend(args, dev, msg, peaks),
+                "graph": lambda: run_graph_decode(args, dev, msg),
+                "large": lambda: run_large_decode(args, dev, msg, peaks),
+                "mixed": lambda: run_long_mixed(args, dev, msg, peaks)}
+        print(json.dumps(legs[args.only]()), flush=True)
         return
     dist = None
     if world > 1:

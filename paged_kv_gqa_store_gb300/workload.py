@@ -220,11 +220,13 @@ def torch_to_bits(t) -> np.ndarray:
 
 
 def device_tensors(spec: BatchSpec, layer: int = 0, device="cuda", pools=True,
-                   chunk_rows: int = 1 << 16) -> dict:
+                   chunk_rows: int = 1 << 16, canary: bool = True) -> dict:
     """Inputs for one layer generated directly on the GPU (large configs): q and
     the new k/v as N(0,1) bf16, and (if pools) K/V pools filled with the canary
     except the cached prefixes, which get N(0,1) bf16 rows.  Values come from
-    torch's CUDA generator seeded by (seed, layer); nothing of the method runs."""
+    torch's CUDA generator seeded by (seed, layer); nothing of the method runs.
+    With canary=False the unused slots are left uninitialised (timing only: no
+    slot outside the prefixes and the new tokens is ever read)."""
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(int(spec.seed) * 1009 + layer)
@@ -236,10 +238,14 @@ def device_tensors(spec: BatchSpec, layer: int = 0, device="cuda", pools=True,
 
     out = {"q": randn(T, H, D), "k_new": randn(T, Hk, D), "v_new": randn(T, Hk, D)}
     if pools:
-        canary = torch.tensor([CANARY_BF16], dtype=torch.int32).to(torch.int16).view(
-            torch.bfloat16).item()
-        kp = torch.full((spec.num_slots, Hk, D), canary, dtype=torch.bfloat16, device=device)
-        vp = torch.full((spec.num_slots, Hk, D), canary, dtype=torch.bfloat16, device=device)
+        if canary:
+            fill = torch.tensor([CANARY_BF16], dtype=torch.int32).to(torch.int16).view(
+                torch.bfloat16).item()
+            kp = torch.full((spec.num_slots, Hk, D), fill, dtype=torch.bfloat16, device=device)
+            vp = torch.full((spec.num_slots, Hk, D), fill, dtype=torch.bfloat16, device=device)
+        else:
+            kp = torch.empty((spec.num_slots, Hk, D), dtype=torch.bfloat16, device=device)
+            vp = torch.empty((spec.num_slots, Hk, D), dtype=torch.bfloat16, device=device)
         slots = torch.from_numpy(prefix_slots(spec)).to(device)
         for i in range(0, slots.numel(), chunk_rows):
             idx = slots[i:i + chunk_rows]
