@@ -348,16 +348,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = load_item(p, w);
       const int64_t row = p.req_rows ? p.req_rows[it.r] : it.r;
       const int32_t *row_ptr = p.page_table + row * p.pt_stride;
+      // Page-table entries of this lane's 4 keys are read one tile ahead of their
+      // use, so their latency hides behind the previous tile's waits.
+      auto read_pt = [&](int j, int32_t (&raw)[4]) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
+          raw[e] = (active && j < it.n_tiles && key < it.kv_end)
+                       ? __ldg(row_ptr + (p.page_size == 1 ? key : (key & ~(int64_t)(p.page_size - 1))))
+                       : 0;
+        }
+      };
+      int32_t cur[4], nxt[4];
+      read_pt(0, cur);
       for (int j = 0; ok && j < it.n_tiles; ++j) {
-        // gather rows of this lane's 4 keys (page-table reads before the waits)
+        read_pt(j + 1, nxt);
+        // gather rows of this lane's 4 keys
         int rk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
           rk[e] = oob;
           if (active && key < it.kv_end) {
-            const int64_t first =
-                __ldg(row_ptr + (p.page_size == 1 ? key : (key & ~(int64_t)(p.page_size - 1))));
+            const int64_t first = cur[e];
             int64_t slot = -1;
             if (p.page_size == 1) {
               if (first >= 0 && first < p.num_slots) slot = first;
@@ -371,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (slot >= 0) rk[e] = (int)(slot * ep.kv_rows_per_slot + 2 * it.gh + half);
           }
+          cur[e] = nxt[e];
         }
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
