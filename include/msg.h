@@ -14,7 +14,9 @@
  *            (the attention operator: GQA by repeat_interleave, scale
  *            1/sqrt(D), causal mask at absolute positions).
  *   [WALK]   "Mini-SGLang 完整剖析": 4.4.3 (KV pool layout, store_kv),
- *            4.6.4 (page table reading per backend), 4.6.5 (cu_seqlens),
+ *            4.6.4 (page table reading per backend: the dense per-request
+ *            page-id table of the FlashAttention / TRT-LLM backends and the
+ *            1-D ragged index list of FlashInfer), 4.6.5 (cu_seqlens),
  *            4.6.7 (store before attend), 4.9.4-4.9.5 (store kernel contract).
  *
  * Conventions shared by every entry point
@@ -74,20 +76,61 @@ extern "C" {
 #define MSG_DEV_OK 0
 #define MSG_DEV_SLOT_OUT_OF_RANGE 1  /* out_loc or page-table slot not in [0, num_slots) */
 #define MSG_DEV_PAGE_MISALIGNED 2    /* page_size > 1 and a page's first slot % page_size != 0 */
-#define MSG_DEV_BAD_LENGTHS 3        /* negative length, device_len > page_table_stride,
+#define MSG_DEV_BAD_LENGTHS 3        /* negative length, a row shorter than device_len,
                                         or qo_indptr inconsistent with extend_len */
 #define MSG_DEV_TIMEOUT 4            /* a bounded wait inside a kernel expired */
 #define MSG_DEV_WRONG_PHASE 5        /* decode-only / extend-only flag contradicted */
 
 /* Flags of msg_paged_attention. */
 #define MSG_ATTN_REUSE_PLAN 1u   /* workspace already holds the plan of this batch
-                                    (made by msg_plan, or by a previous
-                                    msg_paged_attention with the same metadata);
-                                    skip the plan kernel */
+                                    (made by msg_plan / msg_plan_ex, or by a
+                                    previous attention call, with the same
+                                    lengths and the same KV index); skip the
+                                    plan kernel */
 #define MSG_ATTN_DECODE_ONLY 2u  /* every request has extend_len <= 1: skip the
                                     extend kernel launch */
 #define MSG_ATTN_EXTEND_ONLY 4u  /* no request has extend_len == 1: skip the
                                     decode kernel launch */
+
+/*
+ * KV index layouts ([WALK] 4.6.4).  The engine keeps one global, token
+ * granular page table; the attention backends read it in one of three forms:
+ *
+ *   MSG_KV_TOKEN_TABLE  table[row, j] is the pool slot of token j (the global
+ *                       table itself).  With page_size P > 1 only the entry of
+ *                       each page's first token is read (j rounded down to a
+ *                       multiple of P) and must be P-aligned; slot = entry +
+ *                       j % P.  This is what msg_plan / msg_paged_attention use.
+ *   MSG_KV_PAGE_TABLE   table[row, j / P] is a page id (FlashAttention and
+ *                       TRT-LLM: every P-th column of the global table divided
+ *                       by P, a dense [requests, ceil(max_len / P)] table);
+ *                       slot = id * P + j % P.
+ *   MSG_KV_RAGGED       table[indptr[r] + j / P] is a page id (FlashInfer: the
+ *                       per-request lists concatenated in one 1-D array with
+ *                       int32 offsets indptr [num_reqs + 1]; with P = 1 the
+ *                       entries are slots); slot = id * P + j % P.
+ *
+ * Rows of the two table forms are req_rows[r] (NULL = r) and table_stride
+ * entries apart; the ragged form ignores req_rows and table_stride.
+ * table_len (entries of `table`, or -1 if unknown) lets the plan reject rows
+ * or offsets that would leave the array (MSG_DEV_BAD_LENGTHS).  A request of
+ * device_len n needs n entries in its row (token table) or ceil(n / P)
+ * (page-id forms); fewer is MSG_DEV_BAD_LENGTHS, and an entry that names a
+ * slot outside the pool MSG_DEV_SLOT_OUT_OF_RANGE.
+ */
+#define MSG_KV_TOKEN_TABLE 0
+#define MSG_KV_PAGE_TABLE 1
+#define MSG_KV_RAGGED 2
+
+typedef struct msg_kv_index {
+  int32_t kind;              /* MSG_KV_* */
+  int32_t page_size;         /* power of two in [1, 128] */
+  const int32_t *table;      /* device int32 entries */
+  int64_t table_stride;      /* entries between rows (table forms) */
+  int64_t table_len;         /* entries in `table`, or -1 */
+  const int32_t *req_rows;   /* device int32 [num_reqs] or NULL (table forms) */
+  const int32_t *indptr;     /* device int32 [num_reqs + 1] (ragged form) */
+} msg_kv_index;
 
 /* Size in bytes of the device status block (4 x int32: code, request index,
  * low and high 32 bits of the offending value).  It sits at the start of the
@@ -139,6 +182,47 @@ int msg_plan(const int32_t *page_table, int64_t page_table_stride,
              int64_t num_slots, int32_t *qo_indptr_out, void *out_loc_out,
              int32_t out_loc_is_int64, int32_t *positions_out, void *workspace,
              size_t workspace_bytes, void *stream);
+
+/*
+ * a1 with any index layout: as msg_plan, but the slots of out_loc are read
+ * through `kv` (a host pointer to the descriptor; its arrays are device
+ * arrays), including its page size.  msg_plan(page_table, stride, req_rows,
+ * ...) equals msg_plan_ex with {MSG_KV_TOKEN_TABLE, page_size 1, page_table,
+ * stride, -1, req_rows, NULL}.
+ * Errors: as msg_plan, plus MSG_ERR_UNSUPPORTED for an unknown kind or a page
+ * size that is not a power of two in [1, 128].
+ */
+int msg_plan_ex(const msg_kv_index *kv, const int32_t *cached_len,
+                const int32_t *extend_len, int32_t num_reqs, int64_t total_q,
+                int64_t num_slots, int32_t *qo_indptr_out, void *out_loc_out,
+                int32_t out_loc_is_int64, int32_t *positions_out, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * a1, backend metadata ([WALK] 4.6.4): the per-request page-id forms of the
+ * global token table for the requests of a batch.
+ *   kind MSG_KV_PAGE_TABLE: out_table[r, i] = page_table[row_r, i * P] / P for
+ *       i < ceil(device_len_r / P); out_stride entries per row (>= the
+ *       longest row); out_indptr unused (NULL).
+ *   kind MSG_KV_RAGGED: out_indptr[0] = 0, out_indptr[r + 1] = out_indptr[r] +
+ *       ceil(device_len_r / P); out_table[out_indptr[r] + i] = page_table[row_r,
+ *       i * P] / P (the slots themselves when P = 1).  out_capacity bounds the
+ *       entries written; the total needed is reported by MSG_DEV_BAD_LENGTHS
+ *       when it does not fit (nothing is written past out_capacity).
+ * page_table is the global token-granular table (MSG_KV_TOKEN_TABLE form);
+ * device_len_r = cached_len[r] + extend_len[r].  The result serves
+ * msg_plan_ex / msg_paged_attention_ex with the same page size.  A page-start
+ * slot that is negative or not a multiple of P is recorded as
+ * MSG_DEV_SLOT_OUT_OF_RANGE / MSG_DEV_PAGE_MISALIGNED in dev_status (may be
+ * NULL) and written as -1.
+ * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_UNSUPPORTED, MSG_ERR_CUDA.
+ */
+int msg_build_kv_index(int32_t kind, int32_t page_size, const int32_t *page_table,
+                       int64_t page_table_stride, const int32_t *req_rows,
+                       const int32_t *cached_len, const int32_t *extend_len,
+                       int32_t num_reqs, int32_t *out_table, int64_t out_stride,
+                       int64_t out_capacity, int32_t *out_indptr, int32_t *dev_status,
+                       void *stream);
 
 /*
  * a2. store_kv ([WALK] 4.4.3, 4.6.7 step 1; shape contract of 4.9.4):
@@ -200,6 +284,24 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
                         int32_t head_dim, float scale, void *out,
                         void *workspace, size_t workspace_bytes, uint32_t flags,
                         void *stream);
+
+/*
+ * a3-a6 with any index layout: as msg_paged_attention, with the slots of each
+ * request's keys read through `kv` (host pointer to the descriptor, device
+ * arrays; its page_size replaces the page_size argument).
+ * msg_paged_attention(..., page_table, stride, req_rows, ..., page_size, ...)
+ * equals msg_paged_attention_ex with {MSG_KV_TOKEN_TABLE, page_size,
+ * page_table, stride, -1, req_rows, NULL}.
+ * Errors: as msg_paged_attention.
+ */
+int msg_paged_attention_ex(const void *q, int64_t q_row_stride, const void *k_pool,
+                           const void *v_pool, int64_t pool_row_stride, int64_t num_slots,
+                           const msg_kv_index *kv, const int32_t *cached_len,
+                           const int32_t *extend_len, const int32_t *qo_indptr,
+                           int32_t num_reqs, int64_t total_q, int32_t max_kv_len,
+                           int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                           float scale, void *out, void *workspace, size_t workspace_bytes,
+                           uint32_t flags, void *stream);
 
 /*
  * Copy the device status block (a workspace, or a standalone

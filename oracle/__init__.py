@@ -19,6 +19,11 @@ What it computes (each function cites its page and section; see ``oracle.c``):
                            operator).
 * ``complete_one``      -- the request length transition after a forward
                            ("核心数据结构", Req：请求的三个长度).
+* ``build_kv_index``    -- the backends' page-id forms of the global token
+                           table: dense per-request page-id table, ragged
+                           page-id list with offsets ("Mini-SGLang 完整剖析" 4.6.4).
+* ``token_slots``       -- the slot of every token of every request read back
+                           through any of the three index forms (same section).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (worked examples printed on the pages, a brute-force contiguous attention,
@@ -160,6 +165,67 @@ def paged_attention(q, k_pool, v_pool, page_table, cached_len, qo_indptr,
         pt.shape[1], _ptr(rr), _ptr(c), _ptr(qo), c.shape[0], num_qo_heads,
         num_kv_heads, head_dim, float(scale), _ptr(rows), rows.shape[0], _ptr(out))
     return out
+
+
+KV_TOKEN_TABLE, KV_PAGE_TABLE, KV_RAGGED = 0, 1, 2
+
+
+def build_kv_index(kind, page_size, page_table, cached_len, extend_len, req_rows=None):
+    """The backends' form of the global token table for a batch ("Mini-SGLang
+    完整剖析" 4.6.4): the global table stores one slot per token; the
+    FlashAttention / TRT-LLM backends take every page_size-th column and divide
+    it by page_size (a dense [requests, pages] table of page ids), FlashInfer
+    concatenates the per-request lists into one 1-D array with offsets.
+
+    Returns a list of per-request page-id lists (plain Python ints), and, for
+    the two kinds, the dense table (padded with -1) or (indices, indptr)."""
+    P = int(page_size)
+    pages = []
+    for r in range(len(cached_len)):
+        row = r if req_rows is None else int(req_rows[r])
+        n = int(cached_len[r]) + int(extend_len[r])
+        ids = []
+        for i in range((n + P - 1) // P):
+            first = int(page_table[row][i * P])
+            ids.append(first // P)
+        pages.append(ids)
+    if kind == KV_PAGE_TABLE:
+        width = max([len(x) for x in pages] + [1])
+        table = np.full((len(pages), width), -1, np.int32)
+        for r, ids in enumerate(pages):
+            table[r, :len(ids)] = ids
+        return pages, table
+    indptr = [0]
+    flat = []
+    for ids in pages:
+        flat.extend(ids)
+        indptr.append(len(flat))
+    return pages, (np.array(flat, np.int32), np.array(indptr, np.int32))
+
+
+def token_slots(kind, page_size, table, kv_len, req_rows=None, indptr=None):
+    """Slot of token j of request r for j < kv_len[r], read through an index of
+    the given kind ("Mini-SGLang 完整剖析" 4.6.4):
+      token table : table[row_r][j]                     (every token's own entry)
+      page table  : table[row_r][j // P] * P + j % P
+      ragged      : table[indptr[r] + j // P] * P + j % P
+    Returns an int32 [num_reqs, max(kv_len)] token table (rows = requests,
+    unused entries -1) that the other oracle functions read with req_rows=None."""
+    P = int(page_size)
+    n_req = len(kv_len)
+    width = max([int(x) for x in kv_len] + [1])
+    out = np.full((n_req, width), -1, np.int64)
+    for r in range(n_req):
+        for j in range(int(kv_len[r])):
+            if kind == KV_TOKEN_TABLE:
+                row = r if req_rows is None else int(req_rows[r])
+                out[r, j] = int(table[row][j])
+            elif kind == KV_PAGE_TABLE:
+                row = r if req_rows is None else int(req_rows[r])
+                out[r, j] = int(table[row][j // P]) * P + j % P
+            else:
+                out[r, j] = int(table[int(indptr[r]) + j // P]) * P + j % P
+    return out.astype(np.int32)
 
 
 def complete_one(cached_len: int, device_len: int) -> tuple[int, int]:

@@ -46,6 +46,43 @@ MSG_ATTN_EXTEND_ONLY = 4
 
 MSG_STATUS_BYTES = 16
 
+MSG_KV_TOKEN_TABLE = 0
+MSG_KV_PAGE_TABLE = 1
+MSG_KV_RAGGED = 2
+
+
+class _KvIndexC(ctypes.Structure):
+    """struct msg_kv_index of include/msg.h."""
+    _fields_ = [("kind", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("table", ctypes.c_void_p), ("table_stride", ctypes.c_int64),
+                ("table_len", ctypes.c_int64), ("req_rows", ctypes.c_void_p),
+                ("indptr", ctypes.c_void_p)]
+
+
+class KvIndex:
+    """Where the pool slot of each token is found (msg_kv_index): the global
+    token table, a dense per-request page-id table, or a ragged page-id list
+    with int32 offsets ``indptr``.  Tensors are int32 CUDA tensors."""
+
+    def __init__(self, kind: int, table, page_size: int = 1, req_rows=None, indptr=None):
+        self.kind, self.table, self.page_size = int(kind), table, int(page_size)
+        self.req_rows, self.indptr = req_rows, indptr
+
+    def c_struct(self) -> _KvIndexC:
+        import torch
+        _expect(self.table, torch.int32, "table")
+        if self.kind == MSG_KV_RAGGED:
+            if self.indptr is None:
+                raise ValueError("a ragged index needs indptr")
+            _expect(self.indptr, torch.int32, "indptr")
+            stride = 0
+        else:
+            if self.table.dim() != 2 or (self.table.numel() and self.table.stride(1) != 1):
+                raise ValueError("a table index is a row-contiguous 2-D tensor")
+            stride = int(self.table.stride(0))
+        return _KvIndexC(self.kind, self.page_size, _ptr(self.table), stride,
+                         int(self.table.numel()), _ptr(self.req_rows), _ptr(self.indptr))
+
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "msg.h")
 LIB_PATH = _build.LIB
@@ -100,6 +137,15 @@ def load_library(path: str | None = None):
         lib.msg_read_device_status.restype = ctypes.c_int
         lib.msg_clear_device_status.argtypes = [P, P]
         lib.msg_clear_device_status.restype = ctypes.c_int
+        KV = ctypes.POINTER(_KvIndexC)
+        lib.msg_plan_ex.argtypes = [KV, P, P, I32, I64, I64, P, P, I32, P, P, SZ, P]
+        lib.msg_plan_ex.restype = ctypes.c_int
+        lib.msg_paged_attention_ex.argtypes = [
+            P, I64, P, P, I64, I64, KV, P, P, P, I32, I64, I32, I32, I32, I32, ctypes.c_float,
+            P, P, SZ, U32, P]
+        lib.msg_paged_attention_ex.restype = ctypes.c_int
+        lib.msg_build_kv_index.argtypes = [I32, I32, P, I64, P, P, P, I32, P, I64, I64, P, P, P]
+        lib.msg_build_kv_index.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -188,6 +234,51 @@ def msg_plan(page_table, cached_len, extend_len, total_q: int, num_slots: int, w
     _check("msg_plan", st)
 
 
+def msg_plan_ex(kv: KvIndex, cached_len, extend_len, total_q: int, num_slots: int, workspace,
+                qo_indptr_out=None, out_loc_out=None, positions_out=None, stream=None) -> None:
+    """msg_plan with the slots read through any KV index layout."""
+    import torch
+    _expect(cached_len, torch.int32, "cached_len")
+    _expect(extend_len, torch.int32, "extend_len")
+    is64 = 0
+    if out_loc_out is not None:
+        if out_loc_out.dtype not in (torch.int32, torch.int64):
+            raise ValueError("out_loc_out must be int32 or int64")
+        is64 = int(out_loc_out.dtype == torch.int64)
+    c = kv.c_struct()
+    st = load_library().msg_plan_ex(
+        ctypes.byref(c), _ptr(cached_len), _ptr(extend_len), int(cached_len.numel()),
+        int(total_q), int(num_slots), _ptr(qo_indptr_out), _ptr(out_loc_out), is64,
+        _ptr(positions_out), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        _stream(stream))
+    _check("msg_plan_ex", st)
+
+
+def msg_build_kv_index(kind: int, page_size: int, page_table, cached_len, extend_len,
+                       out_table, req_rows=None, out_indptr=None, dev_status=None,
+                       stream=None) -> None:
+    """Page-id form of the global token table for a batch: a dense table
+    (MSG_KV_PAGE_TABLE, out_table [num_reqs, >= max pages]) or a ragged list
+    (MSG_KV_RAGGED, out_table 1-D, out_indptr [num_reqs + 1])."""
+    import torch
+    for t, n in ((page_table, "page_table"), (cached_len, "cached_len"),
+                 (extend_len, "extend_len"), (out_table, "out_table")):
+        _expect(t, torch.int32, n)
+    if page_table.numel() and page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    if kind == MSG_KV_PAGE_TABLE:
+        if out_table.dim() != 2 or (out_table.numel() and out_table.stride(1) != 1):
+            raise ValueError("out_table is a row-contiguous [num_reqs, width] tensor")
+        out_stride = int(out_table.stride(0))
+    else:
+        out_stride = 0
+    st = load_library().msg_build_kv_index(
+        int(kind), int(page_size), _ptr(page_table), int(page_table.stride(0)), _ptr(req_rows),
+        _ptr(cached_len), _ptr(extend_len), int(cached_len.numel()), _ptr(out_table), out_stride,
+        int(out_table.numel()), _ptr(out_indptr), _ptr(dev_status), _stream(stream))
+    _check("msg_build_kv_index", st)
+
+
 def msg_store_kv(k, v, k_pool, v_pool, out_loc, dev_status=None, stream=None) -> None:
     import torch
     for t, n in ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool")):
@@ -237,6 +328,33 @@ def msg_paged_attention(q, k_pool, v_pool, page_table, cached_len, extend_len, q
     _check("msg_paged_attention", st)
 
 
+def msg_paged_attention_ex(q, k_pool, v_pool, kv: KvIndex, cached_len, extend_len, qo_indptr,
+                           out, workspace, scale: float | None = None, max_kv_len: int = 0,
+                           flags: int = 0, stream=None) -> None:
+    """msg_paged_attention with the keys' slots read through any KV index layout."""
+    import torch
+    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (out, "out")):
+        _expect(t, torch.bfloat16, n)
+    if q.dim() != 3 or k_pool.dim() != 3:
+        raise ValueError("q is [total_q, Hq, D] and the pools are [slots, Hkv, D]")
+    if not out.is_contiguous() or out.shape != q.shape:
+        raise ValueError("out must be contiguous with q's shape")
+    hq, d = int(q.shape[1]), int(q.shape[2])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pst = _row_stride(k_pool, "k_pool")
+    if _row_stride(v_pool, "v_pool") != pst:
+        raise ValueError("k_pool and v_pool must share a row stride")
+    c = kv.c_struct()
+    st = load_library().msg_paged_attention_ex(
+        _ptr(q), _row_stride(q, "q"), _ptr(k_pool), _ptr(v_pool), pst, int(k_pool.shape[0]),
+        ctypes.byref(c), _ptr(cached_len), _ptr(extend_len), _ptr(qo_indptr),
+        int(cached_len.numel()), int(q.shape[0]), int(max_kv_len), hq, int(k_pool.shape[1]), d,
+        float(scale), _ptr(out), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream))
+    _check("msg_paged_attention_ex", st)
+
+
 def msg_read_device_status(dev_status, stream=None) -> tuple[int, list[int]]:
     """Synchronise and read a status block; returns (status, [code, req, lo, hi])."""
     buf = (ctypes.c_int32 * 4)()
@@ -253,7 +371,7 @@ def msg_clear_device_status(dev_status, stream=None) -> None:
 
 
 __all__ = [n for n in dir() if n.startswith(("msg_", "MSG_"))] + [
-    "MsgError", "load_library", "header_functions", "LIB_PATH"]
+    "MsgError", "KvIndex", "load_library", "header_functions", "LIB_PATH"]
 
 
 def msg_paged_attention_noalloc(q, k_pool, v_pool, page_table, cached_len, extend_len,

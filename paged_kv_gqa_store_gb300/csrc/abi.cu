@@ -39,6 +39,103 @@ int check_heads(int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim) {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? MSG_OK : MSG_ERR_CUDA; }
 
+bool pow2_page(int32_t page_size) {
+  return page_size >= 1 && page_size <= 128 && (page_size & (page_size - 1)) == 0;
+}
+
+int32_t log2_page(int32_t page_size) {
+  int32_t shift = 0;
+  while ((1 << shift) < page_size) ++shift;
+  return shift;
+}
+
+KvIndex token_table(const int32_t *page_table, int64_t stride, const int32_t *req_rows,
+                    int32_t page_size) {
+  KvIndex x{};
+  x.table = page_table;
+  x.stride = stride;
+  x.len = -1;
+  x.req_rows = req_rows;
+  x.indptr = nullptr;
+  x.kind = MSG_KV_TOKEN_TABLE;
+  x.page_size = page_size;
+  x.page_shift = log2_page(page_size);
+  return x;
+}
+
+// Validate a caller's msg_kv_index (host struct) into the device-side form.
+int make_kv(const msg_kv_index *kv, KvIndex &x) {
+  if (kv == nullptr) return MSG_ERR_INVALID_ARG;
+  if (kv->kind != MSG_KV_TOKEN_TABLE && kv->kind != MSG_KV_PAGE_TABLE && kv->kind != MSG_KV_RAGGED)
+    return MSG_ERR_UNSUPPORTED;
+  if (!pow2_page(kv->page_size)) return MSG_ERR_UNSUPPORTED;
+  if (kv->kind == MSG_KV_RAGGED ? kv->indptr == nullptr : kv->table_stride < 0)
+    return MSG_ERR_INVALID_ARG;
+  x = token_table(kv->table, kv->kind == MSG_KV_RAGGED ? 0 : kv->table_stride,
+                  kv->kind == MSG_KV_RAGGED ? nullptr : kv->req_rows, kv->page_size);
+  x.kind = kv->kind;
+  x.len = kv->table_len < 0 ? -1 : kv->table_len;
+  x.indptr = kv->kind == MSG_KV_RAGGED ? kv->indptr : nullptr;
+  return MSG_OK;
+}
+
+int plan_impl(const KvIndex &kv, const int32_t *cached_len, const int32_t *extend_len,
+              int32_t num_reqs, int64_t total_q, int64_t num_slots, int32_t *qo_indptr_out,
+              void *out_loc_out, int32_t out_loc_is_int64, int32_t *positions_out,
+              void *workspace, size_t workspace_bytes, void *stream) {
+  if (num_reqs < 0 || total_q < 0 || total_q > INT32_MAX || num_slots < 0)
+    return MSG_ERR_INVALID_ARG;
+  if (workspace == nullptr) return MSG_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(num_reqs, total_q, 0, 0);
+  if (workspace_bytes < L.plan_end) return MSG_ERR_WORKSPACE;
+  if (num_reqs > 0 && (cached_len == nullptr || extend_len == nullptr)) return MSG_ERR_INVALID_ARG;
+  if (total_q > 0 && (out_loc_out || positions_out) && kv.table == nullptr)
+    return MSG_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  PlanParams pp{};
+  pp.kv = kv;
+  pp.cached_len = cached_len;
+  pp.extend_len = extend_len;
+  pp.qo_in = nullptr;
+  pp.num_reqs = num_reqs;
+  pp.total_q = total_q;
+  pp.status = reinterpret_cast<int32_t *>(ws + L.status);
+  pp.hdr = reinterpret_cast<PlanHeader *>(ws + L.header);
+  pp.qo_ws = reinterpret_cast<int32_t *>(ws + L.qo_indptr);
+  pp.qo_out = qo_indptr_out;
+  pp.dec_req = reinterpret_cast<int32_t *>(ws + L.dec_req);
+  pp.dec_start = reinterpret_cast<int64_t *>(ws + L.dec_start);
+  pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
+  pp.max_tiles = L.max_tiles;
+  int rc = from_cuda(launch_plan(pp, s));
+  if (rc != MSG_OK) return rc;
+  if (total_q > 0 && (out_loc_out || positions_out)) {
+    TokenMetaParams tp{};
+    tp.kv = kv;
+    tp.cached_len = cached_len;
+    tp.qo_ws = pp.qo_ws;
+    tp.num_reqs = num_reqs;
+    tp.total_q = total_q;
+    tp.num_slots = num_slots;
+    tp.out_loc = out_loc_out;
+    tp.out_loc_is_int64 = out_loc_is_int64 ? 1 : 0;
+    tp.positions = positions_out;
+    tp.status = pp.status;
+    rc = from_cuda(launch_token_meta(tp, s));
+  }
+  return rc;
+}
+
+int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, const void *v_pool,
+                   int64_t pool_row_stride, int64_t num_slots, const KvIndex &kv,
+                   const int32_t *cached_len, const int32_t *extend_len,
+                   const int32_t *qo_indptr, int32_t num_reqs, int64_t total_q,
+                   int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
+                   int32_t head_dim, float scale, void *out, void *workspace,
+                   size_t workspace_bytes, uint32_t flags, void *stream);
+
 }  // namespace
 
 extern "C" {
@@ -70,52 +167,22 @@ int msg_plan(const int32_t *page_table, int64_t page_table_stride, const int32_t
              int64_t total_q, int64_t num_slots, int32_t *qo_indptr_out, void *out_loc_out,
              int32_t out_loc_is_int64, int32_t *positions_out, void *workspace,
              size_t workspace_bytes, void *stream) {
-  if (num_reqs < 0 || total_q < 0 || total_q > INT32_MAX || page_table_stride < 0 || num_slots < 0)
-    return MSG_ERR_INVALID_ARG;
-  if (workspace == nullptr) return MSG_ERR_WORKSPACE;
-  const WsLayout L = ws_layout(num_reqs, total_q, 0, 0);
-  if (workspace_bytes < L.plan_end) return MSG_ERR_WORKSPACE;
-  if (num_reqs > 0 && (cached_len == nullptr || extend_len == nullptr)) return MSG_ERR_INVALID_ARG;
-  if (total_q > 0 && (out_loc_out || positions_out) && page_table == nullptr)
-    return MSG_ERR_INVALID_ARG;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  PlanParams pp{};
-  pp.req_rows = req_rows;
-  pp.cached_len = cached_len;
-  pp.extend_len = extend_len;
-  pp.qo_in = nullptr;
-  pp.num_reqs = num_reqs;
-  pp.total_q = total_q;
-  pp.pt_stride = page_table_stride;
-  pp.status = reinterpret_cast<int32_t *>(ws + L.status);
-  pp.hdr = reinterpret_cast<PlanHeader *>(ws + L.header);
-  pp.qo_ws = reinterpret_cast<int32_t *>(ws + L.qo_indptr);
-  pp.qo_out = qo_indptr_out;
-  pp.dec_req = reinterpret_cast<int32_t *>(ws + L.dec_req);
-  pp.dec_start = reinterpret_cast<int64_t *>(ws + L.dec_start);
-  pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
-  pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
-  pp.max_tiles = L.max_tiles;
-  int rc = from_cuda(launch_plan(pp, s));
+  if (page_table_stride < 0) return MSG_ERR_INVALID_ARG;
+  return plan_impl(token_table(page_table, page_table_stride, req_rows, 1), cached_len, extend_len,
+                   num_reqs, total_q, num_slots, qo_indptr_out, out_loc_out, out_loc_is_int64,
+                   positions_out, workspace, workspace_bytes, stream);
+}
+
+int msg_plan_ex(const msg_kv_index *kv, const int32_t *cached_len, const int32_t *extend_len,
+                int32_t num_reqs, int64_t total_q, int64_t num_slots, int32_t *qo_indptr_out,
+                void *out_loc_out, int32_t out_loc_is_int64, int32_t *positions_out,
+                void *workspace, size_t workspace_bytes, void *stream) {
+  KvIndex x;
+  const int rc = make_kv(kv, x);
   if (rc != MSG_OK) return rc;
-  if (total_q > 0 && (out_loc_out || positions_out)) {
-    TokenMetaParams tp{};
-    tp.page_table = page_table;
-    tp.pt_stride = page_table_stride;
-    tp.req_rows = req_rows;
-    tp.cached_len = cached_len;
-    tp.qo_ws = pp.qo_ws;
-    tp.num_reqs = num_reqs;
-    tp.total_q = total_q;
-    tp.num_slots = num_slots;
-    tp.out_loc = out_loc_out;
-    tp.out_loc_is_int64 = out_loc_is_int64 ? 1 : 0;
-    tp.positions = positions_out;
-    tp.status = pp.status;
-    rc = from_cuda(launch_token_meta(tp, s));
-  }
-  return rc;
+  return plan_impl(x, cached_len, extend_len, num_reqs, total_q, num_slots, qo_indptr_out,
+                   out_loc_out, out_loc_is_int64, positions_out, workspace, workspace_bytes,
+                   stream);
 }
 
 int msg_store_kv(const void *k, const void *v, int64_t kv_row_stride, void *k_pool, void *v_pool,
@@ -157,17 +224,56 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
                         int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                         float scale, void *out, void *workspace, size_t workspace_bytes,
                         uint32_t flags, void *stream) {
+  const int rc = check_heads(num_qo_heads, num_kv_heads, head_dim);
+  if (rc != MSG_OK) return rc;
+  if (page_table_stride < 0) return MSG_ERR_INVALID_ARG;
+  if (!pow2_page(page_size)) return MSG_ERR_UNSUPPORTED;
+  return attention_impl(q, q_row_stride, k_pool, v_pool, pool_row_stride, num_slots,
+                        token_table(page_table, page_table_stride, req_rows, page_size),
+                        cached_len, extend_len, qo_indptr, num_reqs, total_q, max_kv_len,
+                        num_qo_heads, num_kv_heads, head_dim, scale, out, workspace,
+                        workspace_bytes, flags, stream);
+}
+
+int msg_paged_attention_ex(const void *q, int64_t q_row_stride, const void *k_pool,
+                           const void *v_pool, int64_t pool_row_stride, int64_t num_slots,
+                           const msg_kv_index *kv, const int32_t *cached_len,
+                           const int32_t *extend_len, const int32_t *qo_indptr,
+                           int32_t num_reqs, int64_t total_q, int32_t max_kv_len,
+                           int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                           float scale, void *out, void *workspace, size_t workspace_bytes,
+                           uint32_t flags, void *stream) {
   int rc = check_heads(num_qo_heads, num_kv_heads, head_dim);
   if (rc != MSG_OK) return rc;
+  KvIndex x;
+  rc = make_kv(kv, x);
+  if (rc != MSG_OK) return rc;
+  return attention_impl(q, q_row_stride, k_pool, v_pool, pool_row_stride, num_slots, x,
+                        cached_len, extend_len, qo_indptr, num_reqs, total_q, max_kv_len,
+                        num_qo_heads, num_kv_heads, head_dim, scale, out, workspace,
+                        workspace_bytes, flags, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, const void *v_pool,
+                   int64_t pool_row_stride, int64_t num_slots, const KvIndex &kv,
+                   const int32_t *cached_len, const int32_t *extend_len,
+                   const int32_t *qo_indptr, int32_t num_reqs, int64_t total_q,
+                   int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
+                   int32_t head_dim, float scale, void *out, void *workspace,
+                   size_t workspace_bytes, uint32_t flags, void *stream) {
+  int rc = MSG_OK;
   if (num_reqs < 0 || total_q < 0 || total_q > INT32_MAX || max_kv_len < 0 || num_slots < 0 ||
-      page_table_stride < 0 || !(scale > 0.f) || !isfinite(scale))
+      !(scale > 0.f) || !isfinite(scale))
     return MSG_ERR_INVALID_ARG;
-  if (page_size < 1 || page_size > 128 || (page_size & (page_size - 1))) return MSG_ERR_UNSUPPORTED;
   if ((flags & ~(MSG_ATTN_REUSE_PLAN | MSG_ATTN_DECODE_ONLY | MSG_ATTN_EXTEND_ONLY)) ||
       ((flags & MSG_ATTN_DECODE_ONLY) && (flags & MSG_ATTN_EXTEND_ONLY)))
     return MSG_ERR_INVALID_ARG;
   if (num_reqs == 0 || total_q == 0) return MSG_OK;
-  if (!q || !k_pool || !v_pool || !page_table || !cached_len || !extend_len || !qo_indptr || !out)
+  if (!q || !k_pool || !v_pool || !kv.table || !cached_len || !extend_len || !qo_indptr || !out)
     return MSG_ERR_INVALID_ARG;
   const int64_t row = (int64_t)num_kv_heads * head_dim;
   if (q_row_stride < (int64_t)num_qo_heads * head_dim || pool_row_stride < row)
@@ -185,13 +291,12 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
   int32_t *status = reinterpret_cast<int32_t *>(ws + L.status);
   if (!(flags & MSG_ATTN_REUSE_PLAN)) {
     PlanParams pp{};
-    pp.req_rows = req_rows;
+    pp.kv = kv;
     pp.cached_len = cached_len;
     pp.extend_len = extend_len;
     pp.qo_in = qo_indptr;
     pp.num_reqs = num_reqs;
     pp.total_q = total_q;
-    pp.pt_stride = page_table_stride;
     pp.status = status;
     pp.hdr = reinterpret_cast<PlanHeader *>(ws + L.header);
     pp.qo_ws = reinterpret_cast<int32_t *>(ws + L.qo_indptr);
@@ -212,19 +317,15 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
   ap.v_pool = static_cast<const uint8_t *>(v_pool);
   ap.pool_stride_bytes = pool_row_stride * 2;
   ap.num_slots = num_slots;
-  ap.page_table = page_table;
-  ap.pt_stride = page_table_stride;
-  ap.req_rows = req_rows;
+  ap.kv = kv;
   ap.cached_len = cached_len;
   ap.extend_len = extend_len;
   ap.qo_indptr = qo_indptr;
   ap.num_reqs = num_reqs;
   ap.total_q = total_q;
   ap.flags = flags;
-  ap.page_size = page_size;
-  int shift = 0;
-  while ((1 << shift) < page_size) ++shift;
-  ap.page_shift = shift;
+  ap.page_size = kv.page_size;
+  ap.page_shift = kv.page_shift;
   ap.num_qo_heads = num_qo_heads;
   ap.num_kv_heads = num_kv_heads;
   ap.scale_log2 = scale * 1.4426950408889634f;
@@ -258,6 +359,10 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
   }
   return MSG_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int msg_read_device_status(const void *dev_status, int32_t *host_out, void *stream) {
   if (dev_status == nullptr || host_out == nullptr) return MSG_ERR_INVALID_ARG;

@@ -107,8 +107,7 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
   s.lo = s.S > begin ? s.S : begin;
   s.hi = s.E < end ? s.E : end;
   s.r = p.dec_req[i];
-  const int64_t row = p.req_rows ? p.req_rows[s.r] : s.r;
-  s.row = p.page_table + row * p.pt_stride;
+  s.row = kv_row(p.kv, s.r);
   const int64_t q = p.qo_indptr[s.r];
   s.qrow = (q >= 0 && q < p.total_q) ? (int32_t)q : -1;
   const bool whole = s.S >= begin && s.E <= end;
@@ -119,30 +118,16 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
   return s;
 }
 
-// Raw page-table entry for local key j (page_size 1: the slot; else the page's
-// first slot).  Loaded ahead of use; validated by raw_to_slot.
+// Raw index entry that locates local key j (token table: the page's first
+// slot; page-id forms: the page).  Loaded ahead of use; validated by raw_to_slot.
 __device__ __forceinline__ int32_t load_raw(const AttnParams &p, const int32_t *row, int64_t j) {
-  return __ldg(row + (p.page_size == 1 ? j : (j & ~(int64_t)(p.page_size - 1))));
+  return __ldg(row + kv_entry(p.kv, j));
 }
+// Slot of key j; an invalid entry is reported and redirected to slot 0.
 __device__ __forceinline__ int64_t raw_to_slot(const AttnParams &p, int32_t raw, int64_t j,
                                                int32_t r) {
-  const int64_t first = raw;
-  if (p.page_size == 1) {
-    if (first < 0 || first >= p.num_slots) {
-      report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
-      return 0;
-    }
-    return first;
-  }
-  if (first < 0 || first + p.page_size > p.num_slots) {
-    report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, first);
-    return 0;
-  }
-  if (first & (p.page_size - 1)) {
-    report(p.status, MSG_DEV_PAGE_MISALIGNED, r, first);
-    return 0;
-  }
-  return first + (j & (p.page_size - 1));
+  const int64_t slot = kv_slot(p.kv, raw, j, p.num_slots, p.status, r);
+  return slot < 0 ? 0 : slot;
 }
 
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {

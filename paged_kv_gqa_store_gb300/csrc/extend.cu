@@ -41,6 +41,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace msg {
@@ -346,69 +348,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = fetch_item(k, warp == 1 && lane == 0, true);
       if (w < 0) break;
       const Item it = load_item(p, w);
-      const int64_t row = p.req_rows ? p.req_rows[it.r] : it.r;
-      const int32_t *row_ptr = p.page_table + row * p.pt_stride;
-      // Page-table entries of this lane's 4 keys are read one tile ahead of their
-      // use, so their latency hides behind the previous tile's waits.
-      auto read_pt = [&](int j, int32_t (&raw)[4]) {
+      const int32_t *row_ptr = kv_row(p.kv, it.r);
+      // The tile loop, compiled once for page_size 1 (the entry is the slot in
+      // every index form) and once for larger pages, so that the common case
+      // carries none of the page arithmetic.
+      auto stream_item = [&](auto page1) {
+        constexpr bool kPage1 = decltype(page1)::value;
+        // Index entries of this lane's 4 keys are read one tile ahead of their
+        // use, so their latency hides behind the previous tile's waits.
+        auto read_pt = [&](int j, int32_t (&raw)[4]) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
-          raw[e] = (active && j < it.n_tiles && key < it.kv_end)
-                       ? __ldg(row_ptr + (p.page_size == 1 ? key : (key & ~(int64_t)(p.page_size - 1))))
-                       : 0;
+          for (int e = 0; e < 4; ++e) {
+            const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
+            if (active && j < it.n_tiles && key < it.kv_end)
+              raw[e] = __ldg(row_ptr + (kPage1 ? key : kv_entry(p.kv, key)));
+            else
+              raw[e] = 0;
+          }
+        };
+        int32_t cur[4], nxt[4];
+        read_pt(0, cur);
+        for (int j = 0; ok && j < it.n_tiles; ++j) {
+          read_pt(j + 1, nxt);
+          // gather rows of this lane's 4 keys; an invalid entry (reported once,
+          // by the half-0 lane) reads zeros
+          int rk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
+            rk[e] = oob;
+            if (active && key < it.kv_end) {
+              int64_t slot = -1;
+              if constexpr (kPage1) {
+                const int64_t first = cur[e];
+                if (first >= 0 && first < p.num_slots) slot = first;
+                else if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, it.r, first);
+              } else {
+                slot = kv_slot(p.kv, cur[e], key, p.num_slots, half == 0 ? p.status : nullptr, it.r);
+              }
+              if (slot >= 0) rk[e] = (int)(slot * ep.kv_rows_per_slot + 2 * it.gh + half);
+            }
+            cur[e] = nxt[e];
+          }
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
+            const uint32_t n = N + 2 * j + kv;
+            const int s = n % kSlots;
+            if (n >= (uint32_t)kSlots && !mbar_wait(&bars[kBarEmpty + s], ((n / kSlots) & 1) ^ 1)) {
+              if (lane == 0) {
+                *abort_flag = 1;
+                report(p.status, MSG_DEV_TIMEOUT, it.r, j);
+              }
+              ok = false;
+              break;
+            }
+            if (aborted(abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)n_units * 512u);
+            __syncwarp();
+            if (active)
+              tma_gather4(smem + kOffRing + s * kSlot + half * kHalf + kg4 * 4 * 128,
+                          kv ? &tmap_v : &tmap_k, 0, rk[0], rk[1], rk[2], rk[3], &bars[kBarFull + s]);
+          }
         }
       };
-      int32_t cur[4], nxt[4];
-      read_pt(0, cur);
-      for (int j = 0; ok && j < it.n_tiles; ++j) {
-        read_pt(j + 1, nxt);
-        // gather rows of this lane's 4 keys
-        int rk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int64_t key = (int64_t)j * kBN + kg4 * 4 + e;
-          rk[e] = oob;
-          if (active && key < it.kv_end) {
-            const int64_t first = cur[e];
-            int64_t slot = -1;
-            if (p.page_size == 1) {
-              if (first >= 0 && first < p.num_slots) slot = first;
-              else if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, it.r, first);
-            } else if (first < 0 || first + p.page_size > p.num_slots) {
-              if (half == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, it.r, first);
-            } else if (first & (p.page_size - 1)) {
-              if (half == 0) report(p.status, MSG_DEV_PAGE_MISALIGNED, it.r, first);
-            } else {
-              slot = first + (key & (p.page_size - 1));
-            }
-            if (slot >= 0) rk[e] = (int)(slot * ep.kv_rows_per_slot + 2 * it.gh + half);
-          }
-          cur[e] = nxt[e];
-        }
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
-          const uint32_t n = N + 2 * j + kv;
-          const int s = n % kSlots;
-          if (n >= (uint32_t)kSlots && !mbar_wait(&bars[kBarEmpty + s], ((n / kSlots) & 1) ^ 1)) {
-            if (lane == 0) {
-              *abort_flag = 1;
-              report(p.status, MSG_DEV_TIMEOUT, it.r, j);
-            }
-            ok = false;
-            break;
-          }
-          if (aborted(abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)n_units * 512u);
-          __syncwarp();
-          if (active)
-            tma_gather4(smem + kOffRing + s * kSlot + half * kHalf + kg4 * 4 * 128,
-                        kv ? &tmap_v : &tmap_k, 0, rk[0], rk[1], rk[2], rk[3], &bars[kBarFull + s]);
-        }
-      }
+      if (p.page_size == 1) stream_item(std::true_type{});
+      else stream_item(std::false_type{});
       N += 2u * it.n_tiles;
     }
     // drain: every issued ring item must have landed before the CTA can exit

@@ -74,14 +74,25 @@ inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t
 }
 
 // ------------------------------------------------------------------ params
+// Where the pool slot of token j of a request is found (msg_kv_index).
+struct KvIndex {
+  const int32_t *table;
+  int64_t stride;               // entries between rows (token / page-id tables)
+  int64_t len;                  // entries in table, -1 unknown
+  const int32_t *req_rows;      // row per request (token / page-id tables), null = r
+  const int32_t *indptr;        // ragged: request r's entries at [indptr[r], indptr[r+1])
+  int32_t kind;                 // MSG_KV_*
+  int32_t page_size;
+  int32_t page_shift;           // log2(page_size)
+};
+
 struct PlanParams {
-  const int32_t *req_rows;      // may be null
+  KvIndex kv;                   // row capacities are checked against device_len
   const int32_t *cached_len;
   const int32_t *extend_len;
   const int32_t *qo_in;         // caller's qo_indptr to check, or null
   int32_t num_reqs;
   int64_t total_q;
-  int64_t pt_stride;
   int32_t *status;
   PlanHeader *hdr;
   int32_t *qo_ws;               // plan's qo_indptr
@@ -94,9 +105,7 @@ struct PlanParams {
 };
 
 struct TokenMetaParams {
-  const int32_t *page_table;
-  int64_t pt_stride;
-  const int32_t *req_rows;
+  KvIndex kv;
   const int32_t *cached_len;
   const int32_t *qo_ws;
   int32_t num_reqs;
@@ -130,9 +139,6 @@ struct AttnParams {
   const uint8_t *v_pool;
   int64_t pool_stride_bytes;
   int64_t num_slots;
-  const int32_t *page_table;
-  int64_t pt_stride;
-  const int32_t *req_rows;
   const int32_t *cached_len;
   const int32_t *extend_len;
   const int32_t *qo_indptr;
@@ -153,6 +159,7 @@ struct AttnParams {
   const int32_t *ext_tiles;
   float *part_lse;
   float *part_o;
+  KvIndex kv;                   // where the keys' slots are found
 };
 
 // ------------------------------------------------------------------ launchers
@@ -267,31 +274,44 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Slot of token j of a page-table row: one entry per page (the page's first
-// token) plus the offset inside the page.  Invalid slots are reported and
-// replaced by slot 0 so that no access leaves the pool.
-__device__ __forceinline__ int64_t page_slot(const int32_t *row_ptr, int64_t j, int32_t page_size,
-                                             int32_t page_shift, int64_t num_slots,
-                                             int32_t *status, int32_t req) {
-  if (page_size == 1) {
-    int64_t s = __ldg(row_ptr + j);
-    if (s < 0 || s >= num_slots) {
-      report(status, MSG_DEV_SLOT_OUT_OF_RANGE, req, s);
-      return 0;
+// ---- KV index layouts ("Mini-SGLang 完整剖析" 4.6.4)
+// Entries of request r: its table row, or its ragged range.
+__device__ __forceinline__ const int32_t *kv_row(const KvIndex &x, int32_t r) {
+  if (x.kind == MSG_KV_RAGGED) return x.table + x.indptr[r];
+  return x.table + (int64_t)(x.req_rows ? x.req_rows[r] : r) * x.stride;
+}
+// Index in the row of the entry that locates token j: the token table holds
+// one entry per token but only page starts are read; the page-id forms hold
+// one entry per page.
+__device__ __forceinline__ int64_t kv_entry(const KvIndex &x, int64_t j) {
+  if (x.page_size == 1) return j;                 // every form: one entry per token
+  return x.kind == MSG_KV_TOKEN_TABLE ? (j & ~(int64_t)(x.page_size - 1)) : (j >> x.page_shift);
+}
+// Entries a row needs for n tokens.
+__device__ __forceinline__ int64_t kv_entries(const KvIndex &x, int64_t n) {
+  return x.kind == MSG_KV_TOKEN_TABLE ? n : (n + x.page_size - 1) >> x.page_shift;
+}
+// Pool slot of token j from the entry e that locates it, or -1 if e names no
+// valid page (recorded in status when `status` is non-null).
+__device__ __forceinline__ int64_t kv_slot(const KvIndex &x, int64_t e, int64_t j, int64_t num_slots,
+                                           int32_t *status, int32_t req) {
+  if (x.page_size == 1) {                          // every form: the entry is the slot
+    if (e < 0 || e >= num_slots) {
+      if (status) report(status, MSG_DEV_SLOT_OUT_OF_RANGE, req, e);
+      return -1;
     }
-    return s;
+    return e;
   }
-  int64_t off = j & (page_size - 1);
-  int64_t first = __ldg(row_ptr + (j - off));
-  if (first < 0 || first + page_size > num_slots) {
-    report(status, MSG_DEV_SLOT_OUT_OF_RANGE, req, first);
-    return 0;
+  const int64_t first = x.kind == MSG_KV_TOKEN_TABLE ? e : e << x.page_shift;
+  if (e < 0 || first + x.page_size > num_slots) {
+    if (status) report(status, MSG_DEV_SLOT_OUT_OF_RANGE, req, e);
+    return -1;
   }
-  if (first & (page_size - 1)) {
-    report(status, MSG_DEV_PAGE_MISALIGNED, req, first);
-    return 0;
+  if (first & (x.page_size - 1)) {
+    if (status) report(status, MSG_DEV_PAGE_MISALIGNED, req, e);
+    return -1;
   }
-  return first + off;
+  return first + (j & (x.page_size - 1));
 }
 
 }  // namespace msg

@@ -5,7 +5,8 @@
 // Batch、Context" (Batch table) and "Engine 与采样器" (手工驱动引擎) define them:
 //   qo_indptr  = exclusive prefix sum of extend_len (ragged concatenation),
 //   positions  = cached_len .. device_len-1 per request,
-//   out_loc    = page_table[row, cached_len .. device_len-1] per request,
+//   out_loc    = the slots of tokens cached_len .. device_len-1 of each request,
+//                through the batch's KV index (token table, page ids, ragged),
 // and the attention plan used by the decode and extend kernels:
 //   - the decode list (requests with extend_len == 1) with the prefix sum of
 //     their KV lengths, over which the decode kernel splits work evenly;
@@ -61,6 +62,18 @@ __device__ __forceinline__ Scan4 block_exclusive_scan(Scan4 x, Scan4 *total, int
   return ex;
 }
 
+// Does request r's row (or ragged range) hold the entries of n tokens, inside
+// the index array when its length is known?
+__device__ __forceinline__ bool row_fits(const KvIndex &x, int32_t r, int64_t n) {
+  const int64_t need = kv_entries(x, n);
+  if (x.kind == MSG_KV_RAGGED) {
+    const int64_t b = x.indptr[r], e = x.indptr[r + 1];
+    return b >= 0 && e - b >= need && (x.len < 0 || e <= x.len);
+  }
+  const int64_t row = x.req_rows ? x.req_rows[r] : r;
+  return row >= 0 && need <= x.stride && (x.len < 0 || (row + 1) * x.stride <= x.len);
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ int64_t warp_sums[32][4];
   __shared__ int64_t carry[4];     // qo, decode count, decode keys, extend tiles
@@ -76,7 +89,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     if (r < p.num_reqs) {
       c = p.cached_len[r];
       e = p.extend_len[r];
-      if (c < 0 || e < 0 || c + e > p.pt_stride) {
+      if (c < 0 || e < 0 || !row_fits(p.kv, r, c + e)) {
         report(p.status, MSG_DEV_BAD_LENGTHS, r, c + e);
         e = 0;
       }
@@ -143,9 +156,8 @@ __global__ void token_meta_kernel(TokenMetaParams p) {
     }
     const int32_t r = lo;
     const int64_t pos = (int64_t)p.cached_len[r] + (t - p.qo_ws[r]);
-    const int64_t row = p.req_rows ? p.req_rows[r] : r;
-    const int64_t slot = p.page_table[row * p.pt_stride + pos];
-    if (slot < 0 || slot >= p.num_slots) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, slot);
+    const int64_t slot = kv_slot(p.kv, kv_row(p.kv, r)[kv_entry(p.kv, pos)], pos, p.num_slots,
+                                 p.status, r);
     if (p.positions) p.positions[t] = (int32_t)pos;
     if (p.out_loc) {
       if (p.out_loc_is_int64) static_cast<int64_t *>(p.out_loc)[t] = slot;

@@ -115,3 +115,49 @@ def test_plan_argument_validation(lib):
         == msg.MSG_ERR_WORKSPACE
     assert lib.msg_plan(P, 32, None, P, P, 4, 4, 10, None, None, 0, None, P, 16, None) \
         == msg.MSG_ERR_WORKSPACE
+
+
+def _kv(**kw):
+    a = dict(kind=msg.MSG_KV_RAGGED, page_size=1, table=FAKE, table_stride=0, table_len=-1,
+             req_rows=None, indptr=FAKE)
+    a.update(kw)
+    return msg._KvIndexC(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kind=3), msg.MSG_ERR_UNSUPPORTED),
+    (dict(page_size=3), msg.MSG_ERR_UNSUPPORTED),
+    (dict(page_size=256), msg.MSG_ERR_UNSUPPORTED),
+    (dict(indptr=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(kind=msg.MSG_KV_PAGE_TABLE, table_stride=-1), msg.MSG_ERR_INVALID_ARG),
+])
+def test_kv_index_validation(lib, kw, status):
+    c = _kv(**kw)
+    assert lib.msg_plan_ex(ctypes.byref(c), FAKE, FAKE, 2, 2, 10, None, None, 0, None, FAKE,
+                           1 << 20, None) == status
+    a = dict(q=FAKE, q_row_stride=2048, k_pool=FAKE, v_pool=FAKE, pool_row_stride=1024,
+             num_slots=100, kv=ctypes.byref(c), cached_len=FAKE, extend_len=FAKE,
+             qo_indptr=FAKE, num_reqs=2, total_q=2, max_kv_len=0, num_qo_heads=16,
+             num_kv_heads=8, head_dim=128, scale=0.088, out=FAKE, workspace=FAKE,
+             workspace_bytes=1 << 30, flags=0, stream=None)
+    assert lib.msg_paged_attention_ex(*a.values()) == status
+
+
+def test_kv_index_null_descriptor(lib):
+    assert lib.msg_plan_ex(None, FAKE, FAKE, 2, 2, 10, None, None, 0, None, FAKE, 1 << 20,
+                           None) == msg.MSG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(kind=msg.MSG_KV_TOKEN_TABLE), msg.MSG_ERR_UNSUPPORTED),
+    (dict(page_size=5), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_reqs=-1), msg.MSG_ERR_INVALID_ARG),
+    (dict(out_indptr=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(num_reqs=0, out_indptr=None, kind=msg.MSG_KV_PAGE_TABLE), msg.MSG_OK),
+])
+def test_build_kv_index_validation(lib, args, status):
+    a = dict(kind=msg.MSG_KV_RAGGED, page_size=16, page_table=FAKE, page_table_stride=64,
+             req_rows=None, cached_len=FAKE, extend_len=FAKE, num_reqs=2, out_table=FAKE,
+             out_stride=0, out_capacity=100, out_indptr=FAKE, dev_status=None, stream=None)
+    a.update(args)
+    assert lib.msg_build_kv_index(*a.values()) == status
