@@ -120,16 +120,27 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
 
 // Raw index entry that locates local key j (token table: the page's first
 // slot; page-id forms: the page).  Loaded ahead of use; validated by raw_to_slot.
+// kPage1: page_size 1, where every index form holds the slot itself.
+template <bool kPage1>
 __device__ __forceinline__ int32_t load_raw(const AttnParams &p, const int32_t *row, int64_t j) {
-  return __ldg(row + kv_entry(p.kv, j));
+  return __ldg(row + (kPage1 ? j : kv_entry(p.kv, j)));
 }
 // Slot of key j; an invalid entry is reported and redirected to slot 0.
+template <bool kPage1>
 __device__ __forceinline__ int64_t raw_to_slot(const AttnParams &p, int32_t raw, int64_t j,
                                                int32_t r) {
+  if (kPage1) {
+    if (raw < 0 || raw >= p.num_slots) {
+      report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, r, raw);
+      return 0;
+    }
+    return raw;
+  }
   const int64_t slot = kv_slot(p.kv, raw, j, p.num_slots, p.status, r);
   return slot < 0 ? 0 : slot;
 }
 
+template <bool kPage1>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   float *pbuf = reinterpret_cast<float *>(smem + (size_t)kStages * kStageBytes);
@@ -177,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
     int32_t raw = 0;
     {
       const int64_t n0 = imin64(kTileKeys, sg.hi - kt);
-      if (lane < n0) raw = load_raw(p, sg.row, kt - sg.S + lane);
+      if (lane < n0) raw = load_raw<kPage1>(p, sg.row, kt - sg.S + lane);
     }
     uint32_t it = 0, issued = 0;
     bool ok = true;
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
           nkt = nsg.lo;
         }
         const int64_t nn = imin64(kTileKeys, nsg.hi - nkt);
-        if (lane < nn) nraw = load_raw(p, nsg.row, nkt - nsg.S + lane);
+        if (lane < nn) nraw = load_raw<kPage1>(p, nsg.row, nkt - nsg.S + lane);
       }
       const int st = it % kStages;
       if (ok && it >= (uint32_t)kStages && !mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1)) {
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
       if (ok) {
         uint8_t *stage = smem + (size_t)st * kStageBytes;
         int64_t slot = 0;
-        if (lane < nkeys) slot = raw_to_slot(p, raw, kt - sg.S + lane, sg.r);
+        if (lane < nkeys) slot = raw_to_slot<kPage1>(p, raw, kt - sg.S + lane, sg.r);
         if (lane == 0) {
           TileHdr *h = reinterpret_cast<TileHdr *>(stage + kOffHdr);
           h->nkeys = nkeys;
@@ -434,11 +445,16 @@ cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  decode_kernel<<<grid, kThreads, kSmem, s>>>(p);
+  if (p.page_size == 1) decode_kernel<true><<<grid, kThreads, kSmem, s>>>(p);
+  else decode_kernel<false><<<grid, kThreads, kSmem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -354,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // carries none of the page arithmetic.
       auto stream_item = [&](auto page1) {
         constexpr bool kPage1 = decltype(page1)::value;
-        // Index entries of this lane's 4 keys are read one tile ahead of their
-        // use, so their latency hides behind the previous tile's waits.
+        // Index entries of this lane's 4 keys are read two tiles ahead of their
+        // use, so their latency hides behind the previous tiles' waits.
         auto read_pt = [&](int j, int32_t (&raw)[4]) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -366,10 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               raw[e] = 0;
           }
         };
-        int32_t cur[4], nxt[4];
+        int32_t cur[4], nxt[4], nxt2[4];
         read_pt(0, cur);
+        read_pt(1, nxt);
         for (int j = 0; ok && j < it.n_tiles; ++j) {
-          read_pt(j + 1, nxt);
+          read_pt(j + 2, nxt2);
           // gather rows of this lane's 4 keys; an invalid entry (reported once,
           // by the half-0 lane) reads zeros
           int rk[4];
@@ -389,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (slot >= 0) rk[e] = (int)(slot * ep.kv_rows_per_slot + 2 * it.gh + half);
             }
             cur[e] = nxt[e];
+            nxt[e] = nxt2[e];
           }
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
