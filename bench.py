@@ -19,6 +19,7 @@ Also printed, in the same JSON line:
   large_decode  -- 256 decode requests, page_size 16, pools at 90% of free HBM;
   long_mixed    -- 32 long decodes + 2 extends (page_size 64): each part alone and
                    the mixed call against the max() and sum() of the two bounds;
+  prologue      -- fused q/k RMSNorm + RoPE + store_kv over the extend batch's tokens;
   cpu_baseline  -- the fp64 oracle on the host cores, on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -290,6 +291,7 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     small = run_graph_decode(args, dev, msg) if rank == 0 and not args.no_extend else None
     large = run_large_decode(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     mixed = run_long_mixed(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
+    prologue = run_prologue(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     cpu = cpu_baseline(spec) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     line = {
@@ -322,6 +324,8 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
         line["large_decode"] = large
     if mixed is not None:
         line["long_mixed"] = mixed
+    if prologue is not None:
+        line["prologue"] = prologue
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
@@ -523,6 +527,49 @@ def run_large_decode(args, dev, msg, peaks):
             "l2": "inputs larger than L2 (~4.8 GB of K/V per launch)"}
 
 
+def prologue_bytes(T: int, max_pos_row_bytes: int = wl.HEAD_DIM * 4) -> int:
+    """Algorithmic bytes of the fused prologue: the qkv rows read, q / K / V
+    written, one cos/sin row, one position and one out_loc per token."""
+    units = wl.HQ + 2 * wl.HKV
+    return int(T * (units * wl.HEAD_DIM * 2 * 2 + max_pos_row_bytes + 4 + 8))
+
+
+def run_prologue(args, dev, msg, peaks):
+    """Fused q/k RMSNorm + RoPE + store_kv over the extend batch's new tokens."""
+    import torch
+    torch.cuda.empty_cache()
+    spec = wl.config_extend()
+    T = spec.total_q
+    b = _planned_batch(spec, dev, msg)
+    positions = torch.zeros(T, dtype=torch.int32, device=dev)
+    msg.msg_plan(b["pt"], b["cached"], b["ext"], T, spec.num_slots, b["ws"], req_rows=b["rows"],
+                 out_loc_out=b["loc"], positions_out=positions)
+    g = torch.Generator(device=dev).manual_seed(4242)
+    qkv = torch.randn(T, wl.HQ + 2 * wl.HKV, wl.HEAD_DIM, generator=g, device=dev).to(
+        torch.bfloat16)
+    qw = (1 + 0.1 * torch.randn(wl.HEAD_DIM, generator=g, device=dev)).to(torch.bfloat16)
+    kw = (1 + 0.1 * torch.randn(wl.HEAD_DIM, generator=g, device=dev)).to(torch.bfloat16)
+    cs = msg.msg_rope_cos_sin_cache(1e6, wl.HEAD_DIM, int(spec.max_kv_len) + 1)
+    q_out = torch.empty(T, wl.HQ, wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    kp = torch.empty(spec.num_slots, wl.HKV, wl.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        msg.msg_qk_norm_rope_store(qkv, positions, qw, kw, 1e-6, cs, q_out, kp, vp, b["loc"],
+                                   wl.HQ, wl.HKV, dev_status=b["ws"])
+
+    ms = _median_launch_ms(call, max(args.steps, 20), flush)
+    _check_status(msg, b, "prologue")
+    by = prologue_bytes(T)
+    gbs = by / (ms * 1e-3) / 1e9
+    del qkv, q_out, kp, vp, flush, b
+    torch.cuda.empty_cache()
+    return {"workload": f"qk_norm_rope_store_{T}tok_16q8kv_d128", "gbs": round(gbs, 1),
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "us": round(ms * 1e3, 2),
+            "bytes_per_launch": by, "l2": "flushed (256 MB write) before every timed launch"}
+
+
 def run_long_mixed(args, dev, msg, peaks):
     """32 decode requests at context 32768 + 2 extend requests of 2048 over 16384
     cached, page_size 64: decode-only, extend-only and the mixed call, the mixed
@@ -648,7 +695,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--extend-only", action="store_true",
                     help="run only the extend sub-benchmark and print its JSON (profiling)")
-    ap.add_argument("--only", choices=["extend", "graph", "large", "mixed"], default=None,
+    ap.add_argument("--only", choices=["extend", "graph", "large", "mixed", "prologue"],
+                    default=None,
                     help="run only one sub-benchmark and print its JSON (profiling)")
     ap.add_argument("--layers", type=int, default=28,
                     help="layers per step (28 for the benchmark; fewer only for profiling)")
@@ -673,7 +721,8 @@ def main():
         legs = {"extend": lambda: run_extend(args, dev, msg, peaks),
                 "graph": lambda: run_graph_decode(args, dev, msg),
                 "large": lambda: run_large_decode(args, dev, msg, peaks),
-                "mixed": lambda: run_long_mixed(args, dev, msg, peaks)}
+                "mixed": lambda: run_long_mixed(args, dev, msg, peaks),
+                "prologue": lambda: run_prologue(args, dev, msg, peaks)}
         print(json.dumps(legs[args.only]()), flush=True)
         return
     dist = None

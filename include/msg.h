@@ -13,7 +13,13 @@
  *   [TINY]   "第 0 步：一个能跑的最小推理引擎": section "这份代码在做什么"
  *            (the attention operator: GQA by repeat_interleave, scale
  *            1/sqrt(D), causal mask at absolute positions).
+ *   [TINY0]  the same page, section "四个算子" (rmsnorm: a scale without mean
+ *            or bias; rope: rotation of the first half against the second
+ *            half of the head; q and k normed before the rotation, Qwen3).
  *   [WALK]   "Mini-SGLang 完整剖析": 4.4.3 (KV pool layout, store_kv),
+ *            4.5.6 (one cos/sin cache of max_position x rotary_dim shared by
+ *            every layer), 4.6.7 (AttentionLayer.forward: q_norm and k_norm
+ *            in place, rotary in place, then store_kv and attention),
  *            4.6.4 (page table reading per backend: the dense per-request
  *            page-id table of the FlashAttention / TRT-LLM backends and the
  *            1-D ragged index list of FlashInfer), 4.6.5 (cu_seqlens),
@@ -80,6 +86,7 @@ extern "C" {
                                         or qo_indptr inconsistent with extend_len */
 #define MSG_DEV_TIMEOUT 4            /* a bounded wait inside a kernel expired */
 #define MSG_DEV_WRONG_PHASE 5        /* decode-only / extend-only flag contradicted */
+#define MSG_DEV_BAD_POSITION 6       /* a position outside the rotary cache */
 
 /* Flags of msg_paged_attention. */
 #define MSG_ATTN_REUSE_PLAN 1u   /* workspace already holds the plan of this batch
@@ -302,6 +309,57 @@ int msg_paged_attention_ex(const void *q, int64_t q_row_stride, const void *k_po
                            int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                            float scale, void *out, void *workspace, size_t workspace_bytes,
                            uint32_t flags, void *stream);
+
+/*
+ * Rotary cos/sin cache ([WALK] 4.5.6; [TINY0] rope): fp32 [max_pos, head_dim],
+ * row p = cos(a_p,0 .. a_p,D/2-1) followed by sin(a_p,0 .. a_p,D/2-1) with
+ *   inv_freq_i = theta^(-2i / D) rounded once to fp32,
+ *   a_p,i      = fp32(p) * inv_freq_i in fp32 (one rounding),
+ *   cos, sin   of that fp32 angle, rounded once to fp32.
+ * Built once per model on the device (double-precision pow / cos / sin), read
+ * by msg_qk_norm_rope_store.  head_dim even, theta > 0, max_pos >= 1.
+ * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_CUDA.
+ */
+int msg_rope_cos_sin_cache(double theta, int32_t head_dim, int64_t max_pos, float *out,
+                           void *stream);
+
+/*
+ * Fused attention prologue ([WALK] 4.6.7; [TINY0] rmsnorm, rope): for token t
+ * of num_tokens, with qkv row t = [q (Hq x D) | k (Hkv x D) | v (Hkv x D)] bf16
+ * as the QKV projection writes it, and p = positions[t]:
+ *   q_out[t, h, :]             = rope(rmsnorm(q[t, h, :], q_norm_w), p)
+ *   k_pool[out_loc[t], g, :]   = rope(rmsnorm(k[t, g, :], k_norm_w), p)
+ *   v_pool[out_loc[t], g, :]   = v[t, g, :]                      (bit copy)
+ * rmsnorm(x, w)_d = w_d * x_d / sqrt(mean_d(x_d^2) + eps);
+ * rope(x, p): x1 = x[0 : D/2], x2 = x[D/2 : D], c = cos_sin[p, 0 : D/2],
+ *   s = cos_sin[p, D/2 : D]; result = [x1 c - x2 s, x1 s + x2 c].
+ * Arithmetic in fp32 from the bf16 inputs, one round-to-nearest-even to bf16
+ * per output.  This is store_kv with the norm and the rotation of K fused in:
+ * the step's K is written to the pool already rotated, and Q lands in q_out
+ * ready for msg_paged_attention (q_out may be qkv itself, same row stride: the
+ * q part is then rotated in place).
+ *
+ * qkv         bf16 rows of (Hq + 2 Hkv) x D values, qkv_row_stride elements apart.
+ * positions   int32 [num_tokens] (from msg_plan), each in [0, max_pos).
+ * q_norm_w, k_norm_w  bf16 [D].
+ * cos_sin     fp32 [max_pos, D] from msg_rope_cos_sin_cache.
+ * q_out       bf16 [num_tokens, Hq, D], rows q_out_row_stride elements apart.
+ * k_pool, v_pool, pool_row_stride, num_slots, out_loc, out_loc_is_int64: as
+ *             msg_store_kv (the slot of token t is out_loc[t]).
+ * dev_status  MSG_STATUS_BYTES block or NULL: a slot outside the pool or a
+ *             position outside the cache is recorded, and that token's K/V
+ *             (resp. its q and K/V) are not written.
+ * Supported: head_dim 128 (other shapes MSG_ERR_UNSUPPORTED); any head counts.
+ * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_UNSUPPORTED, MSG_ERR_ALIGNMENT, MSG_ERR_CUDA.
+ */
+int msg_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, int64_t num_tokens,
+                           const int32_t *positions, const void *q_norm_w,
+                           const void *k_norm_w, float eps, const float *cos_sin,
+                           int64_t max_pos, void *q_out, int64_t q_out_row_stride,
+                           void *k_pool, void *v_pool, int64_t pool_row_stride,
+                           int64_t num_slots, const void *out_loc, int32_t out_loc_is_int64,
+                           int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t *dev_status, void *stream);
 
 /*
  * Copy the device status block (a workspace, or a standalone

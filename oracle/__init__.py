@@ -24,6 +24,10 @@ What it computes (each function cites its page and section; see ``oracle.c``):
                            page-id list with offsets ("Mini-SGLang 完整剖析" 4.6.4).
 * ``token_slots``       -- the slot of every token of every request read back
                            through any of the three index forms (same section).
+* ``rope_cos_sin_cache``, ``rmsnorm``, ``rope``, ``qk_norm_rope`` -- the step
+                           that feeds the path: q_norm / k_norm and the rotary
+                           embedding of the new q and k before store_kv
+                           ("第 0 步" 四个算子; "Mini-SGLang 完整剖析" 4.5.6, 4.6.7).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (worked examples printed on the pages, a brute-force contiguous attention,
@@ -226,6 +230,65 @@ def token_slots(kind, page_size, table, kv_len, req_rows=None, indptr=None):
             else:
                 out[r, j] = int(table[int(indptr[r]) + j // P]) * P + j % P
     return out.astype(np.int32)
+
+
+def rope_cos_sin_cache(theta: float, head_dim: int, max_pos: int) -> np.ndarray:
+    """Rotary cache ("Mini-SGLang 完整剖析" 4.5.6: one [max_position, rotary_dim]
+    table shared by every layer; "第 0 步" rope: inv_freq_i = theta^(-2i/D),
+    angle = pos * inv_freq).  Reading fixed for this library: inv_freq rounded
+    once to fp32, the angle one fp32 product, cos / sin of that angle rounded
+    once to fp32.  Returns float32 [max_pos, D] = [cos | sin]."""
+    half = head_dim // 2
+    inv = np.array([float(theta) ** (-2.0 * i / head_dim) for i in range(half)],
+                   np.float64).astype(np.float32)
+    pos = np.arange(max_pos, dtype=np.float32)
+    angle = (pos[:, None] * inv[None, :]).astype(np.float32)       # one fp32 rounding
+    a = angle.astype(np.float64)
+    return np.concatenate([np.cos(a), np.sin(a)], axis=1).astype(np.float32)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns -> float64 (exact: bf16 is the upper half of a binary32)."""
+    u = np.asarray(bits, np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def rmsnorm(x, w, eps):
+    """RMSNorm over the last axis ("第 0 步" 四个算子: a scale only, no mean or
+    bias): w * x / sqrt(mean(x^2) + eps), in float64."""
+    x = np.asarray(x, np.float64)
+    return np.asarray(w, np.float64) * (x / np.sqrt((x * x).mean(-1, keepdims=True) + eps))
+
+
+def rope(x, cos_sin_rows):
+    """Rotate the first half of the last axis against the second half ("第 0 步"
+    rope, the Hugging Face / Qwen pairing): [x1 c - x2 s, x1 s + x2 c] with c, s
+    the cache row of each leading index; float64."""
+    x = np.asarray(x, np.float64)
+    half = x.shape[-1] // 2
+    cs = np.asarray(cos_sin_rows, np.float64)
+    c, s = cs[..., :half], cs[..., half:]
+    while c.ndim < x.ndim:                        # broadcast over the heads axis
+        c, s = c[..., None, :], s[..., None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)
+
+
+def qk_norm_rope(qkv_bits, positions, q_norm_w_bits, k_norm_w_bits, eps, cos_sin,
+                 num_qo_heads, num_kv_heads, head_dim):
+    """The attention layer's front ("Mini-SGLang 完整剖析" 4.6.7: split qkv, q_norm
+    and k_norm per head, rotary at the batch positions; then store_kv): returns
+    (q float64 [T, Hq, D], k float64 [T, Hkv, D], v bf16 bits [T, Hkv, D])."""
+    T = qkv_bits.shape[0]
+    x = bf16_bits_to_f64(np.asarray(qkv_bits).reshape(T, -1))
+    Hq, Hk, D = num_qo_heads, num_kv_heads, head_dim
+    q = x[:, :Hq * D].reshape(T, Hq, D)
+    k = x[:, Hq * D:(Hq + Hk) * D].reshape(T, Hk, D)
+    v_bits = np.asarray(qkv_bits).reshape(T, -1)[:, (Hq + Hk) * D:(Hq + 2 * Hk) * D]
+    rows = np.asarray(cos_sin)[np.asarray(positions, np.int64)]
+    qn = rope(rmsnorm(q, bf16_bits_to_f64(q_norm_w_bits), eps), rows)
+    kn = rope(rmsnorm(k, bf16_bits_to_f64(k_norm_w_bits), eps), rows)
+    return qn, kn, v_bits.reshape(T, Hk, D).copy()
 
 
 def complete_one(cached_len: int, device_len: int) -> tuple[int, int]:

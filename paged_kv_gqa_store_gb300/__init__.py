@@ -39,6 +39,7 @@ MSG_DEV_PAGE_MISALIGNED = 2
 MSG_DEV_BAD_LENGTHS = 3
 MSG_DEV_TIMEOUT = 4
 MSG_DEV_WRONG_PHASE = 5
+MSG_DEV_BAD_POSITION = 6
 
 MSG_ATTN_REUSE_PLAN = 1
 MSG_ATTN_DECODE_ONLY = 2
@@ -146,6 +147,12 @@ def load_library(path: str | None = None):
         lib.msg_paged_attention_ex.restype = ctypes.c_int
         lib.msg_build_kv_index.argtypes = [I32, I32, P, I64, P, P, P, I32, P, I64, I64, P, P, P]
         lib.msg_build_kv_index.restype = ctypes.c_int
+        lib.msg_rope_cos_sin_cache.argtypes = [ctypes.c_double, I32, I64, P, P]
+        lib.msg_rope_cos_sin_cache.restype = ctypes.c_int
+        lib.msg_qk_norm_rope_store.argtypes = [
+            P, I64, I64, P, P, P, ctypes.c_float, P, I64, P, I64, P, P, I64, I64, P, I32, I32,
+            I32, I32, P, P]
+        lib.msg_qk_norm_rope_store.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -353,6 +360,49 @@ def msg_paged_attention_ex(q, k_pool, v_pool, kv: KvIndex, cached_len, extend_le
         float(scale), _ptr(out), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream))
     _check("msg_paged_attention_ex", st)
+
+
+def msg_rope_cos_sin_cache(theta: float, head_dim: int, max_pos: int, out=None, stream=None):
+    """fp32 [max_pos, head_dim] rotary cache (cos half, then sin half), built on
+    the device; returns `out` (allocated if None)."""
+    import torch
+    if out is None:
+        out = torch.empty(int(max_pos), int(head_dim), dtype=torch.float32, device="cuda")
+    _expect(out, torch.float32, "out")
+    if not out.is_contiguous() or tuple(out.shape) != (int(max_pos), int(head_dim)):
+        raise ValueError("out must be a contiguous [max_pos, head_dim] tensor")
+    _check("msg_rope_cos_sin_cache", load_library().msg_rope_cos_sin_cache(
+        float(theta), int(head_dim), int(max_pos), _ptr(out), _stream(stream)))
+    return out
+
+
+def msg_qk_norm_rope_store(qkv, positions, q_norm_w, k_norm_w, eps: float, cos_sin, q_out,
+                           k_pool, v_pool, out_loc, num_qo_heads: int, num_kv_heads: int,
+                           dev_status=None, stream=None) -> None:
+    """Fused q/k RMSNorm + RoPE + store_kv from the QKV projection output
+    qkv [T, (Hq + 2 Hkv) * D] (or [T, Hq + 2 Hkv, D]); q_out [T, Hq, D] may be
+    a view of qkv's q part (in place)."""
+    import torch
+    for t, n in ((qkv, "qkv"), (q_norm_w, "q_norm_w"), (k_norm_w, "k_norm_w"), (q_out, "q_out"),
+                 (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _expect(t, torch.bfloat16, n)
+    _expect(positions, torch.int32, "positions")
+    _expect(cos_sin, torch.float32, "cos_sin")
+    if out_loc.dtype not in (torch.int32, torch.int64):
+        raise ValueError("out_loc must be int32 or int64")
+    d = int(k_pool.shape[-1])
+    if not cos_sin.is_contiguous() or cos_sin.dim() != 2 or cos_sin.shape[1] != d:
+        raise ValueError("cos_sin must be a contiguous [max_pos, head_dim] tensor")
+    pst = _row_stride(k_pool, "k_pool")
+    if _row_stride(v_pool, "v_pool") != pst:
+        raise ValueError("k_pool and v_pool must share a row stride")
+    st = load_library().msg_qk_norm_rope_store(
+        _ptr(qkv), _row_stride(qkv, "qkv"), int(qkv.shape[0]), _ptr(positions), _ptr(q_norm_w),
+        _ptr(k_norm_w), float(eps), _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(q_out),
+        _row_stride(q_out, "q_out"), _ptr(k_pool), _ptr(v_pool), pst, int(k_pool.shape[0]),
+        _ptr(out_loc), int(out_loc.dtype == torch.int64), int(num_qo_heads), int(num_kv_heads),
+        d, _ptr(dev_status), _stream(stream))
+    _check("msg_qk_norm_rope_store", st)
 
 
 def msg_read_device_status(dev_status, stream=None) -> tuple[int, list[int]]:

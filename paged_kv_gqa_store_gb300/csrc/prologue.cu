@@ -1,0 +1,201 @@
+// prologue.cu -- the step that feeds the path: q_norm / k_norm (RMSNorm per
+// head), rotary embedding, and store_kv of the rotated K and of V, fused into
+// one pass over the QKV projection's output ("Mini-SGLang 完整剖析" 4.6.7,
+// AttentionLayer.forward; "第 0 步：一个能跑的最小推理引擎", 四个算子: rmsnorm is a
+// scale with no mean or bias, rope rotates the first half of a head against
+// the second half, Qwen3 norms q and k before rotating them).
+//
+// One warp per (token, head): lane l holds elements 4l .. 4l+3 of the head, so
+// the rotation partner of each element sits in lane l ^ 16 and the mean of
+// squares is a 5-step butterfly.  Every head row is one coalesced 256-byte
+// read and one 256-byte write; the cos/sin row of the token's position is
+// shared by all its heads through L1.  The rotary cache itself ("Mini-SGLang
+// 完整剖析" 4.5.6) is built once per model by cos_sin_kernel.
+#include <math.h>
+
+#include "internal.cuh"
+
+namespace msg {
+
+namespace {
+
+constexpr int kD = 128;            // head_dim
+constexpr int kHalfD = kD / 2;
+
+struct PrologueParams {
+  const uint16_t *qkv;
+  int64_t qkv_stride;              // elements between token rows
+  int64_t num_tokens;
+  const int32_t *positions;
+  const uint16_t *q_w, *k_w;
+  float eps;
+  const float *cos_sin;
+  int64_t max_pos;
+  uint16_t *q_out;
+  int64_t q_out_stride;
+  uint8_t *k_pool, *v_pool;
+  int64_t pool_stride_bytes;
+  int64_t num_slots;
+  const void *out_loc;
+  int32_t out_loc_is_int64;
+  int32_t hq, hkv;
+  int32_t *status;
+};
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void __launch_bounds__(256) prologue_kernel(PrologueParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t first = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int units = p.hq + p.hkv;                 // q heads, then k heads (each with its v)
+  const int64_t total = p.num_tokens * units;
+  const int ci = 4 * (lane & 15);                 // this lane's index into the cos / sin halves
+  for (int64_t w = first; w < total; w += stride) {
+    const int64_t t = w / units;
+    const int u = (int)(w - t * units);
+    const bool is_q = u < p.hq;
+    const int64_t pos = p.positions[t];
+    if (pos < 0 || pos >= p.max_pos) {
+      if (lane == 0 && u == 0) report(p.status, MSG_DEV_BAD_POSITION, (int32_t)t, pos);
+      continue;
+    }
+    int64_t slot = 0;
+    if (!is_q) {
+      slot = p.out_loc_is_int64 ? static_cast<const int64_t *>(p.out_loc)[t]
+                                : (int64_t) static_cast<const int32_t *>(p.out_loc)[t];
+      if (slot < 0 || slot >= p.num_slots) {
+        if (lane == 0 && u == p.hq) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, (int32_t)t, slot);
+        continue;
+      }
+    }
+    const uint16_t *row = p.qkv + t * p.qkv_stride + (int64_t)u * kD;
+    const uint2 raw = *reinterpret_cast<const uint2 *>(row + 4 * lane);
+    float x[4] = {bf16_lo_f(raw.x), bf16_hi_f(raw.x), bf16_lo_f(raw.y), bf16_hi_f(raw.y)};
+    // RMSNorm: x * w / sqrt(mean(x^2) + eps)
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss * (1.f / kD) + p.eps);
+    const uint2 wr = *reinterpret_cast<const uint2 *>((is_q ? p.q_w : p.k_w) + 4 * lane);
+    const float wt[4] = {bf16_lo_f(wr.x), bf16_hi_f(wr.x), bf16_lo_f(wr.y), bf16_hi_f(wr.y)};
+    float y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = wt[k] * (x[k] * r);
+    // rotation: lanes 0-15 hold x1 (first half), lanes 16-31 x2; partner = lane ^ 16
+    const float4 c = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + ci);
+    const float4 s = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + kHalfD + ci);
+    const float cc[4] = {c.x, c.y, c.z, c.w}, sn[4] = {s.x, s.y, s.z, s.w};
+    float out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float z = __shfl_xor_sync(0xffffffffu, y[k], 16);
+      out[k] = lane < 16 ? y[k] * cc[k] - z * sn[k]      // x1 c - x2 s
+                         : z * sn[k] + y[k] * cc[k];     // x1 s + x2 c
+    }
+    uint2 packed;
+    packed.x = pack_bf16(out[0], out[1]);
+    packed.y = pack_bf16(out[2], out[3]);
+    if (is_q) {
+      *reinterpret_cast<uint2 *>(p.q_out + t * p.q_out_stride + (int64_t)u * kD + 4 * lane) =
+          packed;
+    } else {
+      const int g = u - p.hq;
+      const int64_t off = slot * p.pool_stride_bytes + (int64_t)g * kD * 2 + 8 * lane;
+      *reinterpret_cast<uint2 *>(p.k_pool + off) = packed;
+      // V of the same head: a bit copy
+      const uint2 v = *reinterpret_cast<const uint2 *>(row + (int64_t)p.hkv * kD + 4 * lane);
+      *reinterpret_cast<uint2 *>(p.v_pool + off) = v;
+    }
+  }
+}
+
+// Rotary cache row p: cos of the fp32 angles, then their sin.
+__global__ void cos_sin_kernel(double theta, int32_t d, int64_t max_pos, float *out) {
+  const int32_t half = d / 2;
+  const int64_t n = max_pos * half;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t pos = e / half;
+    const int32_t i = (int32_t)(e - pos * half);
+    const float inv_freq = (float)pow(theta, -2.0 * (double)i / (double)d);
+    const float angle = __fmul_rn((float)pos, inv_freq);
+    out[pos * d + i] = (float)cos((double)angle);
+    out[pos * d + half + i] = (float)sin((double)angle);
+  }
+}
+
+}  // namespace
+
+}  // namespace msg
+
+extern "C" int msg_rope_cos_sin_cache(double theta, int32_t head_dim, int64_t max_pos, float *out,
+                                      void *stream) {
+  using namespace msg;
+  if (!(theta > 0.0) || head_dim <= 0 || (head_dim & 1) || max_pos < 1 || out == nullptr)
+    return MSG_ERR_INVALID_ARG;
+  const int64_t n = max_pos * (head_dim / 2);
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  cos_sin_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(theta, head_dim,
+                                                                                 max_pos, out);
+  return cudaGetLastError() == cudaSuccess ? MSG_OK : MSG_ERR_CUDA;
+}
+
+extern "C" int msg_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, int64_t num_tokens,
+                                      const int32_t *positions, const void *q_norm_w,
+                                      const void *k_norm_w, float eps, const float *cos_sin,
+                                      int64_t max_pos, void *q_out, int64_t q_out_row_stride,
+                                      void *k_pool, void *v_pool, int64_t pool_row_stride,
+                                      int64_t num_slots, const void *out_loc,
+                                      int32_t out_loc_is_int64, int32_t num_qo_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t *dev_status,
+                                      void *stream) {
+  using namespace msg;
+  if (num_tokens < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_pos < 1 ||
+      num_slots < 0 || !(eps >= 0.f) || !isfinite(eps))
+    return MSG_ERR_INVALID_ARG;
+  if (head_dim != kD) return MSG_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MSG_OK;
+  if (!qkv || !positions || !q_norm_w || !k_norm_w || !cos_sin || !q_out || !k_pool || !v_pool ||
+      !out_loc)
+    return MSG_ERR_INVALID_ARG;
+  const int64_t row = (int64_t)(num_qo_heads + 2 * num_kv_heads) * head_dim;
+  if (qkv_row_stride < row || q_out_row_stride < (int64_t)num_qo_heads * head_dim ||
+      pool_row_stride < (int64_t)num_kv_heads * head_dim)
+    return MSG_ERR_INVALID_ARG;
+  auto a16 = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!a16(qkv) || !a16(q_out) || !a16(k_pool) || !a16(v_pool) || !a16(cos_sin) ||
+      !a16(q_norm_w) || !a16(k_norm_w) || qkv_row_stride % 8 || q_out_row_stride % 8 ||
+      pool_row_stride % 8)
+    return MSG_ERR_ALIGNMENT;
+  PrologueParams p{};
+  p.qkv = static_cast<const uint16_t *>(qkv);
+  p.qkv_stride = qkv_row_stride;
+  p.num_tokens = num_tokens;
+  p.positions = positions;
+  p.q_w = static_cast<const uint16_t *>(q_norm_w);
+  p.k_w = static_cast<const uint16_t *>(k_norm_w);
+  p.eps = eps;
+  p.cos_sin = cos_sin;
+  p.max_pos = max_pos;
+  p.q_out = static_cast<uint16_t *>(q_out);
+  p.q_out_stride = q_out_row_stride;
+  p.k_pool = static_cast<uint8_t *>(k_pool);
+  p.v_pool = static_cast<uint8_t *>(v_pool);
+  p.pool_stride_bytes = pool_row_stride * 2;
+  p.num_slots = num_slots;
+  p.out_loc = out_loc;
+  p.out_loc_is_int64 = out_loc_is_int64 ? 1 : 0;
+  p.hq = num_qo_heads;
+  p.hkv = num_kv_heads;
+  p.status = dev_status;
+  const int64_t warps = num_tokens * (num_qo_heads + num_kv_heads);
+  int64_t blocks = (warps + 7) / 8;
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  prologue_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MSG_OK : MSG_ERR_CUDA;
+}

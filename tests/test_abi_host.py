@@ -161,3 +161,36 @@ def test_build_kv_index_validation(lib, args, status):
              out_stride=0, out_capacity=100, out_indptr=FAKE, dev_status=None, stream=None)
     a.update(args)
     assert lib.msg_build_kv_index(*a.values()) == status
+
+
+def _prologue(lib, **kw):
+    a = dict(qkv=FAKE, qkv_row_stride=4096, num_tokens=3, positions=FAKE, q_norm_w=FAKE,
+             k_norm_w=FAKE, eps=1e-6, cos_sin=FAKE, max_pos=100, q_out=FAKE,
+             q_out_row_stride=2048, k_pool=FAKE, v_pool=FAKE, pool_row_stride=1024,
+             num_slots=10, out_loc=FAKE, is64=1, num_qo_heads=16, num_kv_heads=8,
+             head_dim=128, dev_status=None, stream=None)
+    a.update(kw)
+    return lib.msg_qk_norm_rope_store(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_tokens=0), msg.MSG_OK),
+    (dict(num_tokens=-1), msg.MSG_ERR_INVALID_ARG),
+    (dict(head_dim=64, qkv_row_stride=2048, q_out_row_stride=1024, pool_row_stride=512),
+     msg.MSG_ERR_UNSUPPORTED),
+    (dict(qkv_row_stride=4000), msg.MSG_ERR_INVALID_ARG),
+    (dict(eps=-1.0), msg.MSG_ERR_INVALID_ARG),
+    (dict(max_pos=0), msg.MSG_ERR_INVALID_ARG),
+    (dict(positions=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(qkv=FAKE + 8), msg.MSG_ERR_ALIGNMENT),
+    (dict(qkv_row_stride=4100), msg.MSG_ERR_ALIGNMENT),
+])
+def test_prologue_argument_validation(lib, kw, status):
+    assert _prologue(lib, **kw) == status
+
+
+@pytest.mark.parametrize("theta,d,n,status", [
+    (0.0, 128, 10, msg.MSG_ERR_INVALID_ARG), (1e6, 127, 10, msg.MSG_ERR_INVALID_ARG),
+    (1e6, 128, 0, msg.MSG_ERR_INVALID_ARG)])
+def test_rope_cache_argument_validation(lib, theta, d, n, status):
+    assert lib.msg_rope_cos_sin_cache(theta, d, n, FAKE, None) == status
