@@ -5,11 +5,12 @@
 // scale with no mean or bias, rope rotates the first half of a head against
 // the second half, Qwen3 norms q and k before rotating them).
 //
-// One warp per (token, head): lane l holds elements 4l .. 4l+3 of the head, so
-// the rotation partner of each element sits in lane l ^ 16 and the mean of
+// One warp per token: lane l holds elements 4l .. 4l+3 of each head, so the
+// rotation partner of each element sits in lane l ^ 16 and the mean of
 // squares is a 5-step butterfly.  Every head row is one coalesced 256-byte
-// read and one 256-byte write; the cos/sin row of the token's position is
-// shared by all its heads through L1.  The rotary cache itself ("Mini-SGLang
+// read and one 256-byte write; the warp loads 16 head rows before it
+// processes any (4 KB in flight per warp), and reads the token's cos/sin row
+// once for all its heads.  The rotary cache itself ("Mini-SGLang
 // 完整剖析" 4.5.6) is built once per model by cos_sin_kernel.
 #include <math.h>
 
@@ -45,68 +46,78 @@ struct PrologueParams {
 __device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+constexpr int kChunk = 16;         // head rows of a token loaded before any is processed
+
 __global__ void __launch_bounds__(256) prologue_kernel(PrologueParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t first = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int units = p.hq + p.hkv;                 // q heads, then k heads (each with its v)
-  const int64_t total = p.num_tokens * units;
+  const int units = p.hq + 2 * p.hkv;             // q heads, k heads, v heads of a token row
   const int ci = 4 * (lane & 15);                 // this lane's index into the cos / sin halves
-  for (int64_t w = first; w < total; w += stride) {
-    const int64_t t = w / units;
-    const int u = (int)(w - t * units);
-    const bool is_q = u < p.hq;
+  const uint2 qwr = *reinterpret_cast<const uint2 *>(p.q_w + 4 * lane);
+  const uint2 kwr = *reinterpret_cast<const uint2 *>(p.k_w + 4 * lane);
+  const float qw[4] = {bf16_lo_f(qwr.x), bf16_hi_f(qwr.x), bf16_lo_f(qwr.y), bf16_hi_f(qwr.y)};
+  const float kw[4] = {bf16_lo_f(kwr.x), bf16_hi_f(kwr.x), bf16_lo_f(kwr.y), bf16_hi_f(kwr.y)};
+  // one warp per token: all of its head rows, kChunk loads in flight at a time
+  for (int64_t t = first; t < p.num_tokens; t += stride) {
     const int64_t pos = p.positions[t];
     if (pos < 0 || pos >= p.max_pos) {
-      if (lane == 0 && u == 0) report(p.status, MSG_DEV_BAD_POSITION, (int32_t)t, pos);
+      if (lane == 0) report(p.status, MSG_DEV_BAD_POSITION, (int32_t)t, pos);
       continue;
     }
-    int64_t slot = 0;
-    if (!is_q) {
-      slot = p.out_loc_is_int64 ? static_cast<const int64_t *>(p.out_loc)[t]
-                                : (int64_t) static_cast<const int32_t *>(p.out_loc)[t];
-      if (slot < 0 || slot >= p.num_slots) {
-        if (lane == 0 && u == p.hq) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, (int32_t)t, slot);
-        continue;
+    const int64_t slot = p.out_loc_is_int64 ? static_cast<const int64_t *>(p.out_loc)[t]
+                                            : (int64_t) static_cast<const int32_t *>(p.out_loc)[t];
+    const bool slot_ok = slot >= 0 && slot < p.num_slots;
+    if (!slot_ok && lane == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, (int32_t)t, slot);
+    const uint16_t *row = p.qkv + t * p.qkv_stride + 4 * lane;
+    const float4 c4 = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + ci);
+    const float4 s4 = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + kHalfD + ci);
+    const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+    for (int u0 = 0; u0 < units; u0 += kChunk) {
+      uint2 raw[kChunk];
+#pragma unroll
+      for (int k = 0; k < kChunk; ++k)
+        if (u0 + k < units) raw[k] = *reinterpret_cast<const uint2 *>(row + (int64_t)(u0 + k) * kD);
+#pragma unroll
+      for (int k = 0; k < kChunk; ++k) {
+        const int u = u0 + k;
+        if (u >= units) break;
+        if (u >= p.hq + p.hkv) {                  // V: a bit copy
+          if (slot_ok)
+            *reinterpret_cast<uint2 *>(p.v_pool + slot * p.pool_stride_bytes +
+                                       (int64_t)(u - p.hq - p.hkv) * kD * 2 + 8 * lane) = raw[k];
+          continue;
+        }
+        const bool is_q = u < p.hq;
+        if (!is_q && !slot_ok) continue;
+        const float x[4] = {bf16_lo_f(raw[k].x), bf16_hi_f(raw[k].x), bf16_lo_f(raw[k].y),
+                            bf16_hi_f(raw[k].y)};
+        // RMSNorm: x * w / sqrt(mean(x^2) + eps)
+        float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(ss * (1.f / kD) + p.eps);
+        float y[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] = (is_q ? qw[e] : kw[e]) * (x[e] * r);
+        // rotation: lanes 0-15 hold x1 (first half), lanes 16-31 x2; partner = lane ^ 16
+        float out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float z = __shfl_xor_sync(0xffffffffu, y[e], 16);
+          out[e] = lane < 16 ? y[e] * cc[e] - z * sn[e]      // x1 c - x2 s
+                             : z * sn[e] + y[e] * cc[e];     // x1 s + x2 c
+        }
+        uint2 packed;
+        packed.x = pack_bf16(out[0], out[1]);
+        packed.y = pack_bf16(out[2], out[3]);
+        if (is_q)
+          *reinterpret_cast<uint2 *>(p.q_out + t * p.q_out_stride + (int64_t)u * kD + 4 * lane) =
+              packed;
+        else
+          *reinterpret_cast<uint2 *>(p.k_pool + slot * p.pool_stride_bytes +
+                                     (int64_t)(u - p.hq) * kD * 2 + 8 * lane) = packed;
       }
-    }
-    const uint16_t *row = p.qkv + t * p.qkv_stride + (int64_t)u * kD;
-    const uint2 raw = *reinterpret_cast<const uint2 *>(row + 4 * lane);
-    float x[4] = {bf16_lo_f(raw.x), bf16_hi_f(raw.x), bf16_lo_f(raw.y), bf16_hi_f(raw.y)};
-    // RMSNorm: x * w / sqrt(mean(x^2) + eps)
-    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = rsqrtf(ss * (1.f / kD) + p.eps);
-    const uint2 wr = *reinterpret_cast<const uint2 *>((is_q ? p.q_w : p.k_w) + 4 * lane);
-    const float wt[4] = {bf16_lo_f(wr.x), bf16_hi_f(wr.x), bf16_lo_f(wr.y), bf16_hi_f(wr.y)};
-    float y[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) y[k] = wt[k] * (x[k] * r);
-    // rotation: lanes 0-15 hold x1 (first half), lanes 16-31 x2; partner = lane ^ 16
-    const float4 c = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + ci);
-    const float4 s = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + kHalfD + ci);
-    const float cc[4] = {c.x, c.y, c.z, c.w}, sn[4] = {s.x, s.y, s.z, s.w};
-    float out[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float z = __shfl_xor_sync(0xffffffffu, y[k], 16);
-      out[k] = lane < 16 ? y[k] * cc[k] - z * sn[k]      // x1 c - x2 s
-                         : z * sn[k] + y[k] * cc[k];     // x1 s + x2 c
-    }
-    uint2 packed;
-    packed.x = pack_bf16(out[0], out[1]);
-    packed.y = pack_bf16(out[2], out[3]);
-    if (is_q) {
-      *reinterpret_cast<uint2 *>(p.q_out + t * p.q_out_stride + (int64_t)u * kD + 4 * lane) =
-          packed;
-    } else {
-      const int g = u - p.hq;
-      const int64_t off = slot * p.pool_stride_bytes + (int64_t)g * kD * 2 + 8 * lane;
-      *reinterpret_cast<uint2 *>(p.k_pool + off) = packed;
-      // V of the same head: a bit copy
-      const uint2 v = *reinterpret_cast<const uint2 *>(row + (int64_t)p.hkv * kD + 4 * lane);
-      *reinterpret_cast<uint2 *>(p.v_pool + off) = v;
     }
   }
 }
@@ -192,8 +203,7 @@ extern "C" int msg_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, i
   p.hq = num_qo_heads;
   p.hkv = num_kv_heads;
   p.status = dev_status;
-  const int64_t warps = num_tokens * (num_qo_heads + num_kv_heads);
-  int64_t blocks = (warps + 7) / 8;
+  int64_t blocks = (num_tokens + 7) / 8;           // one warp per token
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   prologue_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
