@@ -13,9 +13,10 @@
  *   [TINY]   "第 0 步：一个能跑的最小推理引擎": section "这份代码在做什么"
  *            (the attention operator: GQA by repeat_interleave, scale
  *            1/sqrt(D), causal mask at absolute positions).
- *   [TINY0]  the same page, section "四个算子" (rmsnorm: a scale without mean
- *            or bias; rope: rotation of the first half against the second
- *            half of the head; q and k normed before the rotation, Qwen3).
+ *   [TINY0]  the same page and section, its item "四个算子" (rmsnorm: a
+ *            scale without mean or bias; rope: rotation of the first half
+ *            against the second half of the head; q and k normed before the
+ *            rotation, Qwen3).
  *   [WALK]   "Mini-SGLang 完整剖析": 4.4.3 (KV pool layout, store_kv),
  *            4.5.6 (one cos/sin cache of max_position x rotary_dim shared by
  *            every layer), 4.6.7 (AttentionLayer.forward: q_norm and k_norm
