@@ -106,6 +106,8 @@ int plan_impl(const KvIndex &kv, const int32_t *cached_len, const int32_t *exten
   pp.qo_out = qo_indptr_out;
   pp.dec_req = reinterpret_cast<int32_t *>(ws + L.dec_req);
   pp.dec_start = reinterpret_cast<int64_t *>(ws + L.dec_start);
+  pp.dec_row = reinterpret_cast<int64_t *>(ws + L.dec_row);
+  pp.dec_qrow = reinterpret_cast<int32_t *>(ws + L.dec_qrow);
   pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
   pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
   pp.max_tiles = L.max_tiles;
@@ -303,6 +305,10 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
     pp.qo_out = nullptr;
     pp.dec_req = reinterpret_cast<int32_t *>(ws + L.dec_req);
     pp.dec_start = reinterpret_cast<int64_t *>(ws + L.dec_start);
+    pp.dec_row = reinterpret_cast<int64_t *>(ws + L.dec_row);
+    pp.dec_qrow = reinterpret_cast<int32_t *>(ws + L.dec_qrow);
+  pp.dec_row = reinterpret_cast<int64_t *>(ws + L.dec_row);
+  pp.dec_qrow = reinterpret_cast<int32_t *>(ws + L.dec_qrow);
     pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
     pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
     pp.max_tiles = L.max_tiles;
@@ -334,6 +340,8 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
   ap.hdr = reinterpret_cast<const PlanHeader *>(ws + L.header);
   ap.dec_req = reinterpret_cast<const int32_t *>(ws + L.dec_req);
   ap.dec_start = reinterpret_cast<const int64_t *>(ws + L.dec_start);
+  ap.dec_row = reinterpret_cast<const int64_t *>(ws + L.dec_row);
+  ap.dec_qrow = reinterpret_cast<const int32_t *>(ws + L.dec_qrow);
   ap.counters = reinterpret_cast<int32_t *>(ws + L.counters);
   ap.ext_tiles = reinterpret_cast<const int32_t *>(ws + L.ext_tiles);
   ap.part_lse = reinterpret_cast<float *>(ws + L.part_lse);

@@ -107,8 +107,8 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
   s.lo = s.S > begin ? s.S : begin;
   s.hi = s.E < end ? s.E : end;
   s.r = p.dec_req[i];
-  s.row = kv_row(p.kv, s.r);
-  const int64_t q = p.qo_indptr[s.r];
+  s.row = p.kv.table + p.dec_row[i];
+  const int64_t q = p.dec_qrow[i];
   s.qrow = (q >= 0 && q < p.total_q) ? (int32_t)q : -1;
   const bool whole = s.S >= begin && s.E <= end;
   s.part_slot = whole ? -1 : (int32_t)(2 * b + (s.lo == begin ? 0 : 1));
@@ -174,12 +174,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
 
   if (warp == kWarps) {
     // ------------------------------------------------------------ producer
+    // first request of this CTA's range: the last i with dec_start[i] <= begin,
+    // found by the whole warp 32 entries at a time (2 dependent loads for up
+    // to 1024 decode requests, instead of log2(n))
     int32_t i = 0;
     {
       int32_t lo = 0, hi = nd;   // dec_start[lo] <= begin < dec_start[hi]
       while (hi - lo > 1) {
-        const int32_t mid = (lo + hi) >> 1;
-        if (p.dec_start[mid] <= begin) lo = mid; else hi = mid;
+        const int32_t step = (hi - lo + 31) / 32;
+        const int32_t idx = lo + lane * step;
+        const bool le = idx < hi && p.dec_start[idx] <= begin;
+        const uint32_t m = __ballot_sync(0xffffffffu, le);   // lane 0 always set
+        const int32_t last = 31 - __clz(m);
+        lo = lo + last * step;
+        const int32_t nhi = lo + step;
+        hi = nhi < hi ? nhi : hi;
       }
       i = lo;
     }

@@ -34,6 +34,8 @@ struct WsLayout {
   size_t qo_indptr = 0;    // int32[num_reqs + 1]   (plan's own, checked copy)
   size_t dec_req = 0;      // int32[num_reqs]       decode request list
   size_t dec_start = 0;    // int64[num_reqs + 1]   prefix of decode kv lengths
+  size_t dec_row = 0;      // int64[num_reqs]       index row offset of each decode request
+  size_t dec_qrow = 0;     // int32[num_reqs]       its query row (qo_indptr)
   size_t counters = 0;     // int32[num_reqs * 8]   split merge counters (request, KV head)
   size_t ext_tiles = 0;    // int32x2[max_tiles]    (request, query tile)
   size_t part_lse = 0;     // float[2 * kMaxDecodeCtas * Hq]
@@ -63,6 +65,8 @@ inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t
   L.qo_indptr = take(sizeof(int32_t) * (num_reqs + 1));
   L.dec_req = take(sizeof(int32_t) * (num_reqs + 1));
   L.dec_start = take(sizeof(int64_t) * (num_reqs + 1));
+  L.dec_row = take(sizeof(int64_t) * (num_reqs + 1));
+  L.dec_qrow = take(sizeof(int32_t) * (num_reqs + 1));
   L.counters = take(sizeof(int32_t) * (num_reqs + 1) * kKvHeads);
   L.max_tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + num_reqs + 1;
   L.ext_tiles = take(sizeof(int32_t) * 2 * L.max_tiles);
@@ -99,6 +103,8 @@ struct PlanParams {
   int32_t *qo_out;              // optional user copy
   int32_t *dec_req;
   int64_t *dec_start;
+  int64_t *dec_row;             // offset of the request's row (or ragged range) in the index
+  int32_t *dec_qrow;
   int32_t *counters;
   int32_t *ext_tiles;           // pairs
   int64_t max_tiles;
@@ -155,6 +161,8 @@ struct AttnParams {
   const PlanHeader *hdr;
   const int32_t *dec_req;
   const int64_t *dec_start;
+  const int64_t *dec_row;
+  const int32_t *dec_qrow;
   int32_t *counters;
   const int32_t *ext_tiles;
   float *part_lse;

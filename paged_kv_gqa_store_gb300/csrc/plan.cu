@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
         const int64_t i = carry[1] + ex.v[1];
         p.dec_req[i] = r;
         p.dec_start[i] = carry[2] + ex.v[2];
+        // what the decode kernel needs to start a segment, in one place
+        p.dec_row[i] = kv_row(p.kv, r) - p.kv.table;
+        p.dec_qrow[i] = (int32_t)qo;
       }
       if (is_ext) {
         atomicAdd(&ext_reqs, 1);
