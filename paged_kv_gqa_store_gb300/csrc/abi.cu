@@ -354,7 +354,9 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
       const int64_t want = ((int64_t)num_reqs * max_kv_len + 63) / 64;
       if (want < grid) grid = want > 0 ? want : 1;
     }
-    rc = from_cuda(launch_decode(ap, (int)grid, s));
+    // with a reused plan the decode kernel may start its set-up (which reads
+    // only the plan and the KV index) while the preceding kernel finishes
+    rc = from_cuda(launch_decode(ap, (int)grid, (flags & MSG_ATTN_REUSE_PLAN) != 0, s));
     if (rc != MSG_OK) return rc;
   }
   if (!(flags & MSG_ATTN_DECODE_ONLY)) {

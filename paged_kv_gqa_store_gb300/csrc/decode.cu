@@ -199,6 +199,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
       const int64_t n0 = imin64(kTileKeys, sg.hi - kt);
       if (lane < n0) raw = load_raw<kPage1>(p, sg.row, kt - sg.S + lane);
     }
+    // Everything above reads only the plan and the KV index; K / V (the step's
+    // new rows come from store_kv) and q are read after the preceding kernel.
+    grid_dep_wait();
+    grid_dep_launch();
     uint32_t it = 0, issued = 0;
     bool ok = true;
     while (true) {
@@ -273,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
   }
 
   // -------------------------------------------------------------- consumers
+  grid_dep_wait();      // out, the split partials and the merge counters
   const int gh = warp;                          // KV head
   const int kx = (lane >> 2) & 7, hx = (lane >> 1) & 1;
   const int kl = kx, hl = hx;                   // after the butterfly: this lane's key / head
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
 
 }  // namespace
 
-cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s) {
+cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s) {
   if (p.num_kv_heads != kHkv || p.num_qo_heads != kHq) return cudaErrorInvalidValue;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -462,9 +467,9 @@ cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  if (p.page_size == 1) decode_kernel<true><<<grid, kThreads, kSmem, s>>>(p);
-  else decode_kernel<false><<<grid, kThreads, kSmem, s>>>(p);
-  return cudaGetLastError();
+  if (p.page_size == 1)
+    return launch_k(decode_kernel<true>, dim3(grid), dim3(kThreads), kSmem, s, pdl, p);
+  return launch_k(decode_kernel<false>, dim3(grid), dim3(kThreads), kSmem, s, pdl, p);
 }
 
 int decode_ctas_per_sm() { return 2; }

@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<volatile int32_t *>(smem + kOffBar + kNumBars * 8 + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dep_wait();      // (launched without early start; kept for any launch path)
+  grid_dep_launch();
   const PlanHeader hdr = *p.hdr;
   int32_t *next_ctr = const_cast<int32_t *>(&p.hdr->ext_next);
   // k-th work item of this CTA: grabbed from the global counter by the producer

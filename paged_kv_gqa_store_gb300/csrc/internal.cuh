@@ -171,10 +171,28 @@ struct AttnParams {
 };
 
 // ------------------------------------------------------------------ launchers
+// Launch with an optional programmatic-stream-serialization attribute (see
+// grid_dep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, bool pdl, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 cudaError_t launch_token_meta(const TokenMetaParams &p, cudaStream_t s);
 cudaError_t launch_store_kv(const StoreParams &p, cudaStream_t s);
-cudaError_t launch_decode(const AttnParams &p, int grid, cudaStream_t s);
+cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s);
 int device_sm_count();
 int decode_ctas_per_sm();
@@ -280,6 +298,19 @@ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ?
 // Named barrier over a subset of warps (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---- programmatic dependent launch
+// A kernel launched with launch_k(..., pdl = true) may start while the kernel
+// before it on the stream is still running.  Every such kernel calls
+// grid_dep_wait() before it touches anything the earlier kernels write (and
+// before it writes anything they read), and grid_dep_launch() only after that
+// wait.  So when a kernel starts early, everything launched at least two
+// kernels before it has completed: only data that old (the plan, the KV index)
+// may be read before the wait.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- KV index layouts ("Mini-SGLang 完整剖析" 4.6.4)

@@ -75,6 +75,8 @@ __device__ __forceinline__ bool row_fits(const KvIndex &x, int32_t r, int64_t n)
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+  grid_dep_wait();      // the previous step's kernels still read the plan
+  grid_dep_launch();
   __shared__ int64_t warp_sums[32][4];
   __shared__ int64_t carry[4];     // qo, decode count, decode keys, extend tiles
   __shared__ int32_t ext_reqs;
@@ -148,6 +150,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
 
 // out_loc and positions, one thread per new token.
 __global__ void token_meta_kernel(TokenMetaParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < p.total_q;
        t += (int64_t)gridDim.x * blockDim.x) {
     // request owning token t: last r with qo[r] <= t (empty requests skipped)
@@ -172,8 +176,7 @@ __global__ void token_meta_kernel(TokenMetaParams p) {
 }  // namespace
 
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, true, p);
 }
 
 cudaError_t launch_token_meta(const TokenMetaParams &p, cudaStream_t s) {
@@ -182,8 +185,7 @@ cudaError_t launch_token_meta(const TokenMetaParams &p, cudaStream_t s) {
   int64_t blocks = (p.total_q + threads - 1) / threads;
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  token_meta_kernel<<<(unsigned)blocks, threads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(token_meta_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, true, p);
 }
 
 }  // namespace msg

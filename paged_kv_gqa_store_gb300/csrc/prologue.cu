@@ -49,6 +49,8 @@ __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(
 constexpr int kChunk = 16;         // head rows of a token loaded before any is processed
 
 __global__ void __launch_bounds__(256) prologue_kernel(PrologueParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const int64_t first = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -206,6 +208,8 @@ extern "C" int msg_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, i
   int64_t blocks = (num_tokens + 7) / 8;           // one warp per token
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  prologue_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
-  return cudaGetLastError() == cudaSuccess ? MSG_OK : MSG_ERR_CUDA;
+  return launch_k(prologue_kernel, dim3((unsigned)blocks), dim3(256), 0,
+                  static_cast<cudaStream_t>(stream), true, p) == cudaSuccess
+             ? MSG_OK
+             : MSG_ERR_CUDA;
 }

@@ -30,6 +30,8 @@ __device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
 }
 
 __global__ void __launch_bounds__(kStoreThreads) store_kv_kernel(StoreParams p) {
+  grid_dep_wait();      // k / v come from, and the pools are read by, the kernels around it
+  grid_dep_launch();
   const int64_t per_tok = 2 * (int64_t)p.row_chunks;
   const int64_t total = p.num_tokens * per_tok;
   const int64_t step = (int64_t)gridDim.x * kStoreThreads * kStoreUnroll;
@@ -72,8 +74,7 @@ cudaError_t launch_store_kv(const StoreParams &p, cudaStream_t s) {
   int64_t blocks = (total + kStoreThreads * kStoreUnroll - 1) / (kStoreThreads * kStoreUnroll);
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  store_kv_kernel<<<(unsigned)blocks, kStoreThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(store_kv_kernel, dim3((unsigned)blocks), dim3(kStoreThreads), 0, s, true, p);
 }
 
 }  // namespace msg
