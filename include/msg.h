@@ -53,6 +53,15 @@
  *   qo_indptr[r] is the first token of request r ([CORE] Batch).
  * - Alignment: every bf16 base pointer 16-byte aligned, every row stride a
  *   multiple of 8 elements; otherwise MSG_ERR_ALIGNMENT.
+ * - Early start: the library's kernels are launched with programmatic
+ *   stream serialization, so each may begin while the kernel before it on the
+ *   stream is finishing; it waits for that kernel before touching anything it
+ *   writes or reads.  The one exception is the decode kernel of a call with
+ *   MSG_ATTN_REUSE_PLAN, which reads the plan (workspace) and the KV index
+ *   before that wait: those must not be written by the kernel launched
+ *   immediately before the call unless that kernel completes before it lets
+ *   dependents start (every kernel that does not opt into programmatic
+ *   launch, and every kernel of this library, qualifies).
  * - Errors: entry points return MSG_OK (0) or a negative status before
  *   enqueuing anything; no exception crosses the ABI, nothing aborts and no
  *   kernel traps.  Data-dependent problems found on the device (a slot outside
