@@ -28,9 +28,15 @@ What it computes (each function cites its page and section; see ``oracle.c``):
                            that feeds the path: q_norm / k_norm and the rotary
                            embedding of the new q and k before store_kv
                            ("第 0 步" 四个算子; "Mini-SGLang 完整剖析" 4.5.6, 4.6.7).
+* ``sampling_args``, ``sample_filter``, ``inverse_cdf``, ``sample`` -- the
+                           batched sampler after the forward: temperature,
+                           top-k then top-p, one draw per row from a uniform
+                           passed in ("Engine 与采样器" 采样器; "Mini-SGLang
+                           源码解析（四）" 14).
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(worked examples printed on the pages, a brute-force contiguous attention,
+and its siblings (worked examples printed on the pages, a brute-force
+contiguous attention, a pairwise brute-force sampler filter,
 torch's scaled_dot_product_attention in float64 for the cached_len = 0 case,
 closed forms and invariants).  None is "parity unpinned".
 """
@@ -296,3 +302,101 @@ def complete_one(cached_len: int, device_len: int) -> tuple[int, int]:
     every token of this step is now cached, and the next step computes one more
     position.  Returns the new (cached_len, device_len)."""
     return device_len, device_len + 1
+
+
+# ------------------------------------------------------------------ sampler
+# "Engine 与采样器" (Sampler, sample_torch) and "Mini-SGLang 源码解析（四）"
+# 14.2-14.5, "Mini-SGLang 完整剖析" 4.8.5: the step after the forward in
+# forward_batch turns each request's row of logits into its next token.
+SAMPLE_MIN_T = 1e-6          # smallest temperature (a greedy request in a mixed batch)
+SAMPLE_MIN_P = 1e-6          # smallest top-p
+
+
+def sampling_args(temperature, top_k, top_p, vocab_size):
+    """Per-batch sampling arguments (Sampler.prepare, "Engine 与采样器" 采样器).
+
+    Per request: temperature <= 0 means greedy.  Returns (temperatures,
+    top_k, top_p) as float32 / int32 / float32 arrays or None: temperatures is
+    None when every request is greedy (the sampler then takes the argmax);
+    a greedy request in a mixed batch gets temperature MIN_T; top_k < 1 means
+    the whole vocabulary and the array is None unless some request restricts
+    it; top_p is clamped to [MIN_P, 1] and is None unless some request has
+    top_p < 1."""
+    t = [float(x) for x in temperature]
+    if all(x <= 0.0 for x in t):
+        return None, None, None
+    ts = np.array([max(0.0 if x <= 0.0 else x, SAMPLE_MIN_T) for x in t], np.float32)
+    ks = [int(k) if int(k) >= 1 else int(vocab_size) for k in top_k]
+    ps = [min(max(float(p), SAMPLE_MIN_P), 1.0) for p in top_p]
+    k_arr = np.array(ks, np.int32) if any(k != vocab_size for k in ks) else None
+    p_arr = np.array(ps, np.float32) if any(p < 1.0 for p in ps) else None
+    return ts, k_arr, p_arr
+
+
+def sample_filter(logits_row, temperature, top_k=None, top_p=None):
+    """The distribution one request draws from (sample_torch, "Engine 与采样器";
+    "Mini-SGLang 源码解析（四）" 14.4), float64.
+
+    1. p = softmax(logits / T), T = max(temperature, MIN_T).
+    2. Order the vocabulary by p, largest first; equal p in increasing token
+       index (the pages sort without saying how ties fall: this is the
+       library's reading).
+    3. top-k (k < 1 or k >= V: no cut): ranks >= k get 0.
+    4. top-p (clamped to [MIN_P, 1]): renormalise what is left; a token keeps
+       its mass only if the mass ranked before it is below top_p, so the most
+       likely token always stays (FlashInfer order: top-k first, then top-p).
+    Returns (q, order): q the kept masses renormalised to sum 1, scattered
+    back to vocabulary order; order the ranking of step 2."""
+    T = float(np.float32(max(float(temperature), SAMPLE_MIN_T)))   # a float32 tensor on the pages
+    x = np.asarray(logits_row, np.float64) / T
+    e = np.exp(x - x.max())
+    p = e / e.sum()
+    V = p.shape[0]
+    order = np.argsort(-p, kind="stable")
+    sp = p[order].copy()
+    if top_k is not None:
+        k = int(top_k)
+        if 1 <= k < V:
+            sp[k:] = 0.0
+    P = 1.0 if top_p is None else float(np.float32(min(max(float(top_p), SAMPLE_MIN_P), 1.0)))
+    if P < 1.0:
+        # top_p = 1 cuts nothing: in exact arithmetic the mass before any token
+        # that has mass is below 1 (a rounded cumulative sum reaching 1.0 is not
+        # a cut)
+        sp = sp / sp.sum()
+        before = np.concatenate([[0.0], np.cumsum(sp)[:-1]])
+        sp[before >= P] = 0.0
+    q = np.zeros(V, np.float64)
+    q[order] = sp
+    return q / q.sum(), order
+
+
+def inverse_cdf(q, u):
+    """The draw (torch.multinomial with one sample in sample_torch): with the
+    uniform u in [0, 1) passed in, the token is the smallest index i, in
+    vocabulary order, whose cumulative mass q_0 + ... + q_i exceeds u times
+    the total."""
+    c = np.cumsum(np.asarray(q, np.float64))
+    return int(np.searchsorted(c, float(u) * c[-1], side="right"))
+
+
+def sample(logits, temperatures, top_k, top_p, uniforms):
+    """Batched sampler (Sampler.sample): next token of every row of logits
+    [B, V] (float32 values, or anything float64 holds exactly).
+
+    temperatures None: every request is greedy and the token is the argmax of
+    the row (first index among equal maxima, torch.argmax).  Otherwise each row
+    draws from sample_filter(row, T, k, p) with its uniform.  top_k / top_p
+    None mean no cut for any row.  Returns int32 [B]."""
+    L = np.asarray(logits, np.float64)
+    B = L.shape[0]
+    out = np.empty(B, np.int32)
+    for r in range(B):
+        if temperatures is None:
+            out[r] = int(np.argmax(L[r]))
+            continue
+        q, _ = sample_filter(L[r], temperatures[r],
+                             None if top_k is None else top_k[r],
+                             None if top_p is None else top_p[r])
+        out[r] = inverse_cdf(q, uniforms[r])
+    return out

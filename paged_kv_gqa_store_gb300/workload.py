@@ -292,3 +292,69 @@ def compact_requests(spec: BatchSpec, reqs) -> tuple[BatchSpec, np.ndarray]:
                     num_qo_heads=spec.num_qo_heads, num_kv_heads=spec.num_kv_heads,
                     head_dim=spec.head_dim)
     return sub, src_slots
+
+
+# ------------------------------------------------------------ sampler inputs
+QWEN3_VOCAB = 151936          # Qwen3-0.6B's vocabulary (the model the pages run)
+
+
+@dataclass
+class SamplerSpec:
+    """One batch of logits with each request's raw sampling parameters
+    (temperature <= 0: greedy; top_k < 1: whole vocabulary; top_p: any float)
+    and the uniform each row's draw consumes."""
+    name: str
+    logits: np.ndarray            # float32 [B, V], or bf16 bits uint16 [B, V]
+    is_bf16: bool
+    temperature: np.ndarray       # float32 [B]
+    top_k: np.ndarray             # int32 [B]
+    top_p: np.ndarray             # float32 [B]
+    uniforms: np.ndarray          # float32 [B] in [0, 1)
+
+    @property
+    def batch(self) -> int:
+        return int(self.logits.shape[0])
+
+    @property
+    def vocab(self) -> int:
+        return int(self.logits.shape[1])
+
+    def logits_f64(self) -> np.ndarray:
+        return bf16_bits_to_f64(self.logits) if self.is_bf16 else self.logits.astype(np.float64)
+
+
+_SAMPLER_MIX = (              # (temperature, top_k, top_p) of a request, drawn per row
+    (0.0, -1, 1.0),           # greedy
+    (1.0, -1, 1.0),           # plain draw
+    (0.7, 50, 1.0),
+    (1.0, 20, 0.9),
+    (0.8, -1, 0.95),
+    (1.3, 1000, 0.5),
+    (0.6, 1, 1.0),
+    (1.0, -1, 0.9),
+)
+
+
+def sampler_batch(name: str, seed: int, batch: int, vocab: int, bf16: bool = False,
+                  mix=_SAMPLER_MIX, greedy_only: bool = False) -> SamplerSpec:
+    """Logits shaped like a language model's: N(0, 2^2) per token, plus a few
+    boosted tokens per row (none, 1, 3, 10 or 100 tokens raised by U(2, 12)),
+    so that the top-p nucleus ranges from one token to most of the vocabulary.
+    Rows take their parameters from `mix` in turn (all greedy if
+    greedy_only); uniforms are U[0, 1) in float32."""
+    rng = np.random.default_rng(seed)
+    L = rng.normal(0.0, 2.0, (batch, vocab)).astype(np.float32)
+    for r in range(batch):
+        n = int(rng.choice([0, 1, 3, 10, 100]))
+        n = min(n, vocab)
+        if n:
+            idx = rng.choice(vocab, n, replace=False)
+            L[r, idx] += rng.uniform(2.0, 12.0, n).astype(np.float32)
+    params = [(0.0, -1, 1.0)] * batch if greedy_only else [mix[r % len(mix)] for r in range(batch)]
+    t = np.array([p[0] for p in params], np.float32)
+    k = np.array([p[1] for p in params], np.int32)
+    p = np.array([p[2] for p in params], np.float32)
+    u = rng.random(batch).astype(np.float32)
+    u = np.minimum(u, np.float32(1.0) - np.float32(2.0 ** -24))
+    logits = f32_to_bf16_bits(L) if bf16 else L
+    return SamplerSpec(name, logits, bf16, t, k, p, u)
