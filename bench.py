@@ -300,6 +300,7 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     large = run_large_decode(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     mixed = run_long_mixed(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     prologue = run_prologue(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
+    sampler = run_sampler(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     cpu = cpu_baseline(spec) if (rank == 0 and world == 1 and not args.no_cpu) else None
 
     line = {
@@ -336,6 +337,8 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
         line["long_mixed"] = mixed
     if prologue is not None:
         line["prologue"] = prologue
+    if sampler is not None:
+        line["sampler"] = sampler
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
@@ -580,6 +583,50 @@ def run_prologue(args, dev, msg, peaks):
             "bytes_per_launch": by, "l2": "flushed (256 MB write) before every timed launch"}
 
 
+def sampler_bytes(batch: int, vocab: int, esz: int) -> int:
+    """Algorithmic bytes of one sampler launch: every logit read once, the
+    four per-row arguments read and one token written per row."""
+    return int(batch * vocab * esz + batch * (4 * 4 + 4))
+
+
+def run_sampler(args, dev, msg, peaks):
+    """Batched sampler over 256 rows of Qwen3's 151,936-token vocabulary:
+    bf16 and fp32 logits with the mixed parameter set (greedy, temperature,
+    top-k, top-p, both), and an all-greedy batch (argmax)."""
+    import torch
+    torch.cuda.empty_cache()
+    B, V = 256, wl.QWEN3_VOCAB
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    n = max(args.steps, 20)
+    res = {"workload": f"sample_{B}rows_vocab{V}", "batch": B, "vocab": V,
+           "l2": "flushed (256 MB write) before every timed launch"}
+    for name, bf16, greedy in (("bf16_mixed", True, False), ("f32_mixed", False, False),
+                               ("bf16_greedy", True, True)):
+        spec = wl.sampler_batch(name, 8100 + bf16, B, V, bf16=bf16, greedy_only=greedy)
+        logits = (wl.bits_to_torch(spec.logits, dev) if bf16
+                  else torch.from_numpy(spec.logits).to(dev))
+        t, k, p = msg.sampling_args(spec.temperature, spec.top_k, spec.top_p, V, device=dev)
+        u = torch.from_numpy(spec.uniforms).to(dev)
+        out = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def call():
+            msg.msg_sample(logits, t, k, p, u, tokens_out=out, dev_status=status)
+
+        ms = _median_launch_ms(call, n, flush)
+        st, info = msg.msg_read_device_status(status)
+        if st != msg.MSG_OK:
+            raise RuntimeError(f"sampler {name}: device status {info}")
+        by = sampler_bytes(B, V, 2 if bf16 else 4)
+        gbs = by / (ms * 1e-3) / 1e9
+        res[name] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_launch": by}
+        del logits, out
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_long_mixed(args, dev, msg, peaks):
     """32 decode requests at context 32768 + 2 extend requests of 2048 over 16384
     cached, page_size 64: decode-only, extend-only and the mixed call, the mixed
@@ -705,7 +752,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--extend-only", action="store_true",
                     help="run only the extend sub-benchmark and print its JSON (profiling)")
-    ap.add_argument("--only", choices=["extend", "graph", "large", "mixed", "prologue"],
+    ap.add_argument("--only", choices=["extend", "graph", "large", "mixed", "prologue",
+                                       "sampler"],
                     default=None,
                     help="run only one sub-benchmark and print its JSON (profiling)")
     ap.add_argument("--layers", type=int, default=28,
@@ -732,7 +780,8 @@ def main():
                 "graph": lambda: run_graph_decode(args, dev, msg),
                 "large": lambda: run_large_decode(args, dev, msg, peaks),
                 "mixed": lambda: run_long_mixed(args, dev, msg, peaks),
-                "prologue": lambda: run_prologue(args, dev, msg, peaks)}
+                "prologue": lambda: run_prologue(args, dev, msg, peaks),
+                "sampler": lambda: run_sampler(args, dev, msg, peaks)}
         print(json.dumps(legs[args.only]()), flush=True)
         return
     dist = None

@@ -24,7 +24,14 @@
  *            4.6.4 (page table reading per backend: the dense per-request
  *            page-id table of the FlashAttention / TRT-LLM backends and the
  *            1-D ragged index list of FlashInfer), 4.6.5 (cu_seqlens),
- *            4.6.7 (store before attend), 4.9.4-4.9.5 (store kernel contract).
+ *            4.6.7 (store before attend), 4.9.4-4.9.5 (store kernel contract),
+ *            4.8.5-4.8.6 (Sampler.prepare's sparse arguments, the sampler's
+ *            four-way dispatch).
+ *   [SAMPLE] "Engine 与采样器", section "采样器" (Sampler.prepare,
+ *            Sampler.sample, sample_torch: softmax of logits / T, top-k, then
+ *            top-p on the renormalised rest, one draw per row) and section
+ *            "测试"; "Mini-SGLang 源码解析（四）" 14.2-14.5 (greedy batches
+ *            take the argmax; MIN_T and MIN_P clamps).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -97,6 +104,14 @@ extern "C" {
 #define MSG_DEV_TIMEOUT 4            /* a bounded wait inside a kernel expired */
 #define MSG_DEV_WRONG_PHASE 5        /* decode-only / extend-only flag contradicted */
 #define MSG_DEV_BAD_POSITION 6       /* a position outside the rotary cache */
+#define MSG_DEV_BAD_LOGIT 7          /* msg_sample: a NaN or infinite logit in a row */
+#define MSG_DEV_BAD_SAMPLING 8       /* msg_sample: non-finite temperature, NaN top_p,
+                                        or a uniform outside [0, 1) */
+#define MSG_DEV_INTERNAL 9           /* msg_sample: an internal consistency check failed */
+
+/* Element types of msg_sample's logits. */
+#define MSG_DTYPE_F32 0
+#define MSG_DTYPE_BF16 1
 
 /* Flags of msg_paged_attention. */
 #define MSG_ATTN_REUSE_PLAN 1u   /* workspace already holds the plan of this batch
@@ -426,6 +441,66 @@ int msg_paged_attention_noalloc(const void *q, int64_t q_row_stride, const void 
                                 int32_t num_qo_heads, int32_t num_kv_heads,
                                 int32_t head_dim, float scale, void *out, uint32_t flags,
                                 int32_t *dev_status, void *stream);
+
+/*
+ * Batched sampler: the next token of every row of logits [SAMPLE].
+ *
+ * Per row r (B rows of V logits):
+ *   temperatures == NULL: every request is greedy (Sampler.prepare returned
+ *     no temperatures); token = the first index of the row's maximum
+ *     (torch.argmax).  top_k, top_p and uniforms are ignored and may be NULL.
+ *   otherwise, sample_torch's steps in order:
+ *     T = max(temperatures[r], 1e-6)   (a greedy request of a mixed batch
+ *                                       passes T <= 0 and gets MIN_T);
+ *     p = softmax(logits[r] / T);
+ *     top-k (top_k != NULL and 1 <= top_k[r] < V): keep the top_k[r] most
+ *       likely tokens, equal probabilities in increasing token index;
+ *     top-p (top_p != NULL and clamp(top_p[r], 1e-6, 1) < 1): renormalise
+ *       what is left and keep a token only while the mass ranked ahead of it
+ *       is below top_p (the most likely token always stays);
+ *     draw: token = the smallest index i, in vocabulary order, whose
+ *       cumulative kept mass exceeds uniforms[r] times the kept total (the
+ *       inverse CDF; uniforms[r] in [0, 1) comes from the caller's generator).
+ *   The kernel computes p in fp32 as 2^((l - max) * log2(e) / T), holds each
+ *   weight in fixed point (floor(e * 2^40)) and sums exactly in 64-bit
+ *   integers, so a row's token is deterministic.  It differs from an exact
+ *   (fp64) evaluation only when the uniform or a cut falls within about 1e-5
+ *   (relative to the kept mass) of a boundary between two tokens.
+ *
+ * Arguments:
+ *   logits             device, B rows of V elements of logits_dtype
+ *                      (MSG_DTYPE_F32 or MSG_DTYPE_BF16; bf16 values are used
+ *                      exactly, as logits.float() would); rows
+ *                      logits_row_stride elements apart (>= V, any value); the
+ *                      pointer aligned to the element size (MSG_ERR_ALIGNMENT).
+ *                      Read only.
+ *   batch, vocab       B >= 0, 1 <= V <= 425984 (larger V: MSG_ERR_UNSUPPORTED).
+ *   temperatures       device float32 [B] or NULL (see above).
+ *   top_k              device int32 [B] or NULL (values < 1 or >= V: no cut).
+ *   top_p              device float32 [B] or NULL (clamped to [1e-6, 1]).
+ *   uniforms           device float32 [B], required with temperatures.
+ *   tokens_out         device int32 [B]: the tokens; -1 for a row that failed
+ *                      a device check.
+ *   dev_status         MSG_STATUS_BYTES device block or NULL: a NaN / infinite
+ *                      logit (MSG_DEV_BAD_LOGIT), a non-finite temperature, NaN
+ *                      top_p or a uniform outside [0, 1) (MSG_DEV_BAD_SAMPLING).
+ *   stream             cudaStream_t (NULL: the legacy default stream).
+ * One kernel launch: a cluster of 1-8 CTAs per row (msg_sample_slices gives
+ * the split), each CTA reading its slice of the row from HBM once.
+ * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_UNSUPPORTED, MSG_ERR_ALIGNMENT,
+ *         MSG_ERR_CUDA.
+ */
+int msg_sample(const void *logits, int32_t logits_dtype, int64_t logits_row_stride,
+               int32_t batch, int32_t vocab, const float *temperatures,
+               const int32_t *top_k, const float *top_p, const float *uniforms,
+               int32_t *tokens_out, int32_t *dev_status, void *stream);
+
+/*
+ * How msg_sample splits a row of `vocab` logits: *cluster_out CTAs of
+ * *slice_out elements each (the last one holds the rest).  Host only.
+ * Errors: MSG_ERR_INVALID_ARG (vocab < 1), MSG_ERR_UNSUPPORTED (too large).
+ */
+int msg_sample_slices(int32_t vocab, int32_t *cluster_out, int32_t *slice_out);
 
 #ifdef __cplusplus
 }

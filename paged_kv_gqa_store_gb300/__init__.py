@@ -40,6 +40,12 @@ MSG_DEV_BAD_LENGTHS = 3
 MSG_DEV_TIMEOUT = 4
 MSG_DEV_WRONG_PHASE = 5
 MSG_DEV_BAD_POSITION = 6
+MSG_DEV_BAD_LOGIT = 7
+MSG_DEV_BAD_SAMPLING = 8
+MSG_DEV_INTERNAL = 9
+
+MSG_DTYPE_F32 = 0
+MSG_DTYPE_BF16 = 1
 
 MSG_ATTN_REUSE_PLAN = 1
 MSG_ATTN_DECODE_ONLY = 2
@@ -153,6 +159,10 @@ def load_library(path: str | None = None):
             P, I64, I64, P, P, P, ctypes.c_float, P, I64, P, I64, P, P, I64, I64, P, I32, I32,
             I32, I32, P, P]
         lib.msg_qk_norm_rope_store.restype = ctypes.c_int
+        lib.msg_sample.argtypes = [P, I32, I64, I32, I32, P, P, P, P, P, P, P]
+        lib.msg_sample.restype = ctypes.c_int
+        lib.msg_sample_slices.argtypes = [I32, P, P]
+        lib.msg_sample_slices.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -403,6 +413,82 @@ def msg_qk_norm_rope_store(qkv, positions, q_norm_w, k_norm_w, eps: float, cos_s
         _ptr(out_loc), int(out_loc.dtype == torch.int64), int(num_qo_heads), int(num_kv_heads),
         d, _ptr(dev_status), _stream(stream))
     _check("msg_qk_norm_rope_store", st)
+
+
+SAMPLE_MIN_T = 1e-6
+SAMPLE_MIN_P = 1e-6
+
+
+def sampling_args(temperature, top_k, top_p, vocab_size: int, device="cuda"):
+    """Host side of the sampler's per-batch arguments (Sampler.prepare of
+    "Engine 与采样器"): per-request lists in, device tensors out.
+
+    temperature <= 0 is greedy.  Returns (temperatures, top_k, top_p), each a
+    device tensor or None: no temperatures when every request is greedy (the
+    kernel then takes the argmax), MIN_T for a greedy request of a mixed batch;
+    top_k (< 1: whole vocabulary) only when some request restricts it; top_p
+    (clamped to [MIN_P, 1]) only when some request is below 1.  The copies are
+    asynchronous from pinned host memory."""
+    import torch
+    t = [float(x) for x in temperature]
+    if all(x <= 0.0 for x in t):
+        return None, None, None
+
+    def dev(vals, dtype):
+        t = torch.tensor(vals, dtype=dtype)
+        if torch.device(device).type != "cuda":
+            return t.to(device)
+        return t.pin_memory().to(device, non_blocking=True)
+
+    ts = [max(0.0 if x <= 0.0 else x, SAMPLE_MIN_T) for x in t]
+    ks = [int(k) if int(k) >= 1 else int(vocab_size) for k in top_k]
+    ps = [min(max(float(x), SAMPLE_MIN_P), 1.0) for x in top_p]
+    k_t = dev(ks, torch.int32) if any(k != vocab_size for k in ks) else None
+    p_t = dev(ps, torch.float32) if any(x < 1.0 for x in ps) else None
+    return dev(ts, torch.float32), k_t, p_t
+
+
+def msg_sample_slices(vocab: int) -> tuple[int, int]:
+    """(CTAs per row, elements per CTA) that msg_sample uses for `vocab`."""
+    c, sl = ctypes.c_int32(), ctypes.c_int32()
+    _check("msg_sample_slices", load_library().msg_sample_slices(
+        int(vocab), ctypes.addressof(c), ctypes.addressof(sl)))
+    return c.value, sl.value
+
+
+def msg_sample(logits, temperatures, top_k, top_p, uniforms, tokens_out=None, dev_status=None,
+               stream=None):
+    """Next token of every row of logits [B, V] (float32 or bfloat16, inner dim
+    contiguous): argmax when temperatures is None, otherwise temperature, top-k,
+    top-p and one inverse-CDF draw per row with uniforms [B] (float32 in
+    [0, 1)).  Returns tokens_out (int32 [B], allocated if None)."""
+    import torch
+    _expect(logits, logits.dtype, "logits")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [B, V] with a contiguous inner dim")
+    if logits.dtype == torch.float32:
+        dt = MSG_DTYPE_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = MSG_DTYPE_BF16
+    else:
+        raise ValueError("logits must be float32 or bfloat16")
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    if temperatures is not None:
+        _expect(temperatures, torch.float32, "temperatures")
+        _expect(uniforms, torch.float32, "uniforms")
+    if top_k is not None:
+        _expect(top_k, torch.int32, "top_k")
+    if top_p is not None:
+        _expect(top_p, torch.float32, "top_p")
+    if tokens_out is None:
+        tokens_out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    _expect(tokens_out, torch.int32, "tokens_out")
+    st = load_library().msg_sample(
+        _ptr(logits), dt, int(logits.stride(0)) if B else V, B, V, _ptr(temperatures),
+        _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(tokens_out), _ptr(dev_status),
+        _stream(stream))
+    _check("msg_sample", st)
+    return tokens_out
 
 
 def msg_read_device_status(dev_status, stream=None) -> tuple[int, list[int]]:

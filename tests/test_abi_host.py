@@ -194,3 +194,61 @@ def test_prologue_argument_validation(lib, kw, status):
     (1e6, 128, 0, msg.MSG_ERR_INVALID_ARG)])
 def test_rope_cache_argument_validation(lib, theta, d, n, status):
     assert lib.msg_rope_cos_sin_cache(theta, d, n, FAKE, None) == status
+
+
+# ------------------------------------------------------------------ sampler
+@pytest.mark.parametrize("vocab,split", [
+    (1, (1, 8)), (6, (1, 8)), (24576, (1, 24576)), (24577, (2, 12296)),
+    (128256, (8, 16032)), (151936, (8, 18992)), (425984, (8, 53248))])
+def test_sample_slices(lib, vocab, split):
+    assert msg.msg_sample_slices(vocab) == split
+    C, sl = split
+    assert (C - 1) * sl < vocab <= C * sl and sl % 8 == 0
+
+
+def test_sample_slices_limits(lib):
+    c = ctypes.c_int32()
+    assert lib.msg_sample_slices(0, ctypes.addressof(c), None) == msg.MSG_ERR_INVALID_ARG
+    assert lib.msg_sample_slices(425985, ctypes.addressof(c), None) == msg.MSG_ERR_UNSUPPORTED
+
+
+def _sample(lib, **kw):
+    a = dict(logits=FAKE, dtype=msg.MSG_DTYPE_BF16, stride=152000, batch=4, vocab=151936,
+             temperatures=FAKE, top_k=None, top_p=None, uniforms=FAKE, tokens=FAKE,
+             dev_status=None, stream=None)
+    a.update(kw)
+    return lib.msg_sample(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(batch=0), msg.MSG_OK),
+    (dict(batch=-1), msg.MSG_ERR_INVALID_ARG),
+    (dict(dtype=7), msg.MSG_ERR_UNSUPPORTED),
+    (dict(vocab=0), msg.MSG_ERR_INVALID_ARG),
+    (dict(stride=100000), msg.MSG_ERR_INVALID_ARG),
+    (dict(vocab=500000, stride=500000), msg.MSG_ERR_UNSUPPORTED),
+    (dict(logits=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(tokens=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(uniforms=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(logits=FAKE + 1), msg.MSG_ERR_ALIGNMENT),
+    (dict(dtype=msg.MSG_DTYPE_F32, logits=FAKE + 2), msg.MSG_ERR_ALIGNMENT),
+])
+def test_sample_argument_validation(lib, kw, status):
+    assert _sample(lib, **kw) == status
+
+
+def test_sampling_args_match_the_pages_prepare():
+    # the binding's host half of Sampler.prepare against the oracle's statement
+    import numpy as np
+    import oracle
+    cases = [([0.0, 0.0], [-1, 5], [1.0, 0.5]),
+             ([0.7, 0.0, 1.2], [-1, 0, -3], [1.0, 1.0, 2.0]),
+             ([1.0, 1.0], [50, -1], [0.0, 0.95]),
+             ([0.5], [10**6], [1e-9])]
+    for t, k, p in cases:
+        got = msg.sampling_args(t, k, p, 1000, device="cpu")
+        want = oracle.sampling_args(t, k, p, 1000)
+        for g, w in zip(got, want):
+            assert (g is None) == (w is None)
+            if g is not None:
+                assert np.array_equal(g.numpy(), w)
