@@ -609,9 +609,10 @@ def run_sampler(args, dev, msg, peaks):
         t, k, p = msg.sampling_args(spec.temperature, spec.top_k, spec.top_p, V, device=dev)
         u = torch.from_numpy(spec.uniforms).to(dev)
         out = torch.empty(B, dtype=torch.int32, device=dev)
+        ws = torch.empty(msg.msg_sample_workspace_size(B, V), dtype=torch.uint8, device=dev)
 
         def call():
-            msg.msg_sample(logits, t, k, p, u, tokens_out=out, dev_status=status)
+            msg.msg_sample(logits, t, k, p, u, tokens_out=out, workspace=ws, dev_status=status)
 
         ms = _median_launch_ms(call, n, flush)
         st, info = msg.msg_read_device_status(status)
@@ -621,7 +622,7 @@ def run_sampler(args, dev, msg, peaks):
         gbs = by / (ms * 1e-3) / 1e9
         res[name] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_launch": by}
-        del logits, out
+        del logits, out, ws
     del flush
     torch.cuda.empty_cache()
     return res

@@ -104,7 +104,8 @@ extern "C" {
 #define MSG_DEV_TIMEOUT 4            /* a bounded wait inside a kernel expired */
 #define MSG_DEV_WRONG_PHASE 5        /* decode-only / extend-only flag contradicted */
 #define MSG_DEV_BAD_POSITION 6       /* a position outside the rotary cache */
-#define MSG_DEV_BAD_LOGIT 7          /* msg_sample: a NaN or infinite logit in a row */
+#define MSG_DEV_BAD_LOGIT 7          /* msg_sample: a NaN logit (+inf when sampling),
+                                        or a row of -inf only */
 #define MSG_DEV_BAD_SAMPLING 8       /* msg_sample: non-finite temperature, NaN top_p,
                                         or a uniform outside [0, 1) */
 #define MSG_DEV_INTERNAL 9           /* msg_sample: an internal consistency check failed */
@@ -461,11 +462,10 @@ int msg_paged_attention_noalloc(const void *q, int64_t q_row_stride, const void 
  *     draw: token = the smallest index i, in vocabulary order, whose
  *       cumulative kept mass exceeds uniforms[r] times the kept total (the
  *       inverse CDF; uniforms[r] in [0, 1) comes from the caller's generator).
- *   The kernel computes p in fp32 as 2^((l - max) * log2(e) / T), holds each
- *   weight in fixed point (floor(e * 2^40)) and sums exactly in 64-bit
- *   integers, so a row's token is deterministic.  It differs from an exact
- *   (fp64) evaluation only when the uniform or a cut falls within about 1e-5
- *   (relative to the kept mass) of a boundary between two tokens.
+ *   The kernel computes p in fp32 as 2^((l - max) * log2(e) / T) and sums in
+ *   a fixed order, so a row's token is deterministic.  It differs from an
+ *   exact (fp64) evaluation only when the uniform or a cut falls within about
+ *   1e-5 (relative to the kept mass) of a boundary between two tokens.
  *
  * Arguments:
  *   logits             device, B rows of V elements of logits_dtype
@@ -481,26 +481,40 @@ int msg_paged_attention_noalloc(const void *q, int64_t q_row_stride, const void 
  *   uniforms           device float32 [B], required with temperatures.
  *   tokens_out         device int32 [B]: the tokens; -1 for a row that failed
  *                      a device check.
- *   dev_status         MSG_STATUS_BYTES device block or NULL: a NaN / infinite
- *                      logit (MSG_DEV_BAD_LOGIT), a non-finite temperature, NaN
- *                      top_p or a uniform outside [0, 1) (MSG_DEV_BAD_SAMPLING).
+ *   workspace          device scratch of msg_sample_workspace_size(B, V) bytes
+ *                      or more, 16-byte aligned (MSG_ERR_WORKSPACE if missing
+ *                      or smaller; MSG_ERR_ALIGNMENT if misaligned); owned by
+ *                      the caller, its contents are not kept between calls.
+ *   dev_status         MSG_STATUS_BYTES device block or NULL: a NaN logit, a
+ *                      +inf logit when sampling (softmax is undefined), or a
+ *                      row whose every logit is -inf (MSG_DEV_BAD_LOGIT); a
+ *                      non-finite temperature, NaN top_p or a uniform outside
+ *                      [0, 1) (MSG_DEV_BAD_SAMPLING).  -inf logits are tokens
+ *                      of probability zero; a greedy row takes a +inf logit as
+ *                      its maximum.
  *   stream             cudaStream_t (NULL: the legacy default stream).
- * One kernel launch: a cluster of 1-8 CTAs per row (msg_sample_slices gives
- * the split), each CTA reading its slice of the row from HBM once.
+ * Two kernel launches on `stream`: a scan that reads every logit from HBM
+ * once (many CTAs per row) and a row kernel (one CTA per row, started early
+ * by programmatic dependent launch) that re-reads at most a few chunks of a
+ * row, or, for a top-p boundary deep inside a flat distribution, the row a few
+ * times (from L2 when the batch fits there).
  * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_UNSUPPORTED, MSG_ERR_ALIGNMENT,
- *         MSG_ERR_CUDA.
+ *         MSG_ERR_WORKSPACE, MSG_ERR_CUDA.
  */
 int msg_sample(const void *logits, int32_t logits_dtype, int64_t logits_row_stride,
                int32_t batch, int32_t vocab, const float *temperatures,
                const int32_t *top_k, const float *top_p, const float *uniforms,
-               int32_t *tokens_out, int32_t *dev_status, void *stream);
+               int32_t *tokens_out, void *workspace, size_t workspace_bytes,
+               int32_t *dev_status, void *stream);
 
 /*
- * How msg_sample splits a row of `vocab` logits: *cluster_out CTAs of
- * *slice_out elements each (the last one holds the rest).  Host only.
- * Errors: MSG_ERR_INVALID_ARG (vocab < 1), MSG_ERR_UNSUPPORTED (too large).
+ * Bytes of msg_sample's workspace for `batch` rows of `vocab` logits (per
+ * row: each 256-logit chunk's maximum and mass, a sparse sample, and the scan
+ * parts' partial results; about 14.5 KB per row at V = 151,936).  0 for an
+ * invalid or unsupported size.  Host only.
  */
-int msg_sample_slices(int32_t vocab, int32_t *cluster_out, int32_t *slice_out);
+size_t msg_sample_workspace_size(int32_t batch, int32_t vocab);
+
 
 #ifdef __cplusplus
 }

@@ -159,10 +159,10 @@ def load_library(path: str | None = None):
             P, I64, I64, P, P, P, ctypes.c_float, P, I64, P, I64, P, P, I64, I64, P, I32, I32,
             I32, I32, P, P]
         lib.msg_qk_norm_rope_store.restype = ctypes.c_int
-        lib.msg_sample.argtypes = [P, I32, I64, I32, I32, P, P, P, P, P, P, P]
+        lib.msg_sample.argtypes = [P, I32, I64, I32, I32, P, P, P, P, P, P, SZ, P, P]
         lib.msg_sample.restype = ctypes.c_int
-        lib.msg_sample_slices.argtypes = [I32, P, P]
-        lib.msg_sample_slices.restype = ctypes.c_int
+        lib.msg_sample_workspace_size.argtypes = [I32, I32]
+        lib.msg_sample_workspace_size.restype = SZ
         _lib = lib
         return lib
 
@@ -448,20 +448,17 @@ def sampling_args(temperature, top_k, top_p, vocab_size: int, device="cuda"):
     return dev(ts, torch.float32), k_t, p_t
 
 
-def msg_sample_slices(vocab: int) -> tuple[int, int]:
-    """(CTAs per row, elements per CTA) that msg_sample uses for `vocab`."""
-    c, sl = ctypes.c_int32(), ctypes.c_int32()
-    _check("msg_sample_slices", load_library().msg_sample_slices(
-        int(vocab), ctypes.addressof(c), ctypes.addressof(sl)))
-    return c.value, sl.value
+def msg_sample_workspace_size(batch: int, vocab: int) -> int:
+    return int(load_library().msg_sample_workspace_size(int(batch), int(vocab)))
 
 
-def msg_sample(logits, temperatures, top_k, top_p, uniforms, tokens_out=None, dev_status=None,
-               stream=None):
+def msg_sample(logits, temperatures, top_k, top_p, uniforms, tokens_out=None, workspace=None,
+               dev_status=None, stream=None):
     """Next token of every row of logits [B, V] (float32 or bfloat16, inner dim
     contiguous): argmax when temperatures is None, otherwise temperature, top-k,
     top-p and one inverse-CDF draw per row with uniforms [B] (float32 in
-    [0, 1)).  Returns tokens_out (int32 [B], allocated if None)."""
+    [0, 1)).  Returns tokens_out (int32 [B], allocated if None); the
+    workspace (uint8, msg_sample_workspace_size bytes) is allocated if None."""
     import torch
     _expect(logits, logits.dtype, "logits")
     if logits.dim() != 2 or logits.stride(1) != 1:
@@ -483,10 +480,13 @@ def msg_sample(logits, temperatures, top_k, top_p, uniforms, tokens_out=None, de
     if tokens_out is None:
         tokens_out = torch.empty(B, dtype=torch.int32, device=logits.device)
     _expect(tokens_out, torch.int32, "tokens_out")
+    if workspace is None:
+        workspace = torch.empty(max(16, msg_sample_workspace_size(B, V)), dtype=torch.uint8,
+                                device=logits.device)
     st = load_library().msg_sample(
         _ptr(logits), dt, int(logits.stride(0)) if B else V, B, V, _ptr(temperatures),
-        _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(tokens_out), _ptr(dev_status),
-        _stream(stream))
+        _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(tokens_out), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _ptr(dev_status), _stream(stream))
     _check("msg_sample", st)
     return tokens_out
 

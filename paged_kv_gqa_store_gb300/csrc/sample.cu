@@ -8,16 +8,23 @@
 // vocabulary order, first exceeds u times the kept total.  Without
 // temperatures every row is greedy and the token is the first maximum.
 //
-// GB300 layout: one thread-block cluster per row.  The row is split into
-// C contiguous slices (C = 1..8), each CTA reads its slice from HBM exactly
-// once into shared memory (up to ~76 KB for a 151,936-token vocabulary with
-// C = 8, two CTAs per SM), and every later step runs out of shared memory.
-// There is no sort: the k-th token and the top-p boundary are found by radix
-// selection over a 30-bit order key, one 8-bit digit per pass, with the
-// per-bucket counts or masses of all C CTAs summed through distributed shared
-// memory after a cluster barrier.  Masses are fixed point (e * 2^40, floor),
-// so every sum is exact integer arithmetic, identical in every CTA of the
-// cluster and from run to run.
+// GB300 layout: one CTA per row, streaming the row.  The first pass reads the
+// row from HBM once and keeps, per chunk of 256 logits, its maximum and its
+// mass relative to that maximum, plus a sparse sample of the row; a batch of
+// bf16 logits (78 MB for 256 x 151,936) then stays in L2 for the few later
+// reads.  A row without a cut draws straight from the chunk masses (one more
+// read of a single chunk).  With a cut, the k-th token or the top-p boundary
+// is located inside a small window of logit values: the window is estimated
+// from the chunk maxima or from the sample, tightened when needed by probe
+// passes that count logits and sum masses above four pivots, then gathered
+// (at most kCap logits), sorted by (logit desc, index asc) and resolved
+// exactly.  The kept set is "every token ranked at or before the threshold
+// token", so the draw needs no rank bookkeeping: either the whole kept set is
+// in the window (a sort by index and one scan), or the gather also summed,
+// per chunk, the mass above the window and the draw walks the chunks.
+//
+// Masses are fp32 2^((l - max) * log2(e) / T) summed in a fixed order (no
+// atomics), so a row's token is deterministic.
 #include <math.h>
 
 #include "internal.cuh"
@@ -26,23 +33,25 @@ namespace msg {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kBuckets = 256;
-constexpr int kMaxCluster = 8;
-constexpr int kSliceAlign = 8;                 // elements: every CTA starts 16-byte aligned
-constexpr int kSliceTwoPerSm = 24576;          // <= 96 KB of fp32: two CTAs per SM
-constexpr int kSliceMax = 53248;               // <= 208 KB of fp32: one CTA per SM
-constexpr uint32_t kOneBits = 0x3F800000u;     // bits of 1.0f
-constexpr uint32_t kPadBits = 0x80000000u;     // -0.0f: key above every real key
+constexpr int kT = 512;                        // threads: one CTA per row
+constexpr int kW = kT / 32;
+constexpr int kLE = 8;                         // logits a lane holds of a chunk
+constexpr int kChunk = 32 * kLE;               // logits per chunk
+constexpr int kMaxVocab = 425984;
+constexpr int kMaxChunks = (kMaxVocab / kLE + 31) / 32 + 2;   // + the head and tail chunks
+constexpr int kSortChunks = 2048;              // power of two >= kMaxChunks
+constexpr int kCap = 4096;                     // window capacity (logits)
+constexpr int kMaxSamples = 4096;
+constexpr int kMaxProbes = 48;
 constexpr float kMinT = 1e-6f;                 // Sampler.prepare's MIN_T
 constexpr float kMinP = 1e-6f;                 // Sampler.prepare's MIN_P
-constexpr float kMassScale = 1099511627776.0f; // 2^40
+constexpr unsigned long long kKeyEnd = 1ull << 32;   // one past every order key
+static_assert(kMaxChunks <= kSortChunks, "chunk maxima are sorted in one power-of-two array");
 
 struct SampleParams {
   const uint8_t *logits;
   int64_t row_bytes;                           // bytes between rows
-  int32_t batch, vocab, slice;                 // slice: elements per CTA (multiple of 8)
+  int32_t batch, vocab;
   const float *temperature;                    // null: every row greedy
   const int32_t *top_k;                        // null: no top-k
   const float *top_p;                          // null: no top-p
@@ -51,648 +60,1376 @@ struct SampleParams {
   int32_t *status;
 };
 
-// Shared state beside the staged slice.  Buffers read by other CTAs of the
-// cluster alternate between two slots, so a slot is rewritten only after the
-// barrier that follows every CTA's last read of it.
-struct Shared {
-  unsigned long long hist[2][kBuckets];        // published per-CTA histogram
-  unsigned long long scal[2][2];               // published per-CTA scalars
-  unsigned long long scan[kWarps];
-  unsigned long long wmass[kWarps];            // draw: mass below the threshold key, per warp
-  uint32_t wties[kWarps];                      //       keys equal to it, per warp
-  uint32_t pick[4];                            // selected bucket / flags
-  unsigned long long pick64[2];
+struct Smem {
+  float cmax[kMaxChunks];                      // per chunk: largest logit
+  float cmass[kMaxChunks];                     //   mass (rel. to cmax, then to the row max)
+  float cabove[kMaxChunks];                    //   mass above the window / kept mass
+  uint32_t csort[kSortChunks];                 // ~key of the chunk maxima, sorted ascending
+  uint32_t samp[kMaxSamples];                  // ~key of the sample, sorted ascending
+  unsigned long long list[kCap];               // window: (~key << 32) | index, sorted ascending
+  float lcum[kCap];                            // window: cumulative masses in list order
+  float fred[kW];
+  unsigned long long ured[kW];
+  int ival[8];
+  float fval[4];
 };
-static_assert(sizeof(Shared) % 16 == 0, "the staged slice after Shared must be 16-byte aligned");
 
-// ---- cluster primitives
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+// ---- keys and masses
+// Order key of a logit: increasing with the value (-0 is read as +0).
+__device__ __forceinline__ uint32_t key_of(float f) {
+  const uint32_t u = __float_as_uint(f + 0.f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-// Every thread of every CTA of the cluster arrives (release) and waits
-// (acquire): shared-memory writes before it are visible to every CTA after it.
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ float value_of(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
-__device__ __forceinline__ unsigned long long ld_cluster_u64(const void *local, uint32_t rank) {
-  uint32_t remote;
-  unsigned long long v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// Order key: ascending key = descending probability (e in [0, 1]).
-__device__ __forceinline__ uint32_t key_of(uint32_t bits) { return kOneBits - bits; }
-// Fixed-point mass of a probability weight: floor(e * 2^40).
-__device__ __forceinline__ unsigned long long mass_of(uint32_t bits) {
-  return __float2ull_rz(__uint_as_float(bits) * kMassScale);
-}
-// Float -> unsigned key with the same order (finite values).
-__device__ __forceinline__ uint32_t orderable(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ unsigned long long warp_sum(unsigned long long v) {
+// ---- block primitives (every thread calls; every thread gets the result)
+__device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-
-// Exclusive scan over the block of one value per thread (thread order);
-// `total` receives the block sum.  Contains two __syncthreads.
-__device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v, Shared &sh,
-                                                              unsigned long long &total) {
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float block_sum_f(float v, Smem &sm) {
+  v = warp_sum_f(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.fred[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) s += sm.fred[w];
+  return s;
+}
+__device__ __forceinline__ float block_max_f(float v, Smem &sm) {
+  v = warp_max_f(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.fred[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float s = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) s = fmaxf(s, sm.fred[w]);
+  return s;
+}
+__device__ __forceinline__ unsigned long long block_sum_u(unsigned long long v, Smem &sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.ured[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long s = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) s += sm.ured[w];
+  return s;
+}
+__device__ __forceinline__ unsigned long long block_max_u(unsigned long long v, Smem &sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, v, o);
+    v = y > v ? y : v;
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.ured[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long s = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) s = sm.ured[w] > s ? sm.ured[w] : s;
+  return s;
+}
+__device__ __forceinline__ int block_min_i(int v, Smem &sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sm.ured[threadIdx.x >> 5] = (unsigned long long)(uint32_t)v;
+  __syncthreads();
+  int s = v;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) s = min(s, (int)(uint32_t)sm.ured[w]);
+  return s;
+}
+// Exclusive scan of one float per thread, in thread order; the total in *tot.
+__device__ __forceinline__ float block_excl_scan_f(float v, Smem &sm, float *tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned long long x = v;
+  float x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) sh.scan[warp] = x;
   __syncthreads();
-  unsigned long long before = 0, tot = 0;
+  if (lane == 31) sm.fred[warp] = x;
+  __syncthreads();
+  float before = 0.f, all = 0.f;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const unsigned long long t = sh.scan[w];
+  for (int w = 0; w < kW; ++w) {
+    const float t = sm.fred[w];
     if (w < warp) before += t;
-    tot += t;
+    all += t;
   }
-  __syncthreads();
-  total = tot;
+  *tot = all;
   return before + x - v;
 }
 
-// Digit d of the 30-bit key: bits [shift, shift + width).
-__device__ __forceinline__ int digit_shift(int d) { return d < 3 ? 22 - 8 * d : 0; }
-__device__ __forceinline__ int digit_width(int d) { return d < 3 ? 8 : 6; }
-
-// Cluster sum of this thread's bucket (thread b, bucket b), then the bucket
-// with excl(b) < target <= excl(b) + h(b), published in shared memory:
-// pick[0] = bucket, pick64[0] = excl, pick64[1] = h.  `adjust` is taken off
-// bucket adj_bucket first.  False if no bucket qualifies (target above the
-// total).
-__device__ __forceinline__ bool select_bucket(Shared &sh, int slot, int C,
-                                              unsigned long long target, int adj_bucket,
-                                              unsigned long long adjust,
-                                              unsigned long long *total_out) {
-  const int b = threadIdx.x;
-  unsigned long long h = 0;
-  for (int c = 0; c < C; ++c) h += ld_cluster_u64(&sh.hist[slot][b], (uint32_t)c);
-  if (b == adj_bucket) h -= adjust;
-  unsigned long long total;
-  const unsigned long long excl = block_excl_scan(h, sh, total);
-  if (threadIdx.x == 0) sh.pick[1] = 0;
-  __syncthreads();
-  if (excl < target && target <= excl + h) {
-    sh.pick[0] = (uint32_t)b;
-    sh.pick[1] = 1;
-    sh.pick64[0] = excl;
-    sh.pick64[1] = h;
+// Ascending bitonic sort of n (a power of two, >= 2) entries in shared
+// memory.  Stages whose pairs lie inside one warp's contiguous segment of
+// n / kW entries synchronise only that warp; the others the whole block.
+template <typename T>
+__device__ void bitonic_sort(T *a, int n) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = n >= 2 * kW ? n / kW : n;     // entries per warp segment
+  const bool warp_local = n >= 2 * kW;
+  for (int k = 2; k <= n; k <<= 1) {
+    int j = k >> 1;
+    for (; j > 0 && (!warp_local || j >= seg); j >>= 1) {   // block-wide stages
+      for (int i = threadIdx.x; i < (n >> 1); i += kT) {
+        const int lo = 2 * i - (i & (j - 1)), hi = lo + j;
+        const T x = a[lo], y = a[hi];
+        if ((x > y) == ((lo & k) == 0)) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+    if (j == 0) continue;
+    T *b = a + warp * seg;                      // warp-local stages
+    const int base = warp * seg;
+    for (; j > 0; j >>= 1) {
+      for (int i = lane; i < (seg >> 1); i += 32) {
+        const int lo = 2 * i - (i & (j - 1)), hi = lo + j;
+        const T x = b[lo], y = b[hi];
+        if ((x > y) == (((base + lo) & k) == 0)) {
+          b[lo] = y;
+          b[hi] = x;
+        }
+      }
+      __syncwarp();
+    }
+    __syncthreads();
   }
-  if (total_out) *total_out = total;
-  __syncthreads();
-  return sh.pick[1] != 0;
+}
+__device__ __forceinline__ int pow2_at_least(int n) {
+  int p = 2;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+// ---- the row: a head of h logits up to the first 16-byte boundary, nvec
+// vectors of 8 logits (16 bytes of bf16, 32 of fp32), a tail of < 8 logits.
+// Logical chunk 0 is the head (lane 0), chunks 1..nch hold 32 vectors each,
+// chunk nch + 1 is the tail (lane 0); chunk order is index order.
+struct RowRef {
+  const uint8_t *p;
+  int V, h, nvec, nch, tail;
+};
+
+template <bool kBf16>
+__device__ __forceinline__ RowRef row_ref(const uint8_t *p, int V) {
+  constexpr int esz = kBf16 ? 2 : 4;
+  int h = (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) / esz);
+  if (h > V) h = V;
+  const int nvec = (V - h) / kLE;
+  return {p, V, h, nvec, (nvec + 31) / 32, V - h - kLE * nvec};
 }
 
 template <bool kBf16>
-__device__ __forceinline__ void load8(const uint8_t *p, float v[8]) {
+__device__ __forceinline__ float load1(const uint8_t *row, int j) {
+  if (kBf16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(row)[j] << 16);
+  return reinterpret_cast<const float *>(row)[j];
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void load8(const uint8_t *p, float v[kLE]) {
   if (kBf16) {
     uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     v[0] = bf16lo(r.x); v[1] = bf16hi(r.x); v[2] = bf16lo(r.y); v[3] = bf16hi(r.y);
     v[4] = bf16lo(r.z); v[5] = bf16hi(r.z); v[6] = bf16lo(r.w); v[7] = bf16hi(r.w);
   } else {
     float4 a, b;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
                  : "=f"(a.x), "=f"(a.y), "=f"(a.z), "=f"(a.w) : "l"(p));
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
                  : "=f"(b.x), "=f"(b.y), "=f"(b.z), "=f"(b.w) : "l"(p + 16));
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   }
 }
 
+// The lane's logits of logical chunk c: how many (0..8), and the first one's index.
 template <bool kBf16>
-__device__ __forceinline__ float load1(const uint8_t *row, int64_t j) {
-  if (kBf16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(row)[j] << 16);
-  return reinterpret_cast<const float *>(row)[j];
+__device__ __forceinline__ int chunk_lane(const RowRef &r, int c, int lane, float v[kLE], int &idx0) {
+  constexpr int esz = kBf16 ? 2 : 4;
+  int n = 0;
+  if (c == 0 || c == r.nch + 1) {
+    idx0 = c == 0 ? 0 : r.h + kLE * r.nvec;
+    n = lane == 0 ? (c == 0 ? r.h : r.tail) : 0;
+#pragma unroll
+    for (int j = 0; j < kLE; ++j) v[j] = j < n ? load1<kBf16>(r.p, idx0 + j) : 0.f;
+  } else {
+    const int vi = 32 * (c - 1) + lane;
+    idx0 = r.h + kLE * vi;
+    if (vi < r.nvec) {
+      n = kLE;
+      load8<kBf16>(r.p + (int64_t)idx0 * esz, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kLE; ++j) v[j] = 0.f;
+    }
+  }
+  return n;
 }
 
-template <bool kBf16, bool kGreedy>
-__global__ void __launch_bounds__(kThreads, kGreedy ? 4 : 2) sample_kernel(SampleParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  Shared &sh = *reinterpret_cast<Shared *>(smem);
-  uint32_t *val = reinterpret_cast<uint32_t *>(smem + sizeof(Shared));
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int C = (int)(gridDim.x / (uint32_t)p.batch);     // cluster size
-  const uint32_t rank = cluster_rank();
-  const int row = (int)(blockIdx.x / (uint32_t)C);
-  const int64_t lo = (int64_t)rank * p.slice;
-  const int64_t left = (int64_t)p.vocab - lo;
-  const int n = left <= 0 ? 0 : (int)(left < p.slice ? left : p.slice);
-  const uint8_t *rowp = p.logits + (int64_t)row * p.row_bytes;
-  constexpr int kEsz = kBf16 ? 2 : 4;
+// Chunk holding token index i.
+__device__ __forceinline__ int chunk_of(const RowRef &r, int i) {
+  if (i < r.h) return 0;
+  if (i >= r.h + kLE * r.nvec) return r.nch + 1;
+  return 1 + (i - r.h) / kChunk;
+}
 
-  // ---- pass 0: the slice from HBM (once), its maximum, finiteness.  Rows need
-  //      not be 16-byte aligned: the first h < 16 / esz elements (up to the
-  //      next 16-byte boundary) and the ragged end are read one by one, the
-  //      rest as 16-byte vectors.  Element j of the slice sits at val[off + j]
-  //      with off chosen so that the vector part lands 16-byte aligned in
-  //      shared memory; val[0, off) and the end of the last group hold pads.
-  float vmax = -INFINITY;
-  bool finite = true;
-  unsigned long long best = 0;                 // greedy: (orderable value, ~index), max wins
-  const uint8_t *sp = rowp + lo * kEsz;        // first element of the slice
-  const int h = min(n, (int)(((16u - (uint32_t)(reinterpret_cast<uintptr_t>(sp) & 15u)) & 15u) / kEsz));
-  const int off = (4 - (h & 3)) & 3;
-  const int nchunk = (n - h) >> 3;
-  const int n4 = (off + n + 3) >> 2;
-  auto take = [&](float x, int j) {            // element j of the slice, read one by one
-    finite &= isfinite(x);
-    if (kGreedy) {
-      const unsigned long long key = ((unsigned long long)orderable(x + 0.f) << 32) |
-                                     (0xffffffffu - (uint32_t)(lo + j));
-      best = key > best ? key : best;
-    } else {
-      vmax = fmaxf(vmax, x);
-      val[off + j] = __float_as_uint(x);
+constexpr int kPassUnrollBf16 = 4;             // chunks a warp has in flight in a row pass
+constexpr int kPassUnrollF32 = 2;
+
+// A pass over the row's chunks: warp w takes logical chunks 1 + w, 1 + w + kW,
+// ... with 4 (bf16) or 2 (fp32) chunks' loads in flight, then the head and tail chunks
+// (warps 0 and 1).  A chunk with keep(c) false is not read; skip(c) runs
+// instead (lane-uniform).  body(v, n, i0, c) sees the lane's logits.
+template <bool kBf16, typename Keep, typename Skip, typename Body>
+__device__ __forceinline__ void for_chunks(const RowRef &r, Keep keep, Skip skip, Body body) {
+  constexpr int esz = kBf16 ? 2 : 4;
+  constexpr int kWords = kBf16 ? 1 : 2;
+  constexpr int kPassUnroll = kBf16 ? kPassUnrollBf16 : kPassUnrollF32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int c0 = 1 + warp; c0 <= r.nch; c0 += kW * kPassUnroll) {
+    uint4 raw[kPassUnroll][kWords];
+    bool on[kPassUnroll];
+#pragma unroll
+    for (int q = 0; q < kPassUnroll; ++q) {
+      const int c = c0 + q * kW;
+      on[q] = c <= r.nch && keep(c);
+      const int vi = 32 * (c - 1) + lane;
+      if (on[q] && vi < r.nvec) {
+        const uint8_t *src = r.p + (int64_t)(r.h + kLE * vi) * esz;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w)
+          asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(raw[q][w].x), "=r"(raw[q][w].y), "=r"(raw[q][w].z), "=r"(raw[q][w].w)
+                       : "l"(src + 16 * w));
+      }
     }
-  };
-  for (int c0 = tid; c0 < nchunk; c0 += 4 * kThreads) {
-    float v[4][8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (c0 + u * kThreads < nchunk) load8<kBf16>(sp + (h + 8 * (c0 + u * kThreads)) * kEsz, v[u]);
+    for (int q = 0; q < kPassUnroll; ++q) {
+      const int c = c0 + q * kW;
+      if (c > r.nch) break;                     // warp-uniform
+      if (!on[q]) {
+        skip(c);
+        continue;
+      }
+      const int vi = 32 * (c - 1) + lane;
+      const int n = vi < r.nvec ? kLE : 0;
+      float v[kLE];
+      if (kBf16) {
+        const uint4 w = raw[q][0];
+        v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+        v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+      } else {
+        const uint4 a = raw[q][0], b = raw[q][kWords - 1];
+        v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+        v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+        v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+        v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+      }
+      body(v, n, r.h + kLE * vi, c);
+    }
+  }
+  if (warp < 2) {                               // head (warp 0) and tail (warp 1)
+    const int c = warp == 0 ? 0 : r.nch + 1;
+    if (!keep(c)) {
+      skip(c);
+    } else {
+      float v[kLE];
+      int i0;
+      const int n = chunk_lane<kBf16>(r, c, lane, v, i0);
+      body(v, n, i0, c);
+    }
+  }
+}
+
+// ---- row state (every thread holds the same copy)
+struct Ctx {
+  RowRef r;
+  int nl;                                      // logical chunks
+  float M, kx;                                 // row maximum, log2(e) / T
+  float S;                                     // row mass (relative to M)
+  int ns;                                      // valid samples (sorted, first)
+  int spc;                                     // samples per vector chunk
+};
+
+__device__ __forceinline__ float mass_of(const Ctx &x, float l) { return ex2((l - x.M) * x.kx); }
+
+// Window [lo, hi) of order keys: gather its logits into the list (at most kCap
+// stored; the full count is returned), and per chunk the mass of the logits
+// at or above hi (cabove); *cnt_above / *mass_above get their totals.
+template <bool kBf16>
+__device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi,
+                      unsigned long long *cnt_above, float *mass_above) {
+  const int lane = threadIdx.x & 31;
+  __syncthreads();
+  if (threadIdx.x == 0) sm.ival[0] = 0;
+  __syncthreads();
+  uint32_t ca = 0;
+  // keys in [lo, top] are in the window, keys above top above it
+  const uint32_t top = hi >= kKeyEnd ? 0xffffffffu : (uint32_t)(hi - 1);
+  const bool has_above = hi < kKeyEnd;
+  for_chunks<kBf16>(
+      x.r, [&](int c) { return sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= lo; },
+      [&](int c) {
+        if (lane == 0) sm.cabove[c] = 0.f;
+      },
+      [&](const float v[kLE], int n, int i0, int c) {
+        float ma = 0.f;
+        uint32_t wmask = 0;                     // the lane's window logits
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = c0 + u * kThreads;
-      if (c >= nchunk) break;
+        for (int j = 0; j < kLE; ++j) {
+          const uint32_t k = key_of(v[j]);
+          if (j < n && k >= lo) {
+            if (has_above && k > top) {
+              ++ca;
+              ma += mass_of(x, v[j]);
+            } else {
+              wmask |= 1u << j;
+            }
+          }
+        }
+        // append the window logits, one warp-wide slot reservation per chunk
+        const int cnt = __popc(wmask);
+        int incl = cnt;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        finite &= isfinite(v[u][e]);
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (total) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&sm.ival[0], total);
+          base = __shfl_sync(0xffffffffu, base, 0) + incl - cnt;
+#pragma unroll
+          for (int j = 0; j < kLE; ++j)
+            if ((wmask >> j) & 1u) {
+              if (base < kCap)
+                sm.list[base] = ((unsigned long long)(~key_of(v[j])) << 32) | (uint32_t)(i0 + j);
+              ++base;
+            }
+        }
+        if (has_above) {
+          ma = warp_sum_f(ma);
+          if (lane == 0) sm.cabove[c] = ma;
+        } else if (lane == 0) {
+          sm.cabove[c] = 0.f;
+        }
+      });
+  *cnt_above = block_sum_u(ca, sm);
+  float part = 0.f;                            // fixed order: thread t sums chunks t, t + kT, ...
+  for (int c = threadIdx.x; c < x.nl; c += kT) part += sm.cabove[c];
+  *mass_above = block_sum_f(part, sm);
+  return sm.ival[0];
+}
+
+// Sort the gathered window (n <= kCap entries) and write cumulative masses.
+__device__ void sort_window(const Ctx &x, Smem &sm, int n) {
+  const int np = pow2_at_least(n);
+  for (int i = n + threadIdx.x; i < np; i += kT) sm.list[i] = ~0ull;
+  __syncthreads();
+  bitonic_sort(sm.list, np);
+  const int per = (n + kT - 1) / kT;           // thread t owns entries [t * per, (t + 1) * per)
+  const int a = min(n, (int)threadIdx.x * per), b = min(n, a + per);
+  float s = 0.f;
+  for (int i = a; i < b; ++i) s += mass_of(x, value_of(~(uint32_t)(sm.list[i] >> 32)));
+  float tot;
+  float run = block_excl_scan_f(s, sm, &tot);
+  for (int i = a; i < b; ++i) {
+    run += mass_of(x, value_of(~(uint32_t)(sm.list[i] >> 32)));
+    sm.lcum[i] = run;
+  }
+  __syncthreads();
+}
+
+// First list position (< n) whose cumulative mass plus `base` reaches tau; n if none.
+__device__ int window_crossing(Smem &sm, int n, float base, float tau) {
+  int best = n;
+  for (int i = threadIdx.x; i < n; i += kT)
+    if (base + sm.lcum[i] >= tau) {
+      best = i;
+      break;
+    }
+  return block_min_i(best, sm);
+}
+
+// Probe pass: count and mass of the logits at or above each of four pivots
+// (descending keys); chunks whose maximum is below the smallest are skipped.
+template <bool kBf16>
+__device__ void probe(const Ctx &x, Smem &sm, const uint32_t piv[4], bool want_mass,
+                      unsigned long long cnt[4], float mass[4]) {
+  uint32_t c4[4] = {0, 0, 0, 0};
+  float m4[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t p0 = piv[0], p1 = piv[1], p2 = piv[2], p3 = piv[3];
+  for_chunks<kBf16>(
+      x.r, [&](int c) { return sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= p3; },
+      [&](int) {},
+      [&](const float v[kLE], int n, int, int) {
+#pragma unroll
+        for (int j = 0; j < kLE; ++j) {
+          const uint32_t k = key_of(v[j]);
+          if (j >= n || k < p3) continue;
+          const float e = want_mass ? mass_of(x, v[j]) : 0.f;
+          ++c4[3];
+          m4[3] += e;
+          if (k >= p2) {
+            ++c4[2];
+            m4[2] += e;
+          }
+          if (k >= p1) {
+            ++c4[1];
+            m4[1] += e;
+          }
+          if (k >= p0) {
+            ++c4[0];
+            m4[0] += e;
+          }
+        }
+      });
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    cnt[q] = block_sum_u(c4[q], sm);
+    mass[q] = want_mass ? block_sum_f(m4[q], sm) : 0.f;
+  }
+}
+
+// Lower bound for the top-p boundary from the chunk maxima (csort, descending
+// keys): the maxima at or above `lo` are distinct logits, so if the first r of
+// them hold tau the boundary is at or above the r-th.  0 if they never do.
+__device__ uint32_t chunk_max_bound(const Ctx &x, Smem &sm, uint32_t lo, float tau) {
+  const int per = (x.nl + kT - 1) / kT;
+  const int a = min(x.nl, (int)threadIdx.x * per), b = min(x.nl, a + per);
+  float part = 0.f;
+  for (int i = a; i < b; ++i) {
+    const uint32_t kk = ~sm.csort[i];
+    if (sm.csort[i] != ~0u && kk >= lo) part += mass_of(x, value_of(kk));
+  }
+  float tot;
+  float run = block_excl_scan_f(part, sm, &tot);
+  int first = x.nl;
+  for (int i = a; i < b; ++i) {
+    const uint32_t kk = ~sm.csort[i];
+    if (sm.csort[i] != ~0u && kk >= lo) {
+      run += mass_of(x, value_of(kk));
+      if (run >= tau) {
+        first = i;
+        break;
+      }
+    }
+  }
+  first = block_min_i(first, sm);
+  return first < x.nl ? ~sm.csort[first] : 0u;
+}
+
+// Last position in [p0, p1) of a descending-key array stored as ~key
+// (ascending) whose key is >= K; p0 - 1 if none.
+__device__ __forceinline__ int last_at_least(const uint32_t *arr, int p0, int p1, uint32_t K) {
+  int lo = p0, hi = p1;                         // first position with key < K
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (~arr[mid] >= K) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo - 1;
+}
+
+// Pivots for a top-p target inside (lo, hi): the mass at or above a key X is
+// estimated as the exact mass at hi, plus the chunk maxima in [X, hi) (real
+// logits, so the heavy tail of a peaked row is counted exactly), plus the
+// sample points in [X, hi) weighted by the logits they stand for (the sample
+// leaves out points that are their chunk's maximum, so nothing is counted
+// twice; it carries the bulk of a flat row).  The
+// pivots are the highest keys where the estimate reaches tau + g * f,
+// f = -1/4, -1/12, 1/12, 1/4, with the spread g given by the caller.  Uses
+// lcum and cabove as scratch.
+__device__ void estimate_pivots(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi, int a,
+                                int b, int s, float g, float mass_hi, float tau, uint32_t piv[4]) {
+  // chunk maxima strictly inside (lo, hi): positions [ca, cb) of csort
+  unsigned long long ge_hi = 0, gt_lo = 0;
+  for (int i = threadIdx.x; i < x.nl; i += kT) {
+    if (sm.csort[i] == ~0u) continue;
+    const uint32_t kk = ~sm.csort[i];
+    ge_hi += (unsigned long long)kk >= hi;
+    gt_lo += kk > lo;
+  }
+  const int ca = (int)block_sum_u(ge_hi, sm), cb = (int)block_sum_u(gt_lo, sm);
+  // prefix masses: samples into lcum[a, b), chunk maxima into cabove[ca, cb)
+  {
+    const int per = (b - a + kT - 1) / kT;
+    const int ta = min(b, a + (int)threadIdx.x * per), tb = min(b, ta + per);
+    float part = 0.f;
+    for (int i = ta; i < tb; ++i) part += (float)s * mass_of(x, value_of(~sm.samp[i]));
+    float tot;
+    float run = block_excl_scan_f(part, sm, &tot);
+    for (int i = ta; i < tb; ++i) {
+      run += (float)s * mass_of(x, value_of(~sm.samp[i]));
+      sm.lcum[i] = run;
+    }
+  }
+  {
+    const int per = (cb - ca + kT - 1) / kT;
+    const int ta = min(cb, ca + (int)threadIdx.x * per), tb = min(cb, ta + per);
+    float part = 0.f;
+    for (int i = ta; i < tb; ++i) part += mass_of(x, value_of(~sm.csort[i]));
+    float tot;
+    float run = block_excl_scan_f(part, sm, &tot);
+    for (int i = ta; i < tb; ++i) {
+      run += mass_of(x, value_of(~sm.csort[i]));
+      sm.cabove[i] = run;
+    }
+  }
+  __syncthreads();
+  const float frac[4] = {-0.25f, -1.f / 12.f, 1.f / 12.f, 0.25f};
+  const int ps = (b - a + kT - 1) / kT, pc = (cb - ca + kT - 1) / kT;
+  const int sa = min(b, a + (int)threadIdx.x * ps), sb = min(b, sa + ps);
+  const int qa = min(cb, ca + (int)threadIdx.x * pc), qb = min(cb, qa + pc);
+  for (int t = 0; t < 4; ++t) {
+    const float want = tau + frac[t] * g;
+    int fs = b, fc = cb;
+    for (int i = sa; i < sb; ++i) {
+      const int r = last_at_least(sm.csort, ca, cb, ~sm.samp[i]);
+      const float e = mass_hi + sm.lcum[i] + (r >= ca ? sm.cabove[r] : 0.f);
+      if (e >= want) {
+        fs = i;
+        break;
+      }
+    }
+    for (int i = qa; i < qb; ++i) {
+      const int r = last_at_least(sm.samp, a, b, ~sm.csort[i]);
+      const float e = mass_hi + sm.cabove[i] + (r >= a ? sm.lcum[r] : 0.f);
+      if (e >= want) {
+        fc = i;
+        break;
+      }
+    }
+    fs = block_min_i(fs, sm);
+    fc = block_min_i(fc, sm);
+    uint32_t kp = lo + 1;                       // nothing reaches it: the bottom
+    if (fs < b) kp = ~sm.samp[fs];
+    if (fc < cb && ~sm.csort[fc] > kp) kp = ~sm.csort[fc];
+    piv[t] = kp;
+  }
+}
+
+// Sort the sample once (descending keys, invalid points last); x.ns = valid points.
+__device__ void sort_sample(Ctx &x, Smem &sm) {
+  if (x.ns >= 0) return;
+  const int nsamp = x.r.nch * x.spc;
+  const int np = pow2_at_least(nsamp);
+  for (int i = nsamp + threadIdx.x; i < np; i += kT) sm.samp[i] = ~0u;
+  __syncthreads();
+  bitonic_sort(sm.samp, np);
+  unsigned long long valid = 0;
+  for (int i = threadIdx.x; i < nsamp; i += kT) valid += sm.samp[i] != ~0u;
+  x.ns = (int)block_sum_u(valid, sm);
+}
+
+// Sample points strictly inside (lo, hi): positions [a, b) of the sorted sample.
+__device__ void sample_span(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi, int &a,
+                            int &b) {
+  unsigned long long ge_hi = 0, gt_lo = 0;
+  for (int i = threadIdx.x; i < x.ns; i += kT) {
+    const uint32_t kk = ~sm.samp[i];
+    ge_hi += (unsigned long long)kk >= hi;
+    gt_lo += kk > lo;
+  }
+  a = (int)block_sum_u(ge_hi, sm);
+  b = (int)block_sum_u(gt_lo, sm);
+}
+
+// Pivots strictly inside (lo, hi), non-increasing.
+__device__ __forceinline__ void clamp_pivots(uint32_t piv[4], uint32_t lo, unsigned long long hi) {
+  for (int t = 0; t < 4; ++t) {
+    if ((unsigned long long)piv[t] >= hi) piv[t] = (uint32_t)(hi - 1);
+    if (piv[t] <= lo) piv[t] = lo + 1;
+    if (t && piv[t] > piv[t - 1]) piv[t] = piv[t - 1];
+  }
+}
+
+// Tighten [lo, hi) (with the counts and masses at lo and at hi) until it holds
+// at most kCap logits or a single key.  Target: the k-th logit (count(>= X)
+// >= k) or the top-p boundary (mass(>= X) >= tau).  Pivots are sample points
+// around the sample's estimate of the target while the sample has enough
+// points inside, else the key range split in five.  False if the probes ran out.
+template <bool kBf16>
+__device__ bool narrow(Ctx &x, Smem &sm, bool want_mass, unsigned long long k, float tau,
+                       uint32_t &lo, unsigned long long &hi, unsigned long long &cnt_lo,
+                       float &mass_lo, unsigned long long &cnt_hi, float &mass_hi) {
+  const int s = kChunk / x.spc;                // logits per sample point
+  sort_sample(x, sm);
+  float spread = 0.16f * x.S;                   // top-p pivot spread; widens after a miss
+  for (int it = 0; it < kMaxProbes; ++it) {
+    if (cnt_lo - cnt_hi <= (unsigned long long)kCap || hi - lo <= 1) return true;
+    int a, b;
+    sample_span(x, sm, lo, hi, a, b);
+    uint32_t piv[4];
+    if (want_mass && it < kMaxProbes / 2) {
+      estimate_pivots(x, sm, lo, hi, a, b, s, fminf(spread, mass_lo - mass_hi), mass_hi, tau, piv);
+    } else if (b - a >= 8 && it < kMaxProbes / 2) {
+      // the k-th logit: the sample point at the estimated rank, and around it
+      long long need = ((long long)k - (long long)cnt_hi) / s;
+      if (need < 0) need = 0;
+      if (need > b - a - 1) need = b - a - 1;
+      const int centre = a + (int)need;
+      const int span = max(2, (int)(3.f * sqrtf((float)(centre - a + 1))) + 2);
+      const int q[4] = {centre - span, centre - span / 3, centre + span / 3, centre + span};
+      for (int t = 0; t < 4; ++t) piv[t] = ~sm.samp[min(b - 1, max(a, q[t]))];
+    } else {
+      const unsigned long long w = hi - lo;
+      for (int t = 0; t < 4; ++t) piv[t] = (uint32_t)(lo + (w * (unsigned long long)(4 - t)) / 5);
+    }
+    clamp_pivots(piv, lo, hi);
+    unsigned long long pc[4];
+    float pm[4];
+    probe<kBf16>(x, sm, piv, want_mass, pc, pm);
+    // the largest pivot that still holds the target becomes lo, the one above it hi
+    int sel = -1;
+    for (int t = 0; t < 4 && sel < 0; ++t)
+      if (want_mass ? pm[t] >= tau : pc[t] >= k) sel = t;
+    spread = (sel == 0 || sel < 0) ? spread * 4.f : spread * 0.5f;   // a miss widens
+    if (sel >= 0) {
+      if (sel > 0) {
+        hi = piv[sel - 1];
+        cnt_hi = pc[sel - 1];
+        mass_hi = pm[sel - 1];
+      }
+      lo = piv[sel];
+      cnt_lo = pc[sel];
+      mass_lo = pm[sel];
+    } else {
+      hi = piv[3];
+      cnt_hi = pc[3];
+      mass_hi = pm[3];
+    }
+  }
+  return cnt_lo - cnt_hi <= (unsigned long long)kCap || hi - lo <= 1;
+}
+
+// Ties: the window is the single key v, holding more logits than kCap.  Writes
+// per chunk the mass above v (cabove) and the count of v (cmass, as a float),
+// and returns the index of the t-th (0-based) logit equal to v in index order.
+template <bool kBf16>
+__device__ int tie_index(const Ctx &x, Smem &sm, uint32_t v, unsigned long long t) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for_chunks<kBf16>(
+      x.r, [&](int) { return true; }, [&](int) {},
+      [&](const float vv[kLE], int n, int, int c) {
+        float ma = 0.f;
+        int ties = 0;
+#pragma unroll
+        for (int j = 0; j < kLE; ++j) {
+          const uint32_t k = key_of(vv[j]);
+          if (j < n && k > v) ma += mass_of(x, vv[j]);
+          ties += j < n && k == v;
+        }
+        ma = warp_sum_f(ma);
+        ties = __reduce_add_sync(0xffffffffu, ties);
+        if (lane == 0) {
+          sm.cabove[c] = ma;
+          sm.cmass[c] = (float)ties;
+        }
+      });
+  __syncthreads();
+  const int per = (x.nl + kT - 1) / kT;
+  const int a = min(x.nl, (int)threadIdx.x * per), b = min(x.nl, a + per);
+  float s = 0.f;
+  for (int c = a; c < b; ++c) s += sm.cmass[c];
+  float tot;
+  float run = block_excl_scan_f(s, sm, &tot);
+  if (threadIdx.x == 0) {
+    sm.ival[1] = -1;
+    sm.ival[3] = -1;
+  }
+  __syncthreads();
+  for (int c = a; c < b; ++c) {
+    if (run <= (float)t && (float)t < run + sm.cmass[c]) {
+      sm.ival[1] = c;
+      sm.ival[2] = (int)((float)t - run);
+    }
+    run += sm.cmass[c];
+  }
+  __syncthreads();
+  const int c = sm.ival[1], want = sm.ival[2];
+  if (c >= 0 && warp == 0) {
+    float vv[kLE];
+    int i0;
+    const int n = chunk_lane<kBf16>(x.r, c, lane, vv, i0);
+    int mine = 0;
+#pragma unroll
+    for (int j = 0; j < kLE; ++j) mine += j < n && key_of(vv[j]) == v;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - mine;
+    if (excl <= want && want < incl) {
+      int r = excl;
+      for (int j = 0; j < n; ++j)
+        if (key_of(vv[j]) == v) {
+          if (r == want) sm.ival[3] = i0 + j;
+          ++r;
+        }
+    }
+  }
+  __syncthreads();
+  return sm.ival[3];
+}
+
+// The draw over the per-chunk kept masses in cabove: the chunk whose
+// cumulative mass first exceeds u times the total, then the token inside it.
+// Kept: key > vk, or key == vk and index <= ik.
+template <bool kBf16>
+__device__ int draw_chunks(const Ctx &x, Smem &sm, float u, uint32_t vk, int ik) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (x.nl + kT - 1) / kT;
+  const int a = min(x.nl, (int)threadIdx.x * per), b = min(x.nl, a + per);
+  float s = 0.f;
+  for (int c = a; c < b; ++c) s += sm.cabove[c];
+  float tot;
+  float run = block_excl_scan_f(s, sm, &tot);
+  const float U = u * tot;
+  if (threadIdx.x == 0) {
+    sm.ival[4] = -1;
+    sm.ival[5] = -1;
+  }
+  __syncthreads();
+  for (int c = a; c < b; ++c) {
+    const float K = sm.cabove[c];
+    if (K > 0.f) {
+      if (run <= U && U < run + K) {
+        sm.ival[4] = c;
+        sm.fval[0] = U - run;
+      }
+      atomicMax(&sm.ival[5], c);               // the last chunk with mass (rounding fallback)
+    }
+    run += K;
+  }
+  __syncthreads();
+  int c = sm.ival[4];
+  float target = sm.fval[0];
+  if (c < 0) {                                  // u * total rounded past the last mass
+    c = sm.ival[5];
+    target = INFINITY;
+  }
+  if (warp == 0 && c >= 0) {
+    float v[kLE];
+    int i0;
+    const int n = chunk_lane<kBf16>(x.r, c, lane, v, i0);
+    float m[kLE], mine = 0.f;
+    int last = -1;
+#pragma unroll
+    for (int j = 0; j < kLE; ++j) {
+      const uint32_t k = key_of(v[j]);
+      const bool kept = j < n && (k > vk || (k == vk && i0 + j <= ik));
+      m[j] = kept ? mass_of(x, v[j]) : 0.f;
+      if (m[j] > 0.f) last = i0 + j;
+      mine += m[j];
+    }
+    float incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, incl > target && mine > 0.f);
+    int tok = -1;
+    if (hit) {
+      const int hl = __ffs(hit) - 1;
+      if (lane == hl) {
+        float acc = incl - mine;
+        for (int j = 0; j < kLE; ++j)
+          if (m[j] > 0.f) {
+            acc += m[j];
+            if (acc > target) {
+              tok = i0 + j;
+              break;
+            }
+          }
+        if (tok < 0) tok = last;
+      }
+      tok = __shfl_sync(0xffffffffu, tok, hl);
+    } else {
+      // rounding left the target past the chunk: its last kept token
+      const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
+      if (has) tok = __shfl_sync(0xffffffffu, last, 31 - __clz(has));
+    }
+    if (lane == 0) sm.ival[6] = tok;
+  }
+  __syncthreads();
+  return c >= 0 ? sm.ival[6] : -1;
+}
+
+// Rewrite the first n window entries as (index << 32) | mass bits, sorted by index.
+__device__ void window_by_index(const Ctx &x, Smem &sm, int n) {
+  for (int i = threadIdx.x; i < n; i += kT) {
+    const unsigned long long e = sm.list[i];
+    const float l = value_of(~(uint32_t)(e >> 32));
+    sm.list[i] = ((unsigned long long)(uint32_t)e << 32) | __float_as_uint(mass_of(x, l));
+  }
+  const int np = pow2_at_least(n);
+  for (int i = n + threadIdx.x; i < np; i += kT) sm.list[i] = ~0ull;
+  __syncthreads();
+  bitonic_sort(sm.list, np);
+}
+
+// The draw when the whole kept set is the first n window entries.
+__device__ int draw_list(const Ctx &x, Smem &sm, int n, float u) {
+  window_by_index(x, sm, n);
+  const int per = (n + kT - 1) / kT;
+  const int a = min(n, (int)threadIdx.x * per), b = min(n, a + per);
+  float s = 0.f;
+  for (int i = a; i < b; ++i) s += __uint_as_float((uint32_t)sm.list[i]);
+  float tot;
+  float run = block_excl_scan_f(s, sm, &tot);
+  const float U = u * tot;
+  if (threadIdx.x == 0) sm.ival[7] = -1;
+  __syncthreads();
+  int last = -1;
+  for (int i = a; i < b; ++i) {
+    const float m = __uint_as_float((uint32_t)sm.list[i]);
+    if (m > 0.f) {
+      if (run <= U && U < run + m) sm.ival[7] = (int)(sm.list[i] >> 32);
+      last = (int)(sm.list[i] >> 32);
+    }
+    run += m;
+  }
+  __syncthreads();
+  const int tok = sm.ival[7];
+  if (tok >= 0) return tok;
+  return (int)block_max_u((unsigned long long)(last + 1), sm) - 1;   // rounding: the last one
+}
+
+// Per-chunk summaries written by the scan kernel for the row kernel.
+struct WsRef {
+  float *cmax, *cmass;                         // [row][nl_cap]
+  uint32_t *samp;                              // [row][ns_cap]
+  unsigned long long *best;                    // [row][nparts]: greedy key of the part
+  uint32_t *bad;                               // [row][nparts]: a non-finite logit seen
+  int nl_cap, ns_cap, nparts;
+};
+
+constexpr int kScanThreads = 256;
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kChunksPerCta = 64;              // vector chunks of a scan CTA (16384 logits)
+constexpr int kScanPerWarp = kChunksPerCta / kScanWarps;
+
+// ---- the scan (HBM, once): per chunk its maximum and its mass relative to
+// it, the sample, the part's first maximum and finiteness.  Grid (parts, rows).
+template <bool kBf16, bool kGreedy>
+__global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams p, WsRef ws) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int part = blockIdx.x, row = blockIdx.y;
+  const RowRef r = row_ref<kBf16>(p.logits + (int64_t)row * p.row_bytes, p.vocab);
+  const int spc = r.nch <= kMaxSamples / 4 ? 4 : 2;
+  float kx = 0.f;
+  if (!kGreedy) kx = 1.4426950408889634f / fmaxf(p.temperature[row], kMinT);
+  float *cmax = ws.cmax + (int64_t)row * ws.nl_cap, *cmass = ws.cmass + (int64_t)row * ws.nl_cap;
+  uint32_t *samp = ws.samp + (int64_t)row * ws.ns_cap;
+  bool finite = true;
+  unsigned long long best = 0;                  // (key << 32) | ~index, max wins
+  auto chunk = [&](const float v[kLE], int n, int c_logical, int i0, int sample_slot) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kLE; ++j)
+      if (j < n) {
         if (kGreedy) {
-          const unsigned long long key = ((unsigned long long)orderable(v[u][e] + 0.f) << 32) |
-                                         (0xffffffffu - (uint32_t)(lo + h + 8 * c + e));
-          best = key > best ? key : best;
+          finite &= v[j] == v[j];               // NaN
+          const unsigned long long kk =
+              ((unsigned long long)key_of(v[j]) << 32) | (0xffffffffu - (uint32_t)(i0 + j));
+          best = kk > best ? kk : best;
         } else {
-          vmax = fmaxf(vmax, v[u][e]);
+          m = fmaxf(m, v[j]);
         }
       }
-      if (!kGreedy) {
-        uint4 *dst = reinterpret_cast<uint4 *>(val + off + h + 8 * c);
-        dst[0] = make_uint4(__float_as_uint(v[u][0]), __float_as_uint(v[u][1]),
-                            __float_as_uint(v[u][2]), __float_as_uint(v[u][3]));
-        dst[1] = make_uint4(__float_as_uint(v[u][4]), __float_as_uint(v[u][5]),
-                            __float_as_uint(v[u][6]), __float_as_uint(v[u][7]));
+    if (!kGreedy) {
+      m = warp_max_f(m);
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < kLE; ++j)
+        if (j < n) s += ex2((v[j] - m) * kx);
+      s = warp_sum_f(s);
+      // a NaN turns the mass into NaN, +inf the maximum; -inf is a zero-mass logit
+      if (m == -INFINITY) s = 0.f;
+      finite &= m != INFINITY && s == s;
+      if (lane == 0) {
+        cmax[c_logical] = m;
+        cmass[c_logical] = s;
       }
+      if (sample_slot >= 0) samp[sample_slot] = (n && v[0] != m) ? ~key_of(v[0]) : ~0u;
+    }
+  };
+  const int cbeg = part * kChunksPerCta + warp;
+  uint4 raw[kScanPerWarp][kBf16 ? 1 : 2];
+  int n[kScanPerWarp];
+#pragma unroll
+  for (int q = 0; q < kScanPerWarp; ++q) {     // every load of the warp in flight at once
+    const int c = cbeg + q * kScanWarps, vi = 32 * c + lane;
+    n[q] = (c < r.nch && vi < r.nvec) ? kLE : 0;
+    if (n[q]) {
+      const uint8_t *src = r.p + (int64_t)(r.h + kLE * vi) * (kBf16 ? 2 : 4);
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(raw[q][0].x), "=r"(raw[q][0].y), "=r"(raw[q][0].z), "=r"(raw[q][0].w)
+                   : "l"(src));
+      if (!kBf16)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(raw[q][kBf16 ? 0 : 1].x), "=r"(raw[q][kBf16 ? 0 : 1].y),
+                       "=r"(raw[q][kBf16 ? 0 : 1].z), "=r"(raw[q][kBf16 ? 0 : 1].w)
+                     : "l"(src + 16));
     }
   }
-  if (tid < h) take(load1<kBf16>(sp, tid), tid);                      // head
-  {
-    const int j = h + 8 * nchunk + (tid - 32);                      // ragged end (warp 1)
-    if (tid >= 32 && j < n && tid < 40) take(load1<kBf16>(sp, j), j);
+#pragma unroll
+  for (int q = 0; q < kScanPerWarp; ++q) {
+    const int c = cbeg + q * kScanWarps;
+    if (c >= r.nch) break;                      // warp-uniform
+    float v[kLE];
+    if (kBf16) {
+      const uint4 w = raw[q][0];
+      v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+      v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+    } else {
+      const uint4 a = raw[q][0], b = raw[q][kBf16 ? 0 : 1];
+      v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+      v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+      v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+      v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+    }
+    const int every = 32 / spc;
+    const int slot = (lane & (every - 1)) == 0 ? c * spc + lane / every : -1;
+    chunk(v, n[q], c + 1, r.h + kLE * (32 * c + lane), slot);
   }
-  if (!kGreedy) {                                                   // pads
-    if (tid >= 64 && tid < 64 + off) val[tid - 64] = kPadBits;
-    const int i = off + n + (tid - 96);
-    if (tid >= 96 && tid < 100 && i < 4 * n4) val[i] = kPadBits;
+  if (part == 0 && warp == 0) {                 // head and tail chunks
+    for (int c = 0; c < r.nch + 2; c += r.nch + 1) {
+      float v[kLE];
+      int i0;
+      const int nn = chunk_lane<kBf16>(r, c, lane, v, i0);
+      chunk(v, nn, c, i0, -1);
+    }
   }
-  // block reduce, publish, cluster reduce
-  const int any_bad = __syncthreads_or(!finite);
+  const bool bad = __syncthreads_or(!finite);
   if (kGreedy) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
       best = y > best ? y : best;
     }
-    if (lane == 0) sh.scan[warp] = best;
-  } else {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-    if (lane == 0) sh.scan[warp] = __float_as_uint(vmax);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    unsigned long long r = 0;
-    float m = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) {
-      if (kGreedy) r = sh.scan[w] > r ? sh.scan[w] : r;
-      else m = fmaxf(m, __uint_as_float((uint32_t)sh.scan[w]));
+    __shared__ unsigned long long wbest[kScanWarps];
+    if (lane == 0) wbest[warp] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kScanWarps; ++w) best = wbest[w] > best ? wbest[w] : best;
+      ws.best[(int64_t)row * ws.nparts + part] = best;
     }
-    sh.scal[0][0] = kGreedy ? r : (unsigned long long)__float_as_uint(m);
-    sh.scal[0][1] = any_bad ? 1ull : 0ull;
   }
-  cluster_barrier();
-  unsigned long long red = 0;
-  float M = -INFINITY;
+  if (threadIdx.x == 0) ws.bad[(int64_t)row * ws.nparts + part] = bad ? 1u : 0u;
+  grid_dep_launch();
+}
+
+// ---- the row (one CTA each): everything after the scan
+template <bool kBf16, bool kGreedy>
+__global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef ws) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row = blockIdx.x;
+  Ctx x;
+  x.r = row_ref<kBf16>(p.logits + (int64_t)row * p.row_bytes, p.vocab);
+  x.nl = x.r.nch + 2;
+  x.spc = x.r.nch <= kMaxSamples / 4 ? 4 : 2;
+  x.ns = -1;                                    // the sample is sorted on first use
+  x.M = 0.f;
+
+  // ---- row parameters (Sampler.prepare's clamps)
+  float T = 1.f, u = 0.f, P = 1.f;
+  unsigned long long k = (unsigned long long)p.vocab;
+  bool params_ok = true;
+  if (!kGreedy) {
+    T = p.temperature[row];
+    u = p.uniform[row];
+    if (p.top_k != nullptr && p.top_k[row] >= 1 && p.top_k[row] < p.vocab) k = p.top_k[row];
+    if (p.top_p != nullptr) {
+      P = fminf(fmaxf(p.top_p[row], kMinP), 1.f);
+      params_ok = !isnan(p.top_p[row]);
+    }
+    params_ok = params_ok && isfinite(T) && u >= 0.f && u < 1.f;
+  }
+  x.kx = 1.4426950408889634f / fmaxf(T, kMinT);
+  grid_dep_wait();                              // the scan's summaries
   bool bad = false;
-  for (int c = 0; c < C; ++c) {
-    const unsigned long long a = ld_cluster_u64(&sh.scal[0][0], (uint32_t)c);
-    bad |= ld_cluster_u64(&sh.scal[0][1], (uint32_t)c) != 0;
-    if (kGreedy) red = a > red ? a : red;
-    else M = fmaxf(M, __uint_as_float((uint32_t)a));
-  }
-  if (kGreedy) {
-    if (tid == 0 && rank == 0) {
-      if (bad) {
-        report(p.status, MSG_DEV_BAD_LOGIT, row, 0);
-        p.tokens[row] = -1;
-      } else {
-        p.tokens[row] = (int32_t)(0xffffffffu - (uint32_t)(red & 0xffffffffu));
-      }
+  unsigned long long best = 0;
+  for (int i = threadIdx.x; i < ws.nparts; i += kT) {
+    bad |= ws.bad[(int64_t)row * ws.nparts + i] != 0;
+    if (kGreedy) {
+      const unsigned long long b = ws.best[(int64_t)row * ws.nparts + i];
+      best = b > best ? b : best;
     }
-    cluster_barrier();                         // no CTA leaves while its scalars are read
+  }
+  bad = __syncthreads_or(bad);
+  if (kGreedy) {
+    best = block_max_u(best, sm);
+    if (threadIdx.x == 0) {
+      if (bad) report(p.status, MSG_DEV_BAD_LOGIT, row, 0);
+      p.tokens[row] = bad ? -1 : (int32_t)(0xffffffffu - (uint32_t)(best & 0xffffffffu));
+    }
     return;
   }
-
-  // ---- row parameters (Sampler.prepare's clamps), identical in every CTA
-  const float T = p.temperature[row];
-  const float u = p.uniform[row];
-  int64_t k = p.vocab;
-  if (p.top_k != nullptr && p.top_k[row] >= 1 && p.top_k[row] < p.vocab) k = p.top_k[row];
-  float P = 1.f;
-  if (p.top_p != nullptr) P = fminf(fmaxf(p.top_p[row], kMinP), 1.f);
-  const bool params_ok = isfinite(T) && u >= 0.f && u < 1.f &&
-                         (p.top_p == nullptr || !isnan(p.top_p[row]));
   if (bad || !params_ok) {
-    if (tid == 0 && rank == 0) {
+    if (threadIdx.x == 0) {
       report(p.status, bad ? MSG_DEV_BAD_LOGIT : MSG_DEV_BAD_SAMPLING, row, 0);
       p.tokens[row] = -1;
     }
-    cluster_barrier();
     return;
   }
-  const bool topk_on = k < p.vocab;
-  const bool topp_on = P < 1.f;
-  // (l - max) * log2(e) / T, then 2^x: the pages' softmax(logits / T) numerator
-  const float kx = 1.4426950408889634f / fmaxf(T, kMinT);
-
-  // ---- pass 1: e = exp((l - max) / T) in place (pads stay above every key),
-  //      and the first digit's histogram when a cut is on
-  int slot = 1;
-  const bool hist1 = topk_on || topp_on;
-  if (hist1) {
-    sh.hist[slot][tid] = 0;
-    __syncthreads();
-  }
-  for (int g = tid; g < n4; g += kThreads) {
-    uint4 w = reinterpret_cast<uint4 *>(val)[g];
-    uint32_t b[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = 4 * g + q - off;            // element of the slice, or a pad
-      if (j >= 0 && j < n) b[q] = __float_as_uint(ex2((__uint_as_float(b[q]) - M) * kx));
-      else b[q] = kPadBits;
-      if (hist1) {
-        const uint32_t key = key_of(b[q]);
-        if ((key >> 30) == 0)
-          atomicAdd(&sh.hist[slot][key >> 22], topk_on ? 1ull : mass_of(b[q]));
-      }
-    }
-    reinterpret_cast<uint4 *>(val)[g] = make_uint4(b[0], b[1], b[2], b[3]);
-  }
-  __syncthreads();                              // the draw reads other threads' groups
-
-  // ---- top-k: the key d_k of rank k-1 (ascending key, ties in token order)
-  uint32_t dk = 0x7fffffffu;                    // every real key is below this when top-k is off
-  unsigned long long rk = 0, ties_k = 0;        // ties of d_k kept, ties of d_k in all
-  bool ok = true;
-  if (topk_on) {
-    uint32_t prefix = 0;
-    unsigned long long need = (unsigned long long)k;
-    for (int d = 0; d < 4; ++d) {
-      const int sh_ = digit_shift(d), wd = digit_width(d), hi = sh_ + wd;
-      if (d > 0) {
-        slot ^= 1;
-        sh.hist[slot][tid] = 0;
-        __syncthreads();
-        for (int g = tid; g < n4; g += kThreads) {
-          const uint4 w = reinterpret_cast<const uint4 *>(val)[g];
-          const uint32_t b[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t key = key_of(b[q]);
-            if ((key >> hi) == (prefix >> hi))
-              atomicAdd(&sh.hist[slot][(key >> sh_) & ((1u << wd) - 1)], 1ull);
-          }
-        }
-      }
-      cluster_barrier();
-      ok &= select_bucket(sh, slot, C, need, -1, 0, nullptr);
-      if (!ok) break;
-      need -= sh.pick64[0];
-      prefix |= sh.pick[0] << sh_;
-      if (d == 3) ties_k = sh.pick64[1];
-    }
-    dk = prefix;
-    rk = need;
-  }
-
-  // ---- top-p over the top-k set: the key d_p where the mass ranked ahead
-  //      first reaches tau = ceil(P * S_k), and how many of its ties stay
-  uint32_t dsel = topk_on ? dk : kOneBits + 1; // final threshold key
-  unsigned long long tsel = topk_on ? rk : 0;  //   and ties of it kept
-  if (ok && topp_on) {
-    const unsigned long long wk = topk_on ? mass_of(kOneBits - dk) : 0;
-    const unsigned long long drop = topk_on ? (ties_k - rk) * wk : 0;
-    uint32_t prefix = 0;
-    unsigned long long tau = 0, A = 0, wsel = 0;
-    for (int d = 0; d < 4; ++d) {
-      const int sh_ = digit_shift(d), wd = digit_width(d), hi = sh_ + wd;
-      if (d > 0 || topk_on) {
-        slot ^= 1;
-        sh.hist[slot][tid] = 0;
-        __syncthreads();
-        for (int g = tid; g < n4; g += kThreads) {
-          const uint4 w = reinterpret_cast<const uint4 *>(val)[g];
-          const uint32_t b[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t key = key_of(b[q]);
-            if ((key >> hi) == (prefix >> hi) && key <= dk)
-              atomicAdd(&sh.hist[slot][(key >> sh_) & ((1u << wd) - 1)], mass_of(b[q]));
-          }
-        }
-      }
-      cluster_barrier();
-      // the ties of d_k beyond the first rk are not in the top-k set
-      const int adj = (topk_on && (dk >> hi) == (prefix >> hi)) ? (int)((dk >> sh_) & ((1u << wd) - 1)) : -1;
-      if (d == 0) {
-        unsigned long long S = 0;
-        // first the total (S_k), then the selection against tau
-        const int b = tid;
-        unsigned long long h = 0;
-        for (int c = 0; c < C; ++c) h += ld_cluster_u64(&sh.hist[slot][b], (uint32_t)c);
-        if (b == adj) h -= drop;
-        S = warp_sum(h);
-        if (lane == 0) sh.scan[warp] = S;
-        __syncthreads();
-        S = 0;
-        for (int w = 0; w < kWarps; ++w) S += sh.scan[w];
-        __syncthreads();
-        tau = (unsigned long long)ceil((double)P * (double)S);
-      }
-      ok &= select_bucket(sh, slot, C, tau - A, adj, drop, nullptr);
-      if (!ok) break;
-      A += sh.pick64[0];
-      prefix |= sh.pick[0] << sh_;
-      if (d == 3) wsel = sh.pick64[1];
-    }
-    if (ok) {
-      // every tie of d_p has the same mass w; keep ties while the mass ahead
-      // of them is below tau
-      const unsigned long long w = mass_of(kOneBits - prefix);
-      const unsigned long long avail = w ? wsel / w : 0;
-      unsigned long long nt = w ? (tau - A + w - 1) / w : 0;
-      if (nt < 1) nt = 1;
-      if (nt > avail) nt = avail;
-      ok = w != 0 && avail != 0;
-      dsel = prefix;
-      tsel = nt;
-    }
-  }
-
-  // ---- the draw, part 1: per warp (contiguous ranges) and per CTA, the
-  //      mass of keys below dsel and the count of keys equal to it
-  const int G = (n4 + kWarps - 1) / kWarps;    // groups of 4 per warp
-  const int g0 = warp * G, g1 = min(n4, g0 + G);
-  unsigned long long mlt = 0, teq = 0;
-  for (int g = g0 + lane; g < g1; g += 32) {
-    const uint4 w = reinterpret_cast<const uint4 *>(val)[g];
-    const uint32_t b[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t key = key_of(b[q]);
-      if (key < dsel) mlt += mass_of(b[q]);
-      teq += key == dsel;
-    }
-  }
-  mlt = warp_sum(mlt);
-  teq = warp_sum(teq);
-  if (lane == 0) {
-    sh.wmass[warp] = mlt;
-    sh.wties[warp] = (uint32_t)teq;
-  }
-  __syncthreads();
-  if (tid == 0) {                               // scal[0] held pass 0's values: use scal[1]
-    unsigned long long a = 0, t = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      a += sh.wmass[w];
-      t += sh.wties[w];
-    }
-    sh.scal[1][0] = a;
-    sh.scal[1][1] = t;
-  }
-  cluster_barrier();
-  const unsigned long long wd = dsel <= kOneBits ? mass_of(kOneBits - dsel) : 0;
-  unsigned long long S = 0, base = 0, tie_base = 0, ties_before = 0;
-  int cstar = -1;
   {
-    unsigned long long Kc[kMaxCluster], tc[kMaxCluster];
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {
-      Kc[c] = tc[c] = 0;
-      if (c >= C) continue;
-      const unsigned long long m = ld_cluster_u64(&sh.scal[1][0], (uint32_t)c);
-      tc[c] = ld_cluster_u64(&sh.scal[1][1], (uint32_t)c);
-      const unsigned long long keep =
-          tsel > ties_before ? (tsel - ties_before < tc[c] ? tsel - ties_before : tc[c]) : 0;
-      Kc[c] = m + keep * wd;
-      ties_before += tc[c];
-      S += Kc[c];
+    const float *cmax = ws.cmax + (int64_t)row * ws.nl_cap, *cmass = ws.cmass + (int64_t)row * ws.nl_cap;
+    float m = -INFINITY;
+    for (int c = threadIdx.x; c < x.nl; c += kT) {
+      sm.cmax[c] = cmax[c];
+      sm.cmass[c] = cmass[c];
+      m = fmaxf(m, sm.cmax[c]);
     }
-    const unsigned long long U = (unsigned long long)floor((double)u * (double)S);
-    unsigned long long run = 0, tb = 0;
-#pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) {
-      if (c >= C) break;
-      if (cstar < 0 && run + Kc[c] > U) {
-        cstar = c;
-        base = U - run;                         // target inside CTA c: first cum > base
-        tie_base = tb;
-      }
-      run += Kc[c];
-      tb += tc[c];
-    }
+    x.M = block_max_f(m, sm);
   }
-  cluster_barrier();                            // every remote read is done
-  if (!ok || S == 0 || cstar < 0) {
-    if (tid == 0 && rank == 0) {
-      report(p.status, MSG_DEV_INTERNAL, row, 0);
+  if (x.M == -INFINITY) {                       // every logit -inf: no distribution
+    if (threadIdx.x == 0) {
+      report(p.status, MSG_DEV_BAD_LOGIT, row, 1);
       p.tokens[row] = -1;
     }
     return;
   }
-  if ((int)rank != cstar) return;
-
-  // ---- the draw, part 2 (one CTA): the warp, then the token
-  int wstar = -1;
-  unsigned long long wbase = 0, wtie = 0;
+  float S;                                      // chunk masses relative to the row maximum
   {
-    unsigned long long run = 0, tb = tie_base;
-    for (int w = 0; w < kWarps; ++w) {
-      const unsigned long long keep =
-          tsel > tb ? (tsel - tb < sh.wties[w] ? tsel - tb : sh.wties[w]) : 0;
-      const unsigned long long Kw = sh.wmass[w] + keep * wd;
-      if (wstar < 0 && run + Kw > base) {
-        wstar = w;
-        wbase = base - run;
-        wtie = tb;
-      }
-      run += Kw;
-      tb += sh.wties[w];
+    float part = 0.f;
+    for (int c = threadIdx.x; c < x.nl; c += kT) {
+      const float cm = sm.cmass[c] > 0.f ? sm.cmass[c] * ex2((sm.cmax[c] - x.M) * x.kx) : 0.f;
+      sm.cmass[c] = cm;
+      part += cm;
     }
+    S = block_sum_f(part, sm);
+    x.S = S;
   }
-  if (warp != wstar) return;
-  unsigned long long run = 0, ties = wtie;
-  for (int gb = g0; gb < g1; gb += 32) {
-    const int g = gb + lane;
-    uint32_t b[4] = {kPadBits, kPadBits, kPadBits, kPadBits};
-    if (g < g1) {
-      const uint4 w = reinterpret_cast<const uint4 *>(val)[g];
-      b[0] = w.x; b[1] = w.y; b[2] = w.z; b[3] = w.w;
+  const bool topk_on = k < (unsigned long long)p.vocab;
+  const bool topp_on = P < 1.f;
+  int tok = -1;
+  if (!topk_on && !topp_on) {
+    // ---- no cut: the chunk masses are the kept masses
+    for (int c = threadIdx.x; c < x.nl; c += kT) sm.cabove[c] = sm.cmass[c];
+    __syncthreads();
+    tok = draw_chunks<kBf16>(x, sm, u, 0u, p.vocab);
+  } else {
+    {                                           // the sample (sorted on first use)
+      const uint32_t *samp = ws.samp + (int64_t)row * ws.ns_cap;
+      for (int i = threadIdx.x; i < x.r.nch * x.spc; i += kT) sm.samp[i] = samp[i];
     }
-    uint32_t my_ties = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) my_ties += key_of(b[q]) == dsel;
-    uint32_t tie_excl = my_ties;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, tie_excl, o);
-      if (lane >= o) tie_excl += y;
-    }
-    const uint32_t tie_total = __shfl_sync(0xffffffffu, tie_excl, 31);
-    tie_excl -= my_ties;
-    unsigned long long m[4], mine = 0;
-#pragma unroll
-    for (int q = 0, t = 0; q < 4; ++q) {
-      const uint32_t key = key_of(b[q]);
-      m[q] = 0;
-      if (key < dsel) m[q] = mass_of(b[q]);
-      else if (key == dsel) {
-        if (ties + tie_excl + t < tsel) m[q] = wd;
-        ++t;
-      }
-      mine += m[q];
-    }
-    unsigned long long incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const unsigned int hit = __ballot_sync(0xffffffffu, run + incl > wbase);
-    if (hit) {
-      if (lane == __ffs(hit) - 1) {
-        unsigned long long acc = run + incl - mine;
-        int q = 0;
-        for (; q < 3; ++q) {
-          acc += m[q];
-          if (acc > wbase) break;
+    // chunk maxima sorted by descending key (invalid chunks last)
+    const int npc = pow2_at_least(x.nl);
+    for (int i = threadIdx.x; i < npc; i += kT)
+      sm.csort[i] = (i < x.nl && sm.cmax[i] != -INFINITY) ? ~key_of(sm.cmax[i]) : ~0u;
+    __syncthreads();
+    bitonic_sort(sm.csort, npc);
+    bool ok = true, tie_mode = false;
+    uint32_t vk = 0;                            // the threshold token: its key and index
+    int ik = -1;
+    int n_win = 0;                              // kept entries at the head of the list
+    unsigned long long cnt_above = 0;           // logits above the window
+    float mass_above = 0.f;
+    uint32_t region_lo = 0;                     // where stage 2 may search
+    float S_k = S;
+    // ---- stage 1: the k-th token
+    if (topk_on) {
+      bool gathered = false;
+      if (k <= (unsigned long long)x.nl) {
+        // the k-th largest chunk maximum bounds the k-th logit from below
+        const uint32_t kk = sm.csort[k - 1];
+        if (kk != ~0u) {
+          n_win = gather<kBf16>(x, sm, ~kk, kKeyEnd, &cnt_above, &mass_above);
+          gathered = n_win <= kCap;
         }
-        p.tokens[row] = (int32_t)(lo + 4 * (int64_t)g + q - off);
       }
-      return;
+      if (!gathered) {
+        uint32_t lo = 0;
+        unsigned long long hi = kKeyEnd, cnt_lo = (unsigned long long)p.vocab, cnt_hi = 0;
+        float mass_lo = S, mass_hi = 0.f;
+        ok = narrow<kBf16>(x, sm, false, k, 0.f, lo, hi, cnt_lo, mass_lo, cnt_hi, mass_hi);
+        if (ok && cnt_lo - cnt_hi <= (unsigned long long)kCap) {
+          n_win = gather<kBf16>(x, sm, lo, hi, &cnt_above, &mass_above);
+          ok = n_win <= kCap && cnt_above < k && k <= cnt_above + (unsigned long long)n_win;
+          region_lo = hi >= kKeyEnd ? 0xffffffffu : (uint32_t)hi;
+        } else if (ok) {
+          tie_mode = true;                      // one key with more logits than kCap
+          vk = lo;
+          cnt_above = cnt_hi;
+          region_lo = vk + 1;
+        }
+      }
+      if (ok && !tie_mode) {
+        sort_window(x, sm, n_win);
+        const int pk = (int)(k - cnt_above - 1);
+        vk = ~(uint32_t)(sm.list[pk] >> 32);
+        ik = (int)(uint32_t)sm.list[pk];
+        S_k = mass_above + sm.lcum[pk];
+        n_win = pk + 1;
+      } else if (ok) {
+        const unsigned long long t = k - cnt_above - 1;
+        ik = tie_index<kBf16>(x, sm, vk, t);
+        float part = 0.f;
+        for (int c = threadIdx.x; c < x.nl; c += kT) part += sm.cabove[c];
+        mass_above = block_sum_f(part, sm);
+        S_k = mass_above + (float)(t + 1) * mass_of(x, value_of(vk));
+        ok = ik >= 0;
+      }
     }
-    run += __shfl_sync(0xffffffffu, incl, 31);
-    ties += tie_total;
+    // ---- stage 2: the top-p boundary inside the top-k set
+    if (ok && topp_on) {
+      const float tau = P * S_k;
+      if (topk_on && mass_above < tau) {
+        if (!tie_mode) {                        // inside the sorted window
+          const int pp = window_crossing(sm, n_win, mass_above, tau);
+          const int pos = min(pp, n_win - 1);
+          vk = ~(uint32_t)(sm.list[pos] >> 32);
+          ik = (int)(uint32_t)sm.list[pos];
+          n_win = pos + 1;
+        } else {                                // inside the tie group
+          const float w = mass_of(x, value_of(vk));
+          unsigned long long t = w > 0.f ? (unsigned long long)ceilf((tau - mass_above) / w) : 1;
+          t = max(1ull, min(t, k - cnt_above));
+          ik = tie_index<kBf16>(x, sm, vk, t - 1);
+          ok = ik >= 0;
+        }
+      } else {
+        // the boundary lies above the top-k window (or there is no top-k)
+        uint32_t lo = topk_on ? region_lo : 0;
+        unsigned long long hi = kKeyEnd;
+        unsigned long long cnt_lo = topk_on ? cnt_above : (unsigned long long)p.vocab, cnt_hi = 0;
+        float mass_lo = topk_on ? mass_above : S, mass_hi = 0.f;
+        tie_mode = false;
+        // the largest chunk maxima are logits of their own: the first r of them
+        // whose masses reach tau put the boundary at or above the r-th
+        const uint32_t cm = chunk_max_bound(x, sm, lo, tau);
+        bool gathered = false, sorted = false;
+        if (cm != 0u) {
+          n_win = gather<kBf16>(x, sm, cm, kKeyEnd, &cnt_above, &mass_above);
+          gathered = n_win <= kCap;
+        }
+        if (!gathered) {
+          // one gather around the estimate; a miss still tells which side
+          sort_sample(x, sm);
+          int a, b;
+          sample_span(x, sm, lo, hi, a, b);
+          uint32_t piv[4];
+          estimate_pivots(x, sm, lo, hi, a, b, kChunk / x.spc, fminf(0.1f * x.S, mass_lo - mass_hi),
+                          mass_hi, tau, piv);
+          clamp_pivots(piv, lo, hi);
+          n_win = gather<kBf16>(x, sm, piv[3], piv[0], &cnt_above, &mass_above);
+          if (n_win <= kCap) {
+            sort_window(x, sm, n_win);
+            const float wm = n_win > 0 ? sm.lcum[n_win - 1] : 0.f;
+            if (mass_above < tau && tau <= mass_above + wm) {
+              gathered = sorted = true;
+            } else if (mass_above >= tau) {
+              lo = piv[0];
+              cnt_lo = cnt_above;
+              mass_lo = mass_above;
+            } else {
+              hi = piv[3];
+              cnt_hi = cnt_above + (unsigned long long)n_win;
+              mass_hi = mass_above + wm;
+            }
+          } else if (mass_above >= tau) {
+            lo = piv[0];
+            cnt_lo = cnt_above;
+            mass_lo = mass_above;
+          }
+        }
+        if (!gathered)
+          ok = narrow<kBf16>(x, sm, true, 0, tau, lo, hi, cnt_lo, mass_lo, cnt_hi, mass_hi);
+        if (gathered || (ok && cnt_lo - cnt_hi <= (unsigned long long)kCap)) {
+          if (!gathered) n_win = gather<kBf16>(x, sm, lo, hi, &cnt_above, &mass_above);
+          ok = n_win <= kCap && n_win > 0;
+          if (ok) {
+            if (!sorted) sort_window(x, sm, n_win);
+            const int pp = window_crossing(sm, n_win, mass_above, tau);
+            const int pos = min(pp, n_win - 1);
+            vk = ~(uint32_t)(sm.list[pos] >> 32);
+            ik = (int)(uint32_t)sm.list[pos];
+            n_win = pos + 1;
+          }
+        } else if (ok) {
+          tie_mode = true;
+          vk = lo;
+          cnt_above = cnt_hi;
+          const float w = mass_of(x, value_of(vk));
+          unsigned long long t =
+              w > 0.f ? (unsigned long long)ceilf((tau - mass_hi) / w) : 1;
+          t = max(1ull, min(t, cnt_lo - cnt_hi));
+          ik = tie_index<kBf16>(x, sm, vk, t - 1);
+          ok = ik >= 0;
+        }
+      }
+    }
+    // ---- the draw
+    if (ok) {
+      if (!tie_mode && cnt_above == 0) {
+        tok = draw_list(x, sm, n_win, u);
+      } else {
+        if (!tie_mode) {
+          // add the kept window entries to their chunks: entries by index,
+          // the first entry of each chunk sums the chunk's run
+          window_by_index(x, sm, n_win);
+          for (int i = threadIdx.x; i < n_win; i += kT) {
+            const int c = chunk_of(x.r, (int)(sm.list[i] >> 32));
+            if (i == 0 || chunk_of(x.r, (int)(sm.list[i - 1] >> 32)) != c) {
+              float s = 0.f;
+              for (int j = i; j < n_win && chunk_of(x.r, (int)(sm.list[j] >> 32)) == c; ++j)
+                s += __uint_as_float((uint32_t)sm.list[j]);
+              sm.cabove[c] += s;
+            }
+          }
+        } else {
+          // cabove holds the mass above vk, cmass the count of vk, per chunk:
+          // ties with index <= ik are kept
+          const float w = mass_of(x, value_of(vk));
+          const int cik = chunk_of(x.r, ik);
+          for (int c = threadIdx.x; c < cik; c += kT) sm.cabove[c] += sm.cmass[c] * w;
+          __syncthreads();
+          if (warp == 0) {
+            float v[kLE];
+            int i0;
+            const int n = chunk_lane<kBf16>(x.r, cik, lane, v, i0);
+            int tc = 0;
+            for (int j = 0; j < n; ++j) tc += key_of(v[j]) == vk && i0 + j <= ik;
+            tc = __reduce_add_sync(0xffffffffu, tc);
+            if (lane == 0) sm.cabove[cik] += (float)tc * w;
+          }
+        }
+        __syncthreads();
+        tok = draw_chunks<kBf16>(x, sm, u, vk, ik);
+      }
+    }
   }
-  if (lane == 0) {
-    report(p.status, MSG_DEV_INTERNAL, row, 1);
-    p.tokens[row] = -1;
+  if (threadIdx.x == 0) {
+    if (tok < 0) report(p.status, MSG_DEV_INTERNAL, row, 0);
+    p.tokens[row] = tok;
   }
 }
 
 template <bool kBf16, bool kGreedy>
-cudaError_t launch_sample(const SampleParams &p, int C, cudaStream_t s) {
-  auto kernel = sample_kernel<kBf16, kGreedy>;
-  const size_t smem = sizeof(Shared) + (kGreedy ? 0 : ((size_t)p.slice + 8) * 4);
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
+cudaError_t launch_sample(const SampleParams &p, const WsRef &ws, cudaStream_t s) {
+  auto scan = sample_scan_kernel<kBf16, kGreedy>;
+  auto rowk = sample_row_kernel<kBf16, kGreedy>;
+  static bool configured = false;
+  if (!configured) {
     const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(rowk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
     if (e != cudaSuccess) return e;
-    configured = smem;
+    configured = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.batch * C));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, p);
+  scan<<<dim3((unsigned)ws.nparts, (unsigned)p.batch), kScanThreads, 0, s>>>(p, ws);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_k(rowk, dim3((unsigned)p.batch), dim3(kT), sizeof(Smem), s, true, p, ws);
+}
+
+// Workspace of a batch: per row the chunk maxima and masses, the sample, and
+// per scan part its greedy key and finiteness flag.
+struct WsSizes {
+  int nl_cap, ns_cap, nparts;
+  size_t bytes;
+};
+inline WsSizes ws_sizes(int64_t batch, int32_t vocab) {
+  WsSizes z;
+  const int nch_cap = (vocab + kChunk - 1) / kChunk;
+  z.nl_cap = nch_cap + 2;
+  z.ns_cap = 4 * nch_cap;
+  z.nparts = (nch_cap + kChunksPerCta - 1) / kChunksPerCta;
+  if (z.nparts < 1) z.nparts = 1;
+  const size_t per_row = align_up((size_t)z.nl_cap * 4, 16) * 2 + align_up((size_t)z.ns_cap * 4, 16) +
+                         align_up((size_t)z.nparts * 8, 16) + align_up((size_t)z.nparts * 4, 16);
+  z.bytes = per_row * (size_t)batch;
+  return z;
 }
 
 }  // namespace
 
 }  // namespace msg
 
-extern "C" int msg_sample_slices(int32_t vocab, int32_t *cluster_out, int32_t *slice_out) {
-  using namespace msg;
-  if (vocab < 1) return MSG_ERR_INVALID_ARG;
-  int C = 1;
-  while (C < kMaxCluster && (vocab + C - 1) / C > kSliceTwoPerSm) C *= 2;
-  int64_t slice = ((int64_t)vocab + C - 1) / C;
-  slice = (slice + kSliceAlign - 1) / kSliceAlign * kSliceAlign;
-  if (slice > kSliceMax) return MSG_ERR_UNSUPPORTED;
-  if (cluster_out) *cluster_out = C;
-  if (slice_out) *slice_out = (int32_t)slice;
-  return MSG_OK;
+extern "C" size_t msg_sample_workspace_size(int32_t batch, int32_t vocab) {
+  if (batch < 0 || vocab < 1 || vocab > msg::kMaxVocab) return 0;
+  return msg::ws_sizes(batch, vocab).bytes;
 }
 
 extern "C" int msg_sample(const void *logits, int32_t logits_dtype, int64_t logits_row_stride,
                           int32_t batch, int32_t vocab, const float *temperatures,
                           const int32_t *top_k, const float *top_p, const float *uniforms,
-                          int32_t *tokens_out, int32_t *dev_status, void *stream) {
+                          int32_t *tokens_out, void *workspace, size_t workspace_bytes,
+                          int32_t *dev_status, void *stream) {
   using namespace msg;
   if (logits_dtype != MSG_DTYPE_F32 && logits_dtype != MSG_DTYPE_BF16) return MSG_ERR_UNSUPPORTED;
   if (batch < 0 || vocab < 1 || logits_row_stride < vocab) return MSG_ERR_INVALID_ARG;
-  int32_t C = 0, slice = 0;
-  const int rc = msg_sample_slices(vocab, &C, &slice);
-  if (rc != MSG_OK) return rc;
+  if (vocab > kMaxVocab) return MSG_ERR_UNSUPPORTED;
   if (batch == 0) return MSG_OK;
   if (logits == nullptr || tokens_out == nullptr) return MSG_ERR_INVALID_ARG;
   if (temperatures != nullptr && uniforms == nullptr) return MSG_ERR_INVALID_ARG;
-  if ((int64_t)batch * C > 0x7fffffffLL) return MSG_ERR_INVALID_ARG;
   const int esz = logits_dtype == MSG_DTYPE_BF16 ? 2 : 4;
   if (reinterpret_cast<uintptr_t>(logits) % esz) return MSG_ERR_ALIGNMENT;
+  const WsSizes z = ws_sizes(batch, vocab);
+  if (workspace == nullptr || workspace_bytes < z.bytes) return MSG_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return MSG_ERR_ALIGNMENT;
   SampleParams p{};
   p.logits = static_cast<const uint8_t *>(logits);
   p.row_bytes = logits_row_stride * esz;
   p.batch = batch;
   p.vocab = vocab;
-  p.slice = slice;
   p.temperature = temperatures;
   p.top_k = top_k;
   p.top_p = top_p;
   p.uniform = uniforms;
   p.tokens = tokens_out;
   p.status = dev_status;
+  uint8_t *w = static_cast<uint8_t *>(workspace);
+  WsRef ws{};
+  ws.nl_cap = z.nl_cap;
+  ws.ns_cap = z.ns_cap;
+  ws.nparts = z.nparts;
+  ws.cmax = reinterpret_cast<float *>(w);
+  w += align_up((size_t)z.nl_cap * 4, 16) * batch;
+  ws.cmass = reinterpret_cast<float *>(w);
+  w += align_up((size_t)z.nl_cap * 4, 16) * batch;
+  ws.samp = reinterpret_cast<uint32_t *>(w);
+  w += align_up((size_t)z.ns_cap * 4, 16) * batch;
+  ws.best = reinterpret_cast<unsigned long long *>(w);
+  w += align_up((size_t)z.nparts * 8, 16) * batch;
+  ws.bad = reinterpret_cast<uint32_t *>(w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   const bool bf = logits_dtype == MSG_DTYPE_BF16;
   if (temperatures == nullptr)
-    e = bf ? launch_sample<true, true>(p, C, s) : launch_sample<false, true>(p, C, s);
+    e = bf ? launch_sample<true, true>(p, ws, s) : launch_sample<false, true>(p, ws, s);
   else
-    e = bf ? launch_sample<true, false>(p, C, s) : launch_sample<false, false>(p, C, s);
+    e = bf ? launch_sample<true, false>(p, ws, s) : launch_sample<false, false>(p, ws, s);
   return e == cudaSuccess ? MSG_OK : MSG_ERR_CUDA;
 }

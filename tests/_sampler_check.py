@@ -4,9 +4,10 @@ The kernel computes each weight e_i = 2^y_i, y_i = (l_i - max) * log2(e) / T,
 in fp32: the subtraction, log2(e), the division by T and the product each
 round once (|dy| <= 4 * 2^-24 |y|) and ex2.approx adds at most 2^-22
 relative, so e_i is off by at most rho_i = ln2 * |y_i| * 2^-22 + 2^-22
-relative; the fixed-point weights lose less than 2^-40 each.  A cumulative
+relative.  Its fp32 sums run through at most 48 roundings (a lane's eight
+terms, warp trees, a chunk rescale, block sums and scans).  A cumulative
 share of the kept mass is then off by at most
-    delta = 2 * sum_i p_i rho_i + V * 2^-40 / S        (S = sum_i e_i, max e = 1).
+    delta = 2 * sum_i p_i rho_i + 48 * 2^-24.
 A token is accepted when it is the oracle's own draw, or when the uniform
 lies within 4 delta of its interval under the oracle's kept set with any of
 the decisions that sit within that error of a cut flipped (a top-k boundary
@@ -34,8 +35,8 @@ def _weights(L, T):
 def row_delta(L, T) -> float:
     y, e = _weights(L, T)
     p = e / e.sum()
-    rho = LN2 * np.abs(y) * 2.0 ** -22 + 2.0 ** -22
-    return float(2.0 * (p * rho).sum() + len(L) * 2.0 ** -40 / e.sum())
+    rho = LN2 * np.abs(np.where(p > 0, y, 0.0)) * 2.0 ** -22 + 2.0 ** -22
+    return float(2.0 * (p * rho).sum() + 48.0 * 2.0 ** -24)
 
 
 def check_draw(L, T, k, P, u, tok) -> str:
@@ -54,7 +55,8 @@ def check_draw(L, T, k, P, u, tok) -> str:
     kk = V
     if k is not None and 1 <= int(k) < V:
         kk = int(k)
-        rho_k = LN2 * abs(y[order[kk - 1]]) * 2.0 ** -22 + 2.0 ** -22
+        yk = y[order[kk - 1]]
+        rho_k = LN2 * (abs(yk) if np.isfinite(yk) else 0.0) * 2.0 ** -22 + 2.0 ** -22
         pk = sp[kk - 1]
         amb |= set(order[np.nonzero(np.abs(sp - pk) <= 8.0 * rho_k * pk)[0]].tolist())
     Pc = 1.0 if P is None else float(np.float32(min(max(float(P), oracle.SAMPLE_MIN_P), 1.0)))

@@ -197,25 +197,10 @@ def test_rope_cache_argument_validation(lib, theta, d, n, status):
 
 
 # ------------------------------------------------------------------ sampler
-@pytest.mark.parametrize("vocab,split", [
-    (1, (1, 8)), (6, (1, 8)), (24576, (1, 24576)), (24577, (2, 12296)),
-    (128256, (8, 16032)), (151936, (8, 18992)), (425984, (8, 53248))])
-def test_sample_slices(lib, vocab, split):
-    assert msg.msg_sample_slices(vocab) == split
-    C, sl = split
-    assert (C - 1) * sl < vocab <= C * sl and sl % 8 == 0
-
-
-def test_sample_slices_limits(lib):
-    c = ctypes.c_int32()
-    assert lib.msg_sample_slices(0, ctypes.addressof(c), None) == msg.MSG_ERR_INVALID_ARG
-    assert lib.msg_sample_slices(425985, ctypes.addressof(c), None) == msg.MSG_ERR_UNSUPPORTED
-
-
 def _sample(lib, **kw):
     a = dict(logits=FAKE, dtype=msg.MSG_DTYPE_BF16, stride=152000, batch=4, vocab=151936,
              temperatures=FAKE, top_k=None, top_p=None, uniforms=FAKE, tokens=FAKE,
-             dev_status=None, stream=None)
+             ws=FAKE, ws_bytes=1 << 24, dev_status=None, stream=None)
     a.update(kw)
     return lib.msg_sample(*a.values())
 
@@ -232,6 +217,9 @@ def _sample(lib, **kw):
     (dict(uniforms=None), msg.MSG_ERR_INVALID_ARG),
     (dict(logits=FAKE + 1), msg.MSG_ERR_ALIGNMENT),
     (dict(dtype=msg.MSG_DTYPE_F32, logits=FAKE + 2), msg.MSG_ERR_ALIGNMENT),
+    (dict(ws=None), msg.MSG_ERR_WORKSPACE),
+    (dict(ws_bytes=1000), msg.MSG_ERR_WORKSPACE),
+    (dict(ws=FAKE + 8), msg.MSG_ERR_ALIGNMENT),
 ])
 def test_sample_argument_validation(lib, kw, status):
     assert _sample(lib, **kw) == status
@@ -252,3 +240,12 @@ def test_sampling_args_match_the_pages_prepare():
             assert (g is None) == (w is None)
             if g is not None:
                 assert np.array_equal(g.numpy(), w)
+
+
+def test_sample_workspace_size(lib):
+    per_row = msg.msg_sample_workspace_size(1, 151936)
+    assert 8 * 596 <= per_row <= 16 * 1024
+    assert msg.msg_sample_workspace_size(256, 151936) == 256 * per_row
+    assert msg.msg_sample_workspace_size(0, 151936) == 0
+    assert msg.msg_sample_workspace_size(4, 0) == 0
+    assert msg.msg_sample_workspace_size(4, 425985) == 0

@@ -77,7 +77,7 @@ def test_full_vocab_batch(bf16):
 @pytest.mark.parametrize("vocab", [1, 7, 1000, 24577, wl.QWEN3_VOCAB])
 def test_greedy_is_first_argmax(vocab, bf16):
     spec = wl.sampler_batch("greedy", 9000 + vocab, 96, vocab, bf16=bf16, greedy_only=True)
-    if vocab > 3:                                    # tied maxima across slices
+    if vocab > 3:                                    # tied maxima across chunks
         L = spec.logits_f64()
         for r in range(0, spec.batch, 3):
             m = int(np.argmax(L[r]))
@@ -205,10 +205,41 @@ def test_bad_inputs_are_reported():
     for r in (0, 2, 4, 5):
         check_draw(spec.logits_f64()[r], t[r], None if k is None else k[r],
                    None if p is None else p[r], spec.uniforms[r], int(got[r]))
-    # greedy rows report a bad logit too
+    # +inf has no softmax; greedy rows take it as their maximum but report a NaN
+    st = _status()
+    spec = wl.sampler_batch("badinf", 17, 3, 2000)
+    spec.logits[0, 5] = np.inf
+    got, _ = _run(spec, status=st)
+    assert msg.msg_read_device_status(st)[1][0] == msg.MSG_DEV_BAD_LOGIT and got[0] == -1
     st = _status()
     g = wl.sampler_batch("badg", 16, 4, 2000, greedy_only=True)
-    g.logits[2, 1999] = np.inf
+    g.logits[2, 1999] = np.nan
+    g.logits[3, 7] = np.inf
     got, _ = _run(g, status=st)
     assert msg.msg_read_device_status(st)[1][0] == msg.MSG_DEV_BAD_LOGIT
-    assert got[2] == -1
+    assert got[2] == -1 and got[3] == 7
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_minus_infinity_masks_tokens(bf16):
+    # -inf logits are tokens of probability zero: never drawn, and a row
+    # whose every logit is -inf is reported
+    V, B = 5003, 48
+    spec = wl.sampler_batch("masked", 18, B, V)
+    rng = np.random.default_rng(19)
+    mask = rng.random((B, V)) < 0.7
+    spec.logits[mask] = -np.inf
+    spec.logits[:, 11] = -np.inf
+    spec.logits[B - 1, :] = -np.inf
+    if bf16:
+        spec = wl.SamplerSpec("masked", wl.f32_to_bf16_bits(spec.logits), True, spec.temperature,
+                              spec.top_k, spec.top_p, spec.uniforms)
+    st = _status()
+    got, (t, k, p) = _run(spec, status=st)
+    assert msg.msg_read_device_status(st)[1][0] == msg.MSG_DEV_BAD_LOGIT
+    assert got[B - 1] == -1
+    L = spec.logits_f64()
+    for r in range(B - 1):
+        assert np.isfinite(L[r, got[r]]) and got[r] != 11
+        check_draw(L[r], t[r], None if k is None else k[r], None if p is None else p[r],
+                   spec.uniforms[r], int(got[r]))
