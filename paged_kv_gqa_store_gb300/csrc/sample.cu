@@ -64,7 +64,8 @@ struct Smem {
   float cmax[kMaxChunks];                      // per chunk: largest logit
   float cmass[kMaxChunks];                     //   mass (rel. to cmax, then to the row max)
   float cabove[kMaxChunks];                    //   mass above the window / kept mass
-  uint32_t csort[kSortChunks];                 // ~key of the chunk maxima, sorted ascending
+  unsigned long long csort[kSortChunks];       // (~key << 32) | chunk of the chunk maxima, ascending
+  float csamp[kMaxChunks];                     // per chunk: mass of its sample points
   uint32_t samp[kMaxSamples];                  // ~key of the sample, sorted ascending
   unsigned long long list[kCap];               // window: (~key << 32) | index, sorted ascending
   float lcum[kCap];                            // window: cumulative masses in list order
@@ -83,6 +84,21 @@ __device__ __forceinline__ uint32_t key_of(float f) {
 __device__ __forceinline__ float value_of(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
+// Key of the chunk maximum at position i of csort.
+__device__ __forceinline__ uint32_t ckey(const Smem &sm, int i) {
+  return ~(uint32_t)(sm.csort[i] >> 32);
+}
+// last_at_least over csort positions [p0, p1).
+__device__ __forceinline__ int last_at_least_c(const Smem &sm, int p0, int p1, uint32_t K) {
+  int lo = p0, hi = p1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (ckey(sm, mid) >= K) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo - 1;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -380,10 +396,82 @@ __device__ __forceinline__ float mass_of(const Ctx &x, float l) { return ex2((l 
 // Window [lo, hi) of order keys: gather its logits into the list (at most kCap
 // stored; the full count is returned), and per chunk the mass of the logits
 // at or above hi (cabove); *cnt_above / *mass_above get their totals.
+// Load the lane's 8 logits of vector chunk c (1-based logical index) into raw.
+template <bool kBf16>
+__device__ __forceinline__ bool load_chunk_raw(const RowRef &r, int c, int lane, uint4 raw[2]) {
+  const int vi = 32 * (c - 1) + lane;
+  if (vi >= r.nvec) return false;
+  const uint8_t *src = r.p + (int64_t)(r.h + kLE * vi) * (kBf16 ? 2 : 4);
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(raw[0].x), "=r"(raw[0].y), "=r"(raw[0].z), "=r"(raw[0].w) : "l"(src));
+  if (!kBf16)
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(raw[1].x), "=r"(raw[1].y), "=r"(raw[1].z), "=r"(raw[1].w) : "l"(src + 16));
+  return true;
+}
+template <bool kBf16>
+__device__ __forceinline__ void unpack_raw(const uint4 raw[2], float v[kLE]) {
+  if (kBf16) {
+    const uint4 w = raw[0];
+    v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+    v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+  } else {
+    v[0] = __uint_as_float(raw[0].x); v[1] = __uint_as_float(raw[0].y);
+    v[2] = __uint_as_float(raw[0].z); v[3] = __uint_as_float(raw[0].w);
+    v[4] = __uint_as_float(raw[1].x); v[5] = __uint_as_float(raw[1].y);
+    v[6] = __uint_as_float(raw[1].z); v[7] = __uint_as_float(raw[1].w);
+  }
+}
+
+// One chunk of the gather (all lanes): window logits appended, the mass of
+// those above it summed into cabove[c].
+__device__ __forceinline__ void gather_chunk(const Ctx &x, Smem &sm, const float v[kLE], int n,
+                                             int i0, int c, uint32_t lo, uint32_t top,
+                                             bool has_above, uint32_t &ca) {
+  const int lane = threadIdx.x & 31;
+  float ma = 0.f;
+  uint32_t wmask = 0;
+#pragma unroll
+  for (int j = 0; j < kLE; ++j) {
+    const uint32_t k = key_of(v[j]);
+    if (j < n && k >= lo) {
+      if (has_above && k > top) {
+        ++ca;
+        ma += mass_of(x, v[j]);
+      } else {
+        wmask |= 1u << j;
+      }
+    }
+  }
+  const int cnt = __popc(wmask);
+  const unsigned any = __ballot_sync(0xffffffffu, cnt != 0);
+  if (any) {
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&sm.ival[0], total);
+    base = __shfl_sync(0xffffffffu, base, 0) + incl - cnt;
+#pragma unroll
+    for (int j = 0; j < kLE; ++j)
+      if ((wmask >> j) & 1u) {
+        if (base < kCap) sm.list[base] = ((unsigned long long)(~key_of(v[j])) << 32) | (uint32_t)(i0 + j);
+        ++base;
+      }
+  }
+  if (has_above) ma = warp_sum_f(ma);
+  if (lane == 0) sm.cabove[c] = ma;
+}
+
 template <bool kBf16>
 __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi,
                       unsigned long long *cnt_above, float *mass_above) {
-  const int lane = threadIdx.x & 31;
+  constexpr int U = kBf16 ? kPassUnrollBf16 : kPassUnrollF32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __syncthreads();
   if (threadIdx.x == 0) sm.ival[0] = 0;
   __syncthreads();
@@ -391,54 +479,40 @@ __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi
   // keys in [lo, top] are in the window, keys above top above it
   const uint32_t top = hi >= kKeyEnd ? 0xffffffffu : (uint32_t)(hi - 1);
   const bool has_above = hi < kKeyEnd;
-  for_chunks<kBf16>(
-      x.r, [&](int c) { return sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= lo; },
-      [&](int c) {
+  for (int c0 = 1 + warp; c0 <= x.r.nch; c0 += kW * U) {
+    uint4 raw[U][2];
+    bool on[U], got[U];
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int c = c0 + q * kW;
+      on[q] = c <= x.r.nch && sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= lo;
+      got[q] = on[q] && load_chunk_raw<kBf16>(x.r, c, lane, raw[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int c = c0 + q * kW;
+      if (c > x.r.nch) break;                   // warp-uniform
+      if (!on[q]) {
         if (lane == 0) sm.cabove[c] = 0.f;
-      },
-      [&](const float v[kLE], int n, int i0, int c) {
-        float ma = 0.f;
-        uint32_t wmask = 0;                     // the lane's window logits
-#pragma unroll
-        for (int j = 0; j < kLE; ++j) {
-          const uint32_t k = key_of(v[j]);
-          if (j < n && k >= lo) {
-            if (has_above && k > top) {
-              ++ca;
-              ma += mass_of(x, v[j]);
-            } else {
-              wmask |= 1u << j;
-            }
-          }
-        }
-        // append the window logits, one warp-wide slot reservation per chunk
-        const int cnt = __popc(wmask);
-        int incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
-        if (total) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&sm.ival[0], total);
-          base = __shfl_sync(0xffffffffu, base, 0) + incl - cnt;
-#pragma unroll
-          for (int j = 0; j < kLE; ++j)
-            if ((wmask >> j) & 1u) {
-              if (base < kCap)
-                sm.list[base] = ((unsigned long long)(~key_of(v[j])) << 32) | (uint32_t)(i0 + j);
-              ++base;
-            }
-        }
-        if (has_above) {
-          ma = warp_sum_f(ma);
-          if (lane == 0) sm.cabove[c] = ma;
-        } else if (lane == 0) {
-          sm.cabove[c] = 0.f;
-        }
-      });
+        continue;
+      }
+      float v[kLE];
+      unpack_raw<kBf16>(raw[q], v);
+      gather_chunk(x, sm, v, got[q] ? kLE : 0, x.r.h + kLE * (32 * (c - 1) + lane), c, lo, top,
+                   has_above, ca);
+    }
+  }
+  if (warp < 2) {                               // head (warp 0) and tail (warp 1)
+    const int c = warp == 0 ? 0 : x.r.nch + 1;
+    if (sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= lo) {
+      float v[kLE];
+      int i0;
+      const int n = chunk_lane<kBf16>(x.r, c, lane, v, i0);
+      gather_chunk(x, sm, v, n, i0, c, lo, top, has_above, ca);
+    } else if (lane == 0) {
+      sm.cabove[c] = 0.f;
+    }
+  }
   *cnt_above = block_sum_u(ca, sm);
   float part = 0.f;                            // fixed order: thread t sums chunks t, t + kT, ...
   for (int c = threadIdx.x; c < x.nl; c += kT) part += sm.cabove[c];
@@ -478,37 +552,60 @@ __device__ int window_crossing(Smem &sm, int n, float base, float tau) {
 
 // Probe pass: count and mass of the logits at or above each of four pivots
 // (descending keys); chunks whose maximum is below the smallest are skipped.
+__device__ __forceinline__ void probe_chunk(const Ctx &x, const float v[kLE], int n,
+                                            uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3,
+                                            bool want_mass, uint32_t c4[4], float m4[4]) {
+#pragma unroll
+  for (int j = 0; j < kLE; ++j) {
+    const uint32_t k = key_of(v[j]);
+    if (j >= n || k < p3) continue;
+    const float e = want_mass ? mass_of(x, v[j]) : 0.f;
+    ++c4[3];
+    m4[3] += e;
+    const bool g2 = k >= p2, g1 = k >= p1, g0 = k >= p0;
+    c4[2] += g2;
+    c4[1] += g1;
+    c4[0] += g0;
+    m4[2] += g2 ? e : 0.f;
+    m4[1] += g1 ? e : 0.f;
+    m4[0] += g0 ? e : 0.f;
+  }
+}
+
 template <bool kBf16>
 __device__ void probe(const Ctx &x, Smem &sm, const uint32_t piv[4], bool want_mass,
                       unsigned long long cnt[4], float mass[4]) {
+  constexpr int U = kBf16 ? kPassUnrollBf16 : kPassUnrollF32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t c4[4] = {0, 0, 0, 0};
   float m4[4] = {0.f, 0.f, 0.f, 0.f};
   const uint32_t p0 = piv[0], p1 = piv[1], p2 = piv[2], p3 = piv[3];
-  for_chunks<kBf16>(
-      x.r, [&](int c) { return sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= p3; },
-      [&](int) {},
-      [&](const float v[kLE], int n, int, int) {
+  for (int c0 = 1 + warp; c0 <= x.r.nch; c0 += kW * U) {
+    uint4 raw[U][2];
+    bool got[U];
 #pragma unroll
-        for (int j = 0; j < kLE; ++j) {
-          const uint32_t k = key_of(v[j]);
-          if (j >= n || k < p3) continue;
-          const float e = want_mass ? mass_of(x, v[j]) : 0.f;
-          ++c4[3];
-          m4[3] += e;
-          if (k >= p2) {
-            ++c4[2];
-            m4[2] += e;
-          }
-          if (k >= p1) {
-            ++c4[1];
-            m4[1] += e;
-          }
-          if (k >= p0) {
-            ++c4[0];
-            m4[0] += e;
-          }
-        }
-      });
+    for (int q = 0; q < U; ++q) {
+      const int c = c0 + q * kW;
+      got[q] = c <= x.r.nch && sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= p3 &&
+               load_chunk_raw<kBf16>(x.r, c, lane, raw[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      if (!got[q]) continue;
+      float v[kLE];
+      unpack_raw<kBf16>(raw[q], v);
+      probe_chunk(x, v, kLE, p0, p1, p2, p3, want_mass, c4, m4);
+    }
+  }
+  if (warp < 2) {
+    const int c = warp == 0 ? 0 : x.r.nch + 1;
+    if (sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= p3) {
+      float v[kLE];
+      int i0;
+      const int n = chunk_lane<kBf16>(x.r, c, lane, v, i0);
+      probe_chunk(x, v, n, p0, p1, p2, p3, want_mass, c4, m4);
+    }
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     cnt[q] = block_sum_u(c4[q], sm);
@@ -524,15 +621,15 @@ __device__ uint32_t chunk_max_bound(const Ctx &x, Smem &sm, uint32_t lo, float t
   const int a = min(x.nl, (int)threadIdx.x * per), b = min(x.nl, a + per);
   float part = 0.f;
   for (int i = a; i < b; ++i) {
-    const uint32_t kk = ~sm.csort[i];
-    if (sm.csort[i] != ~0u && kk >= lo) part += mass_of(x, value_of(kk));
+    const uint32_t kk = ckey(sm, i);
+    if (sm.csort[i] != ~0ull && kk >= lo) part += mass_of(x, value_of(kk));
   }
   float tot;
   float run = block_excl_scan_f(part, sm, &tot);
   int first = x.nl;
   for (int i = a; i < b; ++i) {
-    const uint32_t kk = ~sm.csort[i];
-    if (sm.csort[i] != ~0u && kk >= lo) {
+    const uint32_t kk = ckey(sm, i);
+    if (sm.csort[i] != ~0ull && kk >= lo) {
       run += mass_of(x, value_of(kk));
       if (run >= tau) {
         first = i;
@@ -541,7 +638,7 @@ __device__ uint32_t chunk_max_bound(const Ctx &x, Smem &sm, uint32_t lo, float t
     }
   }
   first = block_min_i(first, sm);
-  return first < x.nl ? ~sm.csort[first] : 0u;
+  return first < x.nl ? ckey(sm, first) : 0u;
 }
 
 // Last position in [p0, p1) of a descending-key array stored as ~key
@@ -570,8 +667,8 @@ __device__ void estimate_pivots(const Ctx &x, Smem &sm, uint32_t lo, unsigned lo
   // chunk maxima strictly inside (lo, hi): positions [ca, cb) of csort
   unsigned long long ge_hi = 0, gt_lo = 0;
   for (int i = threadIdx.x; i < x.nl; i += kT) {
-    if (sm.csort[i] == ~0u) continue;
-    const uint32_t kk = ~sm.csort[i];
+    if (sm.csort[i] == ~0ull) continue;
+    const uint32_t kk = ckey(sm, i);
     ge_hi += (unsigned long long)kk >= hi;
     gt_lo += kk > lo;
   }
@@ -593,11 +690,11 @@ __device__ void estimate_pivots(const Ctx &x, Smem &sm, uint32_t lo, unsigned lo
     const int per = (cb - ca + kT - 1) / kT;
     const int ta = min(cb, ca + (int)threadIdx.x * per), tb = min(cb, ta + per);
     float part = 0.f;
-    for (int i = ta; i < tb; ++i) part += mass_of(x, value_of(~sm.csort[i]));
+    for (int i = ta; i < tb; ++i) part += mass_of(x, value_of(ckey(sm, i)));
     float tot;
     float run = block_excl_scan_f(part, sm, &tot);
     for (int i = ta; i < tb; ++i) {
-      run += mass_of(x, value_of(~sm.csort[i]));
+      run += mass_of(x, value_of(ckey(sm, i)));
       sm.cabove[i] = run;
     }
   }
@@ -610,7 +707,7 @@ __device__ void estimate_pivots(const Ctx &x, Smem &sm, uint32_t lo, unsigned lo
     const float want = tau + frac[t] * g;
     int fs = b, fc = cb;
     for (int i = sa; i < sb; ++i) {
-      const int r = last_at_least(sm.csort, ca, cb, ~sm.samp[i]);
+      const int r = last_at_least_c(sm, ca, cb, ~sm.samp[i]);
       const float e = mass_hi + sm.lcum[i] + (r >= ca ? sm.cabove[r] : 0.f);
       if (e >= want) {
         fs = i;
@@ -618,7 +715,7 @@ __device__ void estimate_pivots(const Ctx &x, Smem &sm, uint32_t lo, unsigned lo
       }
     }
     for (int i = qa; i < qb; ++i) {
-      const int r = last_at_least(sm.samp, a, b, ~sm.csort[i]);
+      const int r = last_at_least(sm.samp, a, b, ckey(sm, i));
       const float e = mass_hi + sm.cabove[i] + (r >= a ? sm.lcum[r] : 0.f);
       if (e >= want) {
         fc = i;
@@ -629,9 +726,88 @@ __device__ void estimate_pivots(const Ctx &x, Smem &sm, uint32_t lo, unsigned lo
     fc = block_min_i(fc, sm);
     uint32_t kp = lo + 1;                       // nothing reaches it: the bottom
     if (fs < b) kp = ~sm.samp[fs];
-    if (fc < cb && ~sm.csort[fc] > kp) kp = ~sm.csort[fc];
+    if (fc < cb && ckey(sm, fc) > kp) kp = ckey(sm, fc);
     piv[t] = kp;
   }
+}
+
+// A window [lo, hi) of keys around the top-p boundary of the whole row.  The
+// mass at or above X is the row's mass minus the mass below X, and the mass
+// below is the light part of each chunk: the chunks whose maximum is below X
+// count with their exact mass, and in the others the sample points below X
+// count with the logits they stand for.  The window spans `d` sample points on
+// either side of the first point where that estimate reaches tau.  Needs the
+// sample sorted and csort; uses lcum and the list as scratch.
+__device__ void estimate_window(const Ctx &x, Smem &sm, float tau, int d, uint32_t &lo,
+                                unsigned long long &hi) {
+  const float w = (float)(kChunk / x.spc);
+  float *cs = reinterpret_cast<float *>(sm.list);          // chunk-mass prefix, csort order
+  float *css = cs + kSortChunks;                            // sample-mass prefix, csort order
+  const int nc = x.nl;
+  // prefixes over csort (descending maxima) and over the sorted sample
+  {
+    const int per = (nc + kT - 1) / kT;
+    const int a = min(nc, (int)threadIdx.x * per), b = min(nc, a + per);
+    float p1 = 0.f, p2 = 0.f;
+    for (int i = a; i < b; ++i)
+      if (sm.csort[i] != ~0ull) {
+        const int c = (int)(uint32_t)sm.csort[i];
+        p1 += sm.cmass[c];
+        p2 += sm.csamp[c];
+      }
+    float t1, t2;
+    float r1 = block_excl_scan_f(p1, sm, &t1);
+    float r2 = block_excl_scan_f(p2, sm, &t2);
+    for (int i = a; i < b; ++i) {
+      if (sm.csort[i] != ~0ull) {
+        const int c = (int)(uint32_t)sm.csort[i];
+        r1 += sm.cmass[c];
+        r2 += sm.csamp[c];
+      }
+      cs[i] = r1;
+      css[i] = r2;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      sm.fval[1] = t1;
+      sm.fval[2] = t2;
+    }
+  }
+  {
+    const int per = (x.ns + kT - 1) / kT;
+    const int a = min(x.ns, (int)threadIdx.x * per), b = min(x.ns, a + per);
+    float part = 0.f;
+    for (int i = a; i < b; ++i) part += mass_of(x, value_of(~sm.samp[i]));
+    float tot;
+    float run = block_excl_scan_f(part, sm, &tot);
+    for (int i = a; i < b; ++i) {
+      run += mass_of(x, value_of(~sm.samp[i]));
+      sm.lcum[i] = run;
+    }
+    if (threadIdx.x == 0) sm.fval[3] = tot;
+  }
+  __syncthreads();
+  const float cs_tot = sm.fval[1], css_tot = sm.fval[2], samp_tot = sm.fval[3];
+  // first sample point (descending) whose estimate reaches tau
+  int first = x.ns;
+  const int per = (x.ns + kT - 1) / kT;
+  const int a = min(x.ns, (int)threadIdx.x * per), b = min(x.ns, a + per);
+  for (int i = a; i < b; ++i) {
+    const uint32_t K = ~sm.samp[i];
+    const int r = last_at_least_c(sm, 0, nc, K);            // chunks with maximum >= K
+    const float cs_lt = cs_tot - (r >= 0 ? cs[r] : 0.f);
+    const float css_lt = css_tot - (r >= 0 ? css[r] : 0.f);
+    const float samp_lt = samp_tot - sm.lcum[i];
+    const float e = x.S - cs_lt - w * fmaxf(0.f, samp_lt - css_lt);
+    if (e >= tau) {
+      first = i;
+      break;
+    }
+  }
+  first = block_min_i(first, sm);
+  lo = first + d < x.ns ? ~sm.samp[first + d] : 0u;
+  hi = first - d >= 0 ? (unsigned long long)(~sm.samp[first - d]) : kKeyEnd;
+  if (hi <= lo) hi = kKeyEnd;
 }
 
 // Sort the sample once (descending keys, invalid points last); x.ns = valid points.
@@ -1141,14 +1317,29 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
     __syncthreads();
     tok = draw_chunks<kBf16>(x, sm, u, 0u, p.vocab);
   } else {
-    {                                           // the sample (sorted on first use)
-      const uint32_t *samp = ws.samp + (int64_t)row * ws.ns_cap;
-      for (int i = threadIdx.x; i < x.r.nch * x.spc; i += kT) sm.samp[i] = samp[i];
+    {                                           // the sample (sorted on first use), and
+      const uint32_t *samp = ws.samp + (int64_t)row * ws.ns_cap;   // its mass per chunk
+      const int ns4 = (x.r.nch * x.spc) >> 2;                       // spc is 4 or 2: whole uint4s
+      for (int i = threadIdx.x; i < ns4; i += kT)
+        reinterpret_cast<uint4 *>(sm.samp)[i] = reinterpret_cast<const uint4 *>(samp)[i];
+      for (int i = 4 * ns4 + threadIdx.x; i < x.r.nch * x.spc; i += kT) sm.samp[i] = samp[i];
+      __syncthreads();
+      for (int c = threadIdx.x; c < x.nl; c += kT) {
+        float m = 0.f;
+        if (c >= 1 && c <= x.r.nch)
+          for (int i = 0; i < x.spc; ++i) {
+            const uint32_t e = sm.samp[(c - 1) * x.spc + i];
+            if (e != ~0u) m += mass_of(x, value_of(~e));
+          }
+        sm.csamp[c] = m;
+      }
     }
     // chunk maxima sorted by descending key (invalid chunks last)
     const int npc = pow2_at_least(x.nl);
     for (int i = threadIdx.x; i < npc; i += kT)
-      sm.csort[i] = (i < x.nl && sm.cmax[i] != -INFINITY) ? ~key_of(sm.cmax[i]) : ~0u;
+      sm.csort[i] = (i < x.nl && sm.cmax[i] != -INFINITY)
+                        ? ((unsigned long long)(~key_of(sm.cmax[i])) << 32) | (uint32_t)i
+                        : ~0ull;
     __syncthreads();
     bitonic_sort(sm.csort, npc);
     bool ok = true, tie_mode = false;
@@ -1164,9 +1355,8 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
       bool gathered = false;
       if (k <= (unsigned long long)x.nl) {
         // the k-th largest chunk maximum bounds the k-th logit from below
-        const uint32_t kk = sm.csort[k - 1];
-        if (kk != ~0u) {
-          n_win = gather<kBf16>(x, sm, ~kk, kKeyEnd, &cnt_above, &mass_above);
+        if (sm.csort[k - 1] != ~0ull) {
+          n_win = gather<kBf16>(x, sm, ckey(sm, (int)k - 1), kKeyEnd, &cnt_above, &mass_above);
           gathered = n_win <= kCap;
         }
       }
@@ -1238,11 +1428,20 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
         if (!gathered) {
           // one gather around the estimate; a miss still tells which side
           sort_sample(x, sm);
-          int a, b;
-          sample_span(x, sm, lo, hi, a, b);
           uint32_t piv[4];
-          estimate_pivots(x, sm, lo, hi, a, b, kChunk / x.spc, fminf(0.1f * x.S, mass_lo - mass_hi),
-                          mass_hi, tau, piv);
+          if (lo == 0 && hi == kKeyEnd) {
+            uint32_t wl;
+            unsigned long long wh;
+            estimate_window(x, sm, tau, 16, wl, wh);
+            piv[0] = wh >= kKeyEnd ? 0xffffffffu : (uint32_t)wh;
+            piv[3] = wl;
+            piv[1] = piv[2] = piv[3];
+          } else {
+            int a, b;
+            sample_span(x, sm, lo, hi, a, b);
+            estimate_pivots(x, sm, lo, hi, a, b, kChunk / x.spc,
+                            fminf(0.1f * x.S, mass_lo - mass_hi), mass_hi, tau, piv);
+          }
           clamp_pivots(piv, lo, hi);
           n_win = gather<kBf16>(x, sm, piv[3], piv[0], &cnt_above, &mass_above);
           if (n_win <= kCap) {
