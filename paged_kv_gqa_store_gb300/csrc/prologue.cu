@@ -5,13 +5,16 @@
 // scale with no mean or bias, rope rotates the first half of a head against
 // the second half, Qwen3 norms q and k before rotating them).
 //
-// One warp per token: lane l holds elements 4l .. 4l+3 of each head, so the
-// rotation partner of each element sits in lane l ^ 16 and the mean of
-// squares is a 5-step butterfly.  Every head row is one coalesced 256-byte
-// read and one 256-byte write; the warp loads 16 head rows before it
-// processes any (4 KB in flight per warp), and reads the token's cos/sin row
-// once for all its heads.  The rotary cache itself ("Mini-SGLang
-// 完整剖析" 4.5.6) is built once per model by cos_sin_kernel.
+// One warp per token, two head rows at a time: lane l works on row 2m + l/16
+// of the pair and holds elements 4j .. 4j+3 and 64+4j .. 64+4j+3 (j = l % 16),
+// so each element and its rotation partner sit in the same thread and the
+// mean of squares is a 4-step butterfly within the half-warp.  Every row is
+// two coalesced 128-byte reads and two 128-byte writes; the warp loads 8 row
+// pairs (4 KB) before it processes any, and reads the token's cos/sin row
+// once for all its heads.  Registers are capped for 3 CTAs (24 warps) per SM:
+// the kernel is bound by how many loads are in flight and by issue, not by
+// its arithmetic.  The rotary cache itself ("Mini-SGLang 完整剖析" 4.5.6) is
+// built once per model by cos_sin_kernel.
 #include <math.h>
 
 #include "internal.cuh"
@@ -46,21 +49,32 @@ struct PrologueParams {
 __device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-constexpr int kChunk = 16;         // head rows of a token loaded before any is processed
+constexpr int kPairs = 8;          // row pairs of a token loaded before any is processed
 
-__global__ void __launch_bounds__(256) prologue_kernel(PrologueParams p) {
+__device__ __forceinline__ void unpack4(uint2 w, float (&x)[4]) {
+  x[0] = bf16_lo_f(w.x);
+  x[1] = bf16_hi_f(w.x);
+  x[2] = bf16_lo_f(w.y);
+  x[3] = bf16_hi_f(w.y);
+}
+
+__global__ void __launch_bounds__(256, 3) prologue_kernel(PrologueParams p) {
   grid_dep_wait();
   grid_dep_launch();
   const int lane = threadIdx.x & 31;
+  const int h = lane >> 4;                        // which row of a pair this half-warp takes
+  const int j4 = 4 * (lane & 15);                 // elements j4 .. j4+3 and 64+j4 .. 64+j4+3
   const int64_t first = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int units = p.hq + 2 * p.hkv;             // q heads, k heads, v heads of a token row
-  const int ci = 4 * (lane & 15);                 // this lane's index into the cos / sin halves
-  const uint2 qwr = *reinterpret_cast<const uint2 *>(p.q_w + 4 * lane);
-  const uint2 kwr = *reinterpret_cast<const uint2 *>(p.k_w + 4 * lane);
-  const float qw[4] = {bf16_lo_f(qwr.x), bf16_hi_f(qwr.x), bf16_lo_f(qwr.y), bf16_hi_f(qwr.y)};
-  const float kw[4] = {bf16_lo_f(kwr.x), bf16_hi_f(kwr.x), bf16_lo_f(kwr.y), bf16_hi_f(kwr.y)};
-  // one warp per token: all of its head rows, kChunk loads in flight at a time
+  const int nk = p.hq + p.hkv;                    // q and k rows: normed and rotated
+  const int units = nk + p.hkv;                   // then the v rows: copied
+  const int npn = (nk + 1) / 2, nps = npn + (p.hkv + 1) / 2;   // row pairs
+  float qw1[4], qw2[4], kw1[4], kw2[4];
+  unpack4(*reinterpret_cast<const uint2 *>(p.q_w + j4), qw1);
+  unpack4(*reinterpret_cast<const uint2 *>(p.q_w + kHalfD + j4), qw2);
+  unpack4(*reinterpret_cast<const uint2 *>(p.k_w + j4), kw1);
+  unpack4(*reinterpret_cast<const uint2 *>(p.k_w + kHalfD + j4), kw2);
+  // one warp per token, a row pair per step: kPairs pairs in flight at a time
   for (int64_t t = first; t < p.num_tokens; t += stride) {
     const int64_t pos = p.positions[t];
     if (pos < 0 || pos >= p.max_pos) {
@@ -71,54 +85,69 @@ __global__ void __launch_bounds__(256) prologue_kernel(PrologueParams p) {
                                             : (int64_t) static_cast<const int32_t *>(p.out_loc)[t];
     const bool slot_ok = slot >= 0 && slot < p.num_slots;
     if (!slot_ok && lane == 0) report(p.status, MSG_DEV_SLOT_OUT_OF_RANGE, (int32_t)t, slot);
-    const uint16_t *row = p.qkv + t * p.qkv_stride + 4 * lane;
-    const float4 c4 = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + ci);
-    const float4 s4 = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + kHalfD + ci);
+    const uint16_t *row = p.qkv + t * p.qkv_stride + j4;
+    const float4 c4 = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + j4);
+    const float4 s4 = *reinterpret_cast<const float4 *>(p.cos_sin + pos * kD + kHalfD + j4);
     const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
-    for (int u0 = 0; u0 < units; u0 += kChunk) {
-      uint2 raw[kChunk];
+    for (int s0 = 0; s0 < nps; s0 += kPairs) {
+      uint2 lo[kPairs], hi[kPairs];
 #pragma unroll
-      for (int k = 0; k < kChunk; ++k)
-        if (u0 + k < units) raw[k] = *reinterpret_cast<const uint2 *>(row + (int64_t)(u0 + k) * kD);
+      for (int k = 0; k < kPairs; ++k) {
+        const int s = s0 + k;
+        const int u = s < npn ? 2 * s + h : nk + 2 * (s - npn) + h;
+        const bool ok = s < nps && (s < npn ? u < nk : u < units);
+        lo[k] = ok ? *reinterpret_cast<const uint2 *>(row + (int64_t)u * kD) : make_uint2(0, 0);
+        hi[k] = ok ? *reinterpret_cast<const uint2 *>(row + (int64_t)u * kD + kHalfD)
+                   : make_uint2(0, 0);
+      }
 #pragma unroll
-      for (int k = 0; k < kChunk; ++k) {
-        const int u = u0 + k;
-        if (u >= units) break;
-        if (u >= p.hq + p.hkv) {                  // V: a bit copy
-          if (slot_ok)
-            *reinterpret_cast<uint2 *>(p.v_pool + slot * p.pool_stride_bytes +
-                                       (int64_t)(u - p.hq - p.hkv) * kD * 2 + 8 * lane) = raw[k];
+      for (int k = 0; k < kPairs; ++k) {
+        const int s = s0 + k;
+        if (s >= nps) break;
+        if (s >= npn) {                           // V: a bit copy
+          const int g = 2 * (s - npn) + h;
+          if (g < p.hkv && slot_ok) {
+            uint8_t *dst = p.v_pool + slot * p.pool_stride_bytes + (int64_t)g * kD * 2 + 2 * j4;
+            *reinterpret_cast<uint2 *>(dst) = lo[k];
+            *reinterpret_cast<uint2 *>(dst + kD) = hi[k];
+          }
           continue;
         }
+        const int u = 2 * s + h;
         const bool is_q = u < p.hq;
-        if (!is_q && !slot_ok) continue;
-        const float x[4] = {bf16_lo_f(raw[k].x), bf16_hi_f(raw[k].x), bf16_lo_f(raw[k].y),
-                            bf16_hi_f(raw[k].y)};
-        // RMSNorm: x * w / sqrt(mean(x^2) + eps)
-        float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+        float x1[4], x2[4];
+        unpack4(lo[k], x1);
+        unpack4(hi[k], x2);
+        // RMSNorm: x * w / sqrt(mean(x^2) + eps), the sum over the half-warp
+        float ss = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        for (int e = 0; e < 4; ++e) ss += x1[e] * x1[e] + x2[e] * x2[e];
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const float r = rsqrtf(ss * (1.f / kD) + p.eps);
-        float y[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[e] = (is_q ? qw[e] : kw[e]) * (x[e] * r);
-        // rotation: lanes 0-15 hold x1 (first half), lanes 16-31 x2; partner = lane ^ 16
-        float out[4];
+        float o1[4], o2[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float z = __shfl_xor_sync(0xffffffffu, y[e], 16);
-          out[e] = lane < 16 ? y[e] * cc[e] - z * sn[e]      // x1 c - x2 s
-                             : z * sn[e] + y[e] * cc[e];     // x1 s + x2 c
+          const float y1 = (is_q ? qw1[e] : kw1[e]) * (x1[e] * r);
+          const float y2 = (is_q ? qw2[e] : kw2[e]) * (x2[e] * r);
+          o1[e] = y1 * cc[e] - y2 * sn[e];        // x1 c - x2 s
+          o2[e] = y1 * sn[e] + y2 * cc[e];        // x1 s + x2 c
         }
-        uint2 packed;
-        packed.x = pack_bf16(out[0], out[1]);
-        packed.y = pack_bf16(out[2], out[3]);
-        if (is_q)
-          *reinterpret_cast<uint2 *>(p.q_out + t * p.q_out_stride + (int64_t)u * kD + 4 * lane) =
-              packed;
-        else
-          *reinterpret_cast<uint2 *>(p.k_pool + slot * p.pool_stride_bytes +
-                                     (int64_t)(u - p.hq) * kD * 2 + 8 * lane) = packed;
+        uint2 a, b;
+        a.x = pack_bf16(o1[0], o1[1]);
+        a.y = pack_bf16(o1[2], o1[3]);
+        b.x = pack_bf16(o2[0], o2[1]);
+        b.y = pack_bf16(o2[2], o2[3]);
+        if (u >= nk) continue;
+        if (is_q) {
+          uint16_t *dst = p.q_out + t * p.q_out_stride + (int64_t)u * kD + j4;
+          *reinterpret_cast<uint2 *>(dst) = a;
+          *reinterpret_cast<uint2 *>(dst + kHalfD) = b;
+        } else if (slot_ok) {
+          uint8_t *dst = p.k_pool + slot * p.pool_stride_bytes + (int64_t)(u - p.hq) * kD * 2 + 2 * j4;
+          *reinterpret_cast<uint2 *>(dst) = a;
+          *reinterpret_cast<uint2 *>(dst + kD) = b;
+        }
       }
     }
   }

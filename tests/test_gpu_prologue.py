@@ -153,3 +153,37 @@ def test_prologue_full_extend_batch_sampled():
     sl = torch.from_numpy(loc[pick]).to(dev)
     _check_close(wl.torch_to_bits(kp.index_select(0, sl)), k_ref, "k")
     assert np.array_equal(wl.torch_to_bits(vp.index_select(0, sl)), v_ref)
+
+
+@pytest.mark.parametrize("hq,hkv,T", [(8, 2, 300), (64, 8, 200), (448, 4, 40)])
+def test_prologue_other_head_counts(hq, hkv, T):
+    """Head counts other than 16 / 8: a narrow row (12 head rows a token), a wide
+    one (80 rows: fewer warps and stages per CTA) and one whose two stages do not
+    fit in shared memory (456 rows: the kernel that keeps rows in registers)."""
+    max_pos, num_slots = 5000, 1024
+    rng = np.random.default_rng(970 + hq)
+    qkv = wl.random_bf16(rng, (T, hq + 2 * hkv, D))
+    qw = wl.f32_to_bf16_bits(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    kw = wl.f32_to_bf16_bits(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    pos = rng.integers(0, max_pos, size=T).astype(np.int32)
+    loc = rng.choice(num_slots, size=T, replace=False).astype(np.int64)
+    dev = "cuda"
+    cs = msg.msg_rope_cos_sin_cache(THETA, D, max_pos)
+    q_out = torch.empty(T, hq, D, dtype=torch.bfloat16, device=dev)
+    kp = torch.zeros(num_slots, hkv, D, dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    status = torch.zeros(4, dtype=torch.int32, device=dev)
+    msg.msg_qk_norm_rope_store(wl.bits_to_torch(qkv, dev), torch.from_numpy(pos).to(dev),
+                               wl.bits_to_torch(qw, dev), wl.bits_to_torch(kw, dev), EPS, cs,
+                               q_out, kp, vp, torch.from_numpy(loc).to(dev), hq, hkv,
+                               dev_status=status)
+    torch.cuda.synchronize()
+    assert msg.msg_read_device_status(status)[0] == msg.MSG_OK
+    q_ref, k_ref, v_ref = oracle.qk_norm_rope(qkv, pos, qw, kw, EPS,
+                                              oracle.rope_cos_sin_cache(THETA, D, max_pos),
+                                              hq, hkv, D)
+    _check_close(wl.torch_to_bits(q_out), q_ref, "q")
+    _check_close(wl.torch_to_bits(kp)[loc], k_ref, "k")
+    assert np.array_equal(wl.torch_to_bits(vp)[loc], v_ref), "v"
+    other = np.setdiff1d(np.arange(num_slots), loc)
+    assert not wl.torch_to_bits(kp)[other].any() and not wl.torch_to_bits(vp)[other].any()
