@@ -199,7 +199,7 @@ __device__ __forceinline__ float block_excl_scan_f(float v, Smem &sm, float *tot
 // memory.  Stages whose pairs lie inside one warp's contiguous segment of
 // n / kW entries synchronise only that warp; the others the whole block.
 template <typename T>
-__device__ void bitonic_sort(T *a, int n) {
+__device__ void bitonic_sort_smem(T *a, int n) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int seg = n >= 2 * kW ? n / kW : n;     // entries per warp segment
   const bool warp_local = n >= 2 * kW;
@@ -233,6 +233,85 @@ __device__ void bitonic_sort(T *a, int n) {
     __syncthreads();
   }
 }
+// The same sort for n = kT * E: thread t holds entries t*E .. t*E+E-1 in
+// registers.  A stage with pair distance j < E exchanges registers of one
+// thread, E <= j < 32 E exchanges with lane ^ (j / E) by shuffle, and only
+// the stages with j >= 32 E go through shared memory (the whole block).
+template <typename T, int E>
+__device__ void bitonic_sort_reg(T *a) {
+  constexpr int n = kT * E;
+  const int t = threadIdx.x;
+  T r[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) r[e] = a[t * E + e];
+  for (int k = 2; k <= n; k <<= 1) {
+    int j = k >> 1;
+    if (j >= 32 * E) {                          // pairs across warps: shared memory
+#pragma unroll
+      for (int e = 0; e < E; ++e) a[t * E + e] = r[e];
+      __syncthreads();
+      for (; j >= 32 * E; j >>= 1) {
+        for (int i = t; i < (n >> 1); i += kT) {
+          const int lo = 2 * i - (i & (j - 1)), hi = lo + j;
+          const T x = a[lo], y = a[hi];
+          if ((x > y) == ((lo & k) == 0)) {
+            a[lo] = y;
+            a[hi] = x;
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) r[e] = a[t * E + e];
+    }
+    // pairs across lanes: every register of the thread is on the same side
+    const bool up = ((t * E) & k) == 0;         // k > j >= E: the same for all e
+    for (; j >= E; j >>= 1) {
+      const bool keep_min = (((t * E) & j) == 0) == up;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const T o = __shfl_xor_sync(0xffffffffu, r[e], j / E);
+        r[e] = keep_min ? (o < r[e] ? o : r[e]) : (o > r[e] ? o : r[e]);
+      }
+    }
+    // pairs inside the thread
+#pragma unroll
+    for (int jj = E >> 1; jj > 0; jj >>= 1) {
+      if (jj < k) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if (e & jj) continue;
+          const T x = r[e], y = r[e + jj];
+          if ((x > y) == (((t * E + e) & k) == 0)) {
+            r[e] = y;
+            r[e + jj] = x;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();                              // every read of a[] above is done
+#pragma unroll
+  for (int e = 0; e < E; ++e) a[t * E + e] = r[e];
+  __syncthreads();
+}
+
+// Ascending sort of n (a power of two, >= 2) entries in shared memory.
+template <typename T>
+__device__ void bitonic_sort(T *a, int n) {
+  if (n == 8 * kT) {
+    bitonic_sort_reg<T, 8>(a);
+  } else if (n == 4 * kT) {
+    bitonic_sort_reg<T, 4>(a);
+  } else if (n == 2 * kT) {
+    bitonic_sort_reg<T, 2>(a);
+  } else if (n == kT) {
+    bitonic_sort_reg<T, 1>(a);
+  } else {
+    bitonic_sort_smem(a, n);
+  }
+}
+
 __device__ __forceinline__ int pow2_at_least(int n) {
   int p = 2;
   while (p < n) p <<= 1;
