@@ -502,19 +502,29 @@ __device__ __forceinline__ void unpack_raw(const uint4 raw[2], float v[kLE]) {
   }
 }
 
+// Smallest logit value whose order key is >= K (K up to 2^32): -inf when
+// every value qualifies, NaN (every comparison false) when none does.  So
+// key_of(f) >= K exactly when f >= min_value_at_least(K), for every non-NaN f.
+__device__ __forceinline__ float min_value_at_least(unsigned long long K) {
+  if (K <= key_of(-INFINITY)) return -INFINITY;
+  if (K > key_of(INFINITY)) return __uint_as_float(0x7fffffffu);
+  if (K == 0x7fffffffull) return 0.f;          // the key of -0, which no logit has
+  return value_of((uint32_t)K);
+}
+
 // One chunk of the gather (all lanes): window logits appended, the mass of
-// those above it summed into cabove[c].
+// those above it summed into cabove[c].  f_lo / f_above: the smallest values
+// in the window / above it (min_value_at_least of lo and top + 1).
 __device__ __forceinline__ void gather_chunk(const Ctx &x, Smem &sm, const float v[kLE], int n,
-                                             int i0, int c, uint32_t lo, uint32_t top,
+                                             int i0, int c, float f_lo, float f_above,
                                              bool has_above, uint32_t &ca) {
   const int lane = threadIdx.x & 31;
   float ma = 0.f;
   uint32_t wmask = 0;
 #pragma unroll
   for (int j = 0; j < kLE; ++j) {
-    const uint32_t k = key_of(v[j]);
-    if (j < n && k >= lo) {
-      if (has_above && k > top) {
+    if (j < n && v[j] >= f_lo) {
+      if (v[j] >= f_above) {
         ++ca;
         ma += mass_of(x, v[j]);
       } else {
@@ -522,19 +532,8 @@ __device__ __forceinline__ void gather_chunk(const Ctx &x, Smem &sm, const float
       }
     }
   }
-  const int cnt = __popc(wmask);
-  const unsigned any = __ballot_sync(0xffffffffu, cnt != 0);
-  if (any) {
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int base = 0;
-    if (lane == 0) base = atomicAdd(&sm.ival[0], total);
-    base = __shfl_sync(0xffffffffu, base, 0) + incl - cnt;
+  if (wmask) {                                  // window logits are few: a slot reservation per lane
+    int base = atomicAdd(&sm.ival[0], __popc(wmask));
 #pragma unroll
     for (int j = 0; j < kLE; ++j)
       if ((wmask >> j) & 1u) {
@@ -555,9 +554,10 @@ __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi
   if (threadIdx.x == 0) sm.ival[0] = 0;
   __syncthreads();
   uint32_t ca = 0;
-  // keys in [lo, top] are in the window, keys above top above it
-  const uint32_t top = hi >= kKeyEnd ? 0xffffffffu : (uint32_t)(hi - 1);
+  // keys in [lo, hi) are in the window, keys at or above hi above it
   const bool has_above = hi < kKeyEnd;
+  const float f_lo = min_value_at_least(lo);
+  const float f_above = min_value_at_least(hi);
   for (int c0 = 1 + warp; c0 <= x.r.nch; c0 += kW * U) {
     uint4 raw[U][2];
     bool on[U], got[U];
@@ -577,8 +577,8 @@ __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi
       }
       float v[kLE];
       unpack_raw<kBf16>(raw[q], v);
-      gather_chunk(x, sm, v, got[q] ? kLE : 0, x.r.h + kLE * (32 * (c - 1) + lane), c, lo, top,
-                   has_above, ca);
+      gather_chunk(x, sm, v, got[q] ? kLE : 0, x.r.h + kLE * (32 * (c - 1) + lane), c, f_lo,
+                   f_above, has_above, ca);
     }
   }
   if (warp < 2) {                               // head (warp 0) and tail (warp 1)
@@ -587,7 +587,7 @@ __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi
       float v[kLE];
       int i0;
       const int n = chunk_lane<kBf16>(x.r, c, lane, v, i0);
-      gather_chunk(x, sm, v, n, i0, c, lo, top, has_above, ca);
+      gather_chunk(x, sm, v, n, i0, c, f_lo, f_above, has_above, ca);
     } else if (lane == 0) {
       sm.cabove[c] = 0.f;
     }
@@ -631,17 +631,17 @@ __device__ int window_crossing(Smem &sm, int n, float base, float tau) {
 
 // Probe pass: count and mass of the logits at or above each of four pivots
 // (descending keys); chunks whose maximum is below the smallest are skipped.
-__device__ __forceinline__ void probe_chunk(const Ctx &x, const float v[kLE], int n,
-                                            uint32_t p0, uint32_t p1, uint32_t p2, uint32_t p3,
-                                            bool want_mass, uint32_t c4[4], float m4[4]) {
+// f0..f3: min_value_at_least of the pivots (a value >= f_t has key >= piv[t]).
+__device__ __forceinline__ void probe_chunk(const Ctx &x, const float v[kLE], int n, float f0,
+                                            float f1, float f2, float f3, bool want_mass,
+                                            uint32_t c4[4], float m4[4]) {
 #pragma unroll
   for (int j = 0; j < kLE; ++j) {
-    const uint32_t k = key_of(v[j]);
-    if (j >= n || k < p3) continue;
+    if (j >= n || !(v[j] >= f3)) continue;
     const float e = want_mass ? mass_of(x, v[j]) : 0.f;
     ++c4[3];
     m4[3] += e;
-    const bool g2 = k >= p2, g1 = k >= p1, g0 = k >= p0;
+    const bool g2 = v[j] >= f2, g1 = v[j] >= f1, g0 = v[j] >= f0;
     c4[2] += g2;
     c4[1] += g1;
     c4[0] += g0;
@@ -658,7 +658,9 @@ __device__ void probe(const Ctx &x, Smem &sm, const uint32_t piv[4], bool want_m
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t c4[4] = {0, 0, 0, 0};
   float m4[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint32_t p0 = piv[0], p1 = piv[1], p2 = piv[2], p3 = piv[3];
+  const uint32_t p3 = piv[3];
+  const float f0 = min_value_at_least(piv[0]), f1 = min_value_at_least(piv[1]),
+              f2 = min_value_at_least(piv[2]), f3 = min_value_at_least(p3);
   for (int c0 = 1 + warp; c0 <= x.r.nch; c0 += kW * U) {
     uint4 raw[U][2];
     bool got[U];
@@ -673,7 +675,7 @@ __device__ void probe(const Ctx &x, Smem &sm, const uint32_t piv[4], bool want_m
       if (!got[q]) continue;
       float v[kLE];
       unpack_raw<kBf16>(raw[q], v);
-      probe_chunk(x, v, kLE, p0, p1, p2, p3, want_mass, c4, m4);
+      probe_chunk(x, v, kLE, f0, f1, f2, f3, want_mass, c4, m4);
     }
   }
   if (warp < 2) {
@@ -682,7 +684,7 @@ __device__ void probe(const Ctx &x, Smem &sm, const uint32_t piv[4], bool want_m
       float v[kLE];
       int i0;
       const int n = chunk_lane<kBf16>(x.r, c, lane, v, i0);
-      probe_chunk(x, v, n, p0, p1, p2, p3, want_mass, c4, m4);
+      probe_chunk(x, v, n, f0, f1, f2, f3, want_mass, c4, m4);
     }
   }
 #pragma unroll
