@@ -817,10 +817,14 @@ __device__ void estimate_pivots(const Ctx &x, Smem &sm, uint32_t lo, unsigned lo
 // below is the light part of each chunk: the chunks whose maximum is below X
 // count with their exact mass, and in the others the sample points below X
 // count with the logits they stand for.  The window spans `d` sample points on
-// either side of the first point where that estimate reaches tau.  Needs the
-// sample sorted and csort; uses lcum and the list as scratch.
-__device__ void estimate_window(const Ctx &x, Smem &sm, float tau, int d, uint32_t &lo,
-                                unsigned long long &hi) {
+// either side of the first point where that estimate reaches tau.  The window
+// stays inside [rlo, rhi), where the boundary is known to lie: mass(>= rlo)
+// >= tau (or rlo = 0) and mass(>= rhi) < tau.  With a reference key kref whose
+// exact mass mref a gather has measured, the estimate is shifted by its error
+// there.  Needs the sample sorted and csort; uses lcum and the list as scratch.
+__device__ void estimate_window(const Ctx &x, Smem &sm, float tau, int d, uint32_t rlo,
+                                unsigned long long rhi, bool has_ref, uint32_t kref, float mref,
+                                uint32_t &lo, unsigned long long &hi) {
   const float w = (float)(kChunk / x.spc);
   float *cs = reinterpret_cast<float *>(sm.list);          // chunk-mass prefix, csort order
   float *css = cs + kSortChunks;                            // sample-mass prefix, csort order
@@ -869,18 +873,32 @@ __device__ void estimate_window(const Ctx &x, Smem &sm, float tau, int d, uint32
   }
   __syncthreads();
   const float cs_tot = sm.fval[1], css_tot = sm.fval[2], samp_tot = sm.fval[3];
-  // first sample point (descending) whose estimate reaches tau
+  // estimated mass at or above K, given the mass of the sample points at or above K
+  auto estimate = [&](uint32_t K, float samp_ge) {
+    const int r = last_at_least_c(sm, 0, nc, K);            // chunks with maximum >= K
+    const float cs_lt = cs_tot - (r >= 0 ? cs[r] : 0.f);
+    const float css_lt = css_tot - (r >= 0 ? css[r] : 0.f);
+    return x.S - cs_lt - w * fmaxf(0.f, samp_tot - samp_ge - css_lt);
+  };
+  float bias = 0.f;
+  if (has_ref) {
+    int q0 = 0, q1 = x.ns;                                  // sample points with key >= kref
+    while (q0 < q1) {
+      const int mid = (q0 + q1) >> 1;
+      if (~sm.samp[mid] >= kref) q0 = mid + 1;
+      else q1 = mid;
+    }
+    bias = mref - estimate(kref, q0 > 0 ? sm.lcum[q0 - 1] : 0.f);
+  }
+  // first sample point (descending) whose estimate reaches tau; points at or
+  // below rlo reach it, points at or above rhi do not
   int first = x.ns;
   const int per = (x.ns + kT - 1) / kT;
   const int a = min(x.ns, (int)threadIdx.x * per), b = min(x.ns, a + per);
   for (int i = a; i < b; ++i) {
     const uint32_t K = ~sm.samp[i];
-    const int r = last_at_least_c(sm, 0, nc, K);            // chunks with maximum >= K
-    const float cs_lt = cs_tot - (r >= 0 ? cs[r] : 0.f);
-    const float css_lt = css_tot - (r >= 0 ? css[r] : 0.f);
-    const float samp_lt = samp_tot - sm.lcum[i];
-    const float e = x.S - cs_lt - w * fmaxf(0.f, samp_lt - css_lt);
-    if (e >= tau) {
+    if ((unsigned long long)K >= rhi) continue;
+    if ((rlo > 0 && K <= rlo) || estimate(K, sm.lcum[i]) + bias >= tau) {
       first = i;
       break;
     }
@@ -888,7 +906,12 @@ __device__ void estimate_window(const Ctx &x, Smem &sm, float tau, int d, uint32
   first = block_min_i(first, sm);
   lo = first + d < x.ns ? ~sm.samp[first + d] : 0u;
   hi = first - d >= 0 ? (unsigned long long)(~sm.samp[first - d]) : kKeyEnd;
-  if (hi <= lo) hi = kKeyEnd;
+  if (lo < rlo) lo = rlo;
+  if (hi > rhi) hi = rhi;
+  if (hi <= lo) {
+    hi = rhi;
+    if (hi <= lo) lo = rlo;
+  }
 }
 
 // Sort the sample once (descending keys, invalid points last); x.ns = valid points.
@@ -1507,42 +1530,60 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
           gathered = n_win <= kCap;
         }
         if (!gathered) {
-          // one gather around the estimate; a miss still tells which side
+          // a gather around the estimate; a miss still tells which side, and
+          // the exact mass it measured at that edge corrects the estimate for
+          // a second gather on that side
           sort_sample(x, sm);
-          uint32_t piv[4];
-          if (lo == 0 && hi == kKeyEnd) {
-            uint32_t wl;
-            unsigned long long wh;
-            estimate_window(x, sm, tau, 16, wl, wh);
-            piv[0] = wh >= kKeyEnd ? 0xffffffffu : (uint32_t)wh;
-            piv[3] = wl;
-            piv[1] = piv[2] = piv[3];
-          } else {
-            int a, b;
-            sample_span(x, sm, lo, hi, a, b);
-            estimate_pivots(x, sm, lo, hi, a, b, kChunk / x.spc,
-                            fminf(0.1f * x.S, mass_lo - mass_hi), mass_hi, tau, piv);
-          }
-          clamp_pivots(piv, lo, hi);
-          n_win = gather<kBf16>(x, sm, piv[3], piv[0], &cnt_above, &mass_above);
-          if (n_win <= kCap) {
-            sort_window(x, sm, n_win);
-            const float wm = n_win > 0 ? sm.lcum[n_win - 1] : 0.f;
-            if (mass_above < tau && tau <= mass_above + wm) {
-              gathered = sorted = true;
+          bool side_above = false;
+          int dwin = 16;
+          for (int attempt = 0; attempt < 2 && !gathered; ++attempt) {
+            uint32_t piv[4];
+            if (attempt == 1 || (lo == 0 && hi == kKeyEnd)) {
+              uint32_t wl;
+              unsigned long long wh;
+              estimate_window(x, sm, tau, dwin, lo, hi, attempt == 1,
+                              side_above ? lo : (uint32_t)hi, side_above ? mass_lo : mass_hi,
+                              wl, wh);
+              piv[0] = wh >= kKeyEnd ? 0xffffffffu : (uint32_t)wh;
+              piv[3] = wl;
+              piv[1] = piv[2] = piv[3];
+              if (attempt == 0) clamp_pivots(piv, lo, hi);
+            } else {
+              int a, b;
+              sample_span(x, sm, lo, hi, a, b);
+              estimate_pivots(x, sm, lo, hi, a, b, kChunk / x.spc,
+                              fminf(0.1f * x.S, mass_lo - mass_hi), mass_hi, tau, piv);
+              clamp_pivots(piv, lo, hi);
+            }
+            n_win = gather<kBf16>(x, sm, piv[3], piv[0], &cnt_above, &mass_above);
+            if (n_win <= kCap) {
+              sort_window(x, sm, n_win);
+              const float wm = n_win > 0 ? sm.lcum[n_win - 1] : 0.f;
+              if (mass_above < tau && tau <= mass_above + wm) {
+                gathered = sorted = true;
+              } else if (mass_above >= tau) {
+                lo = piv[0];
+                cnt_lo = cnt_above;
+                mass_lo = mass_above;
+                side_above = true;
+              } else {
+                hi = piv[3];
+                cnt_hi = cnt_above + (unsigned long long)n_win;
+                mass_hi = mass_above + wm;
+                side_above = false;
+              }
             } else if (mass_above >= tau) {
               lo = piv[0];
               cnt_lo = cnt_above;
               mass_lo = mass_above;
-            } else {
-              hi = piv[3];
-              cnt_hi = cnt_above + (unsigned long long)n_win;
-              mass_hi = mass_above + wm;
+              side_above = true;
+            } else {                            // too many in the window: the boundary is below its top
+              hi = piv[0];
+              cnt_hi = cnt_above;
+              mass_hi = mass_above;
+              side_above = false;
+              dwin = 8;
             }
-          } else if (mass_above >= tau) {
-            lo = piv[0];
-            cnt_lo = cnt_above;
-            mass_lo = mass_above;
           }
         }
         if (!gathered)
