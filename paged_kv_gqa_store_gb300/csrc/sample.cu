@@ -512,12 +512,11 @@ __device__ __forceinline__ float min_value_at_least(unsigned long long K) {
   return value_of((uint32_t)K);
 }
 
-// One chunk of the gather (all lanes): window logits appended, the mass of
-// those above it summed into cabove[c].  f_lo / f_above: the smallest values
+// One chunk of the gather (all lanes): window logits appended; returns the
+// lane's mass of the logits above the window (the caller sums the warp).  f_lo / f_above: the smallest values
 // in the window / above it (min_value_at_least of lo and top + 1).
-__device__ __forceinline__ void gather_chunk(const Ctx &x, Smem &sm, const float v[kLE], int n,
-                                             int i0, int c, float f_lo, float f_above,
-                                             bool has_above, uint32_t &ca) {
+__device__ __forceinline__ float gather_chunk(const Ctx &x, Smem &sm, const float v[kLE], int n,
+                                              int i0, float f_lo, float f_above, uint32_t &ca) {
   const int lane = threadIdx.x & 31;
   float ma = 0.f;
   uint32_t wmask = 0;
@@ -541,8 +540,7 @@ __device__ __forceinline__ void gather_chunk(const Ctx &x, Smem &sm, const float
         ++base;
       }
   }
-  if (has_above) ma = warp_sum_f(ma);
-  if (lane == 0) sm.cabove[c] = ma;
+  return ma;
 }
 
 template <bool kBf16>
@@ -555,7 +553,6 @@ __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi
   __syncthreads();
   uint32_t ca = 0;
   // keys in [lo, hi) are in the window, keys at or above hi above it
-  const bool has_above = hi < kKeyEnd;
   const float f_lo = min_value_at_least(lo);
   const float f_above = min_value_at_least(hi);
   for (int c0 = 1 + warp; c0 <= x.r.nch; c0 += kW * U) {
@@ -567,18 +564,26 @@ __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi
       on[q] = c <= x.r.nch && sm.cmax[c] != -INFINITY && key_of(sm.cmax[c]) >= lo;
       got[q] = on[q] && load_chunk_raw<kBf16>(x.r, c, lane, raw[q]);
     }
+    float ma[U];
 #pragma unroll
     for (int q = 0; q < U; ++q) {
       const int c = c0 + q * kW;
-      if (c > x.r.nch) break;                   // warp-uniform
-      if (!on[q]) {
-        if (lane == 0) sm.cabove[c] = 0.f;
-        continue;
-      }
+      ma[q] = 0.f;
+      if (c > x.r.nch || !on[q]) continue;      // warp-uniform
       float v[kLE];
       unpack_raw<kBf16>(raw[q], v);
-      gather_chunk(x, sm, v, got[q] ? kLE : 0, x.r.h + kLE * (32 * (c - 1) + lane), c, f_lo,
-                   f_above, has_above, ca);
+      ma[q] = gather_chunk(x, sm, v, got[q] ? kLE : 0, x.r.h + kLE * (32 * (c - 1) + lane), f_lo,
+                           f_above, ca);
+    }
+    // the chunks' above-window masses, reduced together
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < U; ++q) ma[q] += __shfl_xor_sync(0xffffffffu, ma[q], o);
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < U; ++q)
+        if (c0 + q * kW <= x.r.nch) sm.cabove[c0 + q * kW] = ma[q];
     }
   }
   if (warp < 2) {                               // head (warp 0) and tail (warp 1)
@@ -587,7 +592,8 @@ __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi
       float v[kLE];
       int i0;
       const int n = chunk_lane<kBf16>(x.r, c, lane, v, i0);
-      gather_chunk(x, sm, v, n, i0, c, f_lo, f_above, has_above, ca);
+      const float ma = warp_sum_f(gather_chunk(x, sm, v, n, i0, f_lo, f_above, ca));
+      if (lane == 0) sm.cabove[c] = ma;
     } else if (lane == 0) {
       sm.cabove[c] = 0.f;
     }
