@@ -104,6 +104,31 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Pairwise fp32 arithmetic (one instruction for two IEEE round-to-nearest
+// operations) and a maximum that returns NaN when either input is NaN.
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
 
 // ---- block primitives (every thread calls; every thread gets the result)
 __device__ __forceinline__ float warp_sum_f(float v) {
@@ -1239,26 +1264,38 @@ __global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams 
   bool finite = true;
   unsigned long long best = 0;                  // (key << 32) | ~index, max wins
   auto chunk = [&](const float v[kLE], int n, int c_logical, int i0, int sample_slot) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kLE; ++j)
-      if (j < n) {
-        if (kGreedy) {
-          finite &= v[j] == v[j];               // NaN
-          const unsigned long long kk =
-              ((unsigned long long)key_of(v[j]) << 32) | (0xffffffffu - (uint32_t)(i0 + j));
-          best = kk > best ? kk : best;
-        } else {
-          m = fmaxf(m, v[j]);
-        }
-      }
-    if (!kGreedy) {
-      m = warp_max_f(m);
-      float s = 0.f;
+    if (kGreedy) {
+      // the lane's largest value (NaN if any is NaN), then its first position:
+      // the largest (key, ~index) of the lane's logits
+      float mv = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kLE; ++j)
-        if (j < n) s += ex2((v[j] - m) * kx);
-      s = warp_sum_f(s);
+        if (j < n) mv = fmax_nan(mv, v[j]);
+      finite &= mv == mv;
+      int jj = -1;
+#pragma unroll
+      for (int j = kLE - 1; j >= 0; --j)
+        if (j < n && v[j] == mv) jj = j;
+      if (jj >= 0) {
+        const unsigned long long kk =
+            ((unsigned long long)key_of(mv) << 32) | (0xffffffffu - (uint32_t)(i0 + jj));
+        best = kk > best ? kk : best;
+      }
+    } else {
+      float m = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kLE; ++j)
+        if (j < n) m = fmaxf(m, v[j]);
+      m = warp_max_f(m);
+      // sum of 2^((v - m) kx), even and odd positions apart, in pairs
+      float2 s2 = make_float2(0.f, 0.f);
+      const float2 nm2 = make_float2(-m, -m), kx2 = make_float2(kx, kx);
+#pragma unroll
+      for (int j = 0; j < kLE; j += 2) {
+        const float2 y = fmul2(fadd2(make_float2(v[j], v[j + 1]), nm2), kx2);
+        s2 = fadd2(s2, make_float2(j < n ? ex2(y.x) : 0.f, j + 1 < n ? ex2(y.y) : 0.f));
+      }
+      float s = warp_sum_f(s2.x + s2.y);
       // a NaN turns the mass into NaN, +inf the maximum; -inf is a zero-mass logit
       if (m == -INFINITY) s = 0.f;
       finite &= m != INFINITY && s == s;
