@@ -1325,11 +1325,7 @@ __global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams 
                      : "l"(src + 16));
     }
   }
-#pragma unroll
-  for (int q = 0; q < kScanPerWarp; ++q) {
-    const int c = cbeg + q * kScanWarps;
-    if (c >= r.nch) break;                      // warp-uniform
-    float v[kLE];
+  auto unpack = [&](int q, float v[kLE]) {
     if (kBf16) {
       const uint4 w = raw[q][0];
       v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
@@ -1341,9 +1337,68 @@ __global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams 
       v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
       v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
     }
-    const int every = 32 / spc;
-    const int slot = (lane & (every - 1)) == 0 ? c * spc + lane / every : -1;
-    chunk(v, n[q], c + 1, r.h + kLE * (32 * c + lane), slot);
+  };
+  const int every = 32 / spc;
+  if (kGreedy) {
+#pragma unroll
+    for (int q = 0; q < kScanPerWarp; ++q) {
+      const int c = cbeg + q * kScanWarps;
+      if (c >= r.nch) break;                    // warp-uniform
+      float v[kLE];
+      unpack(q, v);
+      chunk(v, n[q], c + 1, r.h + kLE * (32 * c + lane), -1);
+    }
+  } else {
+    // the warp's chunks side by side: maxima, then masses relative to them,
+    // each reduced over the warp for all chunks at once
+    float m[kScanPerWarp], sm2[kScanPerWarp];
+#pragma unroll
+    for (int q = 0; q < kScanPerWarp; ++q) {
+      float v[kLE];
+      unpack(q, v);
+      m[q] = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kLE; ++j)
+        if (j < n[q]) m[q] = fmaxf(m[q], v[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < kScanPerWarp; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
+#pragma unroll
+    for (int q = 0; q < kScanPerWarp; ++q) {
+      float v[kLE];
+      unpack(q, v);
+      float2 s2 = make_float2(0.f, 0.f);
+      const float2 nm2 = make_float2(-m[q], -m[q]), kx2 = make_float2(kx, kx);
+#pragma unroll
+      for (int j = 0; j < kLE; j += 2) {
+        const float2 y = fmul2(fadd2(make_float2(v[j], v[j + 1]), nm2), kx2);
+        s2 = fadd2(s2, make_float2(j < n[q] ? ex2(y.x) : 0.f, j + 1 < n[q] ? ex2(y.y) : 0.f));
+      }
+      sm2[q] = s2.x + s2.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < kScanPerWarp; ++q) sm2[q] += __shfl_xor_sync(0xffffffffu, sm2[q], o);
+#pragma unroll
+    for (int q = 0; q < kScanPerWarp; ++q) {
+      const int c = cbeg + q * kScanWarps;
+      if (c >= r.nch) break;                    // warp-uniform
+      // a NaN turns the mass into NaN, +inf the maximum; -inf is a zero-mass logit
+      const float s = m[q] == -INFINITY ? 0.f : sm2[q];
+      finite &= m[q] != INFINITY && s == s;
+      if (lane == 0) {
+        cmax[c + 1] = m[q];
+        cmass[c + 1] = s;
+      }
+      if ((lane & (every - 1)) == 0) {
+        float v0[kLE];
+        unpack(q, v0);
+        samp[c * spc + lane / every] = (n[q] && v0[0] != m[q]) ? ~key_of(v0[0]) : ~0u;
+      }
+    }
   }
   if (part == 0 && warp == 0) {                 // head and tail chunks
     for (int c = 0; c < r.nch + 2; c += r.nch + 1) {
