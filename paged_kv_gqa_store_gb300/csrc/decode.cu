@@ -121,6 +121,8 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
 // Raw index entry that locates local key j (token table: the page's first
 // slot; page-id forms: the page).  Loaded ahead of use; validated by raw_to_slot.
 // kPage1: page_size 1, where every index form holds the slot itself.
+constexpr int kMergeBatch = 4;                // split partials loaded before any is applied
+
 template <bool kPage1>
 __device__ __forceinline__ int32_t load_raw(const AttnParams &p, const int32_t *row, int64_t j) {
   return __ldg(row + (kPage1 ? j : kv_entry(p.kv, j)));
@@ -410,29 +412,61 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
         if (lane == 0) old = atomicAdd(&p.counters[(int64_t)h.r * kHkv + gh], 1);
         old = __shfl_sync(0xffffffffu, old, 0);
         if (old == h.bl - h.bf) {
-          // last of the (request, KV head) splits: merge them
+          // last of the (request, KV head) splits: merge them.  The splits'
+          // lse values are loaded by the lanes side by side (split bf + k by
+          // lane k % 32), the o rows split after split with several loads in
+          // flight; the sums run in split order.
           __threadfence();
+          const int ns = h.bl - h.bf + 1;
+          auto slot_of = [&](int k) {
+            return 2 * (int64_t)(h.bf + k) + (k == 0 ? h.head_shift : 0);
+          };
           float L0 = -INFINITY, L1 = -INFINITY;
-          for (int bb = h.bf; bb <= h.bl; ++bb) {
-            const int64_t sl = 2 * (int64_t)bb + (bb == h.bf ? h.head_shift : 0);
+          for (int k = lane; k < ns; k += 32) {
+            const int64_t sl = slot_of(k);
             L0 = fmaxf(L0, __ldcg(p.part_lse + sl * kHq + 2 * gh));
             L1 = fmaxf(L1, __ldcg(p.part_lse + sl * kHq + 2 * gh + 1));
           }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            L0 = fmaxf(L0, __shfl_xor_sync(0xffffffffu, L0, o));
+            L1 = fmaxf(L1, __shfl_xor_sync(0xffffffffu, L1, o));
+          }
           float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
           float d0 = 0.f, d1 = 0.f;
-          for (int bb = h.bf; bb <= h.bl; ++bb) {
-            const int64_t sl = 2 * (int64_t)bb + (bb == h.bf ? h.head_shift : 0);
-            const float w0 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh) - L0);
-            const float w1 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh + 1) - L1);
-            const float *pr0 = p.part_o + (sl * kHq + 2 * gh) * kHeadDim + lane * 4;
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(pr0));
-            const float4 y = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
-            n0.x = fmaf(w0, x.x, n0.x); n0.y = fmaf(w0, x.y, n0.y);
-            n0.z = fmaf(w0, x.z, n0.z); n0.w = fmaf(w0, x.w, n0.w);
-            n1.x = fmaf(w1, y.x, n1.x); n1.y = fmaf(w1, y.y, n1.y);
-            n1.z = fmaf(w1, y.z, n1.z); n1.w = fmaf(w1, y.w, n1.w);
-            d0 += w0;
-            d1 += w1;
+          for (int k0 = 0; k0 < ns; k0 += 32) {
+            float w0 = 0.f, w1 = 0.f;
+            if (k0 + lane < ns) {
+              const int64_t sl = slot_of(k0 + lane);
+              w0 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh) - L0);
+              w1 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh + 1) - L1);
+            }
+            const int nk = ns - k0 < 32 ? ns - k0 : 32;
+            for (int j0 = 0; j0 < nk; j0 += kMergeBatch) {
+              float4 xs[kMergeBatch], ys[kMergeBatch];
+#pragma unroll
+              for (int u = 0; u < kMergeBatch; ++u) {   // the batch's loads, all in flight
+                if (j0 + u < nk) {
+                  const float *pr0 =
+                      p.part_o + (slot_of(k0 + j0 + u) * kHq + 2 * gh) * kHeadDim + lane * 4;
+                  xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
+                  ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kMergeBatch; ++u) {
+                if (j0 + u >= nk) break;
+                const float a0 = __shfl_sync(0xffffffffu, w0, j0 + u);
+                const float a1 = __shfl_sync(0xffffffffu, w1, j0 + u);
+                const float4 x = xs[u], y = ys[u];
+                n0.x = fmaf(a0, x.x, n0.x); n0.y = fmaf(a0, x.y, n0.y);
+                n0.z = fmaf(a0, x.z, n0.z); n0.w = fmaf(a0, x.w, n0.w);
+                n1.x = fmaf(a1, y.x, n1.x); n1.y = fmaf(a1, y.y, n1.y);
+                n1.z = fmaf(a1, y.z, n1.z); n1.w = fmaf(a1, y.w, n1.w);
+                d0 += a0;
+                d1 += a1;
+              }
+            }
           }
           if (row_ok) {
             const float e0 = 1.f / d0, e1 = 1.f / d1;
