@@ -8,17 +8,18 @@
 // vocabulary order, first exceeds u times the kept total.  Without
 // temperatures every row is greedy and the token is the first maximum.
 //
-// GB300 layout: one CTA per row, streaming the row.  The first pass reads the
-// row from HBM once and keeps, per chunk of 256 logits, its maximum and its
-// mass relative to that maximum, plus a sparse sample of the row; a batch of
-// bf16 logits (78 MB for 256 x 151,936) then stays in L2 for the few later
-// reads.  A row without a cut draws straight from the chunk masses (one more
-// read of a single chunk).  With a cut, the k-th token or the top-p boundary
-// is located inside a small window of logit values: the window is estimated
-// from the chunk maxima or from the sample, tightened when needed by probe
-// passes that count logits and sum masses above four pivots, then gathered
-// (at most kCap logits), sorted by (logit desc, index asc) and resolved
-// exactly.  The kept set is "every token ranked at or before the threshold
+// GB300 layout: a scan kernel over all SMs reads every row from HBM once and
+// keeps, per chunk of 256 logits, its maximum and its mass relative to that
+// maximum, plus a sparse sample of the row; a batch of bf16 logits (78 MB for
+// 256 x 151,936) then stays in L2 for the few later reads by the row kernel,
+// one CTA per row.  A row without a cut draws straight from the chunk masses
+// (one more read of a single chunk).  With a cut, the k-th token or the top-p
+// boundary is located inside a small window of logit values: the window is
+// estimated from the chunk maxima or from the sample (for top-p, a second
+// estimate corrected by the exact mass the first gather measured at its edge
+// when the first window misses), tightened when needed by probe passes that
+// count logits and sum masses above four pivots, then gathered (at most kCap
+// logits), sorted by (logit desc, index asc) and resolved exactly.  The kept set is "every token ranked at or before the threshold
 // token", so the draw needs no rank bookkeeping: either the whole kept set is
 // in the window (a sort by index and one scan), or the gather also summed,
 // per chunk, the mass above the window and the draw walks the chunks.
@@ -497,9 +498,6 @@ struct Ctx {
 
 __device__ __forceinline__ float mass_of(const Ctx &x, float l) { return ex2((l - x.M) * x.kx); }
 
-// Window [lo, hi) of order keys: gather its logits into the list (at most kCap
-// stored; the full count is returned), and per chunk the mass of the logits
-// at or above hi (cabove); *cnt_above / *mass_above get their totals.
 // Load the lane's 8 logits of vector chunk c (1-based logical index) into raw.
 template <bool kBf16>
 __device__ __forceinline__ bool load_chunk_raw(const RowRef &r, int c, int lane, uint4 raw[2]) {
@@ -538,11 +536,10 @@ __device__ __forceinline__ float min_value_at_least(unsigned long long K) {
 }
 
 // One chunk of the gather (all lanes): window logits appended; returns the
-// lane's mass of the logits above the window (the caller sums the warp).  f_lo / f_above: the smallest values
-// in the window / above it (min_value_at_least of lo and top + 1).
+// lane's mass of the logits above the window (the caller sums the warp).
+// f_lo / f_above: min_value_at_least of the window's bounds lo and hi.
 __device__ __forceinline__ float gather_chunk(const Ctx &x, Smem &sm, const float v[kLE], int n,
                                               int i0, float f_lo, float f_above, uint32_t &ca) {
-  const int lane = threadIdx.x & 31;
   float ma = 0.f;
   uint32_t wmask = 0;
 #pragma unroll
@@ -568,6 +565,9 @@ __device__ __forceinline__ float gather_chunk(const Ctx &x, Smem &sm, const floa
   return ma;
 }
 
+// Window [lo, hi) of order keys: gather its logits into the list (at most kCap
+// stored; the full count is returned), and per chunk the mass of the logits
+// at or above hi (cabove); *cnt_above / *mass_above get their totals.
 template <bool kBf16>
 __device__ int gather(const Ctx &x, Smem &sm, uint32_t lo, unsigned long long hi,
                       unsigned long long *cnt_above, float *mass_above) {
