@@ -27,6 +27,7 @@
 // Masses are fp32 2^((l - max) * log2(e) / T) summed in a fixed order (no
 // atomics), so a row's token is deterministic.
 #include <math.h>
+#include <stddef.h>
 
 #include "internal.cuh"
 
@@ -75,6 +76,9 @@ struct Smem {
   int ival[8];
   float fval[4];
 };
+// the draw reuses the sample's array for per-chunk 64-bit sums
+static_assert(offsetof(Smem, samp) % 8 == 0 && kMaxSamples / 2 >= kMaxChunks,
+              "samp holds kMaxChunks 64-bit sums");
 
 // ---- keys and masses
 // Order key of a logit: increasing with the value (-0 is read as +0).
@@ -1716,18 +1720,21 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
         tok = draw_list(x, sm, n_win, u);
       } else {
         if (!tie_mode) {
-          // add the kept window entries to their chunks: entries by index,
-          // the first entry of each chunk sums the chunk's run
-          window_by_index(x, sm, n_win);
+          // add the kept window entries to their chunks: per chunk a 64-bit
+          // fixed-point sum (2^-40 of the row maximum's mass), exact and so
+          // independent of the order of the atomics; the sample's array is
+          // free by now
+          unsigned long long *acc = reinterpret_cast<unsigned long long *>(sm.samp);
+          for (int c = threadIdx.x; c < x.nl; c += kT) acc[c] = 0ull;
+          __syncthreads();
           for (int i = threadIdx.x; i < n_win; i += kT) {
-            const int c = chunk_of(x.r, (int)(sm.list[i] >> 32));
-            if (i == 0 || chunk_of(x.r, (int)(sm.list[i - 1] >> 32)) != c) {
-              float s = 0.f;
-              for (int j = i; j < n_win && chunk_of(x.r, (int)(sm.list[j] >> 32)) == c; ++j)
-                s += __uint_as_float((uint32_t)sm.list[j]);
-              sm.cabove[c] += s;
-            }
+            const unsigned long long e = sm.list[i];
+            const float m = mass_of(x, value_of(~(uint32_t)(e >> 32)));
+            atomicAdd(&acc[chunk_of(x.r, (int)(uint32_t)e)], __float2ull_rn(m * 1099511627776.f));
           }
+          __syncthreads();
+          for (int c = threadIdx.x; c < x.nl; c += kT)
+            if (acc[c]) sm.cabove[c] += __ull2float_rn(acc[c]) * 9.094947017729282e-13f;
         } else {
           // cabove holds the mass above vk, cmass the count of vk, per chunk:
           // ties with index <= ik are kept
