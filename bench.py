@@ -3,7 +3,8 @@
 
 One step = one pass of the whole hot path over one batch: the metadata plan,
 then for each of the 28 layers store_kv of the step's new K/V and the paged
-attention over the 64-request decode batch (context U[512, 4096], page_size 1,
+attention (one fused kernel per layer, msg_paged_attention_store) over the
+64-request decode batch (context U[512, 4096], page_size 1,
 16 query / 8 KV heads, head_dim 128, bf16, 28 independent 300k-slot layer
 pools, one shared page table).  The headline metric is decode KV-read GB/s
 (algorithmic bytes: every needed K/V row once, q, out and page-table entries,
@@ -194,16 +195,17 @@ def run_ours(args, rank, world, dist):
         msg.msg_plan(pt, cached, ext, T, spec.num_slots, ws, req_rows=rows, qo_indptr_out=qo,
                      out_loc_out=loc)
         for i, t in enumerate(layers):
-            msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], loc)
+            # store_kv of the step's new rows and the decode attention, in one kernel
             if ev is not None:
                 ev[i][0].record(stream)
-            msg.msg_paged_attention(t["q"], t["k_pool"], t["v_pool"], pt, cached, ext, qo,
-                                    outs[i], ws, page_size=spec.page_size, req_rows=rows,
-                                    max_kv_len=spec.max_kv_len, flags=flags)
+            msg.msg_paged_attention_store(t["q"], t["k_new"], t["v_new"], t["k_pool"],
+                                          t["v_pool"], pt, cached, ext, qo, outs[i], ws,
+                                          page_size=spec.page_size, req_rows=rows,
+                                          max_kv_len=spec.max_kv_len, flags=flags)
             if ev is not None:
                 ev[i][1].record(stream)
 
-    launches_per_step = 2 + 2 * L                 # plan + token meta, store + decode per layer
+    launches_per_step = 2 + L                     # plan + token meta, store + decode per layer
 
     def barrier():
         if dist is not None:
@@ -243,7 +245,8 @@ def run_ours(args, rank, world, dist):
     bytes_step = L * (bytes_layer + store_bytes(spec))
     value = weak_scaling_gbs(bytes_step, world, ms)
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
-    achieved = bytes_layer / (attn_ms * 1e-3) / 1e9
+    # the fused launch also writes the step's new K / V rows to the pool
+    achieved = (bytes_layer + spec.total_q * 2 * KV_ROW) / (attn_ms * 1e-3) / 1e9
     traffic = ncu_traffic("decode_kernel")
 
     # ---- end to end through the C ABI from pinned host buffers
@@ -301,10 +304,10 @@ def run_ours(args, rank, world, dist):
         for i, t in enumerate(layers):
             if i == first_wait + 1:
                 stream.wait_event(ev_in[L - 1])
-            msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], loc)
-            msg.msg_paged_attention(t["q"], t["k_pool"], t["v_pool"], pt, cached, ext, qo,
-                                    outs[i], ws, page_size=spec.page_size, req_rows=rows,
-                                    max_kv_len=spec.max_kv_len, flags=flags)
+            msg.msg_paged_attention_store(t["q"], t["k_new"], t["v_new"], t["k_pool"],
+                                          t["v_pool"], pt, cached, ext, qo, outs[i], ws,
+                                          page_size=spec.page_size, req_rows=rows,
+                                          max_kv_len=spec.max_kv_len, flags=flags)
             if i in ev_out:
                 ev_out[i].record(stream)
         with torch.cuda.stream(cs):
@@ -366,7 +369,7 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
         "roofline": {
             "kernel": "decode_kernel", "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "peak_source": peaks["source"], "bytes_per_launch": bytes_layer,
+            "peak_source": peaks["source"], "bytes_per_launch": bytes_layer + spec.total_q * 2 * KV_ROW,
             "launch_ms": round(attn_ms, 5),
             "timing": "CUDA events around each decode launch in a second timed pass of the "
                       "same steps (events between launches disable the early start)",

@@ -319,6 +319,38 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
                         void *stream);
 
 /*
+ * a2 + a3/a4 fused for a decode step ([WALK] 4.6.7 steps 1 and 2: store_kv, then
+ * attention): a decode-only batch (flags must include MSG_ATTN_DECODE_ONLY)
+ * whose new K / V rows have not been stored yet.  Equivalent to
+ *   msg_store_kv(k_new, v_new, kv_row_stride, k_pool, v_pool, ..., out_loc, ...)
+ *   msg_paged_attention(q, ..., k_pool, v_pool, ...)
+ * with out_loc[qo_indptr[r]] = the slot of token cached_len[r] of request r's
+ * row (the slot msg_plan writes to out_loc): the decode kernel gathers each
+ * request's newest key from k_new / v_new row qo_indptr[r] instead of the
+ * pool, and the CTA that owns that key writes the two rows to its pool slot.
+ * Outputs and pools are bit-identical to the two calls; one kernel launch
+ * instead of two.
+ *
+ * k_new, v_new    bf16 [total_q, num_kv_heads, head_dim], rows kv_row_stride
+ *                 elements apart (16-byte aligned rows), in q's row order.
+ * k_pool, v_pool  written at the new tokens' slots (the only writes).
+ * Other arguments as msg_paged_attention.  A slot outside the pool is
+ * recorded in the workspace's status block and not written.
+ * Errors: as msg_paged_attention; MSG_ERR_INVALID_ARG also without
+ *         MSG_ATTN_DECODE_ONLY or with a NULL k_new / v_new.
+ */
+int msg_paged_attention_store(const void *q, int64_t q_row_stride, const void *k_new,
+                              const void *v_new, int64_t kv_row_stride, void *k_pool,
+                              void *v_pool, int64_t pool_row_stride, int64_t num_slots,
+                              const int32_t *page_table, int64_t page_table_stride,
+                              const int32_t *req_rows, const int32_t *cached_len,
+                              const int32_t *extend_len, const int32_t *qo_indptr,
+                              int32_t num_reqs, int64_t total_q, int32_t max_kv_len,
+                              int32_t page_size, int32_t num_qo_heads, int32_t num_kv_heads,
+                              int32_t head_dim, float scale, void *out, void *workspace,
+                              size_t workspace_bytes, uint32_t flags, void *stream);
+
+/*
  * a3-a6 with any index layout: as msg_paged_attention, with the slots of each
  * request's keys read through `kv` (host pointer to the descriptor, device
  * arrays; its page_size replaces the page_size argument).

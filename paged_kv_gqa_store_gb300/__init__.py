@@ -140,6 +140,10 @@ def load_library(path: str | None = None):
             P, I64, P, P, I64, I64, P, I64, P, P, P, P, I32, I64, I32, I32, I32, I32, I32,
             ctypes.c_float, P, P, SZ, U32, P]
         lib.msg_paged_attention.restype = ctypes.c_int
+        lib.msg_paged_attention_store.argtypes = [
+            P, I64, P, P, I64, P, P, I64, I64, P, I64, P, P, P, P, I32, I64, I32, I32, I32, I32,
+            I32, ctypes.c_float, P, P, SZ, U32, P]
+        lib.msg_paged_attention_store.restype = ctypes.c_int
         lib.msg_read_device_status.argtypes = [P, P, P]
         lib.msg_read_device_status.restype = ctypes.c_int
         lib.msg_clear_device_status.argtypes = [P, P]
@@ -343,6 +347,45 @@ def msg_paged_attention(q, k_pool, v_pool, page_table, cached_len, extend_len, q
         int(max_kv_len), int(page_size), hq, hkv, d, float(scale), _ptr(out), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), int(flags), _stream(stream))
     _check("msg_paged_attention", st)
+
+
+def msg_paged_attention_store(q, k_new, v_new, k_pool, v_pool, page_table, cached_len, extend_len,
+                              qo_indptr, out, workspace, page_size: int = 1,
+                              scale: float | None = None, req_rows=None, max_kv_len: int = 0,
+                              flags: int = MSG_ATTN_DECODE_ONLY, stream=None) -> None:
+    """A decode step's store_kv of k_new / v_new and its attention in one kernel
+    (decode-only batches: flags must include MSG_ATTN_DECODE_ONLY)."""
+    import torch
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"),
+                 (v_pool, "v_pool"), (out, "out")):
+        _expect(t, torch.bfloat16, n)
+    _expect(page_table, torch.int32, "page_table")
+    if q.dim() != 3 or k_pool.dim() != 3 or k_new.dim() != 3:
+        raise ValueError("q / k_new are [total_q, H, D] and the pools are [slots, Hkv, D]")
+    if not out.is_contiguous() or out.shape != q.shape:
+        raise ValueError("out must be contiguous with q's shape")
+    if k_new.shape != v_new.shape or k_new.shape[0] != q.shape[0]:
+        raise ValueError("k_new / v_new must have one row per q row")
+    if page_table.numel() and page_table.stride(1) != 1:
+        raise ValueError("page_table rows must be contiguous")
+    hq, d = int(q.shape[1]), int(q.shape[2])
+    hkv = int(k_pool.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pst = _row_stride(k_pool, "k_pool")
+    if _row_stride(v_pool, "v_pool") != pst:
+        raise ValueError("k_pool and v_pool must share a row stride")
+    kst = _row_stride(k_new, "k_new")
+    if _row_stride(v_new, "v_new") != kst:
+        raise ValueError("k_new and v_new must share a row stride")
+    st = load_library().msg_paged_attention_store(
+        _ptr(q), _row_stride(q, "q"), _ptr(k_new), _ptr(v_new), kst, _ptr(k_pool), _ptr(v_pool),
+        pst, int(k_pool.shape[0]), _ptr(page_table), int(page_table.stride(0)), _ptr(req_rows),
+        _ptr(cached_len), _ptr(extend_len), _ptr(qo_indptr), int(cached_len.numel()),
+        int(q.shape[0]), int(max_kv_len), int(page_size), hq, hkv, d, float(scale), _ptr(out),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()), int(flags),
+        _stream(stream))
+    _check("msg_paged_attention_store", st)
 
 
 def msg_paged_attention_ex(q, k_pool, v_pool, kv: KvIndex, cached_len, extend_len, qo_indptr,

@@ -136,7 +136,9 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
                    const int32_t *qo_indptr, int32_t num_reqs, int64_t total_q,
                    int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
                    int32_t head_dim, float scale, void *out, void *workspace,
-                   size_t workspace_bytes, uint32_t flags, void *stream);
+                   size_t workspace_bytes, uint32_t flags, void *stream,
+                   const void *k_new = nullptr, const void *v_new = nullptr,
+                   int64_t kv_row_stride = 0);
 
 }  // namespace
 
@@ -237,6 +239,27 @@ int msg_paged_attention(const void *q, int64_t q_row_stride, const void *k_pool,
                         workspace_bytes, flags, stream);
 }
 
+int msg_paged_attention_store(const void *q, int64_t q_row_stride, const void *k_new,
+                              const void *v_new, int64_t kv_row_stride, void *k_pool,
+                              void *v_pool, int64_t pool_row_stride, int64_t num_slots,
+                              const int32_t *page_table, int64_t page_table_stride,
+                              const int32_t *req_rows, const int32_t *cached_len,
+                              const int32_t *extend_len, const int32_t *qo_indptr,
+                              int32_t num_reqs, int64_t total_q, int32_t max_kv_len,
+                              int32_t page_size, int32_t num_qo_heads, int32_t num_kv_heads,
+                              int32_t head_dim, float scale, void *out, void *workspace,
+                              size_t workspace_bytes, uint32_t flags, void *stream) {
+  const int rc = check_heads(num_qo_heads, num_kv_heads, head_dim);
+  if (rc != MSG_OK) return rc;
+  if (page_table_stride < 0 || k_new == nullptr || v_new == nullptr) return MSG_ERR_INVALID_ARG;
+  if (!pow2_page(page_size)) return MSG_ERR_UNSUPPORTED;
+  return attention_impl(q, q_row_stride, k_pool, v_pool, pool_row_stride, num_slots,
+                        token_table(page_table, page_table_stride, req_rows, page_size),
+                        cached_len, extend_len, qo_indptr, num_reqs, total_q, max_kv_len,
+                        num_qo_heads, num_kv_heads, head_dim, scale, out, workspace,
+                        workspace_bytes, flags, stream, k_new, v_new, kv_row_stride);
+}
+
 int msg_paged_attention_ex(const void *q, int64_t q_row_stride, const void *k_pool,
                            const void *v_pool, int64_t pool_row_stride, int64_t num_slots,
                            const msg_kv_index *kv, const int32_t *cached_len,
@@ -266,7 +289,8 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
                    const int32_t *qo_indptr, int32_t num_reqs, int64_t total_q,
                    int32_t max_kv_len, int32_t num_qo_heads, int32_t num_kv_heads,
                    int32_t head_dim, float scale, void *out, void *workspace,
-                   size_t workspace_bytes, uint32_t flags, void *stream) {
+                   size_t workspace_bytes, uint32_t flags, void *stream,
+                   const void *k_new, const void *v_new, int64_t kv_row_stride) {
   int rc = MSG_OK;
   if (num_reqs < 0 || total_q < 0 || total_q > INT32_MAX || max_kv_len < 0 || num_slots < 0 ||
       !(scale > 0.f) || !isfinite(scale))
@@ -277,6 +301,12 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
   if (num_reqs == 0 || total_q == 0) return MSG_OK;
   if (!q || !k_pool || !v_pool || !kv.table || !cached_len || !extend_len || !qo_indptr || !out)
     return MSG_ERR_INVALID_ARG;
+  if ((k_new != nullptr) != (v_new != nullptr)) return MSG_ERR_INVALID_ARG;
+  if (k_new != nullptr) {                       // the store fused into the decode kernel
+    if (!(flags & MSG_ATTN_DECODE_ONLY)) return MSG_ERR_INVALID_ARG;
+    if (kv_row_stride < (int64_t)num_kv_heads * head_dim) return MSG_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || kv_row_stride % 8 != 0) return MSG_ERR_ALIGNMENT;
+  }
   const int64_t row = (int64_t)num_kv_heads * head_dim;
   if (q_row_stride < (int64_t)num_qo_heads * head_dim || pool_row_stride < row)
     return MSG_ERR_INVALID_ARG;
@@ -338,6 +368,11 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
   ap.out = static_cast<uint16_t *>(out);
   ap.status = status;
   ap.hdr = reinterpret_cast<const PlanHeader *>(ws + L.header);
+  ap.k_new = static_cast<const uint8_t *>(k_new);
+  ap.v_new = static_cast<const uint8_t *>(v_new);
+  ap.new_stride_bytes = kv_row_stride * 2;
+  ap.k_pool_w = static_cast<uint8_t *>(const_cast<void *>(k_pool));
+  ap.v_pool_w = static_cast<uint8_t *>(const_cast<void *>(v_pool));
   ap.dec_req = reinterpret_cast<const int32_t *>(ws + L.dec_req);
   ap.dec_start = reinterpret_cast<const int64_t *>(ws + L.dec_start);
   ap.dec_row = reinterpret_cast<const int64_t *>(ws + L.dec_row);

@@ -127,6 +127,12 @@ template <bool kPage1>
 __device__ __forceinline__ int32_t load_raw(const AttnParams &p, const int32_t *row, int64_t j) {
   return __ldg(row + (kPage1 ? j : kv_entry(p.kv, j)));
 }
+// Whether the index entry of key j names a slot in the pool (no report).
+template <bool kPage1>
+__device__ __forceinline__ bool raw_ok(const AttnParams &p, int32_t raw, int64_t j) {
+  if (kPage1) return raw >= 0 && raw < p.num_slots;
+  return kv_slot(p.kv, raw, j, p.num_slots, nullptr, 0) >= 0;
+}
 // Slot of key j; an invalid entry is reported and redirected to slot 0.
 template <bool kPage1>
 __device__ __forceinline__ int64_t raw_to_slot(const AttnParams &p, int32_t raw, int64_t j,
@@ -252,10 +258,42 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
           mbar_arrive_expect_tx(&full[st], (uint32_t)nkeys * 2 * kRowBytes + (first ? kQBytes : 0));
         }
         __syncwarp();
+        // with the step's new rows given, a request's newest key comes from
+        // them (and is stored to its pool slot below)
+        const int newest =
+            (p.k_new != nullptr && last && sg.hi == sg.E && sg.qrow >= 0) ? nkeys - 1 : -1;
         if (lane < nkeys) {
           const int64_t off = slot * p.pool_stride_bytes;
-          bulk_g2s(stage + lane * kRowBytes, p.k_pool + off, kRowBytes, &full[st]);
-          bulk_g2s(stage + kOffV + lane * kRowBytes, p.v_pool + off, kRowBytes, &full[st]);
+          const uint8_t *ks = p.k_pool + off, *vs = p.v_pool + off;
+          if (lane == newest) {
+            ks = p.k_new + (int64_t)sg.qrow * p.new_stride_bytes;
+            vs = p.v_new + (int64_t)sg.qrow * p.new_stride_bytes;
+          }
+          bulk_g2s(stage + lane * kRowBytes, ks, kRowBytes, &full[st]);
+          bulk_g2s(stage + kOffV + lane * kRowBytes, vs, kRowBytes, &full[st]);
+        }
+        if (newest >= 0) {
+          // store_kv of that token: its slot, the same bits the gathers read
+          const int64_t nslot = __shfl_sync(0xffffffffu, slot, newest);
+          const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + (int64_t)sg.qrow * p.new_stride_bytes);
+          const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + (int64_t)sg.qrow * p.new_stride_bytes);
+          const bool slot_ok = raw_ok<kPage1>(p, __shfl_sync(0xffffffffu, raw, newest),
+                                              kt + newest - sg.S);
+          if (slot_ok) {
+            uint4 *kd = reinterpret_cast<uint4 *>(p.k_pool_w + nslot * p.pool_stride_bytes);
+            uint4 *vd = reinterpret_cast<uint4 *>(p.v_pool_w + nslot * p.pool_stride_bytes);
+            uint4 a[kRowBytes / 16 / 32], c[kRowBytes / 16 / 32];
+#pragma unroll
+            for (int u = 0; u < kRowBytes / 16 / 32; ++u) {
+              a[u] = ks[u * 32 + lane];
+              c[u] = vs[u * 32 + lane];
+            }
+#pragma unroll
+            for (int u = 0; u < kRowBytes / 16 / 32; ++u) {
+              kd[u * 32 + lane] = a[u];
+              vd[u * 32 + lane] = c[u];
+            }
+          }
         }
         if (first && lane == 0) {
           const int64_t qr = sg.qrow < 0 ? 0 : sg.qrow;

@@ -159,6 +159,12 @@ struct AttnParams {
   uint16_t *out;
   int32_t *status;
   const PlanHeader *hdr;
+  // decode only: the step's new K / V rows (row = the request's q row), read
+  // for each request's newest key in place of the pool and stored to the pool
+  // by the decode kernel itself; NULL when they are already in the pool
+  const uint8_t *k_new, *v_new;
+  int64_t new_stride_bytes;
+  uint8_t *k_pool_w, *v_pool_w;
   const int32_t *dec_req;
   const int64_t *dec_start;
   const int64_t *dec_row;

@@ -86,6 +86,35 @@ def test_attention_argument_validation(lib, kw, status):
     assert _attn(lib, **kw) == status
 
 
+def _attn_store(lib, **kw):
+    a = dict(q=FAKE, q_row_stride=2048, k_new=FAKE, v_new=FAKE, kv_row_stride=1024, k_pool=FAKE,
+             v_pool=FAKE, pool_row_stride=1024, num_slots=100, page_table=FAKE,
+             page_table_stride=32, req_rows=None, cached_len=FAKE, extend_len=FAKE,
+             qo_indptr=FAKE, num_reqs=2, total_q=2, max_kv_len=0, page_size=1, num_qo_heads=16,
+             num_kv_heads=8, head_dim=128, scale=0.088, out=FAKE, workspace=FAKE,
+             workspace_bytes=1 << 30, flags=msg.MSG_ATTN_DECODE_ONLY, stream=None)
+    a.update(kw)
+    return lib.msg_paged_attention_store(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(flags=0), msg.MSG_ERR_INVALID_ARG),                 # decode-only batches alone
+    (dict(flags=msg.MSG_ATTN_EXTEND_ONLY), msg.MSG_ERR_INVALID_ARG),
+    (dict(k_new=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(v_new=None), msg.MSG_ERR_INVALID_ARG),
+    (dict(kv_row_stride=512), msg.MSG_ERR_INVALID_ARG),
+    (dict(k_new=FAKE + 8), msg.MSG_ERR_ALIGNMENT),
+    (dict(kv_row_stride=1028), msg.MSG_ERR_ALIGNMENT),
+    (dict(head_dim=64), msg.MSG_ERR_UNSUPPORTED),
+    (dict(page_size=3), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_reqs=0), msg.MSG_OK),
+])
+def test_fused_store_attention_argument_validation(lib, kw, status):
+    """msg_paged_attention_store: the store fused into the decode kernel takes
+    decode-only batches and the step's new K / V rows (16-byte aligned)."""
+    assert _attn_store(lib, **kw) == status
+
+
 def _store(lib, **kw):
     a = dict(k=FAKE, v=FAKE, kv_row_stride=1024, k_pool=FAKE, v_pool=FAKE,
              pool_row_stride=1024, num_slots=10, out_loc=FAKE, is64=0, num_tokens=3,

@@ -83,6 +83,42 @@ def test_long_single_decode_splits_over_all_ctas():
     _check_full(spec, wl.host_tensors(spec))
 
 
+@pytest.mark.parametrize("page_size", [1, 16])
+def test_fused_store_decode_is_store_then_attend(page_size):
+    """msg_paged_attention_store (store_kv done by the decode kernel, the newest
+    key gathered from k_new / v_new) gives the output and pool bits of
+    msg_store_kv followed by msg_paged_attention, with one request cut across
+    most CTAs, and matches the oracle."""
+    rng = np.random.default_rng(560 + page_size)
+    n = 12
+    cached = rng.integers(1, 2000, size=n)
+    cached[0] = 12000
+    pages = int(sum((c + page_size) // page_size + 1 for c in cached)) + 64
+    spec = wl.make_batch("fused", 560 + page_size, cached, np.ones(n, np.int32), page_size,
+                         num_pages=pages)
+    host = wl.host_tensors(spec)
+    ref = run_small(spec, host, flags=msg.MSG_ATTN_DECODE_ONLY)
+    assert ref["status"] == msg.MSG_OK, ref["status_info"]
+    dev = "cuda"
+    gb = GpuBatch(spec, dev)
+    q = wl.bits_to_torch(host["q"], dev)
+    k_new, v_new = wl.bits_to_torch(host["k_new"], dev), wl.bits_to_torch(host["v_new"], dev)
+    k_pool, v_pool = wl.bits_to_torch(host["k_pool"], dev), wl.bits_to_torch(host["v_pool"], dev)
+    gb.plan()
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    msg.msg_paged_attention_store(q, k_new, v_new, k_pool, v_pool, gb.page_table, gb.cached,
+                                  gb.extend, gb.qo, out, gb.ws, page_size=spec.page_size,
+                                  req_rows=gb.rows, max_kv_len=spec.max_kv_len,
+                                  flags=msg.MSG_ATTN_DECODE_ONLY | msg.MSG_ATTN_REUSE_PLAN)
+    torch.cuda.synchronize()
+    st, info = gb.status()
+    assert st == msg.MSG_OK, info
+    assert np.array_equal(wl.torch_to_bits(out), ref["out"])
+    assert np.array_equal(wl.torch_to_bits(k_pool), ref["k_pool"])
+    assert np.array_equal(wl.torch_to_bits(v_pool), ref["v_pool"])
+    assert_attn_close(wl.torch_to_bits(out), oracle_small(spec, host)["out"], "fused")
+
+
 def test_many_tiny_decodes():
     rng = np.random.default_rng(502)
     n = 600
