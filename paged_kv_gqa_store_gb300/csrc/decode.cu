@@ -148,7 +148,10 @@ __device__ __forceinline__ int64_t raw_to_slot(const AttnParams &p, int32_t raw,
   return slot < 0 ? 0 : slot;
 }
 
-template <bool kPage1>
+// kFused: the step's new K / V rows are given (p.k_new): each request's newest
+// key is read from them and stored to the pool here (compiled apart, so the
+// plain kernel carries none of it).
+template <bool kPage1, bool kFused>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   float *pbuf = reinterpret_cast<float *>(smem + (size_t)kStages * kStageBytes);
@@ -260,19 +263,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
         __syncwarp();
         // with the step's new rows given, a request's newest key comes from
         // them (and is stored to its pool slot below)
-        const int newest =
-            (p.k_new != nullptr && last && sg.hi == sg.E && sg.qrow >= 0) ? nkeys - 1 : -1;
+        const int newest = (kFused && last && sg.hi == sg.E && sg.qrow >= 0) ? nkeys - 1 : -1;
         if (lane < nkeys) {
           const int64_t off = slot * p.pool_stride_bytes;
           const uint8_t *ks = p.k_pool + off, *vs = p.v_pool + off;
-          if (lane == newest) {
+          if (kFused && lane == newest) {
             ks = p.k_new + (int64_t)sg.qrow * p.new_stride_bytes;
             vs = p.v_new + (int64_t)sg.qrow * p.new_stride_bytes;
           }
           bulk_g2s(stage + lane * kRowBytes, ks, kRowBytes, &full[st]);
           bulk_g2s(stage + kOffV + lane * kRowBytes, vs, kRowBytes, &full[st]);
         }
-        if (newest >= 0) {
+        if (kFused && newest >= 0) {
           // store_kv of that token: its slot, the same bits the gathers read
           const int64_t nslot = __shfl_sync(0xffffffffu, slot, newest);
           const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + (int64_t)sg.qrow * p.new_stride_bytes);
@@ -531,17 +533,17 @@ cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t 
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kSmem);
-    if (e != cudaSuccess) return e;
+    for (auto k : {decode_kernel<true, false>, decode_kernel<false, false>,
+                   decode_kernel<true, true>, decode_kernel<false, true>}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = true;
   }
-  if (p.page_size == 1)
-    return launch_k(decode_kernel<true>, dim3(grid), dim3(kThreads), kSmem, s, pdl, p);
-  return launch_k(decode_kernel<false>, dim3(grid), dim3(kThreads), kSmem, s, pdl, p);
+  const bool fused = p.k_new != nullptr;
+  auto k = p.page_size == 1 ? (fused ? decode_kernel<true, true> : decode_kernel<true, false>)
+                            : (fused ? decode_kernel<false, true> : decode_kernel<false, false>);
+  return launch_k(k, dim3(grid), dim3(kThreads), kSmem, s, pdl, p);
 }
 
 int decode_ctas_per_sm() { return 2; }
