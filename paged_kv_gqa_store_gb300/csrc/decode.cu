@@ -28,6 +28,11 @@
 //   walks the keys and heads in an XOR-permuted order so that the butterfly
 //   never has to pick halves), then an fp32 online softmax in base 2 (scale *
 //   log2 e folded into q) and the P.V accumulation, with packed f32x2 FMAs.
+// - Fused store (the kFused instantiations, msg_paged_attention_store): with
+//   the step's new K / V rows given, the one CTA whose range holds a request's
+//   newest key gathers it from those rows instead of the pool and its producer
+//   warp writes them to the key's pool slot -- store_kv done by this kernel,
+//   bit-identical to running it first.
 // - Waits are bounded by wall-clock time: an expired wait records
 //   MSG_DEV_TIMEOUT, raises an abort flag that ends every loop, and the
 //   producer drains its copies before the CTA exits.  There are no CTA-wide
