@@ -235,7 +235,7 @@ extern "C" int msg_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, i
   p.hkv = num_kv_heads;
   p.status = dev_status;
   int64_t blocks = (num_tokens + 7) / 8;           // one warp per token
-  const int64_t cap = (int64_t)device_sm_count() * 8;
+  const int64_t cap = (int64_t)device_sm_count() * 3;   // persistent: the 3 CTAs an SM holds
   if (blocks > cap) blocks = cap;
   return launch_k(prologue_kernel, dim3((unsigned)blocks), dim3(256), 0,
                   static_cast<cudaStream_t>(stream), true, p) == cudaSuccess
