@@ -346,13 +346,24 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     import torch
     torch.cuda.empty_cache()
     R, L = spec.num_reqs, args.layers
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu
+    args.cpu_samples = {} if want_cpu else None
+    tiny = run_tiny_mixed(args, dev, msg) if rank == 0 and not args.no_extend else None
+    ladder = run_graph_ladder(args, dev, msg) if rank == 0 and not args.no_extend else None
     extend = run_extend(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     small = run_graph_decode(args, dev, msg) if rank == 0 and not args.no_extend else None
     large = run_large_decode(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     mixed = run_long_mixed(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     prologue = run_prologue(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     sampler = run_sampler(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
-    cpu = cpu_baseline(spec) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    cpu = cpu_baseline(spec) if want_cpu else None
+    cpu_configs = None
+    if want_cpu:
+        import oracle
+        cpu_configs = cpu_oracle_configs()
+        cpu_configs.update(args.cpu_samples)
+        cpu_configs = {"cpu_model": cpu_model(), "cores": oracle.num_threads(),
+                       "kind": "oracle", **dict(sorted(cpu_configs.items()))}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -378,6 +389,10 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if tiny is not None:
+        line["tiny_mixed"] = tiny
+    if ladder is not None:
+        line["graph_ladder"] = ladder
     if extend is not None:
         line["extend"] = extend
     if small is not None:
@@ -391,8 +406,97 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     if sampler is not None:
         line["sampler"] = sampler
     if cpu is not None:
-        line["cpu_baseline"] = cpu
+        line["cpu_baseline"] = {**cpu, "cpu_model": cpu_model()}
+    if cpu_configs is not None:
+        line["cpu_baseline_per_config"] = cpu_configs
     return line
+
+
+def run_tiny_mixed(args, dev, msg):
+    """The tiny mixed batch (1 extend of 4 over 2 cached + decodes at 5, 17 and
+    64 keys): one whole step -- plan, store_kv, attention -- in microseconds,
+    L2 flushed before every timed step (a latency config: no roofline)."""
+    import torch
+    spec = wl.config_tiny_mixed()
+    host = wl.host_tensors(spec)
+    b = _planned_batch(spec, dev, msg)
+    q = wl.bits_to_torch(host["q"], dev)
+    kn, vn = wl.bits_to_torch(host["k_new"], dev), wl.bits_to_torch(host["v_new"], dev)
+    kp, vp = wl.bits_to_torch(host["k_pool"], dev), wl.bits_to_torch(host["v_pool"], dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        msg.msg_plan(b["pt"], b["cached"], b["ext"], b["T"], spec.num_slots, b["ws"],
+                     req_rows=b["rows"], qo_indptr_out=b["qo"], out_loc_out=b["loc"])
+        msg.msg_store_kv(kn, vn, kp, vp, b["loc"], dev_status=b["ws"])
+        msg.msg_paged_attention(q, kp, vp, b["pt"], b["cached"], b["ext"], b["qo"], out, b["ws"],
+                                page_size=1, req_rows=b["rows"], max_kv_len=spec.max_kv_len,
+                                flags=msg.MSG_ATTN_REUSE_PLAN)
+
+    ms = _median_launch_ms(step, max(args.steps, 50), flush)
+    _check_status(msg, b, "tiny mixed")
+    del flush
+    return {"workload": "tiny_mixed_1ext4_cached2_3dec_ctx5-17-64_page1", "us": round(ms * 1e3, 2),
+            "launches": 5, "l2": "flushed (256 MB write) before every timed step",
+            "what": "plan + token metadata + store_kv + decode + extend kernels, one step"}
+
+
+def run_graph_ladder(args, dev, msg):
+    """Launch-bound decode steps: 1, 2, 4 and 8 requests at contexts U[128, 512]
+    over 28 layers, eager launches against CUDA-graph replay of the captured
+    ladder sizes (the graph runner pads nothing here: each is a ladder size)."""
+    import torch
+    from paged_kv_gqa_store_gb300 import graph as mgraph
+    rng = np.random.default_rng(2010)
+    max_bs, L = 8, 28
+    ctx = rng.integers(128, 512 + 1, size=max_bs)
+    n = max(args.steps, 20)
+    steps = 8 * (n + 3) + 8                          # tokens a request gains over the leg
+    spec = wl.make_batch("ladder", 2011, cached_len=ctx - 1 + steps,
+                         extend_len=np.ones(max_bs, np.int32), page_size=1,
+                         num_pages=int((ctx + steps).sum()) + 64, num_layers=L)
+    pt = np.zeros((max_bs + 1, spec.page_table.shape[1]), np.int32)
+    pt[:max_bs] = spec.page_table
+    pt[max_bs] = spec.num_slots                      # the dummy row -> the dummy slot
+    slots = spec.num_slots + 1
+    g = torch.Generator(device=dev).manual_seed(2012)
+    pools = [(torch.randn(slots, wl.HKV, wl.HEAD_DIM, generator=g, device=dev).to(torch.bfloat16),
+              torch.randn(slots, wl.HKV, wl.HEAD_DIM, generator=g, device=dev).to(torch.bfloat16))
+             for _ in range(L)]
+    runner = mgraph.DecodeGraphRunner(pools, torch.from_numpy(pt).to(dev), max_bs, max_bs)
+    for i in range(L):
+        for x in (runner.q[i], runner.k_new[i], runner.v_new[i]):
+            x.copy_(torch.randn(x.shape, generator=g, device=dev).to(torch.bfloat16))
+    runner.capture()
+    res = {"workload": "decode_bs1-8_ctx128-512_28layers_page1",
+           "what": "plan + 28 fused store+decode launches per step; ms per step, back to back",
+           "sizes": runner.sizes}
+    cached = (ctx - 1).astype(np.int64)
+    for bs in (1, 2, 4, 8):
+        live = np.arange(bs)
+        row = {}
+        for mode, fn in (("eager", runner.eager), ("graph", runner.replay)):
+            for _ in range(3):
+                fn(cached[live], live)
+                cached[live] += 1
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(n):
+                fn(cached[live], live)
+                cached[live] += 1
+            b.record()
+            torch.cuda.synchronize()
+            row[f"{mode}_ms"] = round(a.elapsed_time(b) / n, 4)
+        row["speedup"] = round(row["eager_ms"] / row["graph_ms"], 3)
+        res[f"bs{bs}"] = row
+    st, info = msg.msg_read_device_status(runner.ws)
+    if st != msg.MSG_OK:
+        raise RuntimeError(f"graph ladder: device status {info}")
+    del runner, pools
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_graph_decode(args, dev, msg):
@@ -517,7 +621,7 @@ def _planned_batch(spec, dev, msg, sel=None):
     ext = spec.extend_len[sel]
     T = int(ext.sum())
     b = {"pt": i32(spec.page_table), "cached": i32(spec.cached_len[sel]), "ext": i32(ext),
-         "rows": i32(spec.req_rows[sel]), "T": T, "R": len(sel),
+         "rows": i32(spec.req_rows[sel]), "T": T, "R": len(sel), "sel": sel,
          "tok": (int(qo_full[sel[0]]), int(qo_full[sel[0]]) + T),
          "qo": torch.zeros(len(sel) + 1, dtype=torch.int32, device=dev),
          "loc": torch.zeros(T, dtype=torch.int64, device=dev),
@@ -557,6 +661,30 @@ def _attn_call(msg, spec, t, b, out, flags):
     return call
 
 
+def _page_table_call(msg, spec, t, b, out, flags):
+    """The same (sub)batch read through the FlashAttention / TRT-LLM dense
+    page-id table ("Mini-SGLang 完整剖析" 4.6.4) instead of the token table:
+    the index is built on the device, planned with it (the plan's index rows
+    depend on the layout), and attention reads it."""
+    import torch
+    dev = b["pt"].device
+    kv_len = (spec.cached_len.astype(np.int64) + spec.extend_len)[b["sel"]]
+    width = int(((kv_len + spec.page_size - 1) // spec.page_size).max())
+    table = torch.empty(b["R"], width, dtype=torch.int32, device=dev)
+    msg.msg_build_kv_index(msg.MSG_KV_PAGE_TABLE, spec.page_size, b["pt"], b["cached"], b["ext"],
+                           table, req_rows=b["rows"], dev_status=b["ws"])
+    kv = msg.KvIndex(msg.MSG_KV_PAGE_TABLE, table, spec.page_size)
+    ws = torch.zeros_like(b["ws"])
+    msg.msg_plan_ex(kv, b["cached"], b["ext"], b["T"], spec.num_slots, ws)
+    t0, t1 = b["tok"]
+    q, o = t["q"][t0:t1], out[t0:t1]
+
+    def call():
+        msg.msg_paged_attention_ex(q, t["k_pool"], t["v_pool"], kv, b["cached"], b["ext"],
+                                   b["qo"], o, ws, max_kv_len=spec.max_kv_len, flags=flags)
+    return call, {"ws": ws, "table": table}
+
+
 def _check_status(msg, b, what):
     st, info = msg.msg_read_device_status(b["ws"])
     if st != msg.MSG_OK:
@@ -581,10 +709,27 @@ def run_large_decode(args, dev, msg, peaks):
     _check_status(msg, b, "large decode")
     by = decode_attn_bytes(spec)
     gbs = by / (ms * 1e-3) / 1e9
-    del t, b, out
+    # the dense page-id table layout on the same batch (one entry per page
+    # either way at page_size 16: the token table is read at page starts)
+    pcall, pb = _page_table_call(msg, spec, t, b, out,
+                                 msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_DECODE_ONLY)
+    pms = _median_launch_ms(pcall, max(args.steps, 20))
+    _check_status(msg, pb, "large decode, page-id table")
+    cpu = None
+    if getattr(args, "cpu_samples", None) is not None:
+        # the CPU oracle on a sample of requests, their referenced pages
+        # fetched from the device pools (never the whole pool)
+        cpu = cpu_oracle_config3(spec, t)
+    del t, b, out, pb
     torch.cuda.empty_cache()
+    if cpu is not None:
+        args.cpu_samples["3_large_decode"] = cpu
     return {"workload": "decode_256req_ctx1024-8192_page16_pool90pct", "gbs": round(gbs, 1),
             "frac": round(gbs / peaks["hbm_gbs"], 4), "attn_ms": round(ms, 4),
+            "page_table_layout": {"attn_ms": round(pms, 4),
+                                  "gbs": round(by / (pms * 1e-3) / 1e9, 1),
+                                  "frac": round(by / (pms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                  "vs_token_table": round(ms / pms, 4)},
             "bytes_per_launch": by, "pool_pages": pages,
             "pool_gb_k_plus_v": round(2 * spec.num_slots * KV_ROW / 1e9, 1),
             "kv_tokens": int(spec.device_len.sum()),
@@ -702,8 +847,10 @@ def run_long_mixed(args, dev, msg, peaks):
     ext_ms = _median_launch_ms(_attn_call(msg, spec, t, be, out, reuse | msg.MSG_ATTN_EXTEND_ONLY),
                                n, flush)
     mix_ms = _median_launch_ms(_attn_call(msg, spec, t, b, out, reuse), n, flush)
+    pcall, pb = _page_table_call(msg, spec, t, bd, out, reuse | msg.MSG_ATTN_DECODE_ONLY)
+    dec_pt_ms = _median_launch_ms(pcall, n, flush)
     for x, what in ((b, "long mixed"), (bd, "long mixed, decode part"),
-                    (be, "long mixed, extend part")):
+                    (be, "long mixed, extend part"), (pb, "long mixed, page-id table")):
         _check_status(msg, x, what)
     pages = (spec.device_len + spec.page_size - 1) // spec.page_size
     dec_bytes = int((spec.device_len[dec].sum() * 2 * KV_ROW + dec.sum() * 2 * QO_ROW
@@ -711,12 +858,17 @@ def run_long_mixed(args, dev, msg, peaks):
     fl = extend_flops(spec)
     hbm_ms = dec_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
     tc_ms = fl / (peaks["bf16_tflops"] * 1e12) * 1e3
-    del t, b, bd, be, out, flush
+    del t, b, bd, be, out, flush, pb
     torch.cuda.empty_cache()
     return {"workload": "mixed_32dec_ctx32768_2ext2048_cached16384_page64",
             "decode_only_ms": round(dec_ms, 4),
             "decode_gbs": round(dec_bytes / (dec_ms * 1e-3) / 1e9, 1),
             "decode_frac": round(hbm_ms / dec_ms, 4),
+            "decode_page_table_layout": {
+                "attn_ms": round(dec_pt_ms, 4),
+                "gbs": round(dec_bytes / (dec_pt_ms * 1e-3) / 1e9, 1),
+                "frac": round(hbm_ms / dec_pt_ms, 4),
+                "vs_token_table": round(dec_ms / dec_pt_ms, 4)},
             "extend_only_ms": round(ext_ms, 4),
             "extend_tflops": round(fl / (ext_ms * 1e-3) / 1e12, 1),
             "extend_frac": round(tc_ms / ext_ms, 4),
@@ -768,6 +920,148 @@ def cpu_baseline(spec, budget_s: float = 12.0):
                       f"oracle with OpenMP, {elapsed:.1f} s"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def _oracle_sample_inputs(spec, reqs, rows_per_req=None, pools=None, seed=77):
+    """Host inputs for the oracle on a sample of a config: the chosen requests
+    relabelled into a compact pool (values from the device pools when given,
+    fetching only the referenced pages, else seeded N(0,1) bf16), new q/k/v
+    rows, and optionally a sample of query rows per request."""
+    import torch
+    sub, src = wl.compact_requests(spec, reqs)
+    rng = np.random.default_rng([spec.seed, seed])
+    n = src.shape[0]
+    shape = (n, spec.num_kv_heads, spec.head_dim)
+    if pools is None:
+        kp, vp = wl.random_bf16(rng, shape), wl.random_bf16(rng, shape)
+    else:
+        idx = torch.from_numpy(src).to(pools[0].device)
+        kp = wl.torch_to_bits(pools[0].index_select(0, idx))
+        vp = wl.torch_to_bits(pools[1].index_select(0, idx))
+    T = sub.total_q
+    data = {"q": wl.random_bf16(rng, (T, spec.num_qo_heads, spec.head_dim)),
+            "k_new": wl.random_bf16(rng, (T, spec.num_kv_heads, spec.head_dim)),
+            "v_new": wl.random_bf16(rng, (T, spec.num_kv_heads, spec.head_dim)),
+            "k_pool": kp, "v_pool": vp}
+    rows = None
+    if rows_per_req is not None:
+        qo = np.concatenate([[0], np.cumsum(sub.extend_len)]).astype(np.int64)
+        rows = np.concatenate([np.sort(rng.choice(np.arange(qo[r], qo[r + 1]),
+                                                  min(rows_per_req, qo[r + 1] - qo[r]),
+                                                  replace=False))
+                               for r in range(sub.num_reqs)]).astype(np.int64)
+    return sub, data, rows
+
+
+def _oracle_pass_s(sub, data, rows, threads, budget_s):
+    """Mean wall time of one oracle pass (metadata, store_kv, attention of the
+    sampled rows) with `threads` OpenMP threads, over passes filling budget_s
+    (at least one)."""
+    import oracle
+    oracle.set_num_threads(threads)
+    done, elapsed = 0, 0.0
+    while done == 0 or elapsed < budget_s:
+        t0 = time.perf_counter()
+        meta = oracle.metadata(sub.page_table, sub.cached_len, sub.extend_len, sub.req_rows)
+        oracle.store_kv(data["k_new"], data["v_new"], meta["out_loc"], data["k_pool"],
+                        data["v_pool"])
+        oracle.paged_attention(data["q"], data["k_pool"], data["v_pool"], sub.page_table,
+                               sub.cached_len, meta["qo_indptr"], sub.num_qo_heads,
+                               sub.num_kv_heads, sub.head_dim, req_rows=sub.req_rows, rows=rows)
+        elapsed += time.perf_counter() - t0
+        done += 1
+    return elapsed / done, done
+
+
+def _rows_flops(sub, rows):
+    """4 D Hq per visible (query, key) pair of the sampled query rows."""
+    qo = np.concatenate([[0], np.cumsum(sub.extend_len)]).astype(np.int64)
+    r = np.searchsorted(qo, rows, side="right") - 1
+    keys = sub.cached_len[r].astype(np.int64) + (rows - qo[r]) + 1
+    return 4.0 * sub.head_dim * sub.num_qo_heads * float(keys.sum())
+
+
+def _cpu_entry(sub, data, rows, unit, work, all_threads, budget_s, sample):
+    """The oracle on all cores and on one core; value = work / time in unit
+    (GB/s, TFLOP/s) or the time of one pass (us)."""
+    out = {"sample": sample}
+    for name, th in (("all_cores", all_threads), ("one_core", 1)):
+        s, n = _oracle_pass_s(sub, data, rows, th, budget_s)
+        if unit == "us":
+            v = s * 1e6
+        elif unit == "GB/s":
+            v = work / s / 1e9
+        else:
+            v = work / s / 1e12
+        out[name] = {"value": round(v, 6 if unit == "TFLOP/s" else 4), "unit": unit,
+                     "threads": th, "passes": n}
+    return out
+
+
+def cpu_oracle_configs(budget_s: float = 1.5):
+    """The fp64 oracle, as it stands, on bounded samples of configs 1, 2, 4 and
+    5 (config 3 is timed in its GPU leg, on pages fetched from the device)."""
+    import oracle
+    all_threads = oracle.num_threads()
+    res = {}
+    spec = wl.config_tiny_mixed()
+    sub, data, rows = _oracle_sample_inputs(spec, np.arange(spec.num_reqs))
+    res["1_tiny_mixed"] = _cpu_entry(sub, data, None, "us", 0, all_threads, budget_s,
+                                     "the whole batch (4 requests, 7 new tokens)")
+    spec = wl.config_decode_28_layers()
+    reqs = np.arange(0, 64, 8)
+    sub, data, _ = _oracle_sample_inputs(spec, reqs)
+    res["2_decode_64x28"] = _cpu_entry(sub, data, None, "GB/s",
+                                       decode_attn_bytes(sub) + store_bytes(sub), all_threads,
+                                       budget_s, "8 of the 64 requests, one layer")
+    spec = wl.config_extend()
+    sub, data, rows = _oracle_sample_inputs(spec, [0, 5], rows_per_req=24)
+    res["4_extend"] = _cpu_entry(sub, data, rows, "TFLOP/s", _rows_flops(sub, rows),
+                                 all_threads, budget_s,
+                                 "2 of the 8 requests, 24 query rows each")
+    spec = wl.config_long_mixed()
+    sub, data, _ = _oracle_sample_inputs(spec, [0, 1])
+    res["5_long_mixed_decode"] = _cpu_entry(sub, data, None, "GB/s",
+                                            decode_attn_bytes(sub) + store_bytes(sub),
+                                            all_threads, budget_s,
+                                            "2 of the 32 decode requests (32768 keys each)")
+    sub, data, rows = _oracle_sample_inputs(spec, [32], rows_per_req=8)
+    res["5_long_mixed_extend"] = _cpu_entry(sub, data, rows, "TFLOP/s", _rows_flops(sub, rows),
+                                            all_threads, budget_s,
+                                            "1 of the 2 extend requests, 8 query rows")
+    oracle.set_num_threads(all_threads)
+    return res
+
+
+def cpu_oracle_config3(spec, t, budget_s: float = 1.5):
+    import oracle
+    all_threads = oracle.num_threads()
+    reqs = np.arange(0, spec.num_reqs, 32)
+    sub, data, _ = _oracle_sample_inputs(spec, reqs, pools=(t["k_pool"], t["v_pool"]))
+    r = _cpu_entry(sub, data, None, "GB/s", decode_attn_bytes(sub) + store_bytes(sub),
+                   all_threads, budget_s,
+                   f"{len(reqs)} of the 256 requests, their pages fetched from the device pools")
+    oracle.set_num_threads(all_threads)
+    return r
+
+
 def run_reference(args):
     """The oracle as the reference arm: each step is one layer of the same workload."""
     import oracle
@@ -804,8 +1098,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--extend-only", action="store_true",
                     help="run only the extend sub-benchmark and print its JSON (profiling)")
-    ap.add_argument("--only", choices=["extend", "graph", "large", "mixed", "prologue",
-                                       "sampler"],
+    ap.add_argument("--only", choices=["extend", "graph", "ladder", "tiny", "large", "mixed",
+                                       "prologue", "sampler", "cpu"],
                     default=None,
                     help="run only one sub-benchmark and print its JSON (profiling)")
     ap.add_argument("--layers", type=int, default=28,
@@ -830,6 +1124,9 @@ def main():
         peaks = measured_peaks()
         legs = {"extend": lambda: run_extend(args, dev, msg, peaks),
                 "graph": lambda: run_graph_decode(args, dev, msg),
+                "ladder": lambda: run_graph_ladder(args, dev, msg),
+                "tiny": lambda: run_tiny_mixed(args, dev, msg),
+                "cpu": lambda: cpu_oracle_configs(),
                 "large": lambda: run_large_decode(args, dev, msg, peaks),
                 "mixed": lambda: run_long_mixed(args, dev, msg, peaks),
                 "prologue": lambda: run_prologue(args, dev, msg, peaks),

@@ -40,7 +40,9 @@
  *   no device memory, never synchronises the stream, and enqueues all work on
  *   `stream` (a cudaStream_t passed as void*; NULL = legacy default stream).
  * - bf16 tensors are raw bf16 bit patterns.  Attention shapes are the Qwen3
- *   ones: head_dim 128, 16 query heads over 8 KV heads (GQA group of 2); other
+ *   ones: head_dim 128, 16 query heads over 8 KV heads (GQA group of 2), or a
+ *   tensor-parallel rank's slice of them split by KV head ([WALK] 4.5: 8, 4,
+ *   2 or 1 KV heads with 2 query heads each, e.g. 8 q / 4 kv at tp = 2); other
  *   shapes return MSG_ERR_UNSUPPORTED.  store_kv accepts any row of
  *   num_kv_heads * head_dim bf16 values that is a multiple of 16 bytes.
  * - Pool layout ([WALK] 4.4.3): one K pool and one V pool per layer, each a
@@ -186,6 +188,18 @@ int msg_version(void);
  */
 size_t msg_workspace_size(int32_t max_reqs, int64_t max_total_q,
                           int32_t num_qo_heads, int32_t head_dim);
+
+/*
+ * The workspace size under the boundary's planned name: msg_workspace_size for
+ * batches of at most max_reqs requests and max_total_q new tokens.  The
+ * split-KV split count is the library's own choice (at most two partial
+ * results per decode CTA, whose number it caps to what this size holds), so
+ * every max_splits >= 1 gives the same size; max_splits < 1 or any invalid
+ * argument returns 0.
+ */
+size_t msg_paged_attention_workspace_size(int32_t max_reqs, int64_t max_total_q,
+                                          int32_t num_qo_heads, int32_t head_dim,
+                                          int32_t max_splits);
 
 /*
  * a1. Per-batch metadata prep ([CORE] Batch table; [ENGINE] 手工驱动引擎;
@@ -428,6 +442,15 @@ int msg_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, int64_t num_
  */
 int msg_read_device_status(const void *dev_status, int32_t *host_out, void *stream);
 
+/*
+ * The device error of a workspace (or standalone status block) under the
+ * boundary's planned name: synchronises `stream` like msg_read_device_status
+ * and returns the recorded MSG_DEV_* code (MSG_DEV_OK = 0 when none), or a
+ * negative host status (MSG_ERR_INVALID_ARG for NULL, MSG_ERR_CUDA if the
+ * copy failed).
+ */
+int msg_get_device_error(const void *workspace, void *stream);
+
 /* Zero a device status block (asynchronously, on `stream`). */
 int msg_clear_device_status(void *dev_status, void *stream);
 
@@ -454,13 +477,21 @@ int msg_clear_device_status(void *dev_status, void *stream);
  *   capture.
  * - Every call shares the one array and it keeps the last call's contents: the
  *   status block is cleared at the start of each call, and MSG_ATTN_REUSE_PLAN
- *   reuses the plan left by the previous call of this entry point.  Calls that
- *   overlap on the GPU (different streams, or unordered threads) race on the
- *   array and must not be issued.
- * - dev_status: optional MSG_STATUS_BYTES device block that receives this
- *   call's device status (copied at the end of the call), or NULL.
+ *   reuses the plan left by the last successful call of this entry point on
+ *   this device that built one (called without MSG_ATTN_REUSE_PLAN).  The
+ *   library remembers that call's (num_reqs, total_q) on the host and rejects
+ *   MSG_ATTN_REUSE_PLAN with MSG_ERR_INVALID_ARG when no plan was built yet
+ *   or the batch size differs (the plan's place in the array depends on it);
+ *   that the lengths and index are the same is, as for msg_paged_attention,
+ *   the caller's promise.  Calls that overlap on the GPU (different streams,
+ *   or unordered threads) race on the array and must not be issued.
+ * - dev_status: optional MSG_STATUS_BYTES device block, or NULL.  When the
+ *   call returns MSG_OK it receives this call's device status (copied at the
+ *   end of the call; zeroed for an empty batch).  When the call returns an
+ *   error it is not written.
  * - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- * Errors: as msg_paged_attention.
+ * Errors: as msg_paged_attention; MSG_ERR_INVALID_ARG also for
+ *         MSG_ATTN_REUSE_PLAN without a plan of this batch size.
  */
 #define MSG_NOALLOC_SCRATCH_BYTES (9u << 20)
 

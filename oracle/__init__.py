@@ -89,6 +89,8 @@ def _load():
             lib.oracle_paged_attention_rows.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
@@ -103,6 +105,12 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of later oracle calls (for timing on one core); the results do
+    not depend on it."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def metadata(page_table, cached_len, extend_len, req_rows=None):
@@ -312,22 +320,34 @@ SAMPLE_MIN_T = 1e-6          # smallest temperature (a greedy request in a mixed
 SAMPLE_MIN_P = 1e-6          # smallest top-p
 
 
-def sampling_args(temperature, top_k, top_p, vocab_size):
-    """Per-batch sampling arguments (Sampler.prepare, "Engine 与采样器" 采样器).
+def is_greedy(temperature, top_k, top_p):
+    """SamplingParams.is_greedy ("核心数据结构：Req、Batch、Context", section
+    SamplingParams; "Mini-SGLang 完整剖析" 4.8.4): a request is greedy when its
+    temperature is at most 0 or its top_k is 1, and its top_p is exactly 1 --
+    a request with top_p below 1 is not greedy even at temperature 0."""
+    return (float(temperature) <= 0.0 or int(top_k) == 1) and float(top_p) == 1.0
 
-    Per request: temperature <= 0 means greedy.  Returns (temperatures,
-    top_k, top_p) as float32 / int32 / float32 arrays or None: temperatures is
-    None when every request is greedy (the sampler then takes the argmax);
-    a greedy request in a mixed batch gets temperature MIN_T; top_k < 1 means
-    the whole vocabulary and the array is None unless some request restricts
-    it; top_p is clamped to [MIN_P, 1] and is None unless some request has
-    top_p < 1."""
-    t = [float(x) for x in temperature]
-    if all(x <= 0.0 for x in t):
+
+def sampling_args(temperature, top_k, top_p, vocab_size):
+    """Per-batch sampling arguments (Sampler.prepare, "Engine 与采样器" 采样器;
+    "Mini-SGLang 完整剖析" 4.8.5), from per-request (temperature, top_k, top_p).
+
+    Returns (temperatures, top_k, top_p) as float32 / int32 / float32 arrays or
+    None: temperatures is None when every request is_greedy (the sampler then
+    takes the argmax); otherwise a greedy request gets temperature MIN_T and
+    any other max(temperature, MIN_T) (so a temperature <= 0 request with
+    top_p < 1 is sampled at MIN_T); top_k < 1 means the whole vocabulary and
+    the array is None unless some request restricts it; top_p is clamped to
+    [MIN_P, 1] and is None unless some request has top_p < 1."""
+    reqs = list(zip([float(x) for x in temperature], [int(k) for k in top_k],
+                    [float(p) for p in top_p]))
+    greedy = [is_greedy(t, k, p) for t, k, p in reqs]
+    if all(greedy):
         return None, None, None
-    ts = np.array([max(0.0 if x <= 0.0 else x, SAMPLE_MIN_T) for x in t], np.float32)
-    ks = [int(k) if int(k) >= 1 else int(vocab_size) for k in top_k]
-    ps = [min(max(float(p), SAMPLE_MIN_P), 1.0) for p in top_p]
+    ts = np.array([max(0.0 if g else t, SAMPLE_MIN_T) for (t, _, _), g in zip(reqs, greedy)],
+                  np.float32)
+    ks = [k if k >= 1 else int(vocab_size) for _, k, _ in reqs]
+    ps = [min(max(p, SAMPLE_MIN_P), 1.0) for _, _, p in reqs]
     k_arr = np.array(ks, np.int32) if any(k != vocab_size for k in ks) else None
     p_arr = np.array(ps, np.float32) if any(p < 1.0 for p in ps) else None
     return ts, k_arr, p_arr

@@ -179,3 +179,15 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Set the number of OpenMP threads of later calls (timing on one core or on
+ * all of them); no effect without OpenMP.  Changes no arithmetic: every
+ * output element is computed by one thread in the same order. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

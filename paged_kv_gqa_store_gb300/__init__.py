@@ -132,6 +132,10 @@ def load_library(path: str | None = None):
         lib.msg_version.restype = ctypes.c_int
         lib.msg_workspace_size.argtypes = [I32, I64, I32, I32]
         lib.msg_workspace_size.restype = SZ
+        lib.msg_paged_attention_workspace_size.argtypes = [I32, I64, I32, I32, I32]
+        lib.msg_paged_attention_workspace_size.restype = SZ
+        lib.msg_get_device_error.argtypes = [P, P]
+        lib.msg_get_device_error.restype = ctypes.c_int
         lib.msg_plan.argtypes = [P, I64, P, P, P, I32, I64, I64, P, P, I32, P, P, SZ, P]
         lib.msg_plan.restype = ctypes.c_int
         lib.msg_store_kv.argtypes = [P, P, I64, P, P, I64, I64, P, I32, I64, I32, I32, P, P]
@@ -230,6 +234,16 @@ def msg_workspace_size(max_reqs: int, max_total_q: int, num_qo_heads: int = 16,
                                               int(num_qo_heads), int(head_dim)))
     if n == 0:
         raise ValueError("msg_workspace_size: invalid arguments")
+    return n
+
+
+def msg_paged_attention_workspace_size(max_reqs: int, max_total_q: int, num_qo_heads: int = 16,
+                                       head_dim: int = 128, max_splits: int = 1) -> int:
+    """msg_workspace_size under the boundary's planned name (max_splits >= 1)."""
+    n = int(load_library().msg_paged_attention_workspace_size(
+        int(max_reqs), int(max_total_q), int(num_qo_heads), int(head_dim), int(max_splits)))
+    if n == 0:
+        raise ValueError("msg_paged_attention_workspace_size: invalid arguments")
     return n
 
 
@@ -466,27 +480,32 @@ def sampling_args(temperature, top_k, top_p, vocab_size: int, device="cuda"):
     """Host side of the sampler's per-batch arguments (Sampler.prepare of
     "Engine 与采样器"): per-request lists in, device tensors out.
 
-    temperature <= 0 is greedy.  Returns (temperatures, top_k, top_p), each a
-    device tensor or None: no temperatures when every request is greedy (the
-    kernel then takes the argmax), MIN_T for a greedy request of a mixed batch;
-    top_k (< 1: whole vocabulary) only when some request restricts it; top_p
-    (clamped to [MIN_P, 1]) only when some request is below 1.  The copies are
-    asynchronous from pinned host memory."""
+    A request is greedy when (temperature <= 0 or top_k == 1) and top_p == 1
+    (SamplingParams.is_greedy, "核心数据结构：Req、Batch、Context").  Returns
+    (temperatures, top_k, top_p), each a device tensor or None: no
+    temperatures when every request is greedy (the kernel then takes the
+    argmax); otherwise MIN_T for a greedy request and max(temperature, MIN_T)
+    for the rest; top_k (< 1: whole vocabulary) only when some request
+    restricts it; top_p (clamped to [MIN_P, 1]) only when some request is
+    below 1.  The copies are asynchronous from pinned host memory."""
     import torch
     t = [float(x) for x in temperature]
-    if all(x <= 0.0 for x in t):
+    k = [int(x) for x in top_k]
+    p = [float(x) for x in top_p]
+    greedy = [(ti <= 0.0 or ki == 1) and pi == 1.0 for ti, ki, pi in zip(t, k, p)]
+    if all(greedy):
         return None, None, None
 
     def dev(vals, dtype):
-        t = torch.tensor(vals, dtype=dtype)
+        x = torch.tensor(vals, dtype=dtype)
         if torch.device(device).type != "cuda":
-            return t.to(device)
-        return t.pin_memory().to(device, non_blocking=True)
+            return x.to(device)
+        return x.pin_memory().to(device, non_blocking=True)
 
-    ts = [max(0.0 if x <= 0.0 else x, SAMPLE_MIN_T) for x in t]
-    ks = [int(k) if int(k) >= 1 else int(vocab_size) for k in top_k]
-    ps = [min(max(float(x), SAMPLE_MIN_P), 1.0) for x in top_p]
-    k_t = dev(ks, torch.int32) if any(k != vocab_size for k in ks) else None
+    ts = [max(0.0 if g else ti, SAMPLE_MIN_T) for ti, g in zip(t, greedy)]
+    ks = [ki if ki >= 1 else int(vocab_size) for ki in k]
+    ps = [min(max(pi, SAMPLE_MIN_P), 1.0) for pi in p]
+    k_t = dev(ks, torch.int32) if any(x != vocab_size for x in ks) else None
     p_t = dev(ps, torch.float32) if any(x < 1.0 for x in ps) else None
     return dev(ts, torch.float32), k_t, p_t
 
@@ -542,6 +561,14 @@ def msg_read_device_status(dev_status, stream=None) -> tuple[int, list[int]]:
     if st not in (MSG_OK, MSG_ERR_DEVICE_CHECK):
         _check("msg_read_device_status", st)
     return st, list(buf)
+
+
+def msg_get_device_error(workspace, stream=None) -> int:
+    """Synchronise and return the MSG_DEV_* code recorded in a status block (0: none)."""
+    st = int(load_library().msg_get_device_error(_ptr(workspace), _stream(stream)))
+    if st < 0:
+        _check("msg_get_device_error", st)
+    return st
 
 
 def msg_clear_device_status(dev_status, stream=None) -> None:

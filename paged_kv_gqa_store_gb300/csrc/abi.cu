@@ -33,7 +33,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_heads(int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim) {
   if (num_qo_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return MSG_ERR_INVALID_ARG;
   if (head_dim != kHeadDim) return MSG_ERR_UNSUPPORTED;
-  if (num_kv_heads != kKvHeads || num_qo_heads != kGroup * kKvHeads) return MSG_ERR_UNSUPPORTED;
+  // the full layer (8 KV heads) or a tensor-parallel slice of it, GQA group 2
+  if (num_kv_heads != 8 && num_kv_heads != 4 && num_kv_heads != 2 && num_kv_heads != 1)
+    return MSG_ERR_UNSUPPORTED;
+  if (num_qo_heads != kGroup * num_kv_heads) return MSG_ERR_UNSUPPORTED;
   return MSG_OK;
 }
 
@@ -148,8 +151,9 @@ const char *msg_status_string(int status) {
   switch (status) {
     case MSG_OK: return "ok";
     case MSG_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad stride)";
-    case MSG_ERR_UNSUPPORTED: return "unsupported shape (needs head_dim 128, 16 query heads over 8 KV "
-                                     "heads, page_size a power of two <= 128)";
+    case MSG_ERR_UNSUPPORTED: return "unsupported shape (needs head_dim 128, 2 query heads per KV "
+                                     "head with 8, 4, 2 or 1 KV heads, page_size a power of two "
+                                     "<= 128)";
     case MSG_ERR_ALIGNMENT: return "pointer or row stride not 16-byte aligned";
     case MSG_ERR_WORKSPACE: return "workspace missing or smaller than msg_workspace_size()";
     case MSG_ERR_CUDA: return "CUDA runtime error (launch or copy failed)";
@@ -164,6 +168,14 @@ size_t msg_workspace_size(int32_t max_reqs, int64_t max_total_q, int32_t num_qo_
                           int32_t head_dim) {
   if (max_reqs < 0 || max_total_q < 0 || num_qo_heads <= 0 || head_dim <= 0) return 0;
   return ws_layout(max_reqs, max_total_q, num_qo_heads, head_dim).total;
+}
+
+size_t msg_paged_attention_workspace_size(int32_t max_reqs, int64_t max_total_q,
+                                          int32_t num_qo_heads, int32_t head_dim,
+                                          int32_t max_splits) {
+  // the split count is the library's choice and every one it makes fits
+  if (max_splits < 1) return 0;
+  return msg_workspace_size(max_reqs, max_total_q, num_qo_heads, head_dim);
 }
 
 int msg_plan(const int32_t *page_table, int64_t page_table_stride, const int32_t *req_rows,
@@ -337,8 +349,6 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
     pp.dec_start = reinterpret_cast<int64_t *>(ws + L.dec_start);
     pp.dec_row = reinterpret_cast<int64_t *>(ws + L.dec_row);
     pp.dec_qrow = reinterpret_cast<int32_t *>(ws + L.dec_qrow);
-  pp.dec_row = reinterpret_cast<int64_t *>(ws + L.dec_row);
-  pp.dec_qrow = reinterpret_cast<int32_t *>(ws + L.dec_qrow);
     pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
     pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
     pp.max_tiles = L.max_tiles;
@@ -383,8 +393,8 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
   ap.part_o = reinterpret_cast<float *>(ws + L.part_o);
 
   if (!(flags & MSG_ATTN_EXTEND_ONLY)) {
-    int64_t grid = (int64_t)device_sm_count() * decode_ctas_per_sm();
-    if (grid > kMaxDecodeCtas) grid = kMaxDecodeCtas;
+    int64_t grid = (int64_t)device_sm_count() * decode_ctas_per_sm(num_kv_heads);
+    if (grid > max_decode_ctas(num_qo_heads)) grid = max_decode_ctas(num_qo_heads);
     if (max_kv_len > 0) {
       const int64_t want = ((int64_t)num_reqs * max_kv_len + 63) / 64;
       if (want < grid) grid = want > 0 ? want : 1;
@@ -417,6 +427,13 @@ int msg_read_device_status(const void *dev_status, int32_t *host_out, void *stre
     return MSG_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MSG_ERR_CUDA;
   return host_out[0] == MSG_DEV_OK ? MSG_OK : MSG_ERR_DEVICE_CHECK;
+}
+
+int msg_get_device_error(const void *workspace, void *stream) {
+  int32_t host[4] = {0, 0, 0, 0};
+  const int rc = msg_read_device_status(workspace, host, stream);
+  if (rc != MSG_OK && rc != MSG_ERR_DEVICE_CHECK) return rc;
+  return host[0];
 }
 
 int msg_clear_device_status(void *dev_status, void *stream) {

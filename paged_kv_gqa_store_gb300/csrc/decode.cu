@@ -45,22 +45,34 @@ namespace msg {
 
 namespace {
 
-constexpr int kHkv = 8;
-constexpr int kHq = 16;
-constexpr int kWarps = 8;                           // consumer warps, one per KV head
-constexpr int kThreads = (kWarps + 1) * 32;         // + producer warp
 constexpr int kTileKeys = 8;
-constexpr int kRowBytes = kHkv * kHeadDim * 2;      // 2 KiB: one token's K row
-constexpr int kKBytes = kTileKeys * kRowBytes;      // 16 KiB
-constexpr int kQBytes = kHq * kHeadDim * 2;         // 4 KiB: one q row
 constexpr int kStages = 3;
-constexpr int kOffV = kKBytes;
-constexpr int kOffQ = 2 * kKBytes;
-constexpr int kOffHdr = 2 * kKBytes + kQBytes;
-constexpr int kStageBytes = kOffHdr + 64;
-constexpr int kPbufBytes = kWarps * kTileKeys * 4 * 4;   // per key: {p0,p0,p1,p1}
-constexpr size_t kSmem = (size_t)kStages * kStageBytes + kPbufBytes + 2 * kStages * 8 + 16;
 constexpr int64_t kMinKeysPerCta = 64;
+
+// Launch shape for HKV KV heads (query heads 2 HKV): one consumer warp per KV
+// head plus the producer warp; a stage holds kTileKeys whole token rows of K
+// and of V (all HKV heads), one q row and a tile header.
+template <int HKV>
+struct Dec {
+  static constexpr int kHkv = HKV;
+  static constexpr int kHq = kGroup * HKV;
+  static constexpr int kWarps = HKV;                              // consumer warps
+  static constexpr int kThreads = (kWarps + 1) * 32;              // + producer warp
+  static constexpr int kRowBytes = HKV * kHeadDim * 2;            // one token's K row
+  static constexpr int kKBytes = kTileKeys * kRowBytes;
+  static constexpr int kQBytes = kHq * kHeadDim * 2;              // one q row
+  static constexpr int kOffV = kKBytes;
+  static constexpr int kOffQ = 2 * kKBytes;
+  static constexpr int kOffHdr = 2 * kKBytes + kQBytes;
+  static constexpr int kStageBytes = kOffHdr + 64;
+  static constexpr int kPbufBytes = kWarps * kTileKeys * 4 * 4;   // per key: {p0,p0,p1,p1}
+  static constexpr size_t kSmem =
+      (size_t)kStages * kStageBytes + kPbufBytes + 2 * kStages * 8 + 16;
+  // 16 / HKV CTAs per SM would keep the bytes in flight per SM equal for every
+  // head count; the register file (96 per thread, no spills) caps it below 8
+  // KV heads: 2, 4, 6, 10 CTAs for 8, 4, 2, 1 heads.
+  static constexpr int kCtasPerSm = HKV == 8 ? 2 : HKV == 4 ? 4 : HKV == 2 ? 6 : 10;
+};
 
 enum : int32_t { kFirst = 1, kLast = 2, kFinal = 4, kNoRow = 8 };
 
@@ -156,8 +168,13 @@ __device__ __forceinline__ int64_t raw_to_slot(const AttnParams &p, int32_t raw,
 // kFused: the step's new K / V rows are given (p.k_new): each request's newest
 // key is read from them and stored to the pool here (compiled apart, so the
 // plain kernel carries none of it).
-template <bool kPage1, bool kFused>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
+template <int HKV, bool kPage1, bool kFused>
+__global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
+    decode_kernel(AttnParams p) {
+  using S = Dec<HKV>;
+  constexpr int kHkv = S::kHkv, kHq = S::kHq, kWarps = S::kWarps, kRowBytes = S::kRowBytes;
+  constexpr int kQBytes = S::kQBytes, kOffV = S::kOffV, kOffQ = S::kOffQ, kOffHdr = S::kOffHdr;
+  constexpr int kStageBytes = S::kStageBytes, kPbufBytes = S::kPbufBytes;
   extern __shared__ __align__(128) uint8_t smem[];
   float *pbuf = reinterpret_cast<float *>(smem + (size_t)kStages * kStageBytes);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStageBytes + kPbufBytes);
@@ -166,11 +183,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PlanHeader hdr = *p.hdr;
-  if (blockIdx.x == 0 && tid == 0 && (p.flags & MSG_ATTN_DECODE_ONLY) && hdr.ext_tile_count > 0)
-    report(p.status, MSG_DEV_WRONG_PHASE, hdr.ext_count, hdr.ext_tile_count);
+  // A decode-only call whose plan lists extend tiles is reported by thread 0,
+  // after grid_dep_wait(): the status block may still be written by the
+  // kernel before this one.
+  const bool wrong_phase = blockIdx.x == 0 && tid == 0 && (p.flags & MSG_ATTN_DECODE_ONLY) &&
+                           hdr.ext_tile_count > 0;
   const int64_t K = hdr.dec_keys;
   const int32_t nd = hdr.dec_count;
-  if (K <= 0 || nd <= 0) return;
+  if (K <= 0 || nd <= 0) {
+    if (wrong_phase) {
+      grid_dep_wait();
+      report(p.status, MSG_DEV_WRONG_PHASE, hdr.ext_count, hdr.ext_tile_count);
+    }
+    return;
+  }
   int64_t g = gridDim.x;
   const int64_t gmax = K / kMinKeysPerCta > 0 ? K / kMinKeysPerCta : 1;
   if (g > gmax) g = gmax;
@@ -289,16 +315,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
           if (slot_ok) {
             uint4 *kd = reinterpret_cast<uint4 *>(p.k_pool_w + nslot * p.pool_stride_bytes);
             uint4 *vd = reinterpret_cast<uint4 *>(p.v_pool_w + nslot * p.pool_stride_bytes);
-            uint4 a[kRowBytes / 16 / 32], c[kRowBytes / 16 / 32];
+            constexpr int kChunks = kRowBytes / 16, kPer = (kChunks + 31) / 32;
+            uint4 a[kPer], c[kPer];
 #pragma unroll
-            for (int u = 0; u < kRowBytes / 16 / 32; ++u) {
-              a[u] = ks[u * 32 + lane];
-              c[u] = vs[u * 32 + lane];
+            for (int u = 0; u < kPer; ++u) {
+              if (u * 32 + lane < kChunks) {
+                a[u] = ks[u * 32 + lane];
+                c[u] = vs[u * 32 + lane];
+              }
             }
 #pragma unroll
-            for (int u = 0; u < kRowBytes / 16 / 32; ++u) {
-              kd[u * 32 + lane] = a[u];
-              vd[u * 32 + lane] = c[u];
+            for (int u = 0; u < kPer; ++u) {
+              if (u * 32 + lane < kChunks) {
+                kd[u * 32 + lane] = a[u];
+                vd[u * 32 + lane] = c[u];
+              }
             }
           }
         }
@@ -325,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
 
   // -------------------------------------------------------------- consumers
   grid_dep_wait();      // out, the split partials and the merge counters
+  if (wrong_phase) report(p.status, MSG_DEV_WRONG_PHASE, hdr.ext_count, hdr.ext_tile_count);
   const int gh = warp;                          // KV head
   const int kx = (lane >> 2) & 7, hx = (lane >> 1) & 1;
   const int kl = kx, hl = hx;                   // after the butterfly: this lane's key / head
@@ -528,29 +560,71 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(AttnParams p) {
   }
 }
 
-}  // namespace
-
-cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s) {
-  if (p.num_kv_heads != kHkv || p.num_qo_heads != kHq) return cudaErrorInvalidValue;
+template <int HKV>
+cudaError_t launch_decode_h(const AttnParams &p, int grid, bool pdl, cudaStream_t s) {
+  using S = Dec<HKV>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    for (auto k : {decode_kernel<true, false>, decode_kernel<false, false>,
-                   decode_kernel<true, true>, decode_kernel<false, true>}) {
-      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    for (auto k : {decode_kernel<HKV, true, false>, decode_kernel<HKV, false, false>,
+                   decode_kernel<HKV, true, true>, decode_kernel<HKV, false, true>}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kSmem);
       if (e != cudaSuccess) return e;
     }
     attr_set[dev] = true;
   }
   const bool fused = p.k_new != nullptr;
-  auto k = p.page_size == 1 ? (fused ? decode_kernel<true, true> : decode_kernel<true, false>)
-                            : (fused ? decode_kernel<false, true> : decode_kernel<false, false>);
-  return launch_k(k, dim3(grid), dim3(kThreads), kSmem, s, pdl, p);
+  auto k = p.page_size == 1
+               ? (fused ? decode_kernel<HKV, true, true> : decode_kernel<HKV, true, false>)
+               : (fused ? decode_kernel<HKV, false, true> : decode_kernel<HKV, false, false>);
+  return launch_k(k, dim3(grid), dim3(S::kThreads), S::kSmem, s, pdl, p);
 }
 
-int decode_ctas_per_sm() { return 2; }
+template <int HKV>
+int ctas_per_sm_h() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    // the shared memory of the launch decides how many CTAs share an SM
+    if (cudaFuncSetAttribute(decode_kernel<HKV, true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Dec<HKV>::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<HKV, true, false>,
+                                                      Dec<HKV>::kThreads,
+                                                      Dec<HKV>::kSmem) != cudaSuccess ||
+        n <= 0)
+      n = 1;
+    cache[dev] = n < Dec<HKV>::kCtasPerSm ? n : Dec<HKV>::kCtasPerSm;
+  }
+  return cache[dev];
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s) {
+  if (p.num_qo_heads != kGroup * p.num_kv_heads) return cudaErrorInvalidValue;
+  switch (p.num_kv_heads) {
+    case 8: return launch_decode_h<8>(p, grid, pdl, s);
+    case 4: return launch_decode_h<4>(p, grid, pdl, s);
+    case 2: return launch_decode_h<2>(p, grid, pdl, s);
+    case 1: return launch_decode_h<1>(p, grid, pdl, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int decode_ctas_per_sm(int num_kv_heads) {
+  switch (num_kv_heads) {
+    case 8: return ctas_per_sm_h<8>();
+    case 4: return ctas_per_sm_h<4>();
+    case 2: return ctas_per_sm_h<2>();
+    case 1: return ctas_per_sm_h<1>();
+    default: return 1;
+  }
+}
 
 }  // namespace msg

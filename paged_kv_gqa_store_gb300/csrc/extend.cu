@@ -241,8 +241,8 @@ struct Item {
 
 __device__ __forceinline__ Item load_item(const AttnParams &p, int w) {
   Item it;
-  const int tile = w / kKvHeads;
-  it.gh = w % kKvHeads;
+  const int tile = w / p.num_kv_heads;
+  it.gh = w % p.num_kv_heads;
   it.r = p.ext_tiles[2 * tile];
   const int32_t qt = p.ext_tiles[2 * tile + 1];
   it.cached = p.cached_len[it.r];
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = (int)(k % kItemQueue);
     if (grab) {
       int w = atomicAdd(next_ctr, 1);
-      if (w >= hdr.ext_tile_count * kKvHeads) w = -1;
+      if (w >= hdr.ext_tile_count * p.num_kv_heads) w = -1;
       item_q[e] = w;
       mbar_arrive(&bars[kBarItem + e]);
     }
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (blockIdx.x == 0 && tid == 0 && (p.flags & MSG_ATTN_EXTEND_ONLY) && hdr.dec_count > 0)
     report(p.status, MSG_DEV_WRONG_PHASE, hdr.dec_count, hdr.dec_keys);
-  const int items = hdr.ext_tile_count * kKvHeads;
+  const int items = hdr.ext_tile_count * p.num_kv_heads;
   if ((int)blockIdx.x >= items) return;
 
   if (tid == 0) {
@@ -761,7 +761,7 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s
     return cudaErrorInvalidValue;
   // persistent: one CTA per SM (the kernel's shared memory allows no more)
   int64_t grid = (int64_t)device_sm_count();
-  if (grid > max_tiles * kKvHeads) grid = max_tiles * kKvHeads;
+  if (grid > max_tiles * p.num_kv_heads) grid = max_tiles * p.num_kv_heads;
   extend_kernel<<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
   return cudaGetLastError();
 }

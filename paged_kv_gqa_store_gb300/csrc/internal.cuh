@@ -14,8 +14,17 @@ namespace msg {
 
 constexpr int kHeadDim = 128;
 constexpr int kGroup = 2;                 // query heads per KV head
-constexpr int kKvHeads = 8;               // KV heads (16 query heads)
-constexpr int kMaxDecodeCtas = 512;       // partial-result slots are 2 per CTA
+constexpr int kMaxKvHeads = 8;            // KV heads of a full layer (16 query heads); a
+                                          // tensor-parallel slice passes 4, 2 or 1
+constexpr int kMaxDecodeCtas = 512;       // decode CTAs at 8 KV heads (2 partial slots each)
+
+// Decode CTAs the split-KV partials have room for with hq query heads: the
+// partial arrays are sized for 16 heads x kMaxDecodeCtas, so fewer heads per
+// CTA leave room for proportionally more CTAs.
+inline int64_t max_decode_ctas(int64_t hq) {
+  return hq > 0 && hq < kGroup * kMaxKvHeads ? kMaxDecodeCtas * (kGroup * kMaxKvHeads / hq)
+                                             : kMaxDecodeCtas;
+}
 constexpr int kExtendTileTokens = 128;    // query tokens per extend tile
 constexpr int kPlanThreads = 1024;
 
@@ -38,8 +47,8 @@ struct WsLayout {
   size_t dec_qrow = 0;     // int32[num_reqs]       its query row (qo_indptr)
   size_t counters = 0;     // int32[num_reqs * 8]   split merge counters (request, KV head)
   size_t ext_tiles = 0;    // int32x2[max_tiles]    (request, query tile)
-  size_t part_lse = 0;     // float[2 * kMaxDecodeCtas * Hq]
-  size_t part_o = 0;       // float[2 * kMaxDecodeCtas * Hq * D]
+  size_t part_lse = 0;     // float[2 * max_decode_ctas(Hq) * Hq]
+  size_t part_o = 0;       // float[2 * max_decode_ctas(Hq) * Hq * D]
   size_t plan_end = 0;     // bytes used by the plan part
   size_t total = 0;
   int64_t max_tiles = 0;
@@ -67,12 +76,12 @@ inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t
   L.dec_start = take(sizeof(int64_t) * (num_reqs + 1));
   L.dec_row = take(sizeof(int64_t) * (num_reqs + 1));
   L.dec_qrow = take(sizeof(int32_t) * (num_reqs + 1));
-  L.counters = take(sizeof(int32_t) * (num_reqs + 1) * kKvHeads);
+  L.counters = take(sizeof(int32_t) * (num_reqs + 1) * kMaxKvHeads);
   L.max_tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + num_reqs + 1;
   L.ext_tiles = take(sizeof(int32_t) * 2 * L.max_tiles);
   L.plan_end = off;
-  L.part_lse = take(sizeof(float) * 2 * kMaxDecodeCtas * hq);
-  L.part_o = take(sizeof(float) * 2 * (size_t)kMaxDecodeCtas * hq * d);
+  L.part_lse = take(sizeof(float) * 2 * max_decode_ctas(hq) * hq);
+  L.part_o = take(sizeof(float) * 2 * (size_t)max_decode_ctas(hq) * hq * d);
   L.total = off;
   return L;
 }
@@ -201,7 +210,7 @@ cudaError_t launch_store_kv(const StoreParams &p, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s);
 int device_sm_count();
-int decode_ctas_per_sm();
+int decode_ctas_per_sm(int num_kv_heads);
 
 }  // namespace msg
 

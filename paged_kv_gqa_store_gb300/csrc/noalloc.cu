@@ -22,6 +22,16 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[MSG_NOALLOC_SCRATCH_BYTES];
 
+// Batch size (num_reqs, total_q) of the plan the last successful call without
+// MSG_ATTN_REUSE_PLAN left in the array, per device; {-1, -1}: none yet.  The
+// plan's offsets in the array depend on that size, so a call that reuses the
+// plan must have the same one.
+struct PlanSize {
+  int32_t num_reqs = -1;
+  int64_t total_q = -1;
+};
+PlanSize g_plan_size[64];
+
 void *scratch_address(int *rc) {
   static void *addr[64] = {};
   int dev = 0;
@@ -53,22 +63,39 @@ extern "C" int msg_paged_attention_noalloc(
     void *stream) {
   if (num_reqs < 0 || total_q < 0 || num_qo_heads <= 0 || head_dim <= 0)
     return MSG_ERR_INVALID_ARG;
-  if (num_reqs == 0 || total_q == 0) return MSG_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (num_reqs == 0 || total_q == 0) {
+    // nothing to do; the caller's status block reports this call: clean
+    if (dev_status != nullptr &&
+        cudaMemsetAsync(dev_status, 0, MSG_STATUS_BYTES, s) != cudaSuccess)
+      return MSG_ERR_CUDA;
+    return MSG_OK;
+  }
   const size_t need = msg_workspace_size(num_reqs, total_q, num_qo_heads, head_dim);
   if (need == 0) return MSG_ERR_INVALID_ARG;
   if (need > (size_t)MSG_NOALLOC_SCRATCH_BYTES) return MSG_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSG_ERR_CUDA;
+  PlanSize &plan = g_plan_size[dev];
+  const bool reuse = (flags & MSG_ATTN_REUSE_PLAN) != 0;
+  if (reuse && (plan.num_reqs != num_reqs || plan.total_q != total_q))
+    return MSG_ERR_INVALID_ARG;        // no plan of this batch size in the array
   int rc = MSG_OK;
   uint8_t *ws = static_cast<uint8_t *>(scratch_address(&rc));
   if (rc != MSG_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The status block must start at zero so that it reports this call only.
   if (cudaMemsetAsync(ws, 0, MSG_STATUS_BYTES, s) != cudaSuccess) return MSG_ERR_CUDA;
+  if (!reuse) plan = PlanSize{};       // the plan is rewritten below
   rc = msg_paged_attention(q, q_row_stride, k_pool, v_pool, pool_row_stride, num_slots,
                            page_table, page_table_stride, req_rows, cached_len, extend_len,
                            qo_indptr, num_reqs, total_q, max_kv_len, page_size, num_qo_heads,
                            num_kv_heads, head_dim, scale, out, ws, MSG_NOALLOC_SCRATCH_BYTES,
                            flags, stream);
   if (rc != MSG_OK) return rc;
+  if (!reuse) {
+    plan.num_reqs = num_reqs;
+    plan.total_q = total_q;
+  }
   if (dev_status != nullptr &&
       cudaMemcpyAsync(dev_status, ws, MSG_STATUS_BYTES, cudaMemcpyDeviceToDevice, s) !=
           cudaSuccess)

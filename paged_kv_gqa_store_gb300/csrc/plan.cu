@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       p.qo_ws[r] = (int32_t)qo;
       if (p.qo_out) p.qo_out[r] = (int32_t)qo;
       if (p.qo_in && p.qo_in[r] != qo) report(p.status, MSG_DEV_BAD_LENGTHS, r, p.qo_in[r]);
-      for (int h = 0; h < kKvHeads; ++h) p.counters[(int64_t)r * kKvHeads + h] = 0;
+      for (int h = 0; h < kMaxKvHeads; ++h) p.counters[(int64_t)r * kMaxKvHeads + h] = 0;
       if (is_dec) {
         const int64_t i = carry[1] + ex.v[1];
         p.dec_req[i] = r;

@@ -40,6 +40,18 @@ def test_status_strings_and_version(lib):
     assert msg.msg_version() >= 100
 
 
+def test_survey_boundary_names(lib):
+    # the boundary's planned names: the workspace size with a split bound, and
+    # the device-error read; same sizes and codes as msg_workspace_size and the
+    # status block
+    for reqs, q in ((1, 1), (64, 64), (256, 18432)):
+        for hq in (16, 8, 2):
+            assert lib.msg_paged_attention_workspace_size(reqs, q, hq, 128, 64) == \
+                lib.msg_workspace_size(reqs, q, hq, 128)
+    assert lib.msg_paged_attention_workspace_size(4, 4, 16, 128, 0) == 0
+    assert lib.msg_get_device_error(None, None) == msg.MSG_ERR_INVALID_ARG
+
+
 def test_workspace_size_monotone(lib):
     a = msg.msg_workspace_size(64, 64)
     b = msg.msg_workspace_size(256, 18432)
@@ -65,7 +77,9 @@ def _attn(lib, **kw):
     (dict(head_dim=64), msg.MSG_ERR_UNSUPPORTED),
     (dict(num_qo_heads=24), msg.MSG_ERR_UNSUPPORTED),
     (dict(num_qo_heads=6, num_kv_heads=3), msg.MSG_ERR_UNSUPPORTED),
-    (dict(num_qo_heads=8, num_kv_heads=4), msg.MSG_ERR_UNSUPPORTED),
+    (dict(num_qo_heads=16, num_kv_heads=4), msg.MSG_ERR_UNSUPPORTED),    # GQA group 4
+    (dict(num_qo_heads=32, num_kv_heads=16), msg.MSG_ERR_UNSUPPORTED),   # more than 8 KV heads
+    (dict(num_qo_heads=12, num_kv_heads=6), msg.MSG_ERR_UNSUPPORTED),    # not a slice of 8
     (dict(num_qo_heads=16, num_kv_heads=16), msg.MSG_ERR_UNSUPPORTED),
     (dict(page_size=3), msg.MSG_ERR_UNSUPPORTED),
     (dict(page_size=256), msg.MSG_ERR_UNSUPPORTED),
@@ -261,7 +275,10 @@ def test_sampling_args_match_the_pages_prepare():
     cases = [([0.0, 0.0], [-1, 5], [1.0, 0.5]),
              ([0.7, 0.0, 1.2], [-1, 0, -3], [1.0, 1.0, 2.0]),
              ([1.0, 1.0], [50, -1], [0.0, 0.95]),
-             ([0.5], [10**6], [1e-9])]
+             ([0.5], [10**6], [1e-9]),
+             ([0.0, 0.0], [-1, -1], [1.0, 0.9]),
+             ([0.8, 1.5], [1, 1], [1.0, 1.0]),
+             ([0.8, 1.5, 0.0], [1, 3, 1], [1.0, 1.0, 0.7])]
     for t, k, p in cases:
         got = msg.sampling_args(t, k, p, 1000, device="cpu")
         want = oracle.sampling_args(t, k, p, 1000)

@@ -69,6 +69,42 @@ def test_decode_64_reqs_28_layers():
         assert torch.isfinite(o.float()).all()
 
 
+def test_decode_64_reqs_28_layers_fused_store_as_benchmarked():
+    """The benchmark's headline step exactly: one plan, then per layer one
+    msg_paged_attention_store (the decode kernel stores the step's new K/V rows
+    itself) with MSG_ATTN_REUSE_PLAN | MSG_ATTN_DECODE_ONLY and the host
+    max_kv_len hint, 28 layers on one workspace.  Every layer: 6 sampled
+    requests against the oracle, and the 64 stored rows bit-exactly."""
+    spec = wl.config_decode_28_layers()
+    gb = GpuBatch(spec)
+    layers = [wl.device_tensors(spec, layer) for layer in range(spec.num_layers)]
+    rng = np.random.default_rng(15)
+    refs = {}
+    for layer, t in enumerate(layers):
+        reqs = np.sort(rng.choice(spec.num_reqs, 6, replace=False))
+        refs[layer] = sampled_oracle(spec, (t["k_pool"], t["v_pool"]), t["q"], t["k_new"],
+                                     t["v_new"], reqs)
+    loc = gb.plan()
+    outs = []
+    flags = msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_DECODE_ONLY
+    for t in layers:
+        o = torch.full_like(t["q"], float("nan"))
+        msg.msg_paged_attention_store(t["q"], t["k_new"], t["v_new"], t["k_pool"], t["v_pool"],
+                                      gb.page_table, gb.cached, gb.extend, gb.qo, o, gb.ws,
+                                      page_size=spec.page_size, req_rows=gb.rows,
+                                      max_kv_len=spec.max_kv_len, flags=flags)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert gb.status()[0] == msg.MSG_OK
+    _check_qo_and_loc(spec, gb)
+    for layer, (rows, ref) in refs.items():
+        _check_store(layers[layer], loc)
+        got = wl.torch_to_bits(outs[layer][torch.from_numpy(rows).cuda()])
+        assert_attn_close(got, ref, f"layer {layer}")
+    for o in outs:
+        assert torch.isfinite(o.float()).all()
+
+
 def test_decode_256_reqs_page16_pool_90pct_of_free_hbm():
     torch.cuda.empty_cache()
     free, _ = torch.cuda.mem_get_info()

@@ -1,109 +1,154 @@
-"""CUDA-graph replay of the decode step (plan, store_kv, paged attention).
+"""CUDA-graph replay of the decode step, checked against the fp64 oracle.
 
 The whole path runs from device-side metadata with no host synchronisation and
 fixed launch shapes, so one captured graph serves every later step of a
-fixed-size (padded) decode batch: the caller updates cached_len, the page
-table, q and the new k/v in place and replays.  Padding requests point at the
-dummy slot, as in a CUDA-graph-padded engine batch ("Engine 与采样器",
-初始化的顺序: the extra dummy page and the dummy row).  Replays must match eager
-execution of the same step bit for bit."""
+fixed-size (padded) decode batch: the caller updates cached_len, the page-table
+rows, q and the new k/v in place and replays.  Padding requests point at the
+dummy slot, as in a CUDA-graph-padded engine batch ("Engine 与采样器", 初始化的
+顺序: the extra dummy page and the dummy row; "Mini-SGLang 源码解析（四）"
+10.6-10.7: the batch-size ladder and padding to the next captured size).
+
+Every replayed step's outputs and the pools are compared with the oracle run
+on the same inputs; replay and eager execution must also agree bit for bit."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_gqa_store_gb300 as msg
+from paged_kv_gqa_store_gb300 import graph as mgraph
 from paged_kv_gqa_store_gb300 import workload as wl
+
+from _harness import assert_attn_close
 
 pytestmark = pytest.mark.gpu
 
 
-def _decode_batch(seed, n_real, n_pad, ctx_lo, ctx_hi, steps_ahead):
-    rng = np.random.default_rng(seed)
-    ctx = rng.integers(ctx_lo, ctx_hi, size=n_real)
-    # room for `steps_ahead` more decode tokens per request
-    spec = wl.make_batch("graph", seed, cached_len=ctx - 1 + steps_ahead,
-                         extend_len=np.ones(n_real, np.int32), page_size=1,
-                         num_pages=int((ctx + steps_ahead).sum()) + 64)
-    dummy = spec.num_slots
-    width = spec.page_table.shape[1]
-    pt = np.zeros((n_real + 1, width), np.int32)
-    pt[:n_real] = spec.page_table
-    pt[n_real, :] = dummy
-    cached = np.r_[ctx - 1, np.zeros(n_pad, np.int64)].astype(np.int32)
-    ext = np.ones(n_real + n_pad, np.int32)
-    rows = np.r_[np.arange(n_real), np.full(n_pad, n_real)].astype(np.int32)
-    return pt, cached, ext, rows, spec.num_slots + 1
-
-
-def _run_step(pt, cached, ext, rows, qo, loc, ws, q, kn, vn, kp, vp, out):
-    msg.msg_plan(pt, cached, ext, q.shape[0], kp.shape[0], ws, req_rows=rows, qo_indptr_out=qo,
-                 out_loc_out=loc)
-    msg.msg_store_kv(kn, vn, kp, vp, loc)
-    msg.msg_paged_attention(q, kp, vp, pt, cached, ext, qo, out, ws, page_size=1, req_rows=rows,
-                            max_kv_len=0, flags=msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_DECODE_ONLY)
-
-
-def test_graph_replay_matches_eager_over_steps():
+@pytest.fixture(scope="module", autouse=True)
+def _built():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     msg.load_library()
-    dev = "cuda"
-    n_real, n_pad, steps = 6, 2, 3
-    pt_np, cached_np, ext_np, rows_np, num_slots = _decode_batch(7, n_real, n_pad, 200, 3000, steps)
-    B = n_real + n_pad
-    rng = np.random.default_rng(8)
-    pool_k = wl.random_bf16(rng, (num_slots, 8, 128))
-    pool_v = wl.random_bf16(rng, (num_slots, 8, 128))
-    step_in = [{n: wl.random_bf16(rng, shape) for n, shape in
-                (("q", (B, 16, 128)), ("k", (B, 8, 128)), ("v", (B, 8, 128)))}
-               for _ in range(steps)]
 
-    def tensors():
-        return {
-            "pt": torch.from_numpy(pt_np).to(dev), "cached": torch.from_numpy(cached_np).to(dev),
-            "ext": torch.from_numpy(ext_np).to(dev), "rows": torch.from_numpy(rows_np).to(dev),
-            "qo": torch.zeros(B + 1, dtype=torch.int32, device=dev),
-            "loc": torch.zeros(B, dtype=torch.int64, device=dev),
-            "ws": torch.zeros(msg.msg_workspace_size(B, B), dtype=torch.uint8, device=dev),
-            "q": torch.empty(B, 16, 128, dtype=torch.bfloat16, device=dev),
-            "kn": torch.empty(B, 8, 128, dtype=torch.bfloat16, device=dev),
-            "vn": torch.empty(B, 8, 128, dtype=torch.bfloat16, device=dev),
-            "kp": wl.bits_to_torch(pool_k, dev), "vp": wl.bits_to_torch(pool_v, dev),
-            "out": torch.empty(B, 16, 128, dtype=torch.bfloat16, device=dev)}
 
-    def load(t, s):
-        t["q"].copy_(wl.bits_to_torch(step_in[s]["q"], dev))
-        t["kn"].copy_(wl.bits_to_torch(step_in[s]["k"], dev))
-        t["vn"].copy_(wl.bits_to_torch(step_in[s]["v"], dev))
-        # Req.complete_one on real requests: cached_len advances by one per step
-        c = cached_np.copy()
-        c[:n_real] += s
-        t["cached"].copy_(torch.from_numpy(c).to(dev))
+def test_ladder_and_padding_rule():
+    # CPU logic, exercised here with its GPU users: the pages' ladder and
+    # "the first captured size >= the batch"
+    sizes = mgraph.graph_batch_sizes(256)
+    assert sizes[:5] == [1, 2, 4, 8, 16] and sizes[-1] == 256 and len(sizes) == 35
+    assert mgraph.padded_size(sizes, 10) == 16 and mgraph.padded_size(sizes, 3) == 4
+    assert mgraph.padded_size(sizes, 256) == 256
 
-    def args(t):
-        return (t["pt"], t["cached"], t["ext"], t["rows"], t["qo"], t["loc"], t["ws"], t["q"],
-                t["kn"], t["vn"], t["kp"], t["vp"], t["out"])
 
-    eager, graph_t = tensors(), tensors()
-    # warm-up (first calls set kernel attributes), then capture on a side stream
-    load(graph_t, 0)
-    warm = tensors()
-    load(warm, 0)
-    _run_step(*args(warm))
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        _run_step(*args(graph_t))
-    for s in range(steps):
-        load(eager, s)
-        _run_step(*args(eager))
-        load(graph_t, s)
-        g.replay()
+class _Requests:
+    """Decode requests with room for `steps` more tokens each, a dummy row
+    (every entry the dummy slot, the last slot of the pool) and host copies
+    of the pools that the oracle updates step by step."""
+
+    def __init__(self, seed, n, ctx_lo, ctx_hi, steps, layers):
+        rng = np.random.default_rng(seed)
+        self.ctx = rng.integers(ctx_lo, ctx_hi, size=n)
+        spec = wl.make_batch("graph", seed, cached_len=self.ctx - 1 + steps,
+                             extend_len=np.ones(n, np.int32), page_size=1,
+                             num_pages=int((self.ctx + steps).sum()) + 64)
+        self.dummy_slot = spec.num_slots
+        self.num_slots = spec.num_slots + 1
+        width = spec.page_table.shape[1]
+        self.pt = np.zeros((n + 1, width), np.int32)
+        self.pt[:n] = spec.page_table
+        self.pt[n, :] = self.dummy_slot
+        self.dummy_row = n
+        self.cached = (self.ctx - 1).astype(np.int32)        # advances one per step
+        self.pools = [(wl.random_bf16(rng, (self.num_slots, 8, 128)),
+                       wl.random_bf16(rng, (self.num_slots, 8, 128))) for _ in range(layers)]
+        self.rng = rng
+
+    def device_pools(self):
+        return [(wl.bits_to_torch(k, "cuda"), wl.bits_to_torch(v, "cuda")) for k, v in self.pools]
+
+    def oracle_step(self, live, q, kn, vn):
+        """Store the live requests' new rows in the host pools and attend;
+        returns one fp64 output per layer."""
+        cached = self.cached[live]
+        ext = np.ones(len(live), np.int32)
+        meta = oracle.metadata(self.pt, cached, ext, live.astype(np.int32))
+        outs = []
+        for (kp, vp), qq, kk, vv in zip(self.pools, q, kn, vn):
+            oracle.store_kv(kk, vv, meta["out_loc"], kp, vp)
+            outs.append(oracle.paged_attention(qq, kp, vp, self.pt, cached, meta["qo_indptr"],
+                                               16, 8, 128, req_rows=live.astype(np.int32)))
+        self.cached[live] += 1                                # Req.complete_one
+        return outs
+
+
+def test_graph_ladder_replay_matches_oracle():
+    """Graphs captured for the ladder up to 32 (1, 2, 4, 8, 16, 24, 32), live
+    batches of 7 sizes padded to 7 different captured sizes, 2 layers of the
+    fused store + decode step per replay; every step checked against the
+    oracle, and the pools bit-exactly at the end."""
+    layers, max_bs = 2, 32
+    live_sizes = [3, 1, 13, 24, 2, 8, 30, 5]
+    R = _Requests(21, max_bs, 20, 700, len(live_sizes), layers)
+    pools = R.device_pools()
+    runner = mgraph.DecodeGraphRunner(pools, torch.from_numpy(R.pt).cuda(), R.dummy_row, max_bs)
+    runner.capture()
+    seen = set()
+    for step, n in enumerate(live_sizes):
+        live = np.sort(R.rng.choice(max_bs, n, replace=False))
+        q = [wl.random_bf16(R.rng, (n, 16, 128)) for _ in range(layers)]
+        kn = [wl.random_bf16(R.rng, (n, 8, 128)) for _ in range(layers)]
+        vn = [wl.random_bf16(R.rng, (n, 8, 128)) for _ in range(layers)]
+        for i in range(layers):
+            runner.q[i][:n].copy_(wl.bits_to_torch(q[i], "cuda"))
+            runner.k_new[i][:n].copy_(wl.bits_to_torch(kn[i], "cuda"))
+            runner.v_new[i][:n].copy_(wl.bits_to_torch(vn[i], "cuda"))
+        bs = runner.replay(R.cached[live], live)
+        seen.add(bs)
+        assert bs == mgraph.padded_size(runner.sizes, n)
         torch.cuda.synchronize()
-        e = wl.torch_to_bits(eager["out"])[:n_real]
-        r = wl.torch_to_bits(graph_t["out"])[:n_real]
-        assert np.array_equal(e, r), f"step {s}"
-        assert np.isfinite(wl.bf16_bits_to_f64(r)).all()
-    real = np.arange(num_slots) != num_slots - 1
-    assert np.array_equal(wl.torch_to_bits(eager["kp"])[real], wl.torch_to_bits(graph_t["kp"])[real])
-    assert msg.msg_read_device_status(graph_t["ws"])[0] == msg.MSG_OK
+        refs = R.oracle_step(live, q, kn, vn)
+        for i in range(layers):
+            assert_attn_close(wl.torch_to_bits(runner.out[i][:n]), refs[i],
+                              f"step {step} (live {n}, graph {bs}) layer {i}")
+    assert len(seen) == len(live_sizes) - 1 >= 4
+    real = np.arange(R.num_slots) != R.dummy_slot
+    for (kd, vd), (kh, vh) in zip(pools, R.pools):
+        assert np.array_equal(wl.torch_to_bits(kd)[real], kh[real])
+        assert np.array_equal(wl.torch_to_bits(vd)[real], vh[real])
+    assert msg.msg_read_device_status(runner.ws)[0] == msg.MSG_OK
+
+
+def test_graph_replay_matches_eager_and_oracle_over_steps():
+    """The same padded batch (6 live requests in a graph of 8) over 3 steps:
+    replay equals eager execution bit for bit, and both equal the oracle."""
+    layers, max_bs, n, steps = 2, 8, 6, 3
+    R = _Requests(7, n, 200, 3000, steps, layers)
+    pools_g, pools_e = R.device_pools(), R.device_pools()
+    pt = torch.from_numpy(R.pt).cuda()
+    graph_r = mgraph.DecodeGraphRunner(pools_g, pt, R.dummy_row, max_bs)
+    eager_r = mgraph.DecodeGraphRunner(pools_e, pt, R.dummy_row, max_bs)
+    graph_r.capture()
+    live = np.arange(n)
+    for s in range(steps):
+        q = [wl.random_bf16(R.rng, (n, 16, 128)) for _ in range(layers)]
+        kn = [wl.random_bf16(R.rng, (n, 8, 128)) for _ in range(layers)]
+        vn = [wl.random_bf16(R.rng, (n, 8, 128)) for _ in range(layers)]
+        for r in (graph_r, eager_r):
+            for i in range(layers):
+                r.q[i][:n].copy_(wl.bits_to_torch(q[i], "cuda"))
+                r.k_new[i][:n].copy_(wl.bits_to_torch(kn[i], "cuda"))
+                r.v_new[i][:n].copy_(wl.bits_to_torch(vn[i], "cuda"))
+        assert graph_r.replay(R.cached[live], live) == 8
+        assert eager_r.eager(R.cached[live], live) == 8
+        torch.cuda.synchronize()
+        refs = R.oracle_step(live, q, kn, vn)
+        for i in range(layers):
+            g = wl.torch_to_bits(graph_r.out[i][:n])
+            assert np.array_equal(g, wl.torch_to_bits(eager_r.out[i][:n])), f"step {s}"
+            assert_attn_close(g, refs[i], f"step {s} layer {i}")
+    real = np.arange(R.num_slots) != R.dummy_slot
+    for (kg, vg), (ke, ve), (kh, vh) in zip(pools_g, pools_e, R.pools):
+        assert np.array_equal(wl.torch_to_bits(kg)[real], kh[real])
+        assert np.array_equal(wl.torch_to_bits(ke)[real], kh[real])
+        assert np.array_equal(wl.torch_to_bits(vg)[real], vh[real])
+    assert msg.msg_read_device_status(graph_r.ws)[0] == msg.MSG_OK

@@ -45,7 +45,7 @@ def test_tiny_mixed_config(int64_loc):
 
 # ------------------------------------------------------------ random ragged batches
 def _rand_spec(seed, n_dec, n_ext, page_size, max_ctx=700, max_ext=200, shuffle=True,
-               extra_rows=3):
+               extra_rows=3, **kw):
     rng = np.random.default_rng(seed)
     cached = list(rng.integers(0, max_ctx, size=n_dec)) + list(rng.integers(0, max_ctx, size=n_ext))
     ext = [1] * n_dec + list(rng.integers(2, max_ext + 1, size=n_ext))
@@ -54,7 +54,7 @@ def _rand_spec(seed, n_dec, n_ext, page_size, max_ctx=700, max_ext=200, shuffle=
     ext = np.asarray(ext)[order]
     need = int(((np.asarray(cached) + ext + page_size - 1) // page_size).sum())
     return wl.make_batch(f"rand{seed}_p{page_size}", seed, cached, ext, page_size,
-                         num_pages=need + 11, shuffle_rows=shuffle, extra_rows=extra_rows)
+                         num_pages=need + 11, shuffle_rows=shuffle, extra_rows=extra_rows, **kw)
 
 
 @pytest.mark.parametrize("page_size", [1, 16, 64])
@@ -320,3 +320,80 @@ def test_phase_flag_contradiction_is_reported():
     gb.attention(q, kp, vp, flags=msg.MSG_ATTN_DECODE_ONLY)
     st, info = gb.status()
     assert st == msg.MSG_ERR_DEVICE_CHECK and info[0] == msg.MSG_DEV_WRONG_PHASE
+
+
+# ------------------------------------------------------------ tensor-parallel head slices
+@pytest.mark.parametrize("hkv", [4, 2, 1])
+@pytest.mark.parametrize("page_size", [1, 16])
+def test_tp_head_slice_mixed(hkv, page_size):
+    """A tensor-parallel rank holds num_kv_heads / tp KV heads and their 2 query
+    heads each ("Mini-SGLang 完整剖析" 4.5: the QKV projection is split by KV
+    head); its attention is the same call with fewer heads: 8q/4kv at tp = 2,
+    4q/2kv at tp = 4, 2q/1kv at tp = 8."""
+    spec = _rand_spec(700 + 10 * hkv + page_size, n_dec=25, n_ext=4, page_size=page_size,
+                      num_qo_heads=2 * hkv, num_kv_heads=hkv)
+    _check_full(spec, wl.host_tensors(spec))
+
+
+@pytest.mark.parametrize("hkv", [4, 1])
+def test_tp_head_slice_fused_store_long_request(hkv):
+    """The fused store + decode call on a head slice, one request cut over
+    most CTAs; equals store_kv then attention bit for bit, and the oracle."""
+    rng = np.random.default_rng(580 + hkv)
+    n = 9
+    cached = rng.integers(1, 1500, size=n)
+    cached[3] = 20000
+    spec = wl.make_batch("fused_tp", 580 + hkv, cached, np.ones(n, np.int32), 1,
+                         num_pages=int(cached.sum()) + 64, num_qo_heads=2 * hkv,
+                         num_kv_heads=hkv)
+    host = wl.host_tensors(spec)
+    ref = run_small(spec, host, flags=msg.MSG_ATTN_DECODE_ONLY)
+    assert ref["status"] == msg.MSG_OK, ref["status_info"]
+    dev = "cuda"
+    gb = GpuBatch(spec, dev)
+    q = wl.bits_to_torch(host["q"], dev)
+    k_new, v_new = wl.bits_to_torch(host["k_new"], dev), wl.bits_to_torch(host["v_new"], dev)
+    k_pool, v_pool = wl.bits_to_torch(host["k_pool"], dev), wl.bits_to_torch(host["v_pool"], dev)
+    gb.plan()
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    msg.msg_paged_attention_store(q, k_new, v_new, k_pool, v_pool, gb.page_table, gb.cached,
+                                  gb.extend, gb.qo, out, gb.ws, page_size=1, req_rows=gb.rows,
+                                  max_kv_len=spec.max_kv_len,
+                                  flags=msg.MSG_ATTN_DECODE_ONLY | msg.MSG_ATTN_REUSE_PLAN)
+    torch.cuda.synchronize()
+    st, info = gb.status()
+    assert st == msg.MSG_OK, info
+    assert np.array_equal(wl.torch_to_bits(out), ref["out"])
+    assert np.array_equal(wl.torch_to_bits(k_pool), ref["k_pool"])
+    assert np.array_equal(wl.torch_to_bits(v_pool), ref["v_pool"])
+    assert_attn_close(wl.torch_to_bits(out), oracle_small(spec, host)["out"], "fused tp")
+
+
+def test_tp_rank_reads_its_slice_of_the_full_pools():
+    """Rank 1 of tp = 2 on views of a full layer: q heads 8..15 and KV heads
+    4..7 of the pools (rows keep the full layer's stride).  Its store writes
+    only heads 4..7 and its outputs match the full layer's query heads 8..15
+    within tolerance, both checked against the oracle."""
+    spec = _rand_spec(731, n_dec=14, n_ext=3, page_size=16)
+    host = wl.host_tensors(spec)
+    full = oracle_small(spec, host)
+    dev = "cuda"
+    gb = GpuBatch(spec, dev)
+    q = wl.bits_to_torch(host["q"], dev)[:, 8:16]
+    k_new = wl.bits_to_torch(host["k_new"], dev)[:, 4:8]
+    v_new = wl.bits_to_torch(host["v_new"], dev)[:, 4:8]
+    k_pool, v_pool = wl.bits_to_torch(host["k_pool"], dev), wl.bits_to_torch(host["v_pool"], dev)
+    loc = gb.plan()
+    msg.msg_store_kv(k_new, v_new, k_pool[:, 4:8], v_pool[:, 4:8], loc, dev_status=gb.ws)
+    out = torch.empty(q.shape[0], 8, 128, dtype=torch.bfloat16, device=dev)
+    msg.msg_paged_attention(q, k_pool[:, 4:8], v_pool[:, 4:8], gb.page_table, gb.cached,
+                            gb.extend, gb.qo, out, gb.ws, page_size=16, req_rows=gb.rows,
+                            max_kv_len=spec.max_kv_len, flags=msg.MSG_ATTN_REUSE_PLAN)
+    torch.cuda.synchronize()
+    st, info = gb.status()
+    assert st == msg.MSG_OK, info
+    kp, vp = wl.torch_to_bits(k_pool), wl.torch_to_bits(v_pool)
+    assert np.array_equal(kp[:, 4:8], full["k_pool"][:, 4:8])
+    assert np.array_equal(vp[:, 4:8], full["v_pool"][:, 4:8])
+    assert np.array_equal(kp[:, :4], host["k_pool"][:, :4])     # the other rank's heads untouched
+    assert_attn_close(wl.torch_to_bits(out), full["out"][:, 8:16], "tp rank 1 of 2")

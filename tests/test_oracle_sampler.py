@@ -42,6 +42,29 @@ def test_prepare_clamps_and_sparse_arguments():
     assert p.dtype == np.float32 and np.allclose(p, [1e-6, 0.95])
 
 
+def test_is_greedy_follows_the_pages_rule():
+    # the printed property: (temperature <= 0 or top_k == 1) and top_p == 1
+    for c in _golden()["greedy_rule"]["cases"]:
+        assert oracle.is_greedy(c["temperature"], c["top_k"], c["top_p"]) is c["greedy"], c
+
+
+def test_prepare_temperature_zero_with_top_p_is_sampled():
+    # every temperature is 0, but one request has top_p < 1: it is not greedy,
+    # so the batch takes the sampled branch (temperatures present), that
+    # request at MIN_T, and the top-p tensor exists
+    t, k, p = oracle.sampling_args([0.0, 0.0], [-1, -1], [1.0, 0.9], 100)
+    assert t is not None and np.allclose(t, [1e-6, 1e-6])
+    assert k is None and np.allclose(p, [1.0, 0.9])
+
+
+def test_prepare_top_k_one_is_greedy():
+    # temperature > 0 with top_k == 1 and top_p == 1 is greedy: a batch of such
+    # requests takes the argmax, and in a mixed batch it gets MIN_T
+    assert oracle.sampling_args([0.8, 1.5], [1, 1], [1.0, 1.0], 100) == (None, None, None)
+    t, k, p = oracle.sampling_args([0.8, 1.5], [1, 3], [1.0, 1.0], 100)
+    assert np.allclose(t, [1e-6, 1.5]) and k.tolist() == [1, 3] and p is None
+
+
 # --------------------------------------------------------- printed examples
 def test_engine_test_case_support_and_frequency():
     g = _golden()["engine_test"]
