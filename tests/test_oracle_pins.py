@@ -355,3 +355,22 @@ def test_bf16_input_rounding_is_nearest_even():
     big = np.random.default_rng(0).standard_normal(10000, dtype=np.float32)
     ref = torch.from_numpy(big).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(wl.f32_to_bf16_bits(big), ref)
+
+
+def test_thread_count_does_not_change_results():
+    # the CPU baseline times the oracle on one core and on all of them: every
+    # output element is computed by one thread in one order, so the results
+    # are bit-identical whatever the thread count
+    Hq, Hkv, D = 16, 8, 128
+    _, cached, ext, dev, pt, q, kv, ns = _paged_setup(41, [40, 0, 300, 7], [1, 33, 1, 12],
+                                                      Hq, Hkv, D)
+    kp, vp = _pools_from(kv, pt, dev, ns, Hkv, D)
+    n = oracle.num_threads()
+    try:
+        oracle.set_num_threads(1)
+        a = _oracle_out(q, kp, vp, pt, cached, ext, Hq, Hkv, D)
+        oracle.set_num_threads(max(n, 3))
+        b = _oracle_out(q, kp, vp, pt, cached, ext, Hq, Hkv, D)
+    finally:
+        oracle.set_num_threads(n)
+    assert np.array_equal(a, b)
