@@ -152,3 +152,35 @@ def test_graph_replay_matches_eager_and_oracle_over_steps():
         assert np.array_equal(wl.torch_to_bits(ke)[real], kh[real])
         assert np.array_equal(wl.torch_to_bits(vg)[real], vh[real])
     assert msg.msg_read_device_status(graph_r.ws)[0] == msg.MSG_OK
+
+
+def test_mixed_call_captured_in_a_graph():
+    """A mixed batch's step (plan, store_kv, then the decode and the extend
+    kernels) captured in a CUDA graph and replayed gives the oracle's result."""
+    from _harness import GpuBatch, oracle_small
+    rng = np.random.default_rng(33)
+    cached = np.r_[rng.integers(100, 2000, size=20), rng.integers(0, 300, size=3)]
+    ext = np.r_[np.ones(20, np.int64), rng.integers(100, 300, size=3)]
+    spec = wl.make_batch("graph_mixed", 33, cached, ext, 1, num_pages=int((cached + ext).sum()) + 9)
+    host = wl.host_tensors(spec)
+    gb = GpuBatch(spec)
+    q = wl.bits_to_torch(host["q"], "cuda")
+    kn, vn = wl.bits_to_torch(host["k_new"], "cuda"), wl.bits_to_torch(host["v_new"], "cuda")
+    kp, vp = wl.bits_to_torch(host["k_pool"], "cuda"), wl.bits_to_torch(host["v_pool"], "cuda")
+    out = torch.empty_like(q)
+
+    def step():
+        loc = gb.plan()
+        msg.msg_store_kv(kn, vn, kp, vp, loc)
+        gb.attention(q, kp, vp, out=out, flags=msg.MSG_ATTN_REUSE_PLAN)
+
+    step()                                           # warm-up (sets kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert gb.status()[0] == msg.MSG_OK
+    assert_attn_close(wl.torch_to_bits(out), oracle_small(spec, host)["out"], "graph mixed")
