@@ -47,7 +47,7 @@ namespace {
 
 constexpr int kTileKeys = 8;
 constexpr int kStages = 3;
-constexpr int64_t kMinKeysPerCta = 64;
+constexpr int64_t kMinKeysPerCta = 32;
 
 // Launch shape for HKV KV heads (query heads 2 HKV): one consumer warp per KV
 // head plus the producer warp; a stage holds kTileKeys whole token rows of K
