@@ -603,6 +603,8 @@ def run_extend(args, dev, msg, peaks):
     return {"workload": "extend_8req_cached0-2048_ext512-4096_page1", "tflops": round(tf, 1),
             "bound": "tensor", "kernel": "extend_kernel",
             "traffic": None if traffic is None else traffic["bytes_per_launch"],
+            "tensor_pipe_pct_of_active": None if traffic is None
+            else traffic.get("tensor_pipe_pct_of_active"),
             "peak_tflops": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4),
             "peak_source": peaks["source"], "attn_ms": round(at_ms, 4), "flops": fl,
             "store_kv_gbs": round(sb / (st_ms * 1e-3) / 1e9, 1), "store_kv_ms": round(st_ms, 4),
