@@ -33,7 +33,10 @@
 //               over S as a bf16 pair hi + lo (a single bf16 P costs ~2.2e-3
 //               relative L2 on top of the output rounding; the pair keeps ~16
 //               bits).  The row's denominator sums the fp32 P (within 2^-16 of
-//               the pair).  The epilogue normalises O and stores bf16 rows.
+//               the pair).  P is published to the issuer once per key tile
+//               (each wait the issuer makes between MMA groups lets the tensor
+//               pipe drain, and the softmax runs well ahead of its P.V).  The
+//               epilogue normalises O and stores bf16 rows.
 //
 // All cross-role hand-offs are mbarriers; every wait is bounded in time and an
 // expired one records MSG_DEV_TIMEOUT and unwinds.
@@ -69,7 +72,7 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max 
 enum {
   kBarQFull = 0, kBarQFree = 1, kBarFull = 2, kBarEmpty = 7, kBarSFull = 12, kBarPReady = 14,
   kBarODone = 18, kBarOFree = 20, kBarEpi = 22, kBarFinal = 23, kBarItem = 24, kNumBars = 40
-};  // kBarPReady + 2 x + h: P of sub-tile x, key half h written
+};  // kBarPReady + 2 x: P of sub-tile x written (kBarPReady + 2 x + 1 unused)
 constexpr int kItemQueue = 16;                // work items published ahead of the slowest role
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -318,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars[kBarSFull + x], 1);
       mbar_init(&bars[kBarPReady + 2 * x], 4);
-      mbar_init(&bars[kBarPReady + 2 * x + 1], 4);
       mbar_init(&bars[kBarODone + x], 1);
       mbar_init(&bars[kBarOFree + x], 4);
     }
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nx = x ? n : it.n_a;             // tiles this sub-tile uses
             if (j >= 1 && j - 1 < nx) {
               // O_x += P_x(j-1) . V_{j-1}, P as the pair hi + lo
-              if (aborted(abort_flag) ||
+              if ((x == 0 && aborted(abort_flag)) ||
                   !mbar_wait(&bars[kBarPReady + 2 * x], (Ts[x] + j - 1) & 1) ||
                   (!v_ready && !mbar_wait(&bars[kBarFull + nv % kSlots], (nv / kSlots) & 1)) ||
                   (j == 1 && V > 0 && !mbar_wait(&bars[kBarOFree + x], (V - 1) & 1))) {
@@ -482,14 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t o_col = tmem + kColO + 128u * x;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
-                if (kk == 4) {
-                  // keys 64..127: wait for the second half of P
-                  if (!mbar_wait(&bars[kBarPReady + 2 * x + 1], (Ts[x] + j - 1) & 1)) {
-                    ok = false;
-                    break;
-                  }
-                  tc_fence_after();
-                }
                 // keys 16kk .. 16kk+15: P hi at columns 32(kk/2) + 8(kk%2), lo 16 further
                 const uint32_t pc = p_col + 32u * (kk >> 1) + 8u * (kk & 1);
                 const uint64_t bd = vd + (uint64_t)((kk * 2048) >> 4);
@@ -502,8 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (x == 1 && j >= 1) mma_commit(&bars[kBarEmpty + nv % kSlots]);
             if (j < nx) {
               // S_x = Q_x . K_j^T
-              if (aborted(abort_flag) ||
-                  (!k_ready && !mbar_wait(&bars[kBarFull + nk % kSlots], (nk / kSlots) & 1))) {
+              if (!k_ready && !mbar_wait(&bars[kBarFull + nk % kSlots], (nk / kSlots) & 1)) {
                 ok = false;
                 break;
               }
@@ -643,12 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st16(s_col + 32u * c, wh);
         tmem_st16(s_col + 32u * c + 16u, wl);
-        if (c & 1) {
-          // keys 64 (c >> 1) .. +63 of P are in TMEM: let the MMA issuer use them
+        if (c == 3) {
+          // the whole of P is in TMEM: let the MMA issuer use it
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarPReady + 2 * x + (c >> 1)]);
+          if (lane == 0) mbar_arrive(&bars[kBarPReady + 2 * x]);
         }
       }
     }
