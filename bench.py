@@ -436,10 +436,18 @@ def run_tiny_mixed(args, dev, msg):
 
     ms = _median_launch_ms(step, max(args.steps, 50), flush)
     _check_status(msg, b, "tiny mixed")
-    del flush
+    # the same step captured once and replayed (what a graph runner pays per step)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    gms = _median_launch_ms(g.replay, max(args.steps, 50), flush)
+    _check_status(msg, b, "tiny mixed, graph")
+    del flush, g
     return {"workload": "tiny_mixed_1ext4_cached2_3dec_ctx5-17-64_page1", "us": round(ms * 1e3, 2),
+            "graph_us": round(gms * 1e3, 2),
             "launches": 5, "l2": "flushed (256 MB write) before every timed step",
-            "what": "plan + token metadata + store_kv + decode + extend kernels, one step"}
+            "what": "plan + token metadata + store_kv + decode + extend kernels, one step "
+                    "(us: launched one by one; graph_us: one captured graph replayed)"}
 
 
 def run_graph_ladder(args, dev, msg):
