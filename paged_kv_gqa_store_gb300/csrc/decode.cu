@@ -48,6 +48,7 @@ namespace {
 constexpr int kTileKeys = 8;
 constexpr int kStages = 3;
 constexpr int64_t kMinKeysPerCta = 32;
+static_assert(kDecSegPad < kMinKeysPerCta, "a CTA range must reach past any gap");
 
 // Launch shape for HKV KV heads (query heads 2 HKV): one consumer warp per KV
 // head plus the producer warp; a stage holds kTileKeys whole token rows of K
@@ -120,7 +121,7 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
                                         int64_t b, int64_t K, int64_t g) {
   Seg s;
   s.S = p.dec_start[i];
-  s.E = p.dec_start[i + 1];
+  s.E = p.dec_start[i + 1] - kDecSegPad;      // the request's keys; a gap follows them
   s.lo = s.S > begin ? s.S : begin;
   s.hi = s.E < end ? s.E : end;
   s.r = p.dec_req[i];
@@ -235,6 +236,9 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
       i = lo;
     }
     Seg sg = load_seg(p, i, begin, end, b, K, g);
+    // begin in a gap: the range starts with the next request (there is one:
+    // a range is longer than a gap, and the last request's gap ends the space)
+    if (sg.lo >= sg.hi && i + 1 < nd) sg = load_seg(p, ++i, begin, end, b, K, g);
     int64_t kt = sg.lo;                        // flattened key index of the tile
     int32_t raw = 0;
     {
@@ -251,7 +255,8 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
       const int nkeys = (int)imin64(kTileKeys, sg.hi - kt);
       const bool first = (kt == sg.lo);
       const bool last = (kt + nkeys == sg.hi);
-      const bool fin = last && sg.hi == end;
+      // the range ends with this segment, or in the gap after it
+      const bool fin = last && (sg.hi == end || i + 1 >= nd || sg.E + kDecSegPad >= end);
       // look one tile ahead: next segment metadata and page-table entries
       Seg nsg = sg;
       int64_t nkt = kt + nkeys;
@@ -498,8 +503,25 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
           auto slot_of = [&](int k) {
             return 2 * (int64_t)(h.bf + k) + (k == 0 ? h.head_shift : 0);
           };
-          float L0 = -INFINITY, L1 = -INFINITY;
-          for (int k = lane; k < ns; k += 32) {
+          // split `lane`'s lse values and the first batch of o rows, all in
+          // flight at once; the lse values stay in their lanes for the weights
+          float4 xs[kMergeBatch], ys[kMergeBatch];
+#pragma unroll
+          for (int u = 0; u < kMergeBatch; ++u) {
+            if (u < ns) {
+              const float *pr0 = p.part_o + (slot_of(u) * kHq + 2 * gh) * kHeadDim + lane * 4;
+              xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
+              ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+            }
+          }
+          float l0 = -INFINITY, l1 = -INFINITY;
+          if (lane < ns) {
+            const int64_t sl = slot_of(lane);
+            l0 = __ldcg(p.part_lse + sl * kHq + 2 * gh);
+            l1 = __ldcg(p.part_lse + sl * kHq + 2 * gh + 1);
+          }
+          float L0 = l0, L1 = l1;
+          for (int k = lane + 32; k < ns; k += 32) {
             const int64_t sl = slot_of(k);
             L0 = fmaxf(L0, __ldcg(p.part_lse + sl * kHq + 2 * gh));
             L1 = fmaxf(L1, __ldcg(p.part_lse + sl * kHq + 2 * gh + 1));
@@ -513,21 +535,27 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
           float d0 = 0.f, d1 = 0.f;
           for (int k0 = 0; k0 < ns; k0 += 32) {
             float w0 = 0.f, w1 = 0.f;
-            if (k0 + lane < ns) {
+            if (k0 == 0) {
+              if (lane < ns) {
+                w0 = exp2f(l0 - L0);
+                w1 = exp2f(l1 - L1);
+              }
+            } else if (k0 + lane < ns) {
               const int64_t sl = slot_of(k0 + lane);
               w0 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh) - L0);
               w1 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh + 1) - L1);
             }
             const int nk = ns - k0 < 32 ? ns - k0 : 32;
             for (int j0 = 0; j0 < nk; j0 += kMergeBatch) {
-              float4 xs[kMergeBatch], ys[kMergeBatch];
+              if (k0 > 0 || j0 > 0) {
 #pragma unroll
-              for (int u = 0; u < kMergeBatch; ++u) {   // the batch's loads, all in flight
-                if (j0 + u < nk) {
-                  const float *pr0 =
-                      p.part_o + (slot_of(k0 + j0 + u) * kHq + 2 * gh) * kHeadDim + lane * 4;
-                  xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
-                  ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+                for (int u = 0; u < kMergeBatch; ++u) {   // the batch's loads, all in flight
+                  if (j0 + u < nk) {
+                    const float *pr0 =
+                        p.part_o + (slot_of(k0 + j0 + u) * kHq + 2 * gh) * kHeadDim + lane * 4;
+                    xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
+                    ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+                  }
                 }
               }
 #pragma unroll

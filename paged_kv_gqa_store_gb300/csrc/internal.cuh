@@ -17,6 +17,12 @@ constexpr int kGroup = 2;                 // query heads per KV head
 constexpr int kMaxKvHeads = 8;            // KV heads of a full layer (16 query heads); a
                                           // tensor-parallel slice passes 4, 2 or 1
 constexpr int kMaxDecodeCtas = 512;       // decode CTAs at 8 KV heads (2 partial slots each)
+// The decode plan lays the requests' keys end to end with this many empty
+// key positions after each request: the decode CTAs split that space evenly,
+// so a CTA whose range holds a request boundary (a second segment: its q, its
+// own normalisation and partial) gets correspondingly fewer keys.  Below the
+// decode kernel's 32 keys per CTA, so no CTA range lies inside a gap.
+constexpr int kDecSegPad = 24;
 
 // Decode CTAs the split-KV partials have room for with hq query heads: the
 // partial arrays are sized for 16 heads x kMaxDecodeCtas, so fewer heads per
@@ -42,7 +48,7 @@ struct WsLayout {
   size_t header = 0;       // PlanHeader
   size_t qo_indptr = 0;    // int32[num_reqs + 1]   (plan's own, checked copy)
   size_t dec_req = 0;      // int32[num_reqs]       decode request list
-  size_t dec_start = 0;    // int64[num_reqs + 1]   prefix of decode kv lengths
+  size_t dec_start = 0;    // int64[num_reqs + 1]   prefix of decode kv lengths + gaps
   size_t dec_row = 0;      // int64[num_reqs]       index row offset of each decode request
   size_t dec_qrow = 0;     // int32[num_reqs]       its query row (qo_indptr)
   size_t counters = 0;     // int32[num_reqs * 8]   split merge counters (request, KV head)
@@ -59,7 +65,7 @@ struct PlanHeader {
   int32_t dec_count;       // decode requests
   int32_t ext_tile_count;  // extend tiles
   int32_t ext_count;       // extend requests
-  int64_t dec_keys;        // sum of decode kv lengths
+  int64_t dec_keys;        // sum of decode kv lengths + a gap (kDecSegPad) per request
   int64_t total_q;         // sum of extend lengths
   int32_t ext_next;        // extend work-item counter (zeroed before each extend launch)
   int32_t pad;

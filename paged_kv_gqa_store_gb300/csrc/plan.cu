@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const bool is_dec = (e == 1);
     const bool is_ext = (e >= 2);
     const int64_t ntiles = is_ext ? (e + kExtendTileTokens - 1) / kExtendTileTokens : 0;
-    Scan4 x{{e, is_dec ? 1 : 0, is_dec ? c + e : 0, ntiles}};
+    Scan4 x{{e, is_dec ? 1 : 0, is_dec ? c + e + kDecSegPad : 0, ntiles}};
     Scan4 tot;
     Scan4 ex = block_exclusive_scan(x, &tot, warp_sums);
     if (r < p.num_reqs) {
