@@ -67,10 +67,13 @@
  *   stream is finishing; it waits for that kernel before touching anything it
  *   writes or reads.  The one exception is the decode kernel of a call with
  *   MSG_ATTN_REUSE_PLAN, which reads the plan (workspace) and the KV index
- *   before that wait: those must not be written by the kernel launched
- *   immediately before the call unless that kernel completes before it lets
- *   dependents start (every kernel that does not opt into programmatic
- *   launch, and every kernel of this library, qualifies).
+ *   before that wait, and in msg_paged_attention_store also the first K/V
+ *   pool rows of its key range (up to three 32-key tiles per CTA, never a
+ *   request's newest key, which comes from k_new / v_new): those must not be
+ *   written by the kernel launched immediately before the call unless that
+ *   kernel completes before it lets dependents start (every kernel that does
+ *   not opt into programmatic launch, and every kernel of this library,
+ *   qualifies: each lets dependents start only after its own wait).
  * - Errors: entry points return MSG_OK (0) or a negative status before
  *   enqueuing anything; no exception crosses the ABI, nothing aborts and no
  *   kernel traps.  Data-dependent problems found on the device (a slot outside

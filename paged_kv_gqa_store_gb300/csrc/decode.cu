@@ -245,10 +245,33 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
       const int64_t n0 = imin64(kTileKeys, sg.hi - kt);
       if (lane < n0) raw = load_raw<kPage1>(p, sg.row, kt - sg.S + lane);
     }
-    // Everything above reads only the plan and the KV index; K / V (the step's
-    // new rows come from store_kv) and q are read after the preceding kernel.
-    grid_dep_wait();
-    grid_dep_launch();
+    // Everything above reads only the plan and the KV index.  q and the step's
+    // new rows are read after the preceding kernel.  With the new rows given
+    // (kFused) the first ring stages of older pool rows are gathered before
+    // that wait, while the preceding kernel's last CTAs finish.
+    bool waited = !kFused;
+    if (waited) {
+      grid_dep_wait();
+      grid_dep_launch();
+    }
+    // the wait, then the q rows of segments whose first tile went before it
+    // (tiles issued before the wait are tiles 0 .. n-1 in stages 0 .. n-1)
+    auto wait_preceding = [&](uint32_t n) {
+      grid_dep_wait();
+      grid_dep_launch();
+      waited = true;
+      if (lane == 0) {
+        for (uint32_t j = 0; j < n; ++j) {
+          uint8_t *stg = smem + (size_t)j * kStageBytes;
+          const TileHdr *th = reinterpret_cast<const TileHdr *>(stg + kOffHdr);
+          if (th->flags & kFirst) {
+            const int64_t qr = th->qrow < 0 ? 0 : th->qrow;
+            bulk_g2s(stg + kOffQ, p.q + qr * p.q_stride, kQBytes, &full[j]);
+          }
+        }
+      }
+      __syncwarp();
+    };
     uint32_t it = 0, issued = 0;
     bool ok = true;
     while (true) {
@@ -270,6 +293,15 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
         if (lane < nn) nraw = load_raw<kPage1>(p, nsg.row, nkt - nsg.S + lane);
       }
       const int st = it % kStages;
+      if (!waited) {
+        // wait first for a tile with a new row (the segment's last, when it
+        // ends the request), one that would report, or the first to reuse a
+        // stage (the consumers that free it wait too)
+        const bool bad = lane < nkeys && !raw_ok<kPage1>(p, raw, kt - sg.S + lane);
+        if (__any_sync(0xffffffffu, bad) || it >= (uint32_t)kStages || (last && sg.hi == sg.E) ||
+            sg.qrow < 0)
+          wait_preceding(issued);
+      }
       if (ok && it >= (uint32_t)kStages && !mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1)) {
         ok = false;
         if (lane == 0) {
@@ -320,25 +352,31 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
           if (slot_ok) {
             uint4 *kd = reinterpret_cast<uint4 *>(p.k_pool_w + nslot * p.pool_stride_bytes);
             uint4 *vd = reinterpret_cast<uint4 *>(p.v_pool_w + nslot * p.pool_stride_bytes);
+            // two rounds of at most 2 K + 2 V chunks per lane in flight (the
+            // producer's registers are the kernel's tightest)
             constexpr int kChunks = kRowBytes / 16, kPer = (kChunks + 31) / 32;
-            uint4 a[kPer], c[kPer];
+            constexpr int kRound = kPer < 2 ? kPer : 2;
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-              if (u * 32 + lane < kChunks) {
-                a[u] = ks[u * 32 + lane];
-                c[u] = vs[u * 32 + lane];
+            for (int u0 = 0; u0 < kPer; u0 += kRound) {
+              uint4 a[kRound], c[kRound];
+#pragma unroll
+              for (int u = 0; u < kRound; ++u) {
+                if ((u0 + u) * 32 + lane < kChunks) {
+                  a[u] = ks[(u0 + u) * 32 + lane];
+                  c[u] = vs[(u0 + u) * 32 + lane];
+                }
               }
-            }
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-              if (u * 32 + lane < kChunks) {
-                kd[u * 32 + lane] = a[u];
-                vd[u * 32 + lane] = c[u];
+              for (int u = 0; u < kRound; ++u) {
+                if ((u0 + u) * 32 + lane < kChunks) {
+                  kd[(u0 + u) * 32 + lane] = a[u];
+                  vd[(u0 + u) * 32 + lane] = c[u];
+                }
               }
             }
           }
         }
-        if (first && lane == 0) {
+        if (first && lane == 0 && waited) {
           const int64_t qr = sg.qrow < 0 ? 0 : sg.qrow;
           bulk_g2s(stage + kOffQ, p.q + qr * p.q_stride, kQBytes, &full[st]);
         }
@@ -353,6 +391,7 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
       kt = nkt;
       raw = nraw;
     }
+    if (!waited) wait_preceding(issued);
     // Drain: the last issued use of every stage must have landed before exit.
     for (uint32_t j = issued > (uint32_t)kStages ? issued - kStages : 0; j < issued; ++j)
       mbar_wait(&full[j % kStages], (j / kStages) & 1);

@@ -187,3 +187,61 @@ def test_prologue_other_head_counts(hq, hkv, T):
     assert np.array_equal(wl.torch_to_bits(vp)[loc], v_ref), "v"
     other = np.setdiff1d(np.arange(num_slots), loc)
     assert not wl.torch_to_bits(kp)[other].any() and not wl.torch_to_bits(vp)[other].any()
+
+
+def test_prologue_then_fused_decode_reads_the_fresh_step_inputs():
+    """The fused decode call (msg_paged_attention_store with a reused plan)
+    launched straight after the prologue kernel that writes its q, k_new and
+    v_new.  The prologue lets dependent kernels start before it writes them,
+    and the decode kernel gathers its first older pool rows before waiting for
+    it, so a read of q or of a newest row before that wait would show up as a
+    stale value.  Three repeats of the step with new QKV projections: each
+    step's output equals the oracle run on that step's q / k_new / v_new, and
+    the pools bit for bit."""
+    from _harness import GpuBatch, assert_attn_close
+    rng = np.random.default_rng(612)
+    n = 600
+    cached = rng.integers(1, 300, size=n)
+    cached[:4] = (9000, 4000, 2500, 1200)
+    spec = wl.make_batch("prologue_fused", 612, cached, np.ones(n, np.int32), 1,
+                         num_pages=int(cached.sum()) + n + 16)
+    host = wl.host_tensors(spec)
+    dev = "cuda"
+    gb = GpuBatch(spec, dev)
+    gb.plan()
+    T = spec.total_q
+    kp, vp = wl.bits_to_torch(host["k_pool"], dev), wl.bits_to_torch(host["v_pool"], dev)
+    kp_h, vp_h = host["k_pool"].copy(), host["v_pool"].copy()
+    max_pos = int(cached.max()) + 2
+    cs = msg.msg_rope_cos_sin_cache(THETA, D, max_pos)
+    qw = wl.f32_to_bf16_bits(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    kw = wl.f32_to_bf16_bits(rng.uniform(0.5, 1.5, D).astype(np.float32))
+    qw_t, kw_t = wl.bits_to_torch(qw, dev), wl.bits_to_torch(kw, dev)
+    pos = torch.from_numpy(cached.astype(np.int32)).to(dev)        # each new token's position
+    rows = torch.arange(T, dtype=torch.int64, device=dev)          # k_new / v_new row t <- token t
+    q = torch.empty(T, HQ, D, dtype=torch.bfloat16, device=dev)
+    k_new = torch.empty(T, HKV, D, dtype=torch.bfloat16, device=dev)
+    v_new = torch.empty_like(k_new)
+    out = torch.empty_like(q)
+    pstat = torch.zeros(4, dtype=torch.int32, device=dev)
+    meta = oracle.metadata(spec.page_table, spec.cached_len, spec.extend_len, spec.req_rows)
+    for step in range(3):
+        qkv = wl.bits_to_torch(wl.random_bf16(rng, (T, HQ + 2 * HKV, D)), dev)
+        torch.cuda.synchronize()
+        msg.msg_qk_norm_rope_store(qkv, pos, qw_t, kw_t, EPS, cs, q, k_new, v_new, rows, HQ, HKV,
+                                   dev_status=pstat)
+        msg.msg_paged_attention_store(q, k_new, v_new, kp, vp, gb.page_table, gb.cached,
+                                      gb.extend, gb.qo, out, gb.ws, page_size=1,
+                                      req_rows=gb.rows, max_kv_len=spec.max_kv_len,
+                                      flags=msg.MSG_ATTN_DECODE_ONLY | msg.MSG_ATTN_REUSE_PLAN)
+        torch.cuda.synchronize()
+        st, info = gb.status()
+        assert st == msg.MSG_OK, info
+        assert msg.msg_read_device_status(pstat)[0] == msg.MSG_OK
+        qh, kh, vh = (wl.torch_to_bits(t) for t in (q, k_new, v_new))
+        oracle.store_kv(kh, vh, meta["out_loc"], kp_h, vp_h)
+        ref = oracle.paged_attention(qh, kp_h, vp_h, spec.page_table, spec.cached_len,
+                                     meta["qo_indptr"], HQ, HKV, D, req_rows=spec.req_rows)
+        assert_attn_close(wl.torch_to_bits(out), ref, f"step {step}")
+        assert np.array_equal(wl.torch_to_bits(kp), kp_h), f"k pool, step {step}"
+        assert np.array_equal(wl.torch_to_bits(vp), vp_h), f"v pool, step {step}"
