@@ -185,9 +185,17 @@ int msg_version(void);
  * Workspace bytes needed by msg_plan and msg_paged_attention for batches of at
  * most max_reqs requests and max_total_q new tokens, with num_qo_heads query
  * heads of head_dim.  The workspace holds the status block, the plan (per
- * request lengths, decode partition, extend tile list, merge counters) and the
- * split-KV partial results.  Returns 0 on invalid arguments.  Any workspace of
- * at least this size serves every smaller batch.
+ * request lengths, decode partition, extend tile list and list of split
+ * extend items, merge counters) and the split-KV partial results, then
+ * ~42 MB of partial slots for the extend key split: an extend batch of fewer
+ * than 4 work items (query tile x KV head) per SM, whose items hold at least
+ * 8 key tiles of 128 keys per SM (e.g. a chunked-prefill tile over a long
+ * cached prefix), has its key tiles split evenly over every SM and the split
+ * items' partial results merged by a second kernel.  A workspace that holds
+ * everything but those slots is accepted too (the no-alloc entry point's
+ * scratch is one): such batches then take their items whole.  Returns 0 on
+ * invalid arguments.  Any workspace of at least this size serves every
+ * smaller batch.
  */
 size_t msg_workspace_size(int32_t max_reqs, int64_t max_total_q,
                           int32_t num_qo_heads, int32_t head_dim);

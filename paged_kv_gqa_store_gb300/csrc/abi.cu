@@ -114,6 +114,7 @@ int plan_impl(const KvIndex &kv, const int32_t *cached_len, const int32_t *exten
   pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
   pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
   pp.max_tiles = L.max_tiles;
+  pp.ext_items = reinterpret_cast<int32_t *>(ws + L.ext_items);
   int rc = from_cuda(launch_plan(pp, s));
   if (rc != MSG_OK) return rc;
   if (total_q > 0 && (out_loc_out || positions_out)) {
@@ -167,7 +168,7 @@ int msg_version(void) { return 100; }
 size_t msg_workspace_size(int32_t max_reqs, int64_t max_total_q, int32_t num_qo_heads,
                           int32_t head_dim) {
   if (max_reqs < 0 || max_total_q < 0 || num_qo_heads <= 0 || head_dim <= 0) return 0;
-  return ws_layout(max_reqs, max_total_q, num_qo_heads, head_dim).total;
+  return ws_layout(max_reqs, max_total_q, num_qo_heads, head_dim).total_split;
 }
 
 size_t msg_paged_attention_workspace_size(int32_t max_reqs, int64_t max_total_q,
@@ -352,6 +353,7 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
     pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
     pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
     pp.max_tiles = L.max_tiles;
+    pp.ext_items = reinterpret_cast<int32_t *>(ws + L.ext_items);
     rc = from_cuda(launch_plan(pp, s));
     if (rc != MSG_OK) return rc;
   }
@@ -391,6 +393,11 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
   ap.ext_tiles = reinterpret_cast<const int32_t *>(ws + L.ext_tiles);
   ap.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
   ap.part_o = reinterpret_cast<float *>(ws + L.part_o);
+  if (workspace_bytes >= L.total_split) {     // room for the extend key split
+    ap.ext_items = reinterpret_cast<int32_t *>(ws + L.ext_items);
+    ap.ext_lse = reinterpret_cast<float *>(ws + L.ext_lse);
+    ap.ext_o = reinterpret_cast<float *>(ws + L.ext_o);
+  }
 
   if (!(flags & MSG_ATTN_EXTEND_ONLY)) {
     int64_t grid = (int64_t)device_sm_count() * decode_ctas_per_sm(num_kv_heads);
@@ -409,7 +416,7 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + L.header);
     rc = from_cuda(cudaMemsetAsync(&hdr->ext_next, 0, sizeof(int32_t), s));
     if (rc != MSG_OK) return rc;
-    rc = from_cuda(launch_extend(ap, L.max_tiles, s));
+    rc = from_cuda(launch_extend(ap, L.max_tiles, max_kv_len, s));
     if (rc != MSG_OK) return rc;
   }
   return MSG_OK;

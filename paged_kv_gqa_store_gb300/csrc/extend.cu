@@ -62,8 +62,15 @@ constexpr int kSlots = 5;
 constexpr int kOffQ = 0;
 constexpr int kOffRing = 2 * kQSub;
 constexpr int kOffBar = kOffRing + kSlots * kSlot;
-constexpr int kBarBytes = 512;               // mbarriers, item queue, TMEM address, abort flag
-constexpr size_t kSmem = (size_t)kOffBar + kBarBytes + 1024;   // + slack for 1 KiB alignment
+constexpr int kBarBytes = 512;               // mbarriers, TMEM address, abort flag
+constexpr int kItemQueue = 16;                // work pieces published ahead of the slowest role
+// key split (few work items): the tiles' key-tile prefix, then the piece queue
+constexpr int kOffPre = kOffBar + kBarBytes;
+constexpr int kOffQueue = kOffPre + (kExtMaxTiles + 4) * 4;
+constexpr int kOffGrab = kOffQueue + kItemQueue * 16;   // the grabber's state (GrabState)
+constexpr size_t kSmem = (size_t)kOffGrab + 64 + 1024;   // + 1 KiB alignment slack
+static_assert(kSmem <= 232448, "227 KiB of shared memory per CTA");
+static_assert(kBN == kExtendTileTokens, "the plan counts key tiles of kExtendTileTokens keys");
 constexpr uint32_t kTmemCols = 512;           // S_a | S_b | O_a | O_b
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale O when max grows > 2^8
@@ -73,7 +80,7 @@ enum {
   kBarQFull = 0, kBarQFree = 1, kBarFull = 2, kBarEmpty = 7, kBarSFull = 12, kBarPReady = 14,
   kBarODone = 18, kBarOFree = 20, kBarEpi = 22, kBarFinal = 23, kBarItem = 24, kNumBars = 40
 };  // kBarPReady + 2 x: P of sub-tile x written (kBarPReady + 2 x + 1 unused)
-constexpr int kItemQueue = 16;                // work items published ahead of the slowest role
+static_assert(kBarItem + kItemQueue <= kNumBars, "one mbarrier per queue entry");
 
 // ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
@@ -261,11 +268,103 @@ __device__ __forceinline__ Item load_item(const AttnParams &p, int w) {
   return it;
 }
 
+// A piece of work: key tiles [j0, j1) of item w (j1 < 0: to the item's end).
+// meta, for a piece that is not the whole item: the first and the last CTA
+// holding a piece of the item (bits 0-14, 15-29), whether the first CTA's
+// piece is its second piece (bit 30), and bit 31 set.
+struct Piece {
+  int32_t w, j0, j1;
+  uint32_t meta;
+};
+
+// Key split of a batch with few items (< 4 per CTA, at least 8 key tiles per
+// CTA): the items, ordered KV head by KV head and within a head in the plan's
+// tile order (so that neighbouring CTAs read the same K/V), laid end to end
+// as units of one key tile; CTA c takes units [B(c), B(c+1)).  A boundary
+// inside an item moves down (by at most one unit) so that both sub-tiles keep
+// a key tile on each side.  pre[t] = first unit of tile t within a head, bit
+// 31 set when sub-tile a needs one key tile fewer than sub-tile b.
+struct Split {
+  const int32_t *pre;
+  int32_t tiles, heads, G;
+  int64_t wt, w;                 // units per head, in all
+  __device__ int32_t start(int t) const { return pre[t] & 0x7fffffff; }
+  // largest tile t whose first unit is <= u (u within a head's units)
+  __device__ int tile_of(int64_t u) const {
+    int lo = 0, hi = tiles;        // start(lo) <= u < start(hi)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (start(mid) <= u) lo = mid; else hi = mid;
+    }
+    return lo;
+  }
+  __device__ int64_t snap(int64_t u) const {
+    if (u <= 0 || u >= w) return u <= 0 ? 0 : w;
+    const int64_t gh = u / wt, lu = u - gh * wt;
+    const int t = tile_of(lu);
+    const int64_t j = lu - start(t);
+    if (j == 0) return u;
+    const int64_t n = start(t + 1) - start(t), na = n - (pre[t] < 0 ? 1 : 0);
+    int64_t jj = j < na - 1 ? j : na - 1;
+    if (jj < 0) jj = 0;
+    return u - j + jj;
+  }
+  __device__ int64_t bound(int64_t b) const { return snap(b * w / G); }
+  // the CTA whose range holds unit v
+  __device__ int cta_of(int64_t v) const {
+    int64_t b = ((v + 1) * G - 1) / w;
+    if (b > G - 1) b = G - 1;
+    if (b + 1 < G && bound(b + 1) <= v) ++b;
+    return (int)b;
+  }
+};
+// The grabber's state, in shared memory (kept out of the roles' registers).
+struct GrabState {
+  Split sp;
+  int64_t su, su_end;               // its position in this CTA's range
+  int32_t split;                    // key split (else the global counter)
+};
+static_assert(sizeof(GrabState) <= 64, "grabber state block");
+
+// Next piece of CTA c's split range; a split item is also entered in the list
+// (by its first piece, under that piece's slot) for the merge kernel.
+__device__ Piece next_split_piece(GrabState *gs, int c, int32_t *ext_items) {
+  const Split &sp = gs->sp;
+  if (gs->su >= gs->su_end) return Piece{-1, 0, 0, 0u};
+  const int64_t su = gs->su;
+  const int64_t gh = su / sp.wt, lu = su - gh * sp.wt;
+  const int t = sp.tile_of(lu);
+  const int64_t first = gh * sp.wt + sp.start(t);
+  const int64_t n = sp.start(t + 1) - sp.start(t);
+  const int32_t j0 = (int32_t)(su - first);
+  const int32_t j1 = (int32_t)(n < j0 + (gs->su_end - su) ? n : j0 + (gs->su_end - su));
+  const int32_t w = (int32_t)(t * sp.heads + gh);
+  uint32_t meta = 0;
+  if (j0 != 0 || j1 != n) {
+    const int cf = sp.cta_of(first), cl = sp.cta_of(first + n - 1);
+    const int hs = first > sp.bound(cf) ? 1 : 0;
+    meta = (uint32_t)cf | ((uint32_t)cl << 15) | ((uint32_t)hs << 30) | (1u << 31);
+    if (c == cf && 2 * cf + hs < kExtSlots) {
+      int32_t *e = ext_items + 4 * (2 * cf + hs);
+      e[1] = cf;
+      e[2] = cl;
+      e[3] = hs;
+      e[0] = w;
+    }
+  }
+  gs->su = su + (j1 - j0);
+  return Piece{w, j0, j1, meta};
+}
+
 // Persistent: each CTA takes work items of the plan's extend tile list x KV
-// heads (heaviest tiles first) from a global counter until none is left.  TMEM,
+// heads (heaviest tiles first) from a global counter until none is left, or,
+// for a batch with few items, its own range of the key split above.  TMEM,
 // the mbarriers and the K/V ring live across items; every role counts tiles,
 // ring items and items globally, so the phases line up without any CTA-wide
 // sync.
+// kSplit: the instance that may take the key split (the host launches it only
+// for a batch that may have few items); the other is the plain work queue.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     extend_kernel(const __grid_constant__ ExtParams ep, const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
@@ -279,37 +378,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + kNumBars * 8);
   volatile int32_t *abort_flag =
       reinterpret_cast<volatile int32_t *>(smem + kOffBar + kNumBars * 8 + 8);
-  volatile int32_t *item_q =
-      reinterpret_cast<volatile int32_t *>(smem + kOffBar + kNumBars * 8 + 16);
+  volatile int32_t *piece_q = reinterpret_cast<volatile int32_t *>(smem + kOffQueue);
+  int32_t *tile_pre = reinterpret_cast<int32_t *>(smem + kOffPre);
+  GrabState *gs = reinterpret_cast<GrabState *>(smem + kOffGrab);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   grid_dep_wait();      // (launched without early start; kept for any launch path)
   grid_dep_launch();
   const PlanHeader hdr = *p.hdr;
   int32_t *next_ctr = const_cast<int32_t *>(&p.hdr->ext_next);
-  // k-th work item of this CTA: grabbed from the global counter by the producer
-  // warp 1 (lane 0) just before it starts loading it, published through a
-  // 16-entry queue; every role reads the same sequence.  -1 = no more work.
-  auto fetch_item = [&](uint32_t k, bool grab, bool whole_warp) -> int {
+  const int items = hdr.ext_tile_count * p.num_kv_heads;
+  const int G = (int)gridDim.x;
+  const int64_t units = hdr.ext_units * p.num_kv_heads;
+  // the key split, for a batch with few items and enough key tiles
+  const bool split = kSplit && p.ext_o != nullptr && hdr.ext_split_ready != 0 && G <= kExtMaxCtas &&
+                     hdr.ext_tile_count <= kExtMaxTiles && items <= kExtMaxItems &&
+                     items < 4 * G && units >= 8 * (int64_t)G && units < (1ll << 30);
+  // k-th piece of this CTA: taken by the producer warp 1 (lane 0) just before
+  // it starts loading it (from the global counter, or the next piece of this
+  // CTA's split range), published through a 16-entry queue; every role reads
+  // the same sequence.  w = -1: no more work.
+  auto fetch_piece = [&](uint32_t k, bool grab, bool whole_warp) -> Piece {
     const int e = (int)(k % kItemQueue);
     if (grab) {
-      int w = atomicAdd(next_ctr, 1);
-      if (w >= hdr.ext_tile_count * p.num_kv_heads) w = -1;
-      item_q[e] = w;
+      Piece pc{-1, 0, -1, 0u};
+      if (kSplit && gs->split) {
+        pc = next_split_piece(gs, (int)blockIdx.x, p.ext_items);
+      } else {
+        pc.w = atomicAdd(next_ctr, 1);
+        if (pc.w >= hdr.ext_tile_count * p.num_kv_heads) pc.w = -1;
+      }
+      piece_q[4 * e] = pc.w;
+      if (kSplit) {
+        piece_q[4 * e + 1] = pc.j0;
+        piece_q[4 * e + 2] = pc.j1;
+        piece_q[4 * e + 3] = (int32_t)pc.meta;
+      }
       mbar_arrive(&bars[kBarItem + e]);
     }
     if (whole_warp) __syncwarp();
     if (!mbar_wait(&bars[kBarItem + e], (k / kItemQueue) & 1)) {
       *abort_flag = 1;
       report(p.status, MSG_DEV_TIMEOUT, -1, -3);
-      return -1;
+      return Piece{-1, 0, 0, 0u};
     }
-    return item_q[e];
+    if (!kSplit) return Piece{piece_q[4 * e], 0, -1, 0u};   // whole items
+    return Piece{piece_q[4 * e], piece_q[4 * e + 1], piece_q[4 * e + 2],
+                 (uint32_t)piece_q[4 * e + 3]};
   };
   if (blockIdx.x == 0 && tid == 0 && (p.flags & MSG_ATTN_EXTEND_ONLY) && hdr.dec_count > 0)
     report(p.status, MSG_DEV_WRONG_PHASE, hdr.dec_count, hdr.dec_keys);
-  const int items = hdr.ext_tile_count * p.num_kv_heads;
-  if ((int)blockIdx.x >= items) return;
+  if (!split && (int)blockIdx.x >= items) return;
 
   if (tid == 0) {
     mbar_init(&bars[kBarQFull], 1);
@@ -327,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarEpi], 8);
     mbar_init(&bars[kBarFinal], 1);
     for (int e = 0; e < kItemQueue; ++e) mbar_init(&bars[kBarItem + e], 1);
+    gs->split = split ? 1 : 0;
+    gs->su = gs->su_end = 0;
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -346,12 +467,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = u >> 5, kg4 = u & 31;
     const int n_units = (64 - (warp - 1) + 2) / 3;     // units of this warp: 22, 21, 21
     const int oob = ep.kv_rows_total;                   // a row past the map: zero fill
+    if (kSplit && split && warp == 1) {
+      // the tiles' key-tile prefix (and sub-tile a's one tile fewer), then this
+      // CTA's range; only the grabber (lane 0) uses them
+      int64_t carry = 0;
+      for (int base = 0; base < hdr.ext_tile_count; base += 32) {
+        const int t = base + lane;
+        int32_t n = 0, short_a = 0;
+        if (t < hdr.ext_tile_count) {
+          const Item ti = load_item(p, t * p.num_kv_heads);
+          n = ti.n_tiles;
+          short_a = ti.n_a < ti.n_tiles ? 1 : 0;
+        }
+        int32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (t < hdr.ext_tile_count)
+          tile_pre[t] = (int32_t)(carry + incl - n) | (short_a ? (int32_t)0x80000000u : 0);
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncwarp();                                  // every lane's entries, for lane 0
+      if (lane == 0) {
+        tile_pre[hdr.ext_tile_count] = (int32_t)carry;
+        Split &sp = gs->sp;
+        sp.pre = tile_pre;
+        sp.tiles = hdr.ext_tile_count;
+        sp.heads = p.num_kv_heads;
+        sp.G = G;
+        sp.wt = carry;
+        sp.w = carry * p.num_kv_heads;
+        if (sp.w > 0) {
+          gs->su = sp.bound(blockIdx.x);
+          gs->su_end = sp.bound((int64_t)blockIdx.x + 1);
+        }
+      }
+      __syncwarp();
+    }
     uint32_t N = 0;                                     // ring items issued
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
-      const int w = fetch_item(k, warp == 1 && lane == 0, true);
-      if (w < 0) break;
-      const Item it = load_item(p, w);
+      const Piece pc = fetch_piece(k, warp == 1 && lane == 0, true);
+      if (pc.w < 0) break;
+      const Item it = load_item(p, pc.w);
+      const int j0 = pc.j0, j1 = pc.j1 < 0 ? it.n_tiles : pc.j1;
+      const int na = (j1 < it.n_a ? j1 : it.n_a) - j0;
+      if (j1 <= j0 || na <= 0) continue;
       const int32_t *row_ptr = kv_row(p.kv, it.r);
       // The tile loop, compiled once for page_size 1 (the entry is the slot in
       // every index form) and once for larger pages, so that the common case
@@ -371,9 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
         int32_t cur[4], nxt[4], nxt2[4];
-        read_pt(0, cur);
-        read_pt(1, nxt);
-        for (int j = 0; ok && j < it.n_tiles; ++j) {
+        read_pt(j0, cur);
+        read_pt(j0 + 1, nxt);
+        for (int j = j0; ok && j < j1; ++j) {
           read_pt(j + 2, nxt2);
           // gather rows of this lane's 4 keys; an invalid entry (reported once,
           // by the half-0 lane) reads zeros
@@ -398,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
-            const uint32_t n = N + 2 * j + kv;
+            const uint32_t n = N + 2 * (j - j0) + kv;
             const int s = n % kSlots;
             if (n >= (uint32_t)kSlots && !mbar_wait(&bars[kBarEmpty + s], ((n / kSlots) & 1) ^ 1)) {
               if (lane == 0) {
@@ -422,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (p.page_size == 1) stream_item(std::true_type{});
       else stream_item(std::false_type{});
-      N += 2u * it.n_tiles;
+      N += 2u * (uint32_t)(j1 - j0);
     }
     // drain: every issued ring item must have landed before the CTA can exit
     for (uint32_t n = N > (uint32_t)kSlots ? N - kSlots : 0; n < N; ++n)
@@ -442,11 +605,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t Ts[2] = {0, 0}, N = 0, V = 0;       // tiles per sub-tile, ring items, items done
       bool ok = true;
       for (uint32_t k = 0; ok; ++k) {
-        const int w = fetch_item(k, false, false);   // lane 0 alone
-        if (w < 0) break;
-        const Item it = load_item(p, w);
-        const int n = it.n_tiles;
-        if (n == 0) continue;
+        const Piece pc = fetch_piece(k, false, false);   // lane 0 alone
+        if (pc.w < 0) break;
+        const Item it = load_item(p, pc.w);
+        const int j1 = pc.j1 < 0 ? it.n_tiles : pc.j1;
+        const int n = j1 - pc.j0;                        // key tiles of sub-tile b
+        const int na = (j1 < it.n_a ? j1 : it.n_a) - pc.j0;   // of sub-tile a
+        if (n <= 0 || na <= 0) continue;
         // Q of this item, once the previous item's Q.K^T products are done
         if (V > 0 && !mbar_wait(&bars[kBarQFree], (V - 1) & 1)) {
           ok = false;
@@ -467,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t nk = N + 2 * j, nv = N + 2 * j - 1;   // ring items K_j and V_{j-1}
           bool k_ready = false, v_ready = false;
           for (int x = 0; x < 2 && ok; ++x) {
-            const int nx = x ? n : it.n_a;             // tiles this sub-tile uses
+            const int nx = x ? n : na;                 // tiles this sub-tile uses
             if (j >= 1 && j - 1 < nx) {
               // O_x += P_x(j-1) . V_{j-1}, P as the pair hi + lo
               if ((x == 0 && aborted(abort_flag)) ||
@@ -517,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        Ts[0] += (uint32_t)it.n_a;
+        Ts[0] += (uint32_t)na;
         Ts[1] += (uint32_t)n;
         N += 2u * (uint32_t)n;
         V += 1;
@@ -549,17 +714,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t T = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
-    const int w = fetch_item(k, false, true);
-    if (w < 0) break;
-    const Item it = load_item(p, w);
+    const Piece pc = fetch_piece(k, false, true);
+    if (pc.w < 0) break;
+    const Item it = load_item(p, pc.w);
     if (it.n_tiles == 0) {
       if (x == 0 && row == 0 && !it.ok) report(p.status, MSG_DEV_BAD_LENGTHS, it.r, it.qrow0);
       continue;
     }
+    const int j0 = pc.j0, j1 = pc.j1 < 0 ? it.n_tiles : pc.j1;
+    const int na = (j1 < it.n_a ? j1 : it.n_a) - j0;
+    if (j1 <= j0 || na <= 0) continue;
     const int64_t pos = it.cached + it.q0 + tsub;   // this row's absolute position
     const int64_t min_pos = it.cached + it.q0 + x * kSubTok;
-    const int nx = x ? it.n_tiles : it.n_a;          // key tiles this sub-tile uses
-    float m = -INFINITY;
+    const int nx = x ? j1 - j0 : na;                 // key tiles this sub-tile uses
+    float m = -INFINITY;                             // (stays so while every key seen is masked,
+                                                     // possible in a piece that starts late)
     float2 la = make_float2(0.f, 0.f), lb = la;      // independent partial sums
     for (int j = 0; j < nx; ++j) {
       if (aborted(abort_flag) || !mbar_wait(&bars[kBarSFull + x], (T + j) & 1)) {
@@ -567,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int64_t kbase = (int64_t)j * kBN;
+      const int64_t kbase = (int64_t)(j0 + j) * kBN;
       const bool need_mask = kbase + kBN - 1 > min_pos;
       // keys i of the tile with i > lim are masked (only on diagonal tiles)
       const int lim = need_mask ? (int)imin64(pos - kbase, kBN) : kBN;
@@ -591,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mm[i & 3] = fmaxf(mm[i & 3], __uint_as_float(v[i >> 5][i & 31]));
       const float mx = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])) * sl2;
       if (j == 0) {
-        m = mx;
+        m = fmaxf(mx, -1e30f);   // finite even when every key of the tile is masked
       } else if (mx > m + kRescaleThreshold) {
         // O_x holds tiles < j (their P.V completed before this S): rescale in place
         if (!mbar_wait(&bars[kBarODone + x], (T + j - 1) & 1)) {
@@ -653,15 +822,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
     const float2 lsum2 = fadd2(la, lb);
-    const float inv = 1.f / (lsum2.x + lsum2.y);
+    const float lsum = lsum2.x + lsum2.y;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     uint16_t *op = p.out + (it.qrow0 + tsub) * (int64_t)p.num_qo_heads * kHeadDim +
                    (2 * it.gh + hh) * kHeadDim;
+    const bool part = kSplit && (pc.meta >> 31) != 0;   // one piece of a split item
+    const int cf = (int)(pc.meta & 0x7fffu), hs = (int)((pc.meta >> 30) & 1u);
+    // a piece's slot: 2 c for a CTA's first piece, 2 c + 1 for its last
+    const int slot = 2 * (int)blockIdx.x + ((int)blockIdx.x == cf ? hs : 0);
+    const int64_t prow = ((int64_t)slot * 2 + x) * 128 + row;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
       tmem_ld32(o_col + 32u * c, o);
       tmem_wait_ld();
-      if (tsub < it.nq) {
+      if (tsub < it.nq && !part) {
 #pragma unroll
         for (int i = 0; i < 32; i += 8) {
           uint4 q4;
@@ -671,12 +846,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           q4.w = pack_bf16(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv);
           *reinterpret_cast<uint4 *>(op + 32 * c + i) = q4;
         }
+      } else if (tsub < it.nq) {
+        // the piece's normalised rows in fp32, for the merge kernel
+        float4 *po = reinterpret_cast<float4 *>(p.ext_o + prow * kHeadDim + 32 * c);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          po[i / 4] = make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                                  __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
       }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kBarOFree + x]);
     T += (uint32_t)nx;
+    // lse of a piece's rows (log2 units; -inf for a row none of whose keys
+    // the piece holds), for the merge kernel
+    if (part && tsub < it.nq) p.ext_lse[prow] = lsum > 0.f ? m + log2f(lsum) : -INFINITY;
   }
   if (!ok && lane == 0) {
     *abort_flag = 1;
@@ -685,6 +870,93 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&bars[kBarEpi]);
+}
+
+// ---------------------------------------------------------------- split merge
+// One CTA per entry of the split-item list (the extend kernel's grabbers
+// enter each split item once: the item, the first and the last CTA holding a
+// piece of it, and whether the first CTA's piece is its second one):
+// o = sum_k 2^(lse_k - L) o_k / sum_k 2^(lse_k - L) over the pieces in order,
+// written as bf16 rows.  Warp v merges 32 rows of sub-tile v / 4 (consecutive
+// tokens of one query head); lane l holds dims 4 l .. 4 l + 3, so every load
+// and store covers whole rows, and 8 rows' loads of up to 4 pieces are in
+// flight at once.  The entry is cleared for the next call.
+constexpr int kMergeThreads = 256;
+constexpr int kMergePieces = 4;
+__global__ void __launch_bounds__(kMergeThreads) ext_merge_kernel(AttnParams p) {
+  grid_dep_wait();                      // the extend kernel's partials and list
+  grid_dep_launch();
+  int32_t *e = p.ext_items + 4 * blockIdx.x;
+  const int w = __ldcg(e);
+  if (w < 0) return;
+  const int cf = __ldcg(e + 1), cl = __ldcg(e + 2), hs = __ldcg(e + 3);
+  // an entry the extend kernel of this grid cannot have made is reported, not used
+  const int G = (int)gridDim.x / 2;
+  if (w >= p.hdr->ext_tile_count * p.num_kv_heads || cf < 0 || cl < cf || cl >= G ||
+      (hs != 0 && hs != 1)) {
+    if (threadIdx.x == 0) report(p.status, MSG_DEV_BAD_LENGTHS, w, (int64_t)cf * 65536 + cl);
+    return;
+  }
+  const Item it = load_item(p, w);
+  if (!it.ok) return;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int x = warp / 4, r0 = (warp % 4) * 32, tsub0 = x * kSubTok + r0 % kSubTok;
+  int rows_valid = it.nq - tsub0;
+  rows_valid = rows_valid < 0 ? 0 : rows_valid > 32 ? 32 : rows_valid;
+  const int np = cl - cf + 1;
+  auto row_of = [&](int k, int r) {     // partial row of piece k, row r0 + r of sub-tile x
+    return ((int64_t)(2 * (cf + k) + (k == 0 ? hs : 0)) * 2 + x) * 128 + r0 + r;
+  };
+  const int64_t ors = (int64_t)p.num_qo_heads * kHeadDim;
+  uint16_t *out = p.out + (it.qrow0 + tsub0) * ors + (2 * it.gh + r0 / kSubTok) * kHeadDim;
+  // lane r: row r0 + r's largest lse and the weights' sum
+  float L = -INFINITY;
+  for (int k = 0; k < np; ++k) L = fmaxf(L, __ldcg(p.ext_lse + row_of(k, lane)));
+  float den = 0.f;
+  for (int k = 0; k < np; ++k) den += exp2f(__ldcg(p.ext_lse + row_of(k, lane)) - L);
+  for (int r = 0; r < rows_valid; r += 8) {
+    float4 acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < np; k0 += kMergePieces) {
+      float4 v[kMergePieces][8];
+      float wl[kMergePieces];
+#pragma unroll
+      for (int kk = 0; kk < kMergePieces; ++kk) {
+        wl[kk] = 0.f;
+        if (k0 + kk < np) {
+          wl[kk] = exp2f(__ldcg(p.ext_lse + row_of(k0 + kk, lane)) - L);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            v[kk][i] = r + i < rows_valid
+                           ? __ldcg(reinterpret_cast<const float4 *>(
+                                        p.ext_o + row_of(k0 + kk, r + i) * kHeadDim) + lane)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kMergePieces; ++kk) {
+        if (k0 + kk >= np) break;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float wk = __shfl_sync(0xffffffffu, wl[kk], (r + i) & 31);
+          acc[i].x = fmaf(wk, v[kk][i].x, acc[i].x);
+          acc[i].y = fmaf(wk, v[kk][i].y, acc[i].y);
+          acc[i].z = fmaf(wk, v[kk][i].z, acc[i].z);
+          acc[i].w = fmaf(wk, v[kk][i].w, acc[i].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float rd = 1.f / __shfl_sync(0xffffffffu, den, (r + i) & 31);
+      if (r + i < rows_valid)
+        *reinterpret_cast<uint2 *>(out + (int64_t)(r + i) * ors + 4 * lane) = make_uint2(
+            pack_bf16(acc[i].x * rd, acc[i].y * rd), pack_bf16(acc[i].z * rd, acc[i].w * rd));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) e[0] = -1;      // cleared for the next call
 }
 
 // ---------------------------------------------------------------- host side
@@ -727,7 +999,8 @@ bool encode_q(CUtensorMap *m, const void *q, int32_t hq, int64_t total_q, int64_
 
 }  // namespace
 
-cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s) {
+cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, int64_t max_kv_len,
+                          cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
   if (encode_fn() == nullptr) return cudaErrorNotSupported;
   static bool attr_set[64] = {};
@@ -736,8 +1009,10 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
-    if (e != cudaSuccess) return e;
+    for (auto k : {extend_kernel<false>, extend_kernel<true>}) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+      if (e != cudaSuccess) return e;
+    }
     attr_set[dev] = true;
   }
   ExtParams ep{};
@@ -752,11 +1027,27 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s
   if (!encode_q(&mq, p.q, p.num_qo_heads, p.total_q, p.q_stride) ||
       !encode_rows(&mk, p.k_pool, rows) || !encode_rows(&mv, p.v_pool, rows))
     return cudaErrorInvalidValue;
-  // persistent: one CTA per SM (the kernel's shared memory allows no more)
+  // persistent: one CTA per SM (the kernel's shared memory allows no more).
+  // The instance that may take the key split, with a CTA on every SM, only
+  // where the batch may have few items: its partial slots are there, fewer
+  // than 4 items per CTA are possible (every extend token but one per
+  // request sits in a 128-token tile, so at least H (total_q - num_reqs) /
+  // 128 items), and, with max_kv_len given, 8 key tiles per CTA are.
   int64_t grid = (int64_t)device_sm_count();
-  if (grid > max_tiles * p.num_kv_heads) grid = max_tiles * p.num_kv_heads;
-  extend_kernel<<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
-  return cudaGetLastError();
+  const int64_t items = max_tiles * p.num_kv_heads;
+  const int64_t items_lo = (int64_t)p.num_kv_heads * ((p.total_q - p.num_reqs) / kBN);
+  bool may_split = p.ext_o != nullptr && grid <= kExtMaxCtas && items_lo < 4 * grid;
+  if (may_split && max_kv_len > 0 && items * ((max_kv_len + kBN - 1) / kBN) < 8 * grid)
+    may_split = false;
+  if (!may_split && grid > items) grid = items;
+  if (may_split)
+    extend_kernel<true><<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
+  else
+    extend_kernel<false><<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !may_split) return e;
+  // the split items' merge: one CTA per partial slot of this grid
+  return launch_k(ext_merge_kernel, dim3(2 * (unsigned)grid), dim3(kMergeThreads), 0, s, true, p);
 }
 
 }  // namespace msg

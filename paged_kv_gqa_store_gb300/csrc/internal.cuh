@@ -32,6 +32,13 @@ inline int64_t max_decode_ctas(int64_t hq) {
                                              : kMaxDecodeCtas;
 }
 constexpr int kExtendTileTokens = 128;    // query tokens per extend tile
+// Extend batches with few work items split them along the keys over the CTAs
+// (see extend.cu): partial slots for up to kExtMaxCtas CTAs, a tile prefix of
+// up to kExtMaxTiles tiles, a list of the split items (one entry per slot).
+constexpr int kExtMaxCtas = 160;
+constexpr int kExtMaxItems = 4 * kExtMaxCtas;
+constexpr int kExtMaxTiles = 256;
+constexpr int kExtSlots = 2 * kExtMaxCtas;
 constexpr int kPlanThreads = 1024;
 
 // Bound of every mbarrier wait (2 s, far beyond any legitimate wait); on expiry
@@ -56,7 +63,12 @@ struct WsLayout {
   size_t part_lse = 0;     // float[2 * max_decode_ctas(Hq) * Hq]
   size_t part_o = 0;       // float[2 * max_decode_ctas(Hq) * Hq * D]
   size_t plan_end = 0;     // bytes used by the plan part
-  size_t total = 0;
+  size_t total = 0;        // bytes a call needs
+  // optional: the extend key split (used when the workspace holds it)
+  size_t ext_items = 0;    // int32x4[kExtSlots]  split items (item, first CTA, last CTA, shift)
+  size_t ext_lse = 0;      // float[2 * kExtMaxCtas][2][128]
+  size_t ext_o = 0;        // float[2 * kExtMaxCtas][2][128][128]
+  size_t total_split = 0;  // bytes with the extend key split (msg_workspace_size)
   int64_t max_tiles = 0;
 };
 
@@ -68,7 +80,8 @@ struct PlanHeader {
   int64_t dec_keys;        // sum of decode kv lengths + a gap (kDecSegPad) per request
   int64_t total_q;         // sum of extend lengths
   int32_t ext_next;        // extend work-item counter (zeroed before each extend launch)
-  int32_t pad;
+  int32_t ext_split_ready; // the plan cleared the list of split extend items
+  int64_t ext_units;       // key tiles over the extend tiles (128 keys each, per KV head)
 };
 
 inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t d) {
@@ -85,10 +98,14 @@ inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t
   L.counters = take(sizeof(int32_t) * (num_reqs + 1) * kMaxKvHeads);
   L.max_tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + num_reqs + 1;
   L.ext_tiles = take(sizeof(int32_t) * 2 * L.max_tiles);
+  L.ext_items = take(sizeof(int32_t) * 4 * kExtSlots);   // (the plan clears it)
   L.plan_end = off;
   L.part_lse = take(sizeof(float) * 2 * max_decode_ctas(hq) * hq);
   L.part_o = take(sizeof(float) * 2 * (size_t)max_decode_ctas(hq) * hq * d);
   L.total = off;
+  L.ext_lse = take(sizeof(float) * 2 * kExtMaxCtas * 2 * 128);
+  L.ext_o = take(sizeof(float) * (size_t)2 * kExtMaxCtas * 2 * 128 * kHeadDim);
+  L.total_split = off;
   return L;
 }
 
@@ -123,6 +140,7 @@ struct PlanParams {
   int32_t *counters;
   int32_t *ext_tiles;           // pairs
   int64_t max_tiles;
+  int32_t *ext_items;           // list of split extend items to clear
 };
 
 struct TokenMetaParams {
@@ -188,6 +206,10 @@ struct AttnParams {
   const int32_t *ext_tiles;
   float *part_lse;
   float *part_o;
+  // extend key split: the split items and their partial slots (null: not available)
+  int32_t *ext_items;
+  float *ext_lse;
+  float *ext_o;
   KvIndex kv;                   // where the keys' slots are found
 };
 
@@ -214,7 +236,8 @@ cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 cudaError_t launch_token_meta(const TokenMetaParams &p, cudaStream_t s);
 cudaError_t launch_store_kv(const StoreParams &p, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s);
-cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, cudaStream_t s);
+cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, int64_t max_kv_len,
+                          cudaStream_t s);
 int device_sm_count();
 int decode_ctas_per_sm(int num_kv_heads);
 

@@ -71,7 +71,9 @@ extern "C" int msg_paged_attention_noalloc(
       return MSG_ERR_CUDA;
     return MSG_OK;
   }
-  const size_t need = msg_workspace_size(num_reqs, total_q, num_qo_heads, head_dim);
+  // the part a call needs (the scratch leaves out the extend key split's
+  // partial slots: batches with few extend items take them whole here)
+  const size_t need = msg::ws_layout(num_reqs, total_q, num_qo_heads, head_dim).total;
   if (need == 0) return MSG_ERR_INVALID_ARG;
   if (need > (size_t)MSG_NOALLOC_SCRATCH_BYTES) return MSG_ERR_WORKSPACE;
   int dev = 0;

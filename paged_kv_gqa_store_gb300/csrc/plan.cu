@@ -80,9 +80,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   __shared__ int64_t warp_sums[32][4];
   __shared__ int64_t carry[4];     // qo, decode count, decode keys, extend tiles
   __shared__ int32_t ext_reqs;
+  __shared__ unsigned long long ext_units;
   const int tid = threadIdx.x;
   if (tid < 4) carry[tid] = 0;
-  if (tid == 0) ext_reqs = 0;
+  if (tid == 0) {
+    ext_reqs = 0;
+    ext_units = 0;
+  }
+  for (int c = tid; c < kExtSlots; c += kPlanThreads) p.ext_items[4 * c] = -1;
   __syncthreads();
 
   for (int32_t base = 0; base < p.num_reqs; base += kPlanThreads) {
@@ -119,12 +124,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       if (is_ext) {
         atomicAdd(&ext_reqs, 1);
         const int64_t t0 = carry[3] + ex.v[3];
+        unsigned long long units = 0;       // key tiles of the request's query tiles
         for (int64_t t = 0; t < ntiles; ++t) {
           if (t0 + t < p.max_tiles) {
+            const int32_t qt = (int32_t)(ntiles - 1 - t);
             p.ext_tiles[2 * (t0 + t)] = r;
-            p.ext_tiles[2 * (t0 + t) + 1] = (int32_t)(ntiles - 1 - t);
+            p.ext_tiles[2 * (t0 + t) + 1] = qt;
+            const int64_t q0 = (int64_t)qt * kExtendTileTokens;
+            const int64_t kv_end = c + q0 + (e - q0 < kExtendTileTokens ? e - q0 : kExtendTileTokens);
+            units += (unsigned long long)((kv_end + kExtendTileTokens - 1) / kExtendTileTokens);
           }
         }
+        atomicAdd(&ext_units, units);
       }
     }
     __syncthreads();
@@ -145,6 +156,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     p.hdr->ext_tile_count = (int32_t)(carry[3] < p.max_tiles ? carry[3] : p.max_tiles);
     p.hdr->ext_count = ext_reqs;
     p.hdr->total_q = total;
+    p.hdr->ext_units = (int64_t)ext_units;
+    p.hdr->ext_split_ready = 1;
   }
 }
 
