@@ -240,12 +240,11 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
     // a range is longer than a gap, and the last request's gap ends the space)
     if (sg.lo >= sg.hi && i + 1 < nd) sg = load_seg(p, ++i, begin, end, b, K, g);
     int64_t kt = sg.lo;                        // flattened key index of the tile
-    // index entries of the first segment's first kStages tiles, one per lane,
-    // loaded at once (the first tiles then issue back to back)
-    const int64_t pre_end = imin64(sg.hi, sg.lo + kStages * kTileKeys);
-    int32_t pre = 0;
-    if (sg.lo + lane < pre_end) pre = load_raw<kPage1>(p, sg.row, sg.lo + lane - sg.S);
     int32_t raw = 0;
+    {
+      const int64_t n0 = imin64(kTileKeys, sg.hi - kt);
+      if (lane < n0) raw = load_raw<kPage1>(p, sg.row, kt - sg.S + lane);
+    }
     // Everything above reads only the plan and the KV index.  q and the step's
     // new rows are read after the preceding kernel.  With the new rows given
     // (kFused) the first ring stages of older pool rows are gathered before
@@ -273,12 +272,9 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
       }
       __syncwarp();
     };
-    static_assert(kStages * kTileKeys <= 32, "one index entry per lane");
     uint32_t it = 0, issued = 0;
     bool ok = true;
     while (true) {
-      if (kt < pre_end)   // one of the first segment's first tiles (later segments start past it)
-        raw = __shfl_sync(0xffffffffu, pre, (int)(kt - sg.lo) + (lane & (kTileKeys - 1)));
       const int nkeys = (int)imin64(kTileKeys, sg.hi - kt);
       const bool first = (kt == sg.lo);
       const bool last = (kt + nkeys == sg.hi);
@@ -301,10 +297,10 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
         // wait first for a tile with a new row (the segment's last, when it
         // ends the request), one that would report, or the first to reuse a
         // stage (the consumers that free it wait too)
-        bool need = it >= (uint32_t)kStages || (last && sg.hi == sg.E) || sg.qrow < 0;
-        if (!need)   // (the index entries are only waited for when nothing else decides)
-          need = __any_sync(0xffffffffu, lane < nkeys && !raw_ok<kPage1>(p, raw, kt - sg.S + lane));
-        if (need) wait_preceding(issued);
+        const bool bad = lane < nkeys && !raw_ok<kPage1>(p, raw, kt - sg.S + lane);
+        if (__any_sync(0xffffffffu, bad) || it >= (uint32_t)kStages || (last && sg.hi == sg.E) ||
+            sg.qrow < 0)
+          wait_preceding(issued);
       }
       if (ok && it >= (uint32_t)kStages && !mbar_wait(&empty[st], ((it / kStages) & 1) ^ 1)) {
         ok = false;
