@@ -20,6 +20,8 @@ Also printed, in the same JSON line:
   large_decode  -- 256 decode requests, page_size 16, pools at 90% of free HBM;
   long_mixed    -- 32 long decodes + 2 extends (page_size 64): each part alone and
                    the mixed call against the max() and sum() of the two bounds;
+  chunked_prefill -- one 128-token tile over a 32,768-token prefix (8 work items):
+                   the extend key split over every SM vs items taken whole;
   prologue      -- fused q/k RMSNorm + RoPE + store_kv over the extend batch's tokens;
   cpu_baseline  -- the fp64 oracle on the host cores, on a bounded sample.
 
@@ -354,6 +356,7 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
     small = run_graph_decode(args, dev, msg) if rank == 0 and not args.no_extend else None
     large = run_large_decode(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     mixed = run_long_mixed(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
+    chunk = run_chunked_prefill(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     prologue = run_prologue(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     sampler = run_sampler(args, dev, msg, peaks) if rank == 0 and not args.no_extend else None
     cpu = cpu_baseline(spec) if want_cpu else None
@@ -401,6 +404,8 @@ def finish_line(args, rank, world, spec, peaks, value, ms, achieved, attn_ms, by
         line["large_decode"] = large
     if mixed is not None:
         line["long_mixed"] = mixed
+    if chunk is not None:
+        line["chunked_prefill"] = chunk
     if prologue is not None:
         line["prologue"] = prologue
     if sampler is not None:
@@ -889,6 +894,40 @@ def run_long_mixed(args, dev, msg, peaks):
             "decode_bytes": dec_bytes, "extend_flops": fl,
             "l2": "flushed (256 MB write) before every timed launch"}
 
+def run_chunked_prefill(args, dev, msg, peaks):
+    """A chunked-prefill step: one request's next 128 tokens over a 32,768-token
+    cached prefix (page_size 1): 8 work items (one query tile x 8 KV heads) of
+    257 key tiles each.  Timed with the workspace the library asks for (the key
+    split spreads the items' key tiles over every SM) and with one too small
+    for the split's partial slots (the 8 items taken whole, by 8 CTAs)."""
+    import torch
+    torch.cuda.empty_cache()
+    cached, ext = np.array([32768]), np.array([128])
+    spec = wl.make_batch("chunked_prefill", 1009, cached, ext, 1,
+                         num_pages=int(cached[0] + ext[0]) + 9)
+    t = wl.device_tensors(spec, device=dev, canary=False)
+    b = _planned_batch(spec, dev, msg)
+    msg.msg_store_kv(t["k_new"], t["v_new"], t["k_pool"], t["v_pool"], b["loc"])
+    out = torch.empty_like(t["q"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    n = max(args.steps, 20)
+    flags = msg.MSG_ATTN_REUSE_PLAN | msg.MSG_ATTN_EXTEND_ONLY
+    split_ms = _median_launch_ms(_attn_call(msg, spec, t, b, out, flags), n, flush)
+    whole = dict(b, ws=b["ws"][:16 << 20])     # the plan, without the split's slots
+    whole_ms = _median_launch_ms(_attn_call(msg, spec, t, whole, out, flags), n, flush)
+    _check_status(msg, b, "chunked prefill")
+    fl = extend_flops(spec)
+    del t, b, whole, out, flush
+    torch.cuda.empty_cache()
+    return {"workload": "chunked_prefill_1x128_cached32768_page1",
+            "split_ms": round(split_ms, 4), "whole_items_ms": round(whole_ms, 4),
+            "split_tflops": round(fl / (split_ms * 1e-3) / 1e12, 1),
+            "whole_items_tflops": round(fl / (whole_ms * 1e-3) / 1e12, 1),
+            "split_frac": round(fl / (split_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "speedup": round(whole_ms / split_ms, 2), "flops": fl,
+            "l2": "flushed (256 MB write) before every timed launch"}
+
+
 # ------------------------------------------------------------ CPU oracle baseline
 def oracle_layer_inputs(spec, layer):
     """Host copies of one layer's inputs for the oracle (all requests, compacted)."""
@@ -1108,7 +1147,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer leg")
     ap.add_argument("--extend-only", action="store_true",
                     help="run only the extend sub-benchmark and print its JSON (profiling)")
-    ap.add_argument("--only", choices=["extend", "graph", "ladder", "tiny", "large", "mixed",
+    ap.add_argument("--only", choices=["extend", "graph", "ladder", "tiny", "large", "mixed", "chunk",
                                        "prologue", "sampler", "cpu"],
                     default=None,
                     help="run only one sub-benchmark and print its JSON (profiling)")
@@ -1139,6 +1178,7 @@ def main():
                 "cpu": lambda: cpu_oracle_configs(),
                 "large": lambda: run_large_decode(args, dev, msg, peaks),
                 "mixed": lambda: run_long_mixed(args, dev, msg, peaks),
+                "chunk": lambda: run_chunked_prefill(args, dev, msg, peaks),
                 "prologue": lambda: run_prologue(args, dev, msg, peaks),
                 "sampler": lambda: run_sampler(args, dev, msg, peaks)}
         print(json.dumps(legs[args.only]()), flush=True)

@@ -114,7 +114,6 @@ int plan_impl(const KvIndex &kv, const int32_t *cached_len, const int32_t *exten
   pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
   pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
   pp.max_tiles = L.max_tiles;
-  pp.ext_items = reinterpret_cast<int32_t *>(ws + L.ext_items);
   int rc = from_cuda(launch_plan(pp, s));
   if (rc != MSG_OK) return rc;
   if (total_q > 0 && (out_loc_out || positions_out)) {
@@ -353,7 +352,6 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
     pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
     pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
     pp.max_tiles = L.max_tiles;
-    pp.ext_items = reinterpret_cast<int32_t *>(ws + L.ext_items);
     rc = from_cuda(launch_plan(pp, s));
     if (rc != MSG_OK) return rc;
   }
@@ -414,7 +412,7 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
   if (!(flags & MSG_ATTN_DECODE_ONLY)) {
     // the persistent extend kernel takes work items from a counter in the plan header
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(ws + L.header);
-    rc = from_cuda(cudaMemsetAsync(&hdr->ext_next, 0, sizeof(int32_t), s));
+    rc = from_cuda(cudaMemsetAsync(&hdr->ext_next, 0, 2 * sizeof(int32_t), s));
     if (rc != MSG_OK) return rc;
     rc = from_cuda(launch_extend(ap, L.max_tiles, max_kv_len, s));
     if (rc != MSG_OK) return rc;

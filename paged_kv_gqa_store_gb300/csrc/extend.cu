@@ -326,9 +326,9 @@ struct GrabState {
 };
 static_assert(sizeof(GrabState) <= 64, "grabber state block");
 
-// Next piece of CTA c's split range; a split item is also entered in the list
-// (by its first piece, under that piece's slot) for the merge kernel.
-__device__ Piece next_split_piece(GrabState *gs, int c, int32_t *ext_items) {
+// Next piece of CTA c's split range; a split item is also appended to the list
+// (by its first piece) for the merge kernel.
+__device__ Piece next_split_piece(GrabState *gs, int c, int32_t *ext_items, int32_t *count) {
   const Split &sp = gs->sp;
   if (gs->su >= gs->su_end) return Piece{-1, 0, 0, 0u};
   const int64_t su = gs->su;
@@ -344,8 +344,9 @@ __device__ Piece next_split_piece(GrabState *gs, int c, int32_t *ext_items) {
     const int cf = sp.cta_of(first), cl = sp.cta_of(first + n - 1);
     const int hs = first > sp.bound(cf) ? 1 : 0;
     meta = (uint32_t)cf | ((uint32_t)cl << 15) | ((uint32_t)hs << 30) | (1u << 31);
-    if (c == cf && 2 * cf + hs < kExtSlots) {
-      int32_t *e = ext_items + 4 * (2 * cf + hs);
+    const int idx = c == cf ? atomicAdd(count, 1) : kExtSlots;
+    if (idx < kExtSlots) {
+      int32_t *e = ext_items + 4 * idx;
       e[1] = cf;
       e[2] = cl;
       e[3] = hs;
@@ -403,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (grab) {
       Piece pc{-1, 0, -1, 0u};
       if (kSplit && gs->split) {
-        pc = next_split_piece(gs, (int)blockIdx.x, p.ext_items);
+        pc = next_split_piece(gs, (int)blockIdx.x, p.ext_items,
+                              const_cast<int32_t *>(&p.hdr->ext_split_count));
       } else {
         pc.w = atomicAdd(next_ctr, 1);
         if (pc.w >= hdr.ext_tile_count * p.num_kv_heads) pc.w = -1;
@@ -873,90 +875,122 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- split merge
-// One CTA per entry of the split-item list (the extend kernel's grabbers
-// enter each split item once: the item, the first and the last CTA holding a
-// piece of it, and whether the first CTA's piece is its second one):
+// The extend kernel's grabbers append each split item once to the list (the
+// item, the first and the last CTA holding a piece of it, and whether the
+// first CTA's piece is its second one; ext_split_count entries, zeroed before
+// each extend launch).  One wave of CTAs strides over (entry, block rb of 32
+// rows of sub-tile rb / 4: consecutive tokens of one query head), 4 rows per
+// warp:
 // o = sum_k 2^(lse_k - L) o_k / sum_k 2^(lse_k - L) over the pieces in order,
-// written as bf16 rows.  Warp v merges 32 rows of sub-tile v / 4 (consecutive
-// tokens of one query head); lane l holds dims 4 l .. 4 l + 3, so every load
-// and store covers whole rows, and 8 rows' loads of up to 4 pieces are in
-// flight at once.  The entry is cleared for the next call.
+// written as bf16 rows.  Lane k holds piece k's lse (L and the sum are warp
+// reductions); lane l holds dims 4 l .. 4 l + 3 of the rows, so every load and
+// store covers whole rows, and 4 rows of 4 pieces are in flight at once.
 constexpr int kMergeThreads = 256;
-constexpr int kMergePieces = 4;
-__global__ void __launch_bounds__(kMergeThreads) ext_merge_kernel(AttnParams p) {
+constexpr int kMergeBlocks = 8;               // 2 sub-tiles x 4 blocks of 32 rows
+constexpr int kMergeRows = 4;                 // rows per warp
+constexpr int kMergePieces = 4;               // pieces in flight per row
+constexpr int kMergeCtasPerSm = 2;
+// One unit of merge work: 32 rows (4 per warp) of listed split item idx.
+__device__ void merge_unit(const AttnParams &p, int idx, int rb, int G);
+__global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) ext_merge_kernel(AttnParams p) {
   grid_dep_wait();                      // the extend kernel's partials and list
   grid_dep_launch();
-  int32_t *e = p.ext_items + 4 * blockIdx.x;
+  int n = __ldcg(&p.hdr->ext_split_count);
+  if (n > kExtSlots) n = kExtSlots;
+  const int G = (int)gridDim.x / kMergeCtasPerSm;   // the extend grid
+  for (int u = blockIdx.x; u < n * kMergeBlocks; u += gridDim.x)
+    merge_unit(p, u / kMergeBlocks, u % kMergeBlocks, G);
+}
+
+__device__ void merge_unit(const AttnParams &p, int idx, int rb, int G) {
+  const int32_t *e = p.ext_items + 4 * idx;
   const int w = __ldcg(e);
-  if (w < 0) return;
   const int cf = __ldcg(e + 1), cl = __ldcg(e + 2), hs = __ldcg(e + 3);
   // an entry the extend kernel of this grid cannot have made is reported, not used
-  const int G = (int)gridDim.x / 2;
-  if (w >= p.hdr->ext_tile_count * p.num_kv_heads || cf < 0 || cl < cf || cl >= G ||
+  if (w < 0 || w >= p.hdr->ext_tile_count * p.num_kv_heads || cf < 0 || cl < cf || cl >= G ||
       (hs != 0 && hs != 1)) {
-    if (threadIdx.x == 0) report(p.status, MSG_DEV_BAD_LENGTHS, w, (int64_t)cf * 65536 + cl);
+    if (threadIdx.x == 0 && rb == 0)
+      report(p.status, MSG_DEV_BAD_LENGTHS, w, (int64_t)cf * 65536 + cl);
     return;
   }
   const Item it = load_item(p, w);
   if (!it.ok) return;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int x = warp / 4, r0 = (warp % 4) * 32, tsub0 = x * kSubTok + r0 % kSubTok;
-  int rows_valid = it.nq - tsub0;
-  rows_valid = rows_valid < 0 ? 0 : rows_valid > 32 ? 32 : rows_valid;
+  const int x = rb / 4, r0 = (rb % 4) * 32 + warp * kMergeRows;   // this warp's first row
+  const int tsub0 = x * kSubTok + r0 % kSubTok;
+  int rows = it.nq - tsub0;
+  if (rows <= 0) return;
+  if (rows > kMergeRows) rows = kMergeRows;
   const int np = cl - cf + 1;
-  auto row_of = [&](int k, int r) {     // partial row of piece k, row r0 + r of sub-tile x
+  auto prow = [&](int k, int r) {       // partial row of piece k, row r0 + r of sub-tile x
     return ((int64_t)(2 * (cf + k) + (k == 0 ? hs : 0)) * 2 + x) * 128 + r0 + r;
   };
-  const int64_t ors = (int64_t)p.num_qo_heads * kHeadDim;
-  uint16_t *out = p.out + (it.qrow0 + tsub0) * ors + (2 * it.gh + r0 / kSubTok) * kHeadDim;
-  // lane r: row r0 + r's largest lse and the weights' sum
-  float L = -INFINITY;
-  for (int k = 0; k < np; ++k) L = fmaxf(L, __ldcg(p.ext_lse + row_of(k, lane)));
-  float den = 0.f;
-  for (int k = 0; k < np; ++k) den += exp2f(__ldcg(p.ext_lse + row_of(k, lane)) - L);
-  for (int r = 0; r < rows_valid; r += 8) {
-    float4 acc[8];
+  // lane j holds piece k0 + j's lse of each row (32 pieces per group): L is a
+  // warp max over all groups, then each group's weights 2^(lse - L) stay in
+  // their lanes (summed into den by a warp reduction and shuffled to every
+  // lane for its dims), and the group's rows are loaded 8 pieces at a time
+  float L[kMergeRows], den[kMergeRows];
+  float4 acc[kMergeRows];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < np; k0 += kMergePieces) {
-      float4 v[kMergePieces][8];
-      float wl[kMergePieces];
+  for (int r = 0; r < kMergeRows; ++r) {
+    L[r] = -INFINITY;
+    den[r] = 0.f;
+    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int g0 = 0; g0 < np; g0 += 32) {
 #pragma unroll
-      for (int kk = 0; kk < kMergePieces; ++kk) {
-        wl[kk] = 0.f;
-        if (k0 + kk < np) {
-          wl[kk] = exp2f(__ldcg(p.ext_lse + row_of(k0 + kk, lane)) - L);
+    for (int r = 0; r < kMergeRows; ++r)
+      if (g0 + lane < np && r < rows) L[r] = fmaxf(L[r], __ldcg(p.ext_lse + prow(g0 + lane, r)));
+  }
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            v[kk][i] = r + i < rows_valid
-                           ? __ldcg(reinterpret_cast<const float4 *>(
-                                        p.ext_o + row_of(k0 + kk, r + i) * kHeadDim) + lane)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
+  for (int r = 0; r < kMergeRows; ++r)
 #pragma unroll
-      for (int kk = 0; kk < kMergePieces; ++kk) {
-        if (k0 + kk >= np) break;
+    for (int o = 16; o > 0; o >>= 1) L[r] = fmaxf(L[r], __shfl_xor_sync(0xffffffffu, L[r], o));
+  for (int g0 = 0; g0 < np; g0 += 32) {
+    float wl[kMergeRows];               // this lane's piece's weight of each row
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float wk = __shfl_sync(0xffffffffu, wl[kk], (r + i) & 31);
-          acc[i].x = fmaf(wk, v[kk][i].x, acc[i].x);
-          acc[i].y = fmaf(wk, v[kk][i].y, acc[i].y);
-          acc[i].z = fmaf(wk, v[kk][i].z, acc[i].z);
-          acc[i].w = fmaf(wk, v[kk][i].w, acc[i].w);
-        }
-      }
+    for (int r = 0; r < kMergeRows; ++r) {
+      wl[r] = (g0 + lane < np && r < rows) ? exp2f(__ldcg(p.ext_lse + prow(g0 + lane, r)) - L[r])
+                                           : 0.f;
+      float d = wl[r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      den[r] += d;
     }
+    const int gn = np - g0 < 32 ? np - g0 : 32;
+    for (int j0 = 0; j0 < gn; j0 += kMergePieces) {
+      float4 v[kMergePieces][kMergeRows];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float rd = 1.f / __shfl_sync(0xffffffffu, den, (r + i) & 31);
-      if (r + i < rows_valid)
-        *reinterpret_cast<uint2 *>(out + (int64_t)(r + i) * ors + 4 * lane) = make_uint2(
-            pack_bf16(acc[i].x * rd, acc[i].y * rd), pack_bf16(acc[i].z * rd, acc[i].w * rd));
+      for (int j = 0; j < kMergePieces; ++j)
+#pragma unroll
+        for (int r = 0; r < kMergeRows; ++r)
+          v[j][r] = (j0 + j < gn && r < rows)
+                        ? __ldcg(reinterpret_cast<const float4 *>(
+                                     p.ext_o + prow(g0 + j0 + j, r) * kHeadDim) + lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kMergePieces; ++j) {
+#pragma unroll
+        for (int r = 0; r < kMergeRows; ++r) {
+          const float wk = __shfl_sync(0xffffffffu, wl[r], (j0 + j) & 31);
+          acc[r].x = fmaf(wk, v[j][r].x, acc[r].x);
+          acc[r].y = fmaf(wk, v[j][r].y, acc[r].y);
+          acc[r].z = fmaf(wk, v[j][r].z, acc[r].z);
+          acc[r].w = fmaf(wk, v[j][r].w, acc[r].w);
+        }
+      }
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) e[0] = -1;      // cleared for the next call
+  const int64_t ors = (int64_t)p.num_qo_heads * kHeadDim;
+  uint16_t *out = p.out + (it.qrow0 + tsub0) * ors + (2 * it.gh + r0 / kSubTok) * kHeadDim;
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+    if (r < rows) {
+      const float rd = 1.f / den[r];
+      *reinterpret_cast<uint2 *>(out + (int64_t)r * ors + 4 * lane) = make_uint2(
+          pack_bf16(acc[r].x * rd, acc[r].y * rd), pack_bf16(acc[r].z * rd, acc[r].w * rd));
+    }
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1046,8 +1080,9 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, int64_t max_kv
     extend_kernel<false><<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
   e = cudaGetLastError();
   if (e != cudaSuccess || !may_split) return e;
-  // the split items' merge: one CTA per partial slot of this grid
-  return launch_k(ext_merge_kernel, dim3(2 * (unsigned)grid), dim3(kMergeThreads), 0, s, true, p);
+  // the split items' merge: one wave of CTAs over (listed item, 32-row block)
+  return launch_k(ext_merge_kernel, dim3(kMergeCtasPerSm * (unsigned)grid), dim3(kMergeThreads), 0,
+                  s, true, p);
 }
 
 }  // namespace msg

@@ -65,7 +65,8 @@ struct WsLayout {
   size_t plan_end = 0;     // bytes used by the plan part
   size_t total = 0;        // bytes a call needs
   // optional: the extend key split (used when the workspace holds it)
-  size_t ext_items = 0;    // int32x4[kExtSlots]  split items (item, first CTA, last CTA, shift)
+  size_t ext_items = 0;    // int32x4[kExtSlots]  split items (item, first CTA, last CTA, shift),
+                           //                     ext_split_count of them, in arrival order
   size_t ext_lse = 0;      // float[2 * kExtMaxCtas][2][128]
   size_t ext_o = 0;        // float[2 * kExtMaxCtas][2][128][128]
   size_t total_split = 0;  // bytes with the extend key split (msg_workspace_size)
@@ -79,8 +80,10 @@ struct PlanHeader {
   int32_t ext_count;       // extend requests
   int64_t dec_keys;        // sum of decode kv lengths + a gap (kDecSegPad) per request
   int64_t total_q;         // sum of extend lengths
-  int32_t ext_next;        // extend work-item counter (zeroed before each extend launch)
-  int32_t ext_split_ready; // the plan cleared the list of split extend items
+  int32_t ext_next;        // extend work-item counter  } both zeroed before each
+  int32_t ext_split_count; // split extend items listed } extend launch
+  int32_t ext_split_ready; // the plan filled ext_units
+  int32_t pad2;
   int64_t ext_units;       // key tiles over the extend tiles (128 keys each, per KV head)
 };
 
@@ -98,7 +101,7 @@ inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t
   L.counters = take(sizeof(int32_t) * (num_reqs + 1) * kMaxKvHeads);
   L.max_tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + num_reqs + 1;
   L.ext_tiles = take(sizeof(int32_t) * 2 * L.max_tiles);
-  L.ext_items = take(sizeof(int32_t) * 4 * kExtSlots);   // (the plan clears it)
+  L.ext_items = take(sizeof(int32_t) * 4 * kExtSlots);
   L.plan_end = off;
   L.part_lse = take(sizeof(float) * 2 * max_decode_ctas(hq) * hq);
   L.part_o = take(sizeof(float) * 2 * (size_t)max_decode_ctas(hq) * hq * d);
@@ -140,7 +143,6 @@ struct PlanParams {
   int32_t *counters;
   int32_t *ext_tiles;           // pairs
   int64_t max_tiles;
-  int32_t *ext_items;           // list of split extend items to clear
 };
 
 struct TokenMetaParams {

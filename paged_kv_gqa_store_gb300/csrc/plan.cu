@@ -87,7 +87,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     ext_reqs = 0;
     ext_units = 0;
   }
-  for (int c = tid; c < kExtSlots; c += kPlanThreads) p.ext_items[4 * c] = -1;
   __syncthreads();
 
   for (int32_t base = 0; base < p.num_reqs; base += kPlanThreads) {
