@@ -76,3 +76,15 @@ def test_ragged_extends_with_decodes():
     spec = wl.make_batch("split_ragged", 710, cached, ext, 1,
                          num_pages=int((cached + ext).sum()) + 16)
     _check(spec)
+
+
+@pytest.mark.parametrize("hkv", [4, 2])
+def test_chunked_prefill_on_a_head_slice(hkv):
+    """The chunked-prefill step on a tensor-parallel rank's head slice (8q/4kv
+    at tp = 2, 4q/2kv at tp = 4: "Mini-SGLang 完整剖析" 4.5): 256 new tokens
+    over a 40,000-token prefix, 2 query tiles x hkv work items, split the same
+    way."""
+    cached, ext = np.array([40000]), np.array([256])
+    spec = wl.make_batch("split_chunk_tp", 720 + hkv, cached, ext, 1, num_pages=40256 + 9,
+                         num_qo_heads=2 * hkv, num_kv_heads=hkv)
+    _check(spec)
