@@ -88,3 +88,40 @@ def test_chunked_prefill_on_a_head_slice(hkv):
     spec = wl.make_batch("split_chunk_tp", 720 + hkv, cached, ext, 1, num_pages=40256 + 9,
                          num_qo_heads=2 * hkv, num_kv_heads=hkv)
     _check(spec)
+
+
+def test_split_step_captured_in_a_graph():
+    """A chunked-prefill step (plan, store_kv, the split extend kernel and the
+    merge kernel, the counters zeroed between them) captured once in a CUDA
+    graph and replayed: each replay equals the oracle and the eager call bit
+    for bit."""
+    cached, ext = np.array([20000]), np.array([128])
+    spec = wl.make_batch("split_graph", 730, cached, ext, 1, num_pages=20128 + 9)
+    host = wl.host_tensors(spec)
+    ref = oracle_small(spec, host)["out"]
+    eager = _run(spec, host)
+    dev = "cuda"
+    gb = GpuBatch(spec, dev)
+    q = wl.bits_to_torch(host["q"], dev)
+    kn, vn = wl.bits_to_torch(host["k_new"], dev), wl.bits_to_torch(host["v_new"], dev)
+    kp, vp = wl.bits_to_torch(host["k_pool"], dev), wl.bits_to_torch(host["v_pool"], dev)
+    out = torch.empty_like(q)
+
+    def step():
+        loc = gb.plan()
+        msg.msg_store_kv(kn, vn, kp, vp, loc, dev_status=gb.ws)
+        gb.attention(q, kp, vp, out=out, flags=msg.MSG_ATTN_REUSE_PLAN)
+
+    step()                                           # warm-up (kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for rep in range(2):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert gb.status()[0] == msg.MSG_OK
+        got = wl.torch_to_bits(out)
+        assert np.array_equal(got, eager), f"replay {rep} differs from the eager call"
+        assert_attn_close(got, ref, f"graph replay {rep}")
