@@ -38,6 +38,15 @@
 //               pipe drain, and the softmax runs well ahead of its P.V).  The
 //               epilogue normalises O and stores bf16 rows.
 //
+// A batch with fewer than 4 items per SM (a chunked-prefill tile over a long
+// prefix, a few long extends) leaves SMs idle when items are taken whole; for
+// one that has at least 8 key tiles per SM the kernel instead splits the
+// items' key tiles evenly over every CTA (the Split geometry below): a range
+// boundary inside an item leaves each side's rows normalised by their own sum,
+// in fp32, with their lse, and a second kernel (ext_merge_kernel) combines the
+// pieces.  The host launches that split-capable instance (kSplit) only for a
+// batch that can have few items; other batches run the plain work queue.
+//
 // All cross-role hand-offs are mbarriers; every wait is bounded in time and an
 // expired one records MSG_DEV_TIMEOUT and unwinds.
 #include <cuda.h>
@@ -151,18 +160,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-          taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
