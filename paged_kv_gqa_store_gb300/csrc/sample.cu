@@ -1658,16 +1658,17 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
               clamp_pivots(piv, lo, hi);
             }
             n_win = gather<kBf16>(x, sm, piv[3], piv[0], &cnt_above, &mass_above);
-            if (n_win <= kCap) {
+            if (n_win <= kCap && mass_above >= tau) {
+              // the boundary lies above the window: known without sorting it
+              lo = piv[0];
+              cnt_lo = cnt_above;
+              mass_lo = mass_above;
+              side_above = true;
+            } else if (n_win <= kCap) {
               sort_window(x, sm, n_win);
               const float wm = n_win > 0 ? sm.lcum[n_win - 1] : 0.f;
-              if (mass_above < tau && tau <= mass_above + wm) {
+              if (tau <= mass_above + wm) {
                 gathered = sorted = true;
-              } else if (mass_above >= tau) {
-                lo = piv[0];
-                cnt_lo = cnt_above;
-                mass_lo = mass_above;
-                side_above = true;
               } else {
                 hi = piv[3];
                 cnt_hi = cnt_above + (unsigned long long)n_win;
