@@ -17,7 +17,9 @@
 //               TMA tile::gather4 (4 rows of 128 B per instruction, the 64
 //               instructions of a tile spread over the three warps) into
 //               128B-swizzled shared memory, in a ring of five 32 KiB slots
-//               (K_j, V_j, K_j+1, ...).
+//               (K_j, V_j, K_j+1, ...).  With pages of 16 or more keys a
+//               16-key run of one page is contiguous in the pool and comes
+//               in as one 16-row tile load (16 instructions per K or V tile).
 //  warp 0       allocates TMEM (S_a | S_b | O_a | O_b, 128 fp32 columns each),
 //               loads Q by TMA (3-D tensor map over q), and one lane issues the
 //               MMAs, alternating the sub-tiles:
@@ -366,7 +368,9 @@ template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     extend_kernel(const __grid_constant__ ExtParams ep, const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v) {
+                  const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ CUtensorMap tmap_kp,
+                  const __grid_constant__ CUtensorMap tmap_vp) {
   extern __shared__ uint8_t smem_raw[];
   const AttnParams &p = ep.a;
   // 1 KiB-aligned base: the 128B swizzle pattern repeats every 1 KiB.
@@ -465,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool active = u < 64;
     const int half = u >> 5, kg4 = u & 31;
     const int n_units = (64 - (warp - 1) + 2) / 3;     // units of this warp: 22, 21, 21
+    const int n_units16 = (16 - (warp - 1) + 2) / 3;   // with 16-key page units: 6, 5, 5
     const int oob = ep.kv_rows_total;                   // a row past the map: zero fill
     if (kSplit && split && warp == 1) {
       // the tiles' key-tile prefix (and sub-tile a's one tile fewer), then this
@@ -582,7 +587,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      // Pages of 16 or more keys: each unit is 16 consecutive keys of one
+      // page and one 64-dim half (so 16 units per K or V tile instead of 64),
+      // loaded as one 16-row tile (3-D map over (half row, head half, slot))
+      // when all 16 keys belong to the item, else by gather4 with zero rows
+      // past the item's keys.  One index entry per unit, read two tiles ahead.
+      auto stream_pages = [&]() {
+        const bool act = u < 16;
+        const int hf = u >> 3, g = u & 7;
+        auto read_e = [&](int j) -> int32_t {
+          const int64_t key = (int64_t)j * kBN + g * 16;
+          return (act && j < it.n_tiles && key < it.kv_end) ? __ldg(row_ptr + kv_entry(p.kv, key))
+                                                            : 0;
+        };
+        int32_t cur = read_e(j0), nxt = read_e(j0 + 1);
+        for (int j = j0; ok && j < j1; ++j) {
+          const int32_t nxt2 = read_e(j + 2);
+          const int64_t key0 = (int64_t)j * kBN + g * 16;
+          int64_t slot0 = -1;
+          if (act && key0 < it.kv_end)
+            slot0 = kv_slot(p.kv, cur, key0, p.num_slots, hf == 0 ? p.status : nullptr, it.r);
+          const int64_t nvalid = imin64(16, it.kv_end - key0);   // keys of the unit in the item
+          cur = nxt;
+          nxt = nxt2;
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {          // 0: K_j, 1: V_j
+            const uint32_t n = N + 2 * (j - j0) + kv;
+            const int s = n % kSlots;
+            if (n >= (uint32_t)kSlots && !mbar_wait(&bars[kBarEmpty + s], ((n / kSlots) & 1) ^ 1)) {
+              if (lane == 0) {
+                *abort_flag = 1;
+                report(p.status, MSG_DEV_TIMEOUT, it.r, j);
+              }
+              ok = false;
+              break;
+            }
+            if (aborted(abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&bars[kBarFull + s], (uint32_t)n_units16 * 2048u);
+            __syncwarp();
+            if (act) {
+              uint8_t *dst = smem + kOffRing + s * kSlot + hf * kHalf + g * 16 * 128;
+              if (slot0 >= 0 && nvalid >= 16) {
+                tma_load_3d(dst, kv ? &tmap_vp : &tmap_kp, 0, 2 * it.gh + hf, (int)slot0,
+                            &bars[kBarFull + s]);
+              } else {
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  int rr[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int k = 4 * q4 + e;
+                    rr[e] = (slot0 >= 0 && k < nvalid)
+                                ? (int)((slot0 + k) * ep.kv_rows_per_slot + 2 * it.gh + hf)
+                                : oob;
+                  }
+                  tma_gather4(dst + q4 * 4 * 128, kv ? &tmap_v : &tmap_k, 0, rr[0], rr[1], rr[2],
+                              rr[3], &bars[kBarFull + s]);
+                }
+              }
+            }
+          }
+        }
+      };
       if (p.page_size == 1) stream_item(std::true_type{});
+      else if (p.page_size >= 16) stream_pages();
       else stream_item(std::false_type{});
       N += 2u * (uint32_t)(j1 - j0);
     }
@@ -1016,6 +1086,20 @@ bool encode_rows(CUtensorMap *m, const void *base, uint64_t rows) {
          CUDA_SUCCESS;
 }
 
+// 3-D map over a pool as (64-element half rows, half rows per slot, slots):
+// box 64 x 1 x 16, one 64-dim half of 16 consecutive slots, 128B swizzle.
+bool encode_pages(CUtensorMap *m, const void *base, uint64_t rows_per_slot, uint64_t slots,
+                  uint64_t slot_bytes) {
+  const cuuint64_t dims[3] = {64, rows_per_slot, slots};
+  const cuuint64_t strides[2] = {128, slot_bytes};
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // 3-D map over q: (64-element half rows, 2 per head, tokens); box 64 x 1 x 64.
 bool encode_q(CUtensorMap *m, const void *q, int32_t hq, int64_t total_q, int64_t row_stride) {
   const cuuint64_t dims[3] = {64, (cuuint64_t)hq * 2, (cuuint64_t)total_q};
@@ -1054,10 +1138,20 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, int64_t max_kv
   const uint64_t rows = (uint64_t)p.num_slots * (uint64_t)ep.kv_rows_per_slot;
   if (rows == 0 || rows >= (1ull << 31)) return cudaErrorInvalidValue;
   ep.kv_rows_total = (int32_t)rows;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mkp, mvp;
   if (!encode_q(&mq, p.q, p.num_qo_heads, p.total_q, p.q_stride) ||
       !encode_rows(&mk, p.k_pool, rows) || !encode_rows(&mv, p.v_pool, rows))
     return cudaErrorInvalidValue;
+  if (p.page_size >= 16) {
+    if (!encode_pages(&mkp, p.k_pool, (uint64_t)ep.kv_rows_per_slot, (uint64_t)p.num_slots,
+                      (uint64_t)p.pool_stride_bytes) ||
+        !encode_pages(&mvp, p.v_pool, (uint64_t)ep.kv_rows_per_slot, (uint64_t)p.num_slots,
+                      (uint64_t)p.pool_stride_bytes))
+      return cudaErrorInvalidValue;
+  } else {
+    mkp = mk;   // not read: smaller pages take the gather4 path
+    mvp = mv;
+  }
   // persistent: one CTA per SM (the kernel's shared memory allows no more).
   // The instance that may take the key split, with a CTA on every SM, only
   // where the batch may have few items: its partial slots are there, fewer
@@ -1072,9 +1166,9 @@ cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, int64_t max_kv
     may_split = false;
   if (!may_split && grid > items) grid = items;
   if (may_split)
-    extend_kernel<true><<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
+    extend_kernel<true><<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv, mkp, mvp);
   else
-    extend_kernel<false><<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv);
+    extend_kernel<false><<<(unsigned)grid, kThreads, kSmem, s>>>(ep, mq, mk, mv, mkp, mvp);
   e = cudaGetLastError();
   if (e != cudaSuccess || !may_split) return e;
   // the split items' merge: one wave of CTAs over (listed item, 32-row block)

@@ -309,6 +309,32 @@ def test_out_of_range_slot_is_reported_not_faulted():
     assert np.array_equal(after[1:], before[1:])
 
 
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_extend_page_outside_the_pool_is_reported_other_requests_still_match(page_size):
+    """Pages of 16 or more keys, where the extend kernel loads each 16-key run
+    of a page as one tile: an extend request whose first (fully cached) page
+    lies past the pool is reported and read as zeros, its output stays finite,
+    and every other request's rows still match the oracle."""
+    cached = [100, 37, 300, 5, 250, 64]
+    ext = [1, 150, 1, 1, 200, 67]
+    need = sum((c + e + page_size - 1) // page_size for c, e in zip(cached, ext))
+    spec = wl.make_batch(f"badpage_p{page_size}", 1230 + page_size, cached, ext, page_size,
+                         num_pages=need + 7)
+    host = wl.host_tensors(spec)
+    bad_req = 4
+    bad = spec.page_table.copy()
+    bad[spec.req_rows[bad_req], 0] = spec.num_slots + page_size     # a page past the pool
+    g = run_small(wl.BatchSpec(**{**spec.__dict__, "page_table": bad}), host)
+    o = oracle_small(spec, host)
+    assert g["status"] == msg.MSG_ERR_DEVICE_CHECK
+    assert g["status_info"][0] == msg.MSG_DEV_SLOT_OUT_OF_RANGE
+    qo = o["qo_indptr"]
+    keep = np.ones(spec.total_q, bool)
+    keep[qo[bad_req]:qo[bad_req + 1]] = False
+    assert np.isfinite(wl.bf16_bits_to_f64(g["out"][~keep])).all()
+    assert_attn_close(g["out"][keep], o["out"][keep], spec.name)
+
+
 def test_phase_flag_contradiction_is_reported():
     spec = _rand_spec(1300, n_dec=3, n_ext=1, page_size=1)
     host = wl.host_tensors(spec)
