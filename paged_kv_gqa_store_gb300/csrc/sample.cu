@@ -1431,13 +1431,67 @@ __global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams 
   grid_dep_launch();
 }
 
+// ---- which row a CTA takes
+// Cost class of row i from its parameters alone: 0 = a top-p cut with no
+// top-k below the window capacity (its boundary is searched over a whole
+// distribution: the long rows), 1 = another cut, 2 = none.
+__device__ __forceinline__ int row_class(const SampleParams &p, int i) {
+  unsigned long long k = (unsigned long long)p.vocab;
+  if (p.top_k != nullptr && p.top_k[i] >= 1 && p.top_k[i] < p.vocab) k = (unsigned long long)p.top_k[i];
+  const bool topp = p.top_p != nullptr && p.top_p[i] < 1.f;   // NaN: no cut (reported later)
+  if (topp && k > (unsigned long long)kCap) return 0;
+  return (topp || k < (unsigned long long)p.vocab) ? 1 : 2;
+}
+
+// The row of this CTA: rows in order of cost class (the long rows first,
+// index order within a class).  The first wave of CTAs is spread one per SM,
+// so each long row gets an SM of its own instead of sharing its issue slots
+// with another long row for its whole run.  Batches above 2 kT rows keep
+// CTA b on row b.  Reads only the parameters (every thread calls).
+__device__ int row_of_block(const SampleParams &p, Smem &sm) {
+  const int b = (int)blockIdx.x, B = p.batch, t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  if (B > 2 * kT) return b;
+  const int c0 = t < B ? row_class(p, t) : 3, c1 = t + kT < B ? row_class(p, t + kT) : 3;
+  if (t < 4) sm.ival[t] = 0;
+  __syncthreads();
+  if (c0 < 3) atomicAdd(&sm.ival[c0], 1);
+  if (c1 < 3) atomicAdd(&sm.ival[c1], 1);
+  __syncthreads();
+  int cls = 0, off = 0;
+  while (cls < 2 && b >= off + sm.ival[cls]) off += sm.ival[cls++];
+  const int rank = b - off;                     // this CTA takes the rank-th row of class cls
+  const unsigned m0 = __ballot_sync(0xffffffffu, c0 == cls);
+  const unsigned m1 = __ballot_sync(0xffffffffu, c1 == cls);
+  if (lane == 0) sm.ured[warp] = (unsigned long long)__popc(m0) | ((unsigned long long)__popc(m1) << 32);
+  __syncthreads();
+  int pre0 = 0, pre1 = 0, tot0 = 0;
+  for (int w = 0; w < kW; ++w) {
+    const int n0 = (int)(sm.ured[w] & 0xffffffffu), n1 = (int)(sm.ured[w] >> 32);
+    tot0 += n0;
+    if (w < warp) {
+      pre0 += n0;
+      pre1 += n1;
+    }
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  pre0 += __popc(m0 & lt);
+  pre1 += tot0 + __popc(m1 & lt);
+  if (c0 == cls && pre0 == rank) sm.ival[4] = t;
+  if (c1 == cls && pre1 == rank) sm.ival[4] = t + kT;
+  __syncthreads();
+  const int row = sm.ival[4];
+  __syncthreads();                              // ival and ured are reused by the row's work
+  return row;
+}
+
 // ---- the row (one CTA each): everything after the scan
 template <bool kBf16, bool kGreedy>
 __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef ws) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int row = blockIdx.x;
+  const int row = kGreedy ? (int)blockIdx.x : row_of_block(p, sm);
   Ctx x;
   x.r = row_ref<kBf16>(p.logits + (int64_t)row * p.row_bytes, p.vocab);
   x.nl = x.r.nch + 2;
