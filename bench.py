@@ -537,7 +537,8 @@ def run_graph_decode(args, dev, msg):
         for i, t in enumerate(layers):
             msg.msg_paged_attention_store(t["q"], t["k_new"], t["v_new"], t["k_pool"], t["v_pool"],
                                           pt, cached, ext, qo, outs[i], ws, page_size=1,
-                                          req_rows=rows, max_kv_len=0, flags=flags)
+                                          req_rows=rows, max_kv_len=int(spec.max_kv_len),
+                                          flags=flags)
 
     def timed(fn, n):
         for _ in range(3):

@@ -112,6 +112,7 @@ int plan_impl(const KvIndex &kv, const int32_t *cached_len, const int32_t *exten
   pp.dec_row = reinterpret_cast<int64_t *>(ws + L.dec_row);
   pp.dec_qrow = reinterpret_cast<int32_t *>(ws + L.dec_qrow);
   pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  pp.gcounters = reinterpret_cast<int32_t *>(ws + L.gcounters);
   pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
   pp.max_tiles = L.max_tiles;
   int rc = from_cuda(launch_plan(pp, s));
@@ -350,6 +351,7 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
     pp.dec_row = reinterpret_cast<int64_t *>(ws + L.dec_row);
     pp.dec_qrow = reinterpret_cast<int32_t *>(ws + L.dec_qrow);
     pp.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+    pp.gcounters = reinterpret_cast<int32_t *>(ws + L.gcounters);
     pp.ext_tiles = reinterpret_cast<int32_t *>(ws + L.ext_tiles);
     pp.max_tiles = L.max_tiles;
     rc = from_cuda(launch_plan(pp, s));
@@ -388,6 +390,7 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
   ap.dec_row = reinterpret_cast<const int64_t *>(ws + L.dec_row);
   ap.dec_qrow = reinterpret_cast<const int32_t *>(ws + L.dec_qrow);
   ap.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  ap.gcounters = reinterpret_cast<int32_t *>(ws + L.gcounters);
   ap.ext_tiles = reinterpret_cast<const int32_t *>(ws + L.ext_tiles);
   ap.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
   ap.part_o = reinterpret_cast<float *>(ws + L.part_o);
@@ -406,7 +409,12 @@ int attention_impl(const void *q, int64_t q_row_stride, const void *k_pool, cons
     }
     // with a reused plan the decode kernel may start its set-up (which reads
     // only the plan and the KV index) while the preceding kernel finishes
-    rc = from_cuda(launch_decode(ap, (int)grid, (flags & MSG_ATTN_REUSE_PLAN) != 0, s));
+    // Few requests with long contexts are each cut over many CTAs: their
+    // partials are merged in two levels (shorter dependent-load chains).  Only
+    // for such batches: the other instance keeps a leaner merge.
+    const bool two_level = num_reqs <= 16 && max_kv_len > 768;
+    rc = from_cuda(
+        launch_decode(ap, (int)grid, (flags & MSG_ATTN_REUSE_PLAN) != 0, two_level, s));
     if (rc != MSG_OK) return rc;
   }
   if (!(flags & MSG_ATTN_DECODE_ONLY)) {

@@ -140,6 +140,8 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
 // slot; page-id forms: the page).  Loaded ahead of use; validated by raw_to_slot.
 // kPage1: page_size 1, where every index form holds the slot itself.
 constexpr int kMergeBatch = 4;                // split partials loaded before any is applied
+constexpr int kMergeGroup = 8;                // two-level merge: splits per group
+constexpr int kMergeOneLevel = 24;            // ... taken for requests cut more ways than this
 
 template <bool kPage1>
 __device__ __forceinline__ int32_t load_raw(const AttnParams &p, const int32_t *row, int64_t j) {
@@ -169,7 +171,9 @@ __device__ __forceinline__ int64_t raw_to_slot(const AttnParams &p, int32_t raw,
 // kFused: the step's new K / V rows are given (p.k_new): each request's newest
 // key is read from them and stored to the pool here (compiled apart, so the
 // plain kernel carries none of it).
-template <int HKV, bool kPage1, bool kFused>
+// kTwoLevel: the instance for batches of few long requests, whose requests
+// are cut into many splits; it merges those in two levels (see the merge).
+template <int HKV, bool kPage1, bool kFused, bool kTwoLevel>
 __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
     decode_kernel(AttnParams p) {
   using S = Dec<HKV>;
@@ -529,97 +533,236 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
         }
         __threadfence();
         __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(&p.counters[(int64_t)h.r * kHkv + gh], 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == h.bl - h.bf) {
-          // last of the (request, KV head) splits: merge them.  The splits'
-          // lse values are loaded by the lanes side by side (split bf + k by
-          // lane k % 32), the o rows split after split with several loads in
-          // flight; the sums run in split order.
-          __threadfence();
+        if constexpr (kTwoLevel) {
+          // Two-level merge.  A request cut into at most kMergeOneLevel splits
+          // is merged as in the one-level instance.  One cut into more is
+          // merged in two levels, so that the last warp's chain of
+          // dependent loads stays short: each group of kMergeGroup consecutive
+          // splits by the last of its warps to finish (into the group's first
+          // slot, as one more normalised partial with its lse), then the groups
+          // by the last group.  The partials to merge are the slots
+          // slot_of(mb + ms i), i < mn; sums run in index order at each level.
           const int ns = h.bl - h.bf + 1;
           auto slot_of = [&](int k) {
             return 2 * (int64_t)(h.bf + k) + (k == 0 ? h.head_shift : 0);
           };
-          // split `lane`'s lse values and the first batch of o rows, all in
-          // flight at once; the lse values stay in their lanes for the weights
-          float4 xs[kMergeBatch], ys[kMergeBatch];
-#pragma unroll
-          for (int u = 0; u < kMergeBatch; ++u) {
-            if (u < ns) {
-              const float *pr0 = p.part_o + (slot_of(u) * kHq + 2 * gh) * kHeadDim + lane * 4;
-              xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
-              ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+          int mb = 0, ms = 1, mn = ns;
+          bool to_out = ns <= kMergeOneLevel;
+          {
+            int32_t *ctr = &p.counters[(int64_t)h.r * kHkv + gh];
+            if (!to_out) {
+              mb = ((int)blockIdx.x - h.bf) / kMergeGroup * kMergeGroup;
+              mn = ns - mb < kMergeGroup ? ns - mb : kMergeGroup;
+              ctr = &p.gcounters[slot_of(mb) * kHkv + gh];
             }
+            int old = 0;
+            if (lane == 0) old = atomicAdd(ctr, 1);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old != mn - 1) mn = 0;                 // not the last: nothing to merge
           }
-          float l0 = -INFINITY, l1 = -INFINITY;
-          if (lane < ns) {
-            const int64_t sl = slot_of(lane);
-            l0 = __ldcg(p.part_lse + sl * kHq + 2 * gh);
-            l1 = __ldcg(p.part_lse + sl * kHq + 2 * gh + 1);
-          }
-          float L0 = l0, L1 = l1;
-          for (int k = lane + 32; k < ns; k += 32) {
-            const int64_t sl = slot_of(k);
-            L0 = fmaxf(L0, __ldcg(p.part_lse + sl * kHq + 2 * gh));
-            L1 = fmaxf(L1, __ldcg(p.part_lse + sl * kHq + 2 * gh + 1));
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            L0 = fmaxf(L0, __shfl_xor_sync(0xffffffffu, L0, o));
-            L1 = fmaxf(L1, __shfl_xor_sync(0xffffffffu, L1, o));
-          }
-          float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
-          float d0 = 0.f, d1 = 0.f;
-          for (int k0 = 0; k0 < ns; k0 += 32) {
-            float w0 = 0.f, w1 = 0.f;
-            if (k0 == 0) {
-              if (lane < ns) {
-                w0 = exp2f(l0 - L0);
-                w1 = exp2f(l1 - L1);
+          while (mn > 0) {
+            // the last of these partials' warps: merge them.  Their lse values
+            // are loaded by the lanes side by side (partial k by lane k % 32),
+            // the o rows partial after partial with several loads in flight.
+            __threadfence();
+            auto mslot = [&](int k) { return slot_of(mb + ms * k); };
+            // partial `lane`'s lse values and the first batch of o rows, all in
+            // flight at once; the lse values stay in their lanes for the weights
+            float4 xs[kMergeBatch], ys[kMergeBatch];
+  #pragma unroll
+            for (int u = 0; u < kMergeBatch; ++u) {
+              if (u < mn) {
+                const float *pr0 = p.part_o + (mslot(u) * kHq + 2 * gh) * kHeadDim + lane * 4;
+                xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
+                ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
               }
-            } else if (k0 + lane < ns) {
-              const int64_t sl = slot_of(k0 + lane);
-              w0 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh) - L0);
-              w1 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh + 1) - L1);
             }
-            const int nk = ns - k0 < 32 ? ns - k0 : 32;
-            for (int j0 = 0; j0 < nk; j0 += kMergeBatch) {
-              if (k0 > 0 || j0 > 0) {
-#pragma unroll
-                for (int u = 0; u < kMergeBatch; ++u) {   // the batch's loads, all in flight
-                  if (j0 + u < nk) {
-                    const float *pr0 =
-                        p.part_o + (slot_of(k0 + j0 + u) * kHq + 2 * gh) * kHeadDim + lane * 4;
-                    xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
-                    ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+            float l0 = -INFINITY, l1 = -INFINITY;
+            if (lane < mn) {
+              const int64_t sl = mslot(lane);
+              l0 = __ldcg(p.part_lse + sl * kHq + 2 * gh);
+              l1 = __ldcg(p.part_lse + sl * kHq + 2 * gh + 1);
+            }
+            float L0 = l0, L1 = l1;
+            for (int k = lane + 32; k < mn; k += 32) {
+              const int64_t sl = mslot(k);
+              L0 = fmaxf(L0, __ldcg(p.part_lse + sl * kHq + 2 * gh));
+              L1 = fmaxf(L1, __ldcg(p.part_lse + sl * kHq + 2 * gh + 1));
+            }
+  #pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              L0 = fmaxf(L0, __shfl_xor_sync(0xffffffffu, L0, o));
+              L1 = fmaxf(L1, __shfl_xor_sync(0xffffffffu, L1, o));
+            }
+            float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
+            float d0 = 0.f, d1 = 0.f;
+            for (int k0 = 0; k0 < mn; k0 += 32) {
+              float w0 = 0.f, w1 = 0.f;
+              if (k0 == 0) {
+                if (lane < mn) {
+                  w0 = exp2f(l0 - L0);
+                  w1 = exp2f(l1 - L1);
+                }
+              } else if (k0 + lane < mn) {
+                const int64_t sl = mslot(k0 + lane);
+                w0 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh) - L0);
+                w1 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh + 1) - L1);
+              }
+              const int nk = mn - k0 < 32 ? mn - k0 : 32;
+              for (int j0 = 0; j0 < nk; j0 += kMergeBatch) {
+                if (k0 > 0 || j0 > 0) {
+  #pragma unroll
+                  for (int u = 0; u < kMergeBatch; ++u) {   // the batch's loads, all in flight
+                    if (j0 + u < nk) {
+                      const float *pr0 =
+                          p.part_o + (mslot(k0 + j0 + u) * kHq + 2 * gh) * kHeadDim + lane * 4;
+                      xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
+                      ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+                    }
                   }
                 }
-              }
-#pragma unroll
-              for (int u = 0; u < kMergeBatch; ++u) {
-                if (j0 + u >= nk) break;
-                const float a0 = __shfl_sync(0xffffffffu, w0, j0 + u);
-                const float a1 = __shfl_sync(0xffffffffu, w1, j0 + u);
-                const float4 x = xs[u], y = ys[u];
-                n0.x = fmaf(a0, x.x, n0.x); n0.y = fmaf(a0, x.y, n0.y);
-                n0.z = fmaf(a0, x.z, n0.z); n0.w = fmaf(a0, x.w, n0.w);
-                n1.x = fmaf(a1, y.x, n1.x); n1.y = fmaf(a1, y.y, n1.y);
-                n1.z = fmaf(a1, y.z, n1.z); n1.w = fmaf(a1, y.w, n1.w);
-                d0 += a0;
-                d1 += a1;
+  #pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u) {
+                  if (j0 + u >= nk) break;
+                  const float a0 = __shfl_sync(0xffffffffu, w0, j0 + u);
+                  const float a1 = __shfl_sync(0xffffffffu, w1, j0 + u);
+                  const float4 x = xs[u], y = ys[u];
+                  n0.x = fmaf(a0, x.x, n0.x); n0.y = fmaf(a0, x.y, n0.y);
+                  n0.z = fmaf(a0, x.z, n0.z); n0.w = fmaf(a0, x.w, n0.w);
+                  n1.x = fmaf(a1, y.x, n1.x); n1.y = fmaf(a1, y.y, n1.y);
+                  n1.z = fmaf(a1, y.z, n1.z); n1.w = fmaf(a1, y.w, n1.w);
+                  d0 += a0;
+                  d1 += a1;
+                }
               }
             }
-          }
-          if (row_ok) {
             const float e0 = 1.f / d0, e1 = 1.f / d1;
-            *reinterpret_cast<uint2 *>(op) =
-                make_uint2(pack_bf16(n0.x * e0, n0.y * e0), pack_bf16(n0.z * e0, n0.w * e0));
-            *reinterpret_cast<uint2 *>(op + kHeadDim) =
-                make_uint2(pack_bf16(n1.x * e1, n1.y * e1), pack_bf16(n1.z * e1, n1.w * e1));
+            if (to_out) {
+              if (row_ok) {
+                *reinterpret_cast<uint2 *>(op) =
+                    make_uint2(pack_bf16(n0.x * e0, n0.y * e0), pack_bf16(n0.z * e0, n0.w * e0));
+                *reinterpret_cast<uint2 *>(op + kHeadDim) =
+                    make_uint2(pack_bf16(n1.x * e1, n1.y * e1), pack_bf16(n1.z * e1, n1.w * e1));
+              }
+              if (lane == 0) p.counters[(int64_t)h.r * kHkv + gh] = 0;
+              break;
+            }
+            // a group: its merged partial replaces the group's first one
+            const int64_t gs = mslot(0);
+            float *po = p.part_o + (gs * kHq + 2 * gh) * kHeadDim + lane * 4;
+            *reinterpret_cast<float4 *>(po) = make_float4(n0.x * e0, n0.y * e0, n0.z * e0, n0.w * e0);
+            *reinterpret_cast<float4 *>(po + kHeadDim) =
+                make_float4(n1.x * e1, n1.y * e1, n1.z * e1, n1.w * e1);
+            if (lane == 0) {
+              p.part_lse[gs * kHq + 2 * gh] = L0 + log2f(d0);
+              p.part_lse[gs * kHq + 2 * gh + 1] = L1 + log2f(d1);
+              p.gcounters[gs * kHkv + gh] = 0;
+            }
+            __threadfence();
+            __syncwarp();
+            const int ng = (ns + kMergeGroup - 1) / kMergeGroup;
+            int old = 0;
+            if (lane == 0) old = atomicAdd(&p.counters[(int64_t)h.r * kHkv + gh], 1);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old != ng - 1) break;                  // not the last group
+            mb = 0;
+            ms = kMergeGroup;
+            mn = ng;
+            to_out = true;
           }
-          if (lane == 0) p.counters[(int64_t)h.r * kHkv + gh] = 0;
+        } else {
+          int old = 0;
+          if (lane == 0) old = atomicAdd(&p.counters[(int64_t)h.r * kHkv + gh], 1);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if (old == h.bl - h.bf) {
+            // last of the (request, KV head) splits: merge them (one level).  The splits'
+            // lse values are loaded by the lanes side by side (split bf + k by
+            // lane k % 32), the o rows split after split with several loads in
+            // flight; the sums run in split order.
+            __threadfence();
+            const int ns = h.bl - h.bf + 1;
+            auto slot_of = [&](int k) {
+              return 2 * (int64_t)(h.bf + k) + (k == 0 ? h.head_shift : 0);
+            };
+            // split `lane`'s lse values and the first batch of o rows, all in
+            // flight at once; the lse values stay in their lanes for the weights
+            float4 xs[kMergeBatch], ys[kMergeBatch];
+  #pragma unroll
+            for (int u = 0; u < kMergeBatch; ++u) {
+              if (u < ns) {
+                const float *pr0 = p.part_o + (slot_of(u) * kHq + 2 * gh) * kHeadDim + lane * 4;
+                xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
+                ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+              }
+            }
+            float l0 = -INFINITY, l1 = -INFINITY;
+            if (lane < ns) {
+              const int64_t sl = slot_of(lane);
+              l0 = __ldcg(p.part_lse + sl * kHq + 2 * gh);
+              l1 = __ldcg(p.part_lse + sl * kHq + 2 * gh + 1);
+            }
+            float L0 = l0, L1 = l1;
+            for (int k = lane + 32; k < ns; k += 32) {
+              const int64_t sl = slot_of(k);
+              L0 = fmaxf(L0, __ldcg(p.part_lse + sl * kHq + 2 * gh));
+              L1 = fmaxf(L1, __ldcg(p.part_lse + sl * kHq + 2 * gh + 1));
+            }
+  #pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              L0 = fmaxf(L0, __shfl_xor_sync(0xffffffffu, L0, o));
+              L1 = fmaxf(L1, __shfl_xor_sync(0xffffffffu, L1, o));
+            }
+            float4 n0 = make_float4(0.f, 0.f, 0.f, 0.f), n1 = n0;
+            float d0 = 0.f, d1 = 0.f;
+            for (int k0 = 0; k0 < ns; k0 += 32) {
+              float w0 = 0.f, w1 = 0.f;
+              if (k0 == 0) {
+                if (lane < ns) {
+                  w0 = exp2f(l0 - L0);
+                  w1 = exp2f(l1 - L1);
+                }
+              } else if (k0 + lane < ns) {
+                const int64_t sl = slot_of(k0 + lane);
+                w0 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh) - L0);
+                w1 = exp2f(__ldcg(p.part_lse + sl * kHq + 2 * gh + 1) - L1);
+              }
+              const int nk = ns - k0 < 32 ? ns - k0 : 32;
+              for (int j0 = 0; j0 < nk; j0 += kMergeBatch) {
+                if (k0 > 0 || j0 > 0) {
+  #pragma unroll
+                  for (int u = 0; u < kMergeBatch; ++u) {   // the batch's loads, all in flight
+                    if (j0 + u < nk) {
+                      const float *pr0 =
+                          p.part_o + (slot_of(k0 + j0 + u) * kHq + 2 * gh) * kHeadDim + lane * 4;
+                      xs[u] = __ldcg(reinterpret_cast<const float4 *>(pr0));
+                      ys[u] = __ldcg(reinterpret_cast<const float4 *>(pr0 + kHeadDim));
+                    }
+                  }
+                }
+  #pragma unroll
+                for (int u = 0; u < kMergeBatch; ++u) {
+                  if (j0 + u >= nk) break;
+                  const float a0 = __shfl_sync(0xffffffffu, w0, j0 + u);
+                  const float a1 = __shfl_sync(0xffffffffu, w1, j0 + u);
+                  const float4 x = xs[u], y = ys[u];
+                  n0.x = fmaf(a0, x.x, n0.x); n0.y = fmaf(a0, x.y, n0.y);
+                  n0.z = fmaf(a0, x.z, n0.z); n0.w = fmaf(a0, x.w, n0.w);
+                  n1.x = fmaf(a1, y.x, n1.x); n1.y = fmaf(a1, y.y, n1.y);
+                  n1.z = fmaf(a1, y.z, n1.z); n1.w = fmaf(a1, y.w, n1.w);
+                  d0 += a0;
+                  d1 += a1;
+                }
+              }
+            }
+            if (row_ok) {
+              const float e0 = 1.f / d0, e1 = 1.f / d1;
+              *reinterpret_cast<uint2 *>(op) =
+                  make_uint2(pack_bf16(n0.x * e0, n0.y * e0), pack_bf16(n0.z * e0, n0.w * e0));
+              *reinterpret_cast<uint2 *>(op + kHeadDim) =
+                  make_uint2(pack_bf16(n1.x * e1, n1.y * e1), pack_bf16(n1.z * e1, n1.w * e1));
+            }
+            if (lane == 0) p.counters[(int64_t)h.r * kHkv + gh] = 0;
+          }
         }
       }
     }
@@ -628,7 +771,8 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
 }
 
 template <int HKV>
-cudaError_t launch_decode_h(const AttnParams &p, int grid, bool pdl, cudaStream_t s) {
+cudaError_t launch_decode_h(const AttnParams &p, int grid, bool pdl, bool two_level,
+                            cudaStream_t s) {
   using S = Dec<HKV>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -636,17 +780,25 @@ cudaError_t launch_decode_h(const AttnParams &p, int grid, bool pdl, cudaStream_
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    for (auto k : {decode_kernel<HKV, true, false>, decode_kernel<HKV, false, false>,
-                   decode_kernel<HKV, true, true>, decode_kernel<HKV, false, true>}) {
+    for (auto k : {decode_kernel<HKV, true, false, false>, decode_kernel<HKV, false, false, false>,
+                   decode_kernel<HKV, true, true, false>, decode_kernel<HKV, false, true, false>,
+                   decode_kernel<HKV, true, false, true>, decode_kernel<HKV, false, false, true>,
+                   decode_kernel<HKV, true, true, true>, decode_kernel<HKV, false, true, true>}) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kSmem);
       if (e != cudaSuccess) return e;
     }
     attr_set[dev] = true;
   }
   const bool fused = p.k_new != nullptr;
-  auto k = p.page_size == 1
-               ? (fused ? decode_kernel<HKV, true, true> : decode_kernel<HKV, true, false>)
-               : (fused ? decode_kernel<HKV, false, true> : decode_kernel<HKV, false, false>);
+  auto k = two_level
+               ? (p.page_size == 1 ? (fused ? decode_kernel<HKV, true, true, true>
+                                            : decode_kernel<HKV, true, false, true>)
+                                   : (fused ? decode_kernel<HKV, false, true, true>
+                                            : decode_kernel<HKV, false, false, true>))
+               : (p.page_size == 1 ? (fused ? decode_kernel<HKV, true, true, false>
+                                            : decode_kernel<HKV, true, false, false>)
+                                   : (fused ? decode_kernel<HKV, false, true, false>
+                                            : decode_kernel<HKV, false, false, false>));
   return launch_k(k, dim3(grid), dim3(S::kThreads), S::kSmem, s, pdl, p);
 }
 
@@ -658,10 +810,10 @@ int ctas_per_sm_h() {
   if (cache[dev] == 0) {
     int n = 0;
     // the shared memory of the launch decides how many CTAs share an SM
-    if (cudaFuncSetAttribute(decode_kernel<HKV, true, false>,
+    if (cudaFuncSetAttribute(decode_kernel<HKV, true, false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)Dec<HKV>::kSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<HKV, true, false>,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<HKV, true, false, false>,
                                                       Dec<HKV>::kThreads,
                                                       Dec<HKV>::kSmem) != cudaSuccess ||
         n <= 0)
@@ -673,13 +825,14 @@ int ctas_per_sm_h() {
 
 }  // namespace
 
-cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s) {
+cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, bool two_level,
+                          cudaStream_t s) {
   if (p.num_qo_heads != kGroup * p.num_kv_heads) return cudaErrorInvalidValue;
   switch (p.num_kv_heads) {
-    case 8: return launch_decode_h<8>(p, grid, pdl, s);
-    case 4: return launch_decode_h<4>(p, grid, pdl, s);
-    case 2: return launch_decode_h<2>(p, grid, pdl, s);
-    case 1: return launch_decode_h<1>(p, grid, pdl, s);
+    case 8: return launch_decode_h<8>(p, grid, pdl, two_level, s);
+    case 4: return launch_decode_h<4>(p, grid, pdl, two_level, s);
+    case 2: return launch_decode_h<2>(p, grid, pdl, two_level, s);
+    case 1: return launch_decode_h<1>(p, grid, pdl, two_level, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,6 +17,10 @@ constexpr int kGroup = 2;                 // query heads per KV head
 constexpr int kMaxKvHeads = 8;            // KV heads of a full layer (16 query heads); a
                                           // tensor-parallel slice passes 4, 2 or 1
 constexpr int kMaxDecodeCtas = 512;       // decode CTAs at 8 KV heads (2 partial slots each)
+// Group counters of the two-level split merge, one per (partial slot, KV
+// head): slots x KV heads is at most 2 kMaxDecodeCtas x 8 at every head count
+// (fewer heads, proportionally more CTAs).
+constexpr int kGroupCounters = 2 * kMaxDecodeCtas * kMaxKvHeads;
 // The decode plan lays the requests' keys end to end with this many empty
 // key positions after each request: the decode CTAs split that space evenly,
 // so a CTA whose range holds a request boundary (a second segment: its q, its
@@ -59,6 +63,7 @@ struct WsLayout {
   size_t dec_row = 0;      // int64[num_reqs]       index row offset of each decode request
   size_t dec_qrow = 0;     // int32[num_reqs]       its query row (qo_indptr)
   size_t counters = 0;     // int32[num_reqs * 8]   split merge counters (request, KV head)
+  size_t gcounters = 0;    // int32[kGroupCounters] group merge counters (slot, KV head)
   size_t ext_tiles = 0;    // int32x2[max_tiles]    (request, query tile)
   size_t part_lse = 0;     // float[2 * max_decode_ctas(Hq) * Hq]
   size_t part_o = 0;       // float[2 * max_decode_ctas(Hq) * Hq * D]
@@ -99,6 +104,7 @@ inline WsLayout ws_layout(int64_t num_reqs, int64_t total_q, int64_t hq, int64_t
   L.dec_row = take(sizeof(int64_t) * (num_reqs + 1));
   L.dec_qrow = take(sizeof(int32_t) * (num_reqs + 1));
   L.counters = take(sizeof(int32_t) * (num_reqs + 1) * kMaxKvHeads);
+  L.gcounters = take(sizeof(int32_t) * kGroupCounters);
   L.max_tiles = (total_q + kExtendTileTokens - 1) / kExtendTileTokens + num_reqs + 1;
   L.ext_tiles = take(sizeof(int32_t) * 2 * L.max_tiles);
   L.ext_items = take(sizeof(int32_t) * 4 * kExtSlots);
@@ -141,6 +147,7 @@ struct PlanParams {
   int64_t *dec_row;             // offset of the request's row (or ragged range) in the index
   int32_t *dec_qrow;
   int32_t *counters;
+  int32_t *gcounters;           // kGroupCounters, zeroed with the counters
   int32_t *ext_tiles;           // pairs
   int64_t max_tiles;
 };
@@ -205,6 +212,7 @@ struct AttnParams {
   const int64_t *dec_row;
   const int32_t *dec_qrow;
   int32_t *counters;
+  int32_t *gcounters;           // group counters of the two-level split merge
   const int32_t *ext_tiles;
   float *part_lse;
   float *part_o;
@@ -237,7 +245,10 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t launch_plan(const PlanParams &p, cudaStream_t s);
 cudaError_t launch_token_meta(const TokenMetaParams &p, cudaStream_t s);
 cudaError_t launch_store_kv(const StoreParams &p, cudaStream_t s);
-cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, cudaStream_t s);
+// two_level: the decode instance that merges requests cut into many splits in
+// two levels (taken by the host for batches of few long requests).
+cudaError_t launch_decode(const AttnParams &p, int grid, bool pdl, bool two_level,
+                          cudaStream_t s);
 cudaError_t launch_extend(const AttnParams &p, int64_t max_tiles, int64_t max_kv_len,
                           cudaStream_t s);
 int device_sm_count();

@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     ext_reqs = 0;
     ext_units = 0;
   }
+  for (int i = tid; i < kGroupCounters; i += kPlanThreads) p.gcounters[i] = 0;
   __syncthreads();
 
   for (int32_t base = 0; base < p.num_reqs; base += kPlanThreads) {

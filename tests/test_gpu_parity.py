@@ -84,6 +84,37 @@ def test_long_single_decode_splits_over_all_ctas():
 
 
 @pytest.mark.parametrize("page_size", [1, 16])
+def test_few_long_decodes_both_merge_instances(page_size):
+    """A few long decode requests, each cut over 30-70 CTAs: with max_kv_len
+    given the library takes the decode instance that merges the splits in two
+    levels (groups of 8, then the groups); without it the one-level instance.
+    Both match the oracle, and each is bit-identical on repeat."""
+    rng = np.random.default_rng(590 + page_size)
+    cached = rng.integers(2000, 6000, size=6)
+    pages = int(sum((c + page_size) // page_size + 1 for c in cached)) + 32
+    spec = wl.make_batch("few_long", 590 + page_size, cached, np.ones(6, np.int32), page_size,
+                         num_pages=pages)
+    host = wl.host_tensors(spec)
+    ref = oracle_small(spec, host)["out"]
+    for mkv in (spec.max_kv_len, 0):
+        outs = []
+        for _ in range(2):
+            gb = GpuBatch(spec)
+            q = wl.bits_to_torch(host["q"], "cuda")
+            kp = wl.bits_to_torch(host["k_pool"], "cuda")
+            vp = wl.bits_to_torch(host["v_pool"], "cuda")
+            loc = gb.plan()
+            msg.msg_store_kv(wl.bits_to_torch(host["k_new"], "cuda"),
+                             wl.bits_to_torch(host["v_new"], "cuda"), kp, vp, loc, dev_status=gb.ws)
+            out = gb.attention(q, kp, vp, flags=msg.MSG_ATTN_REUSE_PLAN, max_kv_len=mkv)
+            torch.cuda.synchronize()
+            assert gb.status()[0] == msg.MSG_OK, gb.status()
+            outs.append(wl.torch_to_bits(out))
+        assert np.array_equal(outs[0], outs[1])
+        assert_attn_close(outs[0], ref, f"few_long max_kv_len={mkv}")
+
+
+@pytest.mark.parametrize("page_size", [1, 16])
 def test_fused_store_decode_is_store_then_attend(page_size):
     """msg_paged_attention_store (store_kv done by the decode kernel, the newest
     key gathered from k_new / v_new) gives the output and pool bits of
