@@ -74,11 +74,12 @@ constexpr int kOffQ = 0;
 constexpr int kOffRing = 2 * kQSub;
 constexpr int kOffBar = kOffRing + kSlots * kSlot;
 constexpr int kBarBytes = 512;               // mbarriers, TMEM address, abort flag
-constexpr int kItemQueue = 16;                // work pieces published ahead of the slowest role
+constexpr int kItemQueue = 8;                 // work pieces published ahead of the slowest role
+constexpr int kQEntry = 12;                   // int32 per queue entry: the piece, then its item
 // key split (few work items): the tiles' key-tile prefix, then the piece queue
 constexpr int kOffPre = kOffBar + kBarBytes;
 constexpr int kOffQueue = kOffPre + (kExtMaxTiles + 4) * 4;
-constexpr int kOffGrab = kOffQueue + kItemQueue * 16;   // the grabber's state (GrabState)
+constexpr int kOffGrab = kOffQueue + kItemQueue * kQEntry * 4;   // the grabber's state (GrabState)
 constexpr size_t kSmem = (size_t)kOffGrab + 64 + 1024;   // + 1 KiB alignment slack
 static_assert(kSmem <= 232448, "227 KiB of shared memory per CTA");
 static_assert(kBN == kExtendTileTokens, "the plan counts key tiles of kExtendTileTokens keys");
@@ -248,6 +249,34 @@ struct Item {
   bool ok;
 };
 
+// An item as the grabber publishes it in the piece queue (every length and
+// row index fits int32), and as the other roles read it back: the plan's
+// global loads are made once, ahead of the roles that wait on the item.
+__device__ __forceinline__ void put_item(volatile int32_t *q, const Item &it) {
+  q[4] = (int32_t)it.cached;
+  q[5] = (int32_t)it.q0;
+  q[6] = (int32_t)it.qrow0;
+  q[7] = it.r;
+  q[8] = it.gh;
+  q[9] = it.nq;
+  q[10] = it.ok ? 1 : 0;
+}
+__device__ __forceinline__ Item get_item(const volatile int32_t *q) {
+  Item it;
+  it.cached = q[4];
+  it.q0 = q[5];
+  it.qrow0 = q[6];
+  it.r = q[7];
+  it.gh = q[8];
+  it.nq = q[9];
+  it.ok = q[10] != 0;
+  it.kv_end = it.cached + it.q0 + it.nq;
+  it.n_tiles = it.ok ? (int)((it.kv_end + kBN - 1) / kBN) : 0;
+  const int64_t kv_a = it.cached + it.q0 + (it.nq < kSubTok ? it.nq : kSubTok);
+  it.n_a = it.ok ? (int)((kv_a + kBN - 1) / kBN) : 0;
+  return it;
+}
+
 __device__ __forceinline__ Item load_item(const AttnParams &p, int w) {
   Item it;
   const int tile = w / p.num_kv_heads;
@@ -400,8 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // it starts loading it (from the global counter, or the next piece of this
   // CTA's split range), published through a 16-entry queue; every role reads
   // the same sequence.  w = -1: no more work.
-  auto fetch_piece = [&](uint32_t k, bool grab, bool whole_warp) -> Piece {
+  auto fetch_piece = [&](uint32_t k, bool grab, bool whole_warp, Item &it) -> Piece {
     const int e = (int)(k % kItemQueue);
+    volatile int32_t *qe = piece_q + kQEntry * e;
     if (grab) {
       Piece pc{-1, 0, -1, 0u};
       if (kSplit && gs->split) {
@@ -411,12 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         pc.w = atomicAdd(next_ctr, 1);
         if (pc.w >= hdr.ext_tile_count * p.num_kv_heads) pc.w = -1;
       }
-      piece_q[4 * e] = pc.w;
+      qe[0] = pc.w;
       if (kSplit) {
-        piece_q[4 * e + 1] = pc.j0;
-        piece_q[4 * e + 2] = pc.j1;
-        piece_q[4 * e + 3] = (int32_t)pc.meta;
+        qe[1] = pc.j0;
+        qe[2] = pc.j1;
+        qe[3] = (int32_t)pc.meta;
       }
+      if (pc.w >= 0) put_item(qe, load_item(p, pc.w));
       mbar_arrive(&bars[kBarItem + e]);
     }
     if (whole_warp) __syncwarp();
@@ -425,9 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       report(p.status, MSG_DEV_TIMEOUT, -1, -3);
       return Piece{-1, 0, 0, 0u};
     }
-    if (!kSplit) return Piece{piece_q[4 * e], 0, -1, 0u};   // whole items
-    return Piece{piece_q[4 * e], piece_q[4 * e + 1], piece_q[4 * e + 2],
-                 (uint32_t)piece_q[4 * e + 3]};
+    const Piece pc = kSplit ? Piece{qe[0], qe[1], qe[2], (uint32_t)qe[3]}
+                            : Piece{qe[0], 0, -1, 0u};   // whole items
+    if (pc.w >= 0) it = get_item(qe);
+    return pc;
   };
   if (blockIdx.x == 0 && tid == 0 && (p.flags & MSG_ATTN_EXTEND_ONLY) && hdr.dec_count > 0)
     report(p.status, MSG_DEV_WRONG_PHASE, hdr.dec_count, hdr.dec_keys);
@@ -513,9 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t N = 0;                                     // ring items issued
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
-      const Piece pc = fetch_piece(k, warp == 1 && lane == 0, true);
+      Item it;
+      const Piece pc = fetch_piece(k, warp == 1 && lane == 0, true, it);
       if (pc.w < 0) break;
-      const Item it = load_item(p, pc.w);
       const int j0 = pc.j0, j1 = pc.j1 < 0 ? it.n_tiles : pc.j1;
       const int na = (j1 < it.n_a ? j1 : it.n_a) - j0;
       if (j1 <= j0 || na <= 0) continue;
@@ -674,9 +706,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t Ts[2] = {0, 0}, N = 0, V = 0;       // tiles per sub-tile, ring items, items done
       bool ok = true;
       for (uint32_t k = 0; ok; ++k) {
-        const Piece pc = fetch_piece(k, false, false);   // lane 0 alone
+        Item it;
+        const Piece pc = fetch_piece(k, false, false, it);   // lane 0 alone
         if (pc.w < 0) break;
-        const Item it = load_item(p, pc.w);
         const int j1 = pc.j1 < 0 ? it.n_tiles : pc.j1;
         const int n = j1 - pc.j0;                        // key tiles of sub-tile b
         const int na = (j1 < it.n_a ? j1 : it.n_a) - pc.j0;   // of sub-tile a
@@ -783,9 +815,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t T = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
-    const Piece pc = fetch_piece(k, false, true);
+    Item it;
+    const Piece pc = fetch_piece(k, false, true, it);
     if (pc.w < 0) break;
-    const Item it = load_item(p, pc.w);
     if (it.n_tiles == 0) {
       if (x == 0 && row == 0 && !it.ok) report(p.status, MSG_DEV_BAD_LENGTHS, it.r, it.qrow0);
       continue;
