@@ -1243,7 +1243,6 @@ __device__ int draw_list(const Ctx &x, Smem &sm, int n, float u) {
 struct WsRef {
   float *cmax, *cmass;                         // [row][nl_cap]
   uint32_t *samp;                              // [row][ns_cap]
-  unsigned long long *best;                    // [row][nparts]: greedy key of the part
   uint32_t *bad;                               // [row][nparts]: a non-finite logit seen
   int nl_cap, ns_cap, nparts;
 };
@@ -1254,61 +1253,40 @@ constexpr int kChunksPerCta = 64;              // vector chunks of a scan CTA (1
 constexpr int kScanPerWarp = kChunksPerCta / kScanWarps;
 
 // ---- the scan (HBM, once): per chunk its maximum and its mass relative to
-// it, the sample, the part's first maximum and finiteness.  Grid (parts, rows).
-template <bool kBf16, bool kGreedy>
+// it, the sample, and the part's finiteness.  Grid (parts, rows).
+template <bool kBf16>
 __global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams p, WsRef ws) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int part = blockIdx.x, row = blockIdx.y;
   const RowRef r = row_ref<kBf16>(p.logits + (int64_t)row * p.row_bytes, p.vocab);
   const int spc = r.nch <= kMaxSamples / 4 ? 4 : 2;
-  float kx = 0.f;
-  if (!kGreedy) kx = 1.4426950408889634f / fmaxf(p.temperature[row], kMinT);
+  const float kx = 1.4426950408889634f / fmaxf(p.temperature[row], kMinT);
   float *cmax = ws.cmax + (int64_t)row * ws.nl_cap, *cmass = ws.cmass + (int64_t)row * ws.nl_cap;
   uint32_t *samp = ws.samp + (int64_t)row * ws.ns_cap;
   bool finite = true;
-  unsigned long long best = 0;                  // (key << 32) | ~index, max wins
   auto chunk = [&](const float v[kLE], int n, int c_logical, int i0, int sample_slot) {
-    if (kGreedy) {
-      // the lane's largest value (NaN if any is NaN), then its first position:
-      // the largest (key, ~index) of the lane's logits
-      float mv = -INFINITY;
+    float m = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kLE; ++j)
-        if (j < n) mv = fmax_nan(mv, v[j]);
-      finite &= mv == mv;
-      int jj = -1;
+    for (int j = 0; j < kLE; ++j)
+      if (j < n) m = fmaxf(m, v[j]);
+    m = warp_max_f(m);
+    // sum of 2^((v - m) kx), even and odd positions apart, in pairs
+    float2 s2 = make_float2(0.f, 0.f);
+    const float2 nm2 = make_float2(-m, -m), kx2 = make_float2(kx, kx);
 #pragma unroll
-      for (int j = kLE - 1; j >= 0; --j)
-        if (j < n && v[j] == mv) jj = j;
-      if (jj >= 0) {
-        const unsigned long long kk =
-            ((unsigned long long)key_of(mv) << 32) | (0xffffffffu - (uint32_t)(i0 + jj));
-        best = kk > best ? kk : best;
-      }
-    } else {
-      float m = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kLE; ++j)
-        if (j < n) m = fmaxf(m, v[j]);
-      m = warp_max_f(m);
-      // sum of 2^((v - m) kx), even and odd positions apart, in pairs
-      float2 s2 = make_float2(0.f, 0.f);
-      const float2 nm2 = make_float2(-m, -m), kx2 = make_float2(kx, kx);
-#pragma unroll
-      for (int j = 0; j < kLE; j += 2) {
-        const float2 y = fmul2(fadd2(make_float2(v[j], v[j + 1]), nm2), kx2);
-        s2 = fadd2(s2, make_float2(j < n ? ex2(y.x) : 0.f, j + 1 < n ? ex2(y.y) : 0.f));
-      }
-      float s = warp_sum_f(s2.x + s2.y);
-      // a NaN turns the mass into NaN, +inf the maximum; -inf is a zero-mass logit
-      if (m == -INFINITY) s = 0.f;
-      finite &= m != INFINITY && s == s;
-      if (lane == 0) {
-        cmax[c_logical] = m;
-        cmass[c_logical] = s;
-      }
-      if (sample_slot >= 0) samp[sample_slot] = (n && v[0] != m) ? ~key_of(v[0]) : ~0u;
+    for (int j = 0; j < kLE; j += 2) {
+      const float2 y = fmul2(fadd2(make_float2(v[j], v[j + 1]), nm2), kx2);
+      s2 = fadd2(s2, make_float2(j < n ? ex2(y.x) : 0.f, j + 1 < n ? ex2(y.y) : 0.f));
     }
+    float s = warp_sum_f(s2.x + s2.y);
+    // a NaN turns the mass into NaN, +inf the maximum; -inf is a zero-mass logit
+    if (m == -INFINITY) s = 0.f;
+    finite &= m != INFINITY && s == s;
+    if (lane == 0) {
+      cmax[c_logical] = m;
+      cmass[c_logical] = s;
+    }
+    if (sample_slot >= 0) samp[sample_slot] = (n && v[0] != m) ? ~key_of(v[0]) : ~0u;
   };
   const int cbeg = part * kChunksPerCta + warp;
   uint4 raw[kScanPerWarp][kBf16 ? 1 : 2];
@@ -1343,65 +1321,54 @@ __global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams 
     }
   };
   const int every = 32 / spc;
-  if (kGreedy) {
+  // the warp's chunks side by side: maxima, then masses relative to them,
+  // each reduced over the warp for all chunks at once
+  float m[kScanPerWarp], sm2[kScanPerWarp];
 #pragma unroll
-    for (int q = 0; q < kScanPerWarp; ++q) {
-      const int c = cbeg + q * kScanWarps;
-      if (c >= r.nch) break;                    // warp-uniform
-      float v[kLE];
-      unpack(q, v);
-      chunk(v, n[q], c + 1, r.h + kLE * (32 * c + lane), -1);
+  for (int q = 0; q < kScanPerWarp; ++q) {
+    float v[kLE];
+    unpack(q, v);
+    m[q] = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kLE; ++j)
+      if (j < n[q]) m[q] = fmaxf(m[q], v[j]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int q = 0; q < kScanPerWarp; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
+#pragma unroll
+  for (int q = 0; q < kScanPerWarp; ++q) {
+    float v[kLE];
+    unpack(q, v);
+    float2 s2 = make_float2(0.f, 0.f);
+    const float2 nm2 = make_float2(-m[q], -m[q]), kx2 = make_float2(kx, kx);
+#pragma unroll
+    for (int j = 0; j < kLE; j += 2) {
+      const float2 y = fmul2(fadd2(make_float2(v[j], v[j + 1]), nm2), kx2);
+      s2 = fadd2(s2, make_float2(j < n[q] ? ex2(y.x) : 0.f, j + 1 < n[q] ? ex2(y.y) : 0.f));
     }
-  } else {
-    // the warp's chunks side by side: maxima, then masses relative to them,
-    // each reduced over the warp for all chunks at once
-    float m[kScanPerWarp], sm2[kScanPerWarp];
+    sm2[q] = s2.x + s2.y;
+  }
 #pragma unroll
-    for (int q = 0; q < kScanPerWarp; ++q) {
-      float v[kLE];
-      unpack(q, v);
-      m[q] = -INFINITY;
+  for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-      for (int j = 0; j < kLE; ++j)
-        if (j < n[q]) m[q] = fmaxf(m[q], v[j]);
+    for (int q = 0; q < kScanPerWarp; ++q) sm2[q] += __shfl_xor_sync(0xffffffffu, sm2[q], o);
+#pragma unroll
+  for (int q = 0; q < kScanPerWarp; ++q) {
+    const int c = cbeg + q * kScanWarps;
+    if (c >= r.nch) break;                    // warp-uniform
+    // a NaN turns the mass into NaN, +inf the maximum; -inf is a zero-mass logit
+    const float s = m[q] == -INFINITY ? 0.f : sm2[q];
+    finite &= m[q] != INFINITY && s == s;
+    if (lane == 0) {
+      cmax[c + 1] = m[q];
+      cmass[c + 1] = s;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int q = 0; q < kScanPerWarp; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
-#pragma unroll
-    for (int q = 0; q < kScanPerWarp; ++q) {
-      float v[kLE];
-      unpack(q, v);
-      float2 s2 = make_float2(0.f, 0.f);
-      const float2 nm2 = make_float2(-m[q], -m[q]), kx2 = make_float2(kx, kx);
-#pragma unroll
-      for (int j = 0; j < kLE; j += 2) {
-        const float2 y = fmul2(fadd2(make_float2(v[j], v[j + 1]), nm2), kx2);
-        s2 = fadd2(s2, make_float2(j < n[q] ? ex2(y.x) : 0.f, j + 1 < n[q] ? ex2(y.y) : 0.f));
-      }
-      sm2[q] = s2.x + s2.y;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int q = 0; q < kScanPerWarp; ++q) sm2[q] += __shfl_xor_sync(0xffffffffu, sm2[q], o);
-#pragma unroll
-    for (int q = 0; q < kScanPerWarp; ++q) {
-      const int c = cbeg + q * kScanWarps;
-      if (c >= r.nch) break;                    // warp-uniform
-      // a NaN turns the mass into NaN, +inf the maximum; -inf is a zero-mass logit
-      const float s = m[q] == -INFINITY ? 0.f : sm2[q];
-      finite &= m[q] != INFINITY && s == s;
-      if (lane == 0) {
-        cmax[c + 1] = m[q];
-        cmass[c + 1] = s;
-      }
-      if ((lane & (every - 1)) == 0) {
-        float v0[kLE];
-        unpack(q, v0);
-        samp[c * spc + lane / every] = (n[q] && v0[0] != m[q]) ? ~key_of(v0[0]) : ~0u;
-      }
+    if ((lane & (every - 1)) == 0) {
+      float v0[kLE];
+      unpack(q, v0);
+      samp[c * spc + lane / every] = (n[q] && v0[0] != m[q]) ? ~key_of(v0[0]) : ~0u;
     }
   }
   if (part == 0 && warp == 0) {                 // head and tail chunks
@@ -1413,20 +1380,6 @@ __global__ void __launch_bounds__(kScanThreads) sample_scan_kernel(SampleParams 
     }
   }
   const bool bad = __syncthreads_or(!finite);
-  if (kGreedy) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-      best = y > best ? y : best;
-    }
-    __shared__ unsigned long long wbest[kScanWarps];
-    if (lane == 0) wbest[warp] = best;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < kScanWarps; ++w) best = wbest[w] > best ? wbest[w] : best;
-      ws.best[(int64_t)row * ws.nparts + part] = best;
-    }
-  }
   if (threadIdx.x == 0) ws.bad[(int64_t)row * ws.nparts + part] = bad ? 1u : 0u;
   grid_dep_launch();
 }
@@ -1486,12 +1439,12 @@ __device__ int row_of_block(const SampleParams &p, Smem &sm) {
 }
 
 // ---- the row (one CTA each): everything after the scan
-template <bool kBf16, bool kGreedy>
+template <bool kBf16>
 __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef ws) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int row = kGreedy ? (int)blockIdx.x : row_of_block(p, sm);
+  const int row = row_of_block(p, sm);
   Ctx x;
   x.r = row_ref<kBf16>(p.logits + (int64_t)row * p.row_bytes, p.vocab);
   x.nl = x.r.nch + 2;
@@ -1500,39 +1453,21 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
   x.M = 0.f;
 
   // ---- row parameters (Sampler.prepare's clamps)
-  float T = 1.f, u = 0.f, P = 1.f;
+  const float T = p.temperature[row], u = p.uniform[row];
+  float P = 1.f;
   unsigned long long k = (unsigned long long)p.vocab;
   bool params_ok = true;
-  if (!kGreedy) {
-    T = p.temperature[row];
-    u = p.uniform[row];
-    if (p.top_k != nullptr && p.top_k[row] >= 1 && p.top_k[row] < p.vocab) k = p.top_k[row];
-    if (p.top_p != nullptr) {
-      P = fminf(fmaxf(p.top_p[row], kMinP), 1.f);
-      params_ok = !isnan(p.top_p[row]);
-    }
-    params_ok = params_ok && isfinite(T) && u >= 0.f && u < 1.f;
+  if (p.top_k != nullptr && p.top_k[row] >= 1 && p.top_k[row] < p.vocab) k = p.top_k[row];
+  if (p.top_p != nullptr) {
+    P = fminf(fmaxf(p.top_p[row], kMinP), 1.f);
+    params_ok = !isnan(p.top_p[row]);
   }
+  params_ok = params_ok && isfinite(T) && u >= 0.f && u < 1.f;
   x.kx = 1.4426950408889634f / fmaxf(T, kMinT);
   grid_dep_wait();                              // the scan's summaries
   bool bad = false;
-  unsigned long long best = 0;
-  for (int i = threadIdx.x; i < ws.nparts; i += kT) {
-    bad |= ws.bad[(int64_t)row * ws.nparts + i] != 0;
-    if (kGreedy) {
-      const unsigned long long b = ws.best[(int64_t)row * ws.nparts + i];
-      best = b > best ? b : best;
-    }
-  }
+  for (int i = threadIdx.x; i < ws.nparts; i += kT) bad |= ws.bad[(int64_t)row * ws.nparts + i] != 0;
   bad = __syncthreads_or(bad);
-  if (kGreedy) {
-    best = block_max_u(best, sm);
-    if (threadIdx.x == 0) {
-      if (bad) report(p.status, MSG_DEV_BAD_LOGIT, row, 0);
-      p.tokens[row] = bad ? -1 : (int32_t)(0xffffffffu - (uint32_t)(best & 0xffffffffu));
-    }
-    return;
-  }
   if (bad || !params_ok) {
     if (threadIdx.x == 0) {
       report(p.status, bad ? MSG_DEV_BAD_LOGIT : MSG_DEV_BAD_SAMPLING, row, 0);
@@ -1818,10 +1753,107 @@ __global__ void __launch_bounds__(kT, 2) sample_row_kernel(SampleParams p, WsRef
   }
 }
 
+// ---- every row greedy (no temperatures): the token is the row's first
+// maximum.  One CTA per row (two per SM, so a batch of up to twice the SMs is
+// resident at once) reads the row once from HBM, each thread with 128 bytes
+// of logits in flight (8 vectors of 8 bf16, 4 of 8 fp32), keeping the
+// largest (key, ~index) it sees; a NaN anywhere marks the row bad.  One
+// launch, no workspace traffic.
+constexpr int kGreedyThreads = 512;
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kGreedyThreads, 2) sample_greedy_kernel(SampleParams p) {
+  constexpr int esz = kBf16 ? 2 : 4;
+  constexpr int kGreedyUnroll = kBf16 ? 8 : 4;
+  const int row = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const RowRef r = row_ref<kBf16>(p.logits + (int64_t)row * p.row_bytes, p.vocab);
+  bool bad = false;
+  unsigned long long best = 0;                  // (key << 32) | ~index, max wins
+  auto take = [&](const float v[kLE], int n, int i0) {
+    float mv = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kLE; ++j)
+      if (j < n) mv = fmax_nan(mv, v[j]);
+    bad |= mv != mv;
+    const unsigned long long kmv = (unsigned long long)key_of(mv) << 32;
+    if (n > 0 && (kmv | 0xffffffffu) > best) {  // this vector may hold a better (key, index)
+      int jj = 0;
+#pragma unroll
+      for (int j = kLE - 1; j >= 0; --j)
+        if (j < n && v[j] == mv) jj = j;
+      const unsigned long long kk = kmv | (0xffffffffu - (uint32_t)(i0 + jj));
+      best = kk > best ? kk : best;
+    }
+  };
+  for (int base = t; base < r.nvec; base += kGreedyUnroll * kGreedyThreads) {
+    uint4 raw[kGreedyUnroll][kBf16 ? 1 : 2];
+#pragma unroll
+    for (int u = 0; u < kGreedyUnroll; ++u) {   // every load of the round in flight at once
+      const int vi = base + u * kGreedyThreads;
+      if (vi < r.nvec) {
+        const uint8_t *src = r.p + (int64_t)(r.h + kLE * vi) * esz;
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(raw[u][0].x), "=r"(raw[u][0].y), "=r"(raw[u][0].z), "=r"(raw[u][0].w)
+                     : "l"(src));
+        if (!kBf16)
+          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(raw[u][kBf16 ? 0 : 1].x), "=r"(raw[u][kBf16 ? 0 : 1].y),
+                         "=r"(raw[u][kBf16 ? 0 : 1].z), "=r"(raw[u][kBf16 ? 0 : 1].w)
+                       : "l"(src + 16));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kGreedyUnroll; ++u) {
+      const int vi = base + u * kGreedyThreads;
+      if (vi < r.nvec) {
+        float v[kLE];
+        if (kBf16) {
+          const uint4 w = raw[u][0];
+          v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+          v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+        } else {
+          const uint4 a = raw[u][0], b = raw[u][kBf16 ? 0 : 1];
+          v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+          v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+          v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+          v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+        }
+        take(v, kLE, r.h + kLE * vi);
+      }
+    }
+  }
+  if (t == 0) {                                 // the head and the tail (< 8 logits each)
+    for (int c = 0; c < r.nch + 2; c += r.nch + 1) {
+      float v[kLE];
+      int i0;
+      const int n = chunk_lane<kBf16>(r, c, 0, v, i0);
+      take(v, n, i0);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+    best = y > best ? y : best;
+  }
+  __shared__ unsigned long long wbest[kGreedyThreads / 32];
+  if (lane == 0) wbest[warp] = best;
+  bad = __syncthreads_or(bad);
+  if (t == 0) {
+    for (int w = 1; w < kGreedyThreads / 32; ++w) best = wbest[w] > best ? wbest[w] : best;
+    if (bad) report(p.status, MSG_DEV_BAD_LOGIT, row, 0);
+    p.tokens[row] = bad ? -1 : (int32_t)(0xffffffffu - (uint32_t)(best & 0xffffffffu));
+  }
+  grid_dep_launch();
+}
+
 template <bool kBf16, bool kGreedy>
 cudaError_t launch_sample(const SampleParams &p, const WsRef &ws, cudaStream_t s) {
-  auto scan = sample_scan_kernel<kBf16, kGreedy>;
-  auto rowk = sample_row_kernel<kBf16, kGreedy>;
+  if (kGreedy) {
+    sample_greedy_kernel<kBf16><<<dim3((unsigned)p.batch), kGreedyThreads, 0, s>>>(p);
+    return cudaGetLastError();
+  }
+  auto scan = sample_scan_kernel<kBf16>;
+  auto rowk = sample_row_kernel<kBf16>;
   static bool configured = false;
   if (!configured) {
     const cudaError_t e =
@@ -1849,7 +1881,7 @@ inline WsSizes ws_sizes(int64_t batch, int32_t vocab) {
   z.nparts = (nch_cap + kChunksPerCta - 1) / kChunksPerCta;
   if (z.nparts < 1) z.nparts = 1;
   const size_t per_row = align_up((size_t)z.nl_cap * 4, 16) * 2 + align_up((size_t)z.ns_cap * 4, 16) +
-                         align_up((size_t)z.nparts * 8, 16) + align_up((size_t)z.nparts * 4, 16);
+                         align_up((size_t)z.nparts * 4, 16);
   z.bytes = per_row * (size_t)batch;
   return z;
 }
@@ -1902,8 +1934,6 @@ extern "C" int msg_sample(const void *logits, int32_t logits_dtype, int64_t logi
   w += align_up((size_t)z.nl_cap * 4, 16) * batch;
   ws.samp = reinterpret_cast<uint32_t *>(w);
   w += align_up((size_t)z.ns_cap * 4, 16) * batch;
-  ws.best = reinterpret_cast<unsigned long long *>(w);
-  w += align_up((size_t)z.nparts * 8, 16) * batch;
   ws.bad = reinterpret_cast<uint32_t *>(w);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
