@@ -13,7 +13,8 @@
 //   walks the requests its range touches.  A request cut by a range boundary
 //   leaves per-CTA partials (normalised o and its log-sum-exp) for each KV
 //   head; the warp that finishes last for (request, KV head) -- an atomic
-//   counter after a fence -- merges them.  No CTA or warp ever waits on another.
+//   counter with acquire-release semantics -- merges them.  No CTA or warp
+//   ever waits on another.
 // - Data movement.  One producer warp owns all global reads: it prefetches the
 //   page-table entries one tile ahead, gathers whole token rows (8 KV heads x
 //   256 B = 2 KiB) of K and V with cp.async.bulk (TMA, non-tensor) into a
@@ -53,6 +54,16 @@ static_assert(kDecSegPad < kMinKeysPerCta, "a CTA range must reach past any gap"
 // Launch shape for HKV KV heads (query heads 2 HKV): one consumer warp per KV
 // head plus the producer warp; a stage holds kTileKeys whole token rows of K
 // and of V (all HKV heads), one q row and a tile header.
+// Atomic add with acquire-release semantics at GPU scope: the arrival
+// publishes the warp's partial (its lanes' stores ordered before it by
+// __syncwarp), and the last arrival sees every earlier one's.
+__device__ __forceinline__ int32_t atom_add_acq_rel(int32_t *p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 template <int HKV>
 struct Dec {
   static constexpr int kHkv = HKV;
@@ -531,8 +542,7 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
           p.part_lse[slot * kHq + 2 * gh] = m0 + log2f(l0);
           p.part_lse[slot * kHq + 2 * gh + 1] = m1 + log2f(l1);
         }
-        __threadfence();
-        __syncwarp();
+        __syncwarp();                               // released by the counter's atomic
         if constexpr (kTwoLevel) {
           // Two-level merge.  A request cut into at most kMergeOneLevel splits
           // is merged as in the one-level instance.  One cut into more is
@@ -556,7 +566,7 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
               ctr = &p.gcounters[slot_of(mb) * kHkv + gh];
             }
             int old = 0;
-            if (lane == 0) old = atomicAdd(ctr, 1);
+            if (lane == 0) old = atom_add_acq_rel(ctr, 1);
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old != mn - 1) mn = 0;                 // not the last: nothing to merge
           }
@@ -564,7 +574,7 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
             // the last of these partials' warps: merge them.  Their lse values
             // are loaded by the lanes side by side (partial k by lane k % 32),
             // the o rows partial after partial with several loads in flight.
-            __threadfence();
+            __syncwarp();                             // after lane 0's acquire
             auto mslot = [&](int k) { return slot_of(mb + ms * k); };
             // partial `lane`'s lse values and the first batch of o rows, all in
             // flight at once; the lse values stay in their lanes for the weights
@@ -658,11 +668,10 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
               p.part_lse[gs * kHq + 2 * gh + 1] = L1 + log2f(d1);
               p.gcounters[gs * kHkv + gh] = 0;
             }
-            __threadfence();
             __syncwarp();
             const int ng = (ns + kMergeGroup - 1) / kMergeGroup;
             int old = 0;
-            if (lane == 0) old = atomicAdd(&p.counters[(int64_t)h.r * kHkv + gh], 1);
+            if (lane == 0) old = atom_add_acq_rel(&p.counters[(int64_t)h.r * kHkv + gh], 1);
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old != ng - 1) break;                  // not the last group
             mb = 0;
@@ -672,14 +681,14 @@ __global__ void __launch_bounds__(Dec<HKV>::kThreads, Dec<HKV>::kCtasPerSm)
           }
         } else {
           int old = 0;
-          if (lane == 0) old = atomicAdd(&p.counters[(int64_t)h.r * kHkv + gh], 1);
+          if (lane == 0) old = atom_add_acq_rel(&p.counters[(int64_t)h.r * kHkv + gh], 1);
           old = __shfl_sync(0xffffffffu, old, 0);
           if (old == h.bl - h.bf) {
             // last of the (request, KV head) splits: merge them (one level).  The splits'
             // lse values are loaded by the lanes side by side (split bf + k by
             // lane k % 32), the o rows split after split with several loads in
             // flight; the sums run in split order.
-            __threadfence();
+            __syncwarp();                             // after lane 0's acquire
             const int ns = h.bl - h.bf + 1;
             auto slot_of = [&](int k) {
               return 2 * (int64_t)(h.bf + k) + (k == 0 ? h.head_shift : 0);
