@@ -152,7 +152,7 @@ __device__ __forceinline__ Seg load_seg(const AttnParams &p, int32_t i, int64_t 
 // kPage1: page_size 1, where every index form holds the slot itself.
 constexpr int kMergeBatch = 4;                // split partials loaded before any is applied
 constexpr int kMergeGroup = 8;                // two-level merge: splits per group
-constexpr int kMergeOneLevel = 24;            // ... taken for requests cut more ways than this
+constexpr int kMergeOneLevel = 16;            // ... taken for requests cut more ways than this
 
 template <bool kPage1>
 __device__ __forceinline__ int32_t load_raw(const AttnParams &p, const int32_t *row, int64_t j) {
