@@ -567,11 +567,13 @@ int msg_paged_attention_noalloc(const void *q, int64_t q_row_stride, const void 
  *                      of probability zero; a greedy row takes a +inf logit as
  *                      its maximum.
  *   stream             cudaStream_t (NULL: the legacy default stream).
- * Two kernel launches on `stream`: a scan that reads every logit from HBM
- * once (many CTAs per row) and a row kernel (one CTA per row, started early
- * by programmatic dependent launch) that re-reads at most a few chunks of a
- * row, or, for a top-p boundary deep inside a flat distribution, the row a few
- * times (from L2 when the batch fits there).
+ * With temperatures: two kernel launches on `stream`, a scan that reads every
+ * logit from HBM once (many CTAs per row) and a row kernel (one CTA per row,
+ * started early by programmatic dependent launch) that re-reads at most a few
+ * chunks of a row, or, for a top-p boundary deep inside a flat distribution,
+ * the row a few times (from L2 when the batch fits there).  Without them (every
+ * row greedy): one launch, a CTA per row reading it once; the workspace is
+ * still checked but not used.
  * Errors: MSG_ERR_INVALID_ARG, MSG_ERR_UNSUPPORTED, MSG_ERR_ALIGNMENT,
  *         MSG_ERR_WORKSPACE, MSG_ERR_CUDA.
  */
@@ -584,7 +586,7 @@ int msg_sample(const void *logits, int32_t logits_dtype, int64_t logits_row_stri
 /*
  * Bytes of msg_sample's workspace for `batch` rows of `vocab` logits (per
  * row: each 256-logit chunk's maximum and mass, a sparse sample, and the scan
- * parts' partial results; about 14.5 KB per row at V = 151,936).  0 for an
+ * parts' finiteness flags; about 14.0 KB per row at V = 151,936).  0 for an
  * invalid or unsupported size.  Host only.
  */
 size_t msg_sample_workspace_size(int32_t batch, int32_t vocab);
