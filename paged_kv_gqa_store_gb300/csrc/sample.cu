@@ -26,6 +26,12 @@
 //
 // Masses are fp32 2^((l - max) * log2(e) / T) summed in a fixed order (no
 // atomics), so a row's token is deterministic.
+//
+// The row kernel's CTAs take the rows in order of a cost class read from the
+// parameters (top-p cuts over whole distributions first), so each long row
+// gets an SM of its own.  A batch without temperatures (every row greedy)
+// runs one kernel instead: a CTA per row reads it once and keeps its first
+// maximum.
 #include <math.h>
 #include <stddef.h>
 
