@@ -427,8 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      items < 4 * G && units >= 8 * (int64_t)G && units < (1ll << 30);
   // k-th piece of this CTA: taken by the producer warp 1 (lane 0) just before
   // it starts loading it (from the global counter, or the next piece of this
-  // CTA's split range), published through a 16-entry queue; every role reads
-  // the same sequence.  w = -1: no more work.
+  // CTA's split range), published with the item's fields through the
+  // kItemQueue-entry queue; every role reads the same sequence.  w = -1: no
+  // more work.
   auto fetch_piece = [&](uint32_t k, bool grab, bool whole_warp, Item &it) -> Piece {
     const int e = (int)(k % kItemQueue);
     volatile int32_t *qe = piece_q + kQEntry * e;
